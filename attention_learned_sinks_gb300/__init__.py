@@ -1,0 +1,17 @@
+"""Grouped-query attention with learned per-head sinks for GB300 (sm_103a).
+
+The computation lives in libsinkattn.so (C ABI: include/sinkattn.h); this
+package holds its ctypes binding, its build script and the seeded synthetic
+input generators. Importing the package does not load the library; the first
+call does, and raises if the library is missing.
+"""
+from .sinkattn import (  # noqa: F401
+    SinkAttnError,
+    load,
+    sinkattn_decode,
+    sinkattn_decode_workspace_size,
+    sinkattn_get_device_error,
+    sinkattn_merge,
+    sinkattn_prefill,
+    sinkattn_prefill_workspace_size,
+)

@@ -1,0 +1,183 @@
+// C ABI of libsinkattn.so (declared in include/sinkattn.h): argument
+// validation, split planning and dispatch to the kernels. No device memory is
+// allocated and no stream is synchronised here (except by
+// sinkattn_get_device_error, which exists to read a device word back).
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/sinkattn.h"
+#include "launch.h"
+
+using namespace sinkattn;
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool mask_ok(const sinkattn_mask_t &m) {
+  return m.window >= 0 && isfinite(m.scale) && m.scale > 0.f;
+}
+
+sinkattn_status_t from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sinkattn_status_string(sinkattn_status_t s) {
+  switch (s) {
+    case SINKATTN_OK:
+      return "ok";
+    case SINKATTN_ERR_INVALID_ARGUMENT:
+      return "invalid argument";
+    case SINKATTN_ERR_UNSUPPORTED:
+      return "unsupported configuration";
+    case SINKATTN_ERR_WORKSPACE_TOO_SMALL:
+      return "workspace too small";
+    case SINKATTN_ERR_CUDA:
+      return "CUDA error";
+  }
+  return "unknown status";
+}
+
+size_t sinkattn_prefill_workspace_size(int64_t total_k, int hkv, int head_dim) {
+  if (total_k < 0 || hkv <= 0 || head_dim != kHeadDim) return 0;
+  return prefill_workspace_bytes(total_k, hkv);
+}
+
+sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
+                                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                   int batch, int64_t total_q, int64_t total_k, int max_seqlen_q,
+                                   int max_seqlen_k, int hq, int hkv, int head_dim,
+                                   const float *sinks, sinkattn_mask_t mask, void *out, float *lse,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 ||
+      hkv <= 0 || hq % hkv != 0 || !mask_ok(mask))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return SINKATTN_OK;
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (sinks && !aligned(sinks, 4)) ||
+      (lse && !aligned(lse, 4)))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch > 65535 || total_q > INT32_MAX || total_k > INT32_MAX ||
+      (max_seqlen_q + 127) / 128 > 65535)
+    return SINKATTN_ERR_UNSUPPORTED;
+  const size_t need = prefill_workspace_bytes(total_k, hkv);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+    return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
+  PrefillLaunch a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.sinks = sinks;
+  a.causal = mask.causal != 0;
+  a.window = mask.window;
+  a.scale = mask.scale;
+  a.out = out;
+  a.lse = lse;
+  a.v_f16 = workspace;
+  bool encode_failed = false;
+  cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return SINKATTN_ERR_CUDA;
+  return from_cuda(e);
+}
+
+size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int hkv, int head_dim,
+                                      int window, int num_splits) {
+  if (batch <= 0 || hq <= 0 || hkv <= 0 || head_dim != kHeadDim || max_seqlen_k < 0 ||
+      window < 0 || num_splits < 0)
+    return 0;
+  const DecodePlan plan = plan_decode(max_seqlen_k, window, num_splits);
+  return decode_workspace_layout(batch, hq, hkv, plan).bytes;
+}
+
+sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *kv_indptr, const int32_t *block_table,
+                                  const int32_t *seqlens_k, int64_t kv_rows, int max_pages_per_seq,
+                                  int page_size, int batch, int max_seqlen_k, int hq, int hkv,
+                                  int head_dim, const float *sinks, sinkattn_mask_t mask,
+                                  int num_splits, void *out, float *lse, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+  if (batch < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || num_splits < 0 ||
+      kv_rows < 0 || !mask_ok(mask))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (hq / hkv > 8) return SINKATTN_ERR_UNSUPPORTED;
+  const bool paged = block_table != nullptr;
+  if (paged == (kv_indptr != nullptr)) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (paged && (seqlens_k == nullptr || page_size <= 0 || max_pages_per_seq <= 0))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!paged && seqlens_k != nullptr) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch == 0) return SINKATTN_OK;
+  if (!q || !k_cache || !v_cache || !out) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      (kv_indptr && !aligned(kv_indptr, 4)) || (block_table && !aligned(block_table, 4)) ||
+      (seqlens_k && !aligned(seqlens_k, 4)) || (sinks && !aligned(sinks, 4)) ||
+      (lse && !aligned(lse, 4)))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
+  const DecodePlan plan = plan_decode(max_seqlen_k, mask.window, num_splits);
+  if (plan.max_splits > 1) {
+    const size_t need = decode_workspace_layout(batch, hq, hkv, plan).bytes;
+    if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
+  }
+  DecodeLaunch a;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.kv_indptr = kv_indptr;
+  a.block_table = block_table;
+  a.seqlens_k = seqlens_k;
+  a.max_pages = max_pages_per_seq;
+  a.page_size = page_size;
+  a.batch = batch;
+  a.max_seqlen_k = max_seqlen_k;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.window = mask.window;
+  a.sinks = sinks;
+  a.scale = mask.scale;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.plan = plan;
+  return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_lse, int num_splits,
+                                 int64_t rows, int hq, int head_dim, const float *sinks, void *out,
+                                 float *lse, void *stream) {
+  if (num_splits < 0 || rows < 0 || hq <= 0) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (rows == 0) return SINKATTN_OK;
+  if (!out || (num_splits > 0 && (!partial_o || !partial_lse))) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if ((partial_o && !aligned(partial_o, 16)) || (partial_lse && !aligned(partial_lse, 4)) ||
+      !aligned(out, 16) || (sinks && !aligned(sinks, 4)) || (lse && !aligned(lse, 4)))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if ((rows * hq + 7) / 8 > INT32_MAX) return SINKATTN_ERR_UNSUPPORTED;
+  return from_cuda(launch_merge(partial_o, partial_lse, num_splits, rows, hq, sinks, out, lse,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+sinkattn_status_t sinkattn_get_device_error(void *stream, int *code) {
+  if (code == nullptr) return SINKATTN_ERR_INVALID_ARGUMENT;
+  *code = 0;
+  return from_cuda(prefill_read_error(static_cast<cudaStream_t>(stream), code));
+}
+
+}  // extern "C"

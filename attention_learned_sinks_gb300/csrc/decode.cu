@@ -1,0 +1,441 @@
+// Split-KV decode for sink attention: one query token per sequence over a
+// contiguous or paged bf16 KV cache.
+//
+// Page "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention":
+// the online softmax keeps a running maximum m and a running denominator d;
+// the head's sink is folded in by starting m at the sink (with d = 1) instead
+// of at -inf, and when the KV sequence is cut into blocks only one block may
+// start that way. Page "CuTeDSL at Perplexity", section "Prefill and decode
+// specialisation": decode is bound by the DRAM traffic of the KV cache, so it
+// gets its own kernel and grid.
+//
+// Block = (split s, KV head g, sequence b), 4 warps. The block owns a chunk of
+// the visible keys; each warp streams 32-token slabs of K and V (slabs w,
+// w+4, ...) into its own 3-stage shared-memory ring with 16-byte cp.async
+// copies, so no block-wide barrier sits in the loop. All group query heads of
+// KV head g (up to 8) are served from one read of each K/V byte:
+//
+//   S^T[16 tokens x 8 heads] = K[16 x 64] . Q^T   (mma.sync m16n8k16, N = heads)
+//   O^T[64 dims x 8 heads]  += V^T . P^T          (P^T re-used as the B operand
+//                                                  after an in-register 8x8
+//                                                  transpose, movmatrix)
+//
+// The per-warp states (m, d, O) are combined in shared memory; a sequence with
+// one block writes the final bf16 output directly, otherwise each block writes
+// a normalised fp32 partial and its log-sum-exp, and the last block to arrive
+// (per-(sequence, KV head) counter, no grid barrier) merges them
+// (page "CuTeDSL at Perplexity", section "Grid synchronization": prefer kernel
+// boundaries or local counters over grid-wide barriers).
+#include <math.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace sinkattn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlab = 32;                       // tokens per warp step
+constexpr int kStages = 3;                      // per-warp pipeline depth
+constexpr int kRowBytes = kHeadDim * 2;         // one K or V row: 128 B
+constexpr int kSlabBytes = kSlab * kRowBytes;   // 4 KB of K (or of V)
+constexpr int kStageBytes = 2 * kSlabBytes;     // K + V
+constexpr int kWarpBytes = kStages * kStageBytes;
+constexpr int kSmemBytes = kWarps * kWarpBytes;  // 96 KB -> two blocks per SM
+constexpr int kMaxGroup = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Params {
+  const __nv_bfloat16 *q, *k, *v;
+  const int32_t *kv_indptr, *block_table, *seqlens_k;
+  int max_pages, page_size;
+  int batch, hq, hkv, group, window, chunk;
+  const float *sinks;
+  float scale_log2;
+  __nv_bfloat16 *out;
+  float *lse;
+  float *part_o, *part_lse;
+  unsigned int *counters;
+};
+
+// Element offset of row (token j, KV head g) of sequence b in the K/V cache.
+template <bool kPaged>
+__device__ __forceinline__ size_t kv_row(const Params &p, int b, int kv_base, int j, int g) {
+  if (kPaged) {
+    const int page = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + j / p.page_size);
+    return ((static_cast<size_t>(page) * p.hkv + g) * p.page_size + (j % p.page_size)) * kHeadDim;
+  }
+  return (static_cast<size_t>(kv_base + j) * p.hkv + g) * kHeadDim;
+}
+
+// 128-byte rows, 16-byte chunks XOR-swizzled by row so that ldmatrix of 8 rows
+// of one chunk column touches 8 different bank groups.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
+}
+
+template <bool kPaged>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lr = lane >> 2, lc = lane & 3;  // mma fragment row / column group
+
+  int kv_base = 0, L;
+  if (kPaged) {
+    L = p.seqlens_k[b];
+  } else {
+    kv_base = p.kv_indptr[b];
+    L = p.kv_indptr[b + 1] - kv_base;
+  }
+  const int lo = p.window > 0 ? max(0, L - p.window) : 0;
+  const int nkv = max(0, L - lo);
+  // A context longer than the host's max_seqlen_k bound would need more
+  // blocks than the grid has: such a sequence gets longer blocks instead.
+  int chunk = p.chunk;
+  if ((nkv + chunk - 1) / chunk > static_cast<int>(gridDim.x)) {
+    const int unit = kWarps * kSlab;
+    chunk = ((nkv + gridDim.x - 1) / gridDim.x + unit - 1) / unit * unit;
+  }
+  const int nsplit = max(1, (nkv + chunk - 1) / chunk);
+  if (split >= nsplit) return;
+  const int t0 = lo + split * chunk;
+  const int t1 = min(L, t0 + chunk);
+  const int nslab = (max(0, t1 - t0) + kSlab - 1) / kSlab;
+  const int my_slabs = warp < nslab ? (nslab - warp + kWarps - 1) / kWarps : 0;
+
+  // Q^T as the B operand of S^T = K Q^T: lane (lr, lc) holds head lr,
+  // dims ks*16 + 2lc + {0,1} and + 8.
+  uint32_t qf[4][2];
+  {
+    const bool valid = lr < p.group;
+    const __nv_bfloat16 *qrow =
+        p.q + (static_cast<size_t>(b) * p.hq + g * p.group + (valid ? lr : 0)) * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      qf[ks][0] = valid ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * lc) : 0u;
+      qf[ks][1] = valid ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * lc + 8) : 0u;
+    }
+  }
+
+  // Online-softmax state for heads 2lc and 2lc+1 (log2 domain). The sink
+  // initialises block 0, warp 0: m = sink, d = 1 (d kept by lane row 0 only,
+  // since d is summed over the 8 lane rows at the end).
+  float m0 = -INFINITY, m1 = -INFINITY, d0 = 0.f, d1 = 0.f;
+  if (p.sinks != nullptr && split == 0 && warp == 0) {
+    const int h0 = min(2 * lc, p.group - 1), h1 = min(2 * lc + 1, p.group - 1);
+    m0 = p.sinks[g * p.group + h0] * kLog2e;
+    m1 = p.sinks[g * p.group + h1] * kLog2e;
+    if (lr == 0) d0 = d1 = 1.f;
+  }
+  float o[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+
+  const uint32_t wbase = smem_u32(smem) + warp * kWarpBytes;
+
+  auto load_slab = [&](int i) {
+    const int slab0 = t0 + (warp + i * kWarps) * kSlab;
+    const uint32_t kdst = wbase + (i % kStages) * kStageBytes;
+    const uint32_t vdst = kdst + kSlabBytes;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int row = r * 4 + (lane >> 3);
+      const int col = lane & 7;
+      const int j = slab0 + row;
+      const bool ok = j < t1;
+      const size_t off = ok ? kv_row<kPaged>(p, b, kv_base, j, g) + col * 8 : 0;
+      cp_async_16(kdst + swz(row, col), p.k + off, ok ? 16u : 0u);
+      cp_async_16(vdst + swz(row, col), p.v + off, ok ? 16u : 0u);
+    }
+  };
+
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (i < my_slabs) load_slab(i);
+    cp_async_commit();
+  }
+
+  for (int it = 0; it < my_slabs; ++it) {
+    cp_async_wait<kStages - 2>();
+    __syncwarp();
+    if (it + kStages - 1 < my_slabs) load_slab(it + kStages - 1);
+    cp_async_commit();
+
+    const int slab0 = t0 + (warp + it * kWarps) * kSlab;
+    const uint32_t kb = wbase + (it % kStages) * kStageBytes;
+    const uint32_t vb = kb + kSlabBytes;
+    const int mi = lane >> 3, mr = lane & 7;
+
+    // scores: two 16-token m-tiles
+    float s[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[mt][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4];
+        const int row = mt * 16 + (mi & 1) * 8 + mr;
+        ldmatrix_x4(kb + swz(row, ks * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
+      }
+    }
+    // scale to log2 units, mask the ragged end of the chunk, tile maximum
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = slab0 + mt * 16 + lr + ((e & 2) ? 8 : 0);
+        const float x = j < t1 ? s[mt][e] * p.scale_log2 : -INFINITY;
+        s[mt][e] = x;
+        if (e & 1)
+          mx1 = fmaxf(mx1, x);
+        else
+          mx0 = fmaxf(mx0, x);
+      }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
+    m0 = mn0;
+    m1 = mn1;
+    float sum0 = 0.f, sum1 = 0.f;
+    // P enters the tensor core as two bf16 terms, hi + lo, which together
+    // carry 16 significant bits: a single bf16 P (8 bits) alone would add
+    // about 1.6e-3 rms relative error to the output.
+    uint32_t pb[2][2], pl[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const float p0 = fast_exp2(s[mt][0] - base0), p1 = fast_exp2(s[mt][1] - base1);
+      const float p2 = fast_exp2(s[mt][2] - base0), p3 = fast_exp2(s[mt][3] - base1);
+      sum0 += p0 + p2;
+      sum1 += p1 + p3;
+      const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+      const uint32_t l01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+      const uint32_t l23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+      // (token lr, heads 2lc..) -> (head lr, tokens 2lc..): the B fragment of P^T
+      pb[mt][0] = movmatrix_trans(h01);
+      pb[mt][1] = movmatrix_trans(h23);
+      pl[mt][0] = movmatrix_trans(l01);
+      pl[mt][1] = movmatrix_trans(l23);
+    }
+    d0 = d0 * al0 + sum0;
+    d1 = d1 * al1 + sum1;
+#pragma unroll
+    for (int dt = 0; dt < 4; ++dt) {
+      o[dt][0] *= al0;
+      o[dt][1] *= al1;
+      o[dt][2] *= al0;
+      o[dt][3] *= al1;
+    }
+    // O^T += V^T P^T
+#pragma unroll
+    for (int dt = 0; dt < 4; ++dt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t a[4];
+        const int row = mt * 16 + (mi >> 1) * 8 + mr;
+        ldmatrix_x4_trans(vb + swz(row, dt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
+        mma_bf16_16816(o[dt], a, pl[mt][0], pl[mt][1]);
+      }
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    d0 += __shfl_xor_sync(0xffffffffu, d0, off);
+    d1 += __shfl_xor_sync(0xffffffffu, d1, off);
+  }
+
+  // ---- combine the 4 warps through shared memory ----
+  __syncthreads();  // every warp is done with its ring
+  float *sm_m = reinterpret_cast<float *>(smem);          // [4][8]
+  float *sm_d = sm_m + kWarps * kMaxGroup;                 // [4][8]
+  float *sm_o = sm_d + kWarps * kMaxGroup;                 // [4][8][64]
+  if (lr == 0) {
+    sm_m[warp * 8 + 2 * lc] = m0;
+    sm_m[warp * 8 + 2 * lc + 1] = m1;
+    sm_d[warp * 8 + 2 * lc] = d0;
+    sm_d[warp * 8 + 2 * lc + 1] = d1;
+  }
+#pragma unroll
+  for (int dt = 0; dt < 4; ++dt) {
+    float *ow = sm_o + warp * 512;
+    ow[(2 * lc) * 64 + dt * 16 + lr] = o[dt][0];
+    ow[(2 * lc + 1) * 64 + dt * 16 + lr] = o[dt][1];
+    ow[(2 * lc) * 64 + dt * 16 + lr + 8] = o[dt][2];
+    ow[(2 * lc + 1) * 64 + dt * 16 + lr + 8] = o[dt][3];
+  }
+  __syncthreads();
+
+  const int tid = threadIdx.x;
+  const int hh = tid >> 4;          // head within the group
+  const int c0 = (tid & 15) * 4;    // 4 output dims
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 + hh]);
+  const float baseM = M == -INFINITY ? 0.f : M;
+  float Dn = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float f = fast_exp2(sm_m[w * 8 + hh] - baseM);
+    Dn += f * sm_d[w * 8 + hh];
+    const float4 ov = *reinterpret_cast<const float4 *>(sm_o + w * 512 + hh * 64 + c0);
+    acc[0] += f * ov.x;
+    acc[1] += f * ov.y;
+    acc[2] += f * ov.z;
+    acc[3] += f * ov.w;
+  }
+  const float inv = Dn > 0.f ? 1.f / Dn : 0.f;
+  // block lse in natural log (-inf when nothing is visible and no sink)
+  const float blse = Dn > 0.f ? (M + fast_log2(Dn)) * kLn2 : -INFINITY;
+  const bool head_ok = hh < p.group;
+  const int qh = g * p.group + hh;
+  const size_t row_h = static_cast<size_t>(b) * p.hq + qh;
+
+  if (nsplit == 1) {
+    if (head_ok) {
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2 *>(p.out + row_h * kHeadDim + c0) = pk;
+      if (p.lse != nullptr && (tid & 15) == 0) p.lse[row_h] = blse;
+    }
+    return;
+  }
+
+  const size_t rows_hq = static_cast<size_t>(p.batch) * p.hq;
+  if (head_ok) {
+    float4 pv = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<float4 *>(p.part_o + (split * rows_hq + row_h) * kHeadDim + c0) = pv;
+    if ((tid & 15) == 0) p.part_lse[split * rows_hq + row_h] = blse;
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(p.counters + b * p.hkv + g, 1u);
+    s_last = prev == static_cast<unsigned>(nsplit - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- last block: merge the nsplit partials of this (sequence, KV head) ----
+  if (head_ok) {
+    float Mx = -INFINITY;
+    for (int k = 0; k < nsplit; ++k) Mx = fmaxf(Mx, __ldcg(p.part_lse + k * rows_hq + row_h));
+    float W = 0.f, r[4] = {0.f, 0.f, 0.f, 0.f};
+    if (Mx != -INFINITY) {
+      for (int k = 0; k < nsplit; ++k) {
+        const float l = __ldcg(p.part_lse + k * rows_hq + row_h);
+        const float w = fast_exp2((l - Mx) * kLog2e);
+        if (w == 0.f) continue;
+        const float4 ov =
+            __ldcg(reinterpret_cast<const float4 *>(p.part_o + (k * rows_hq + row_h) * kHeadDim + c0));
+        W += w;
+        r[0] += w * ov.x;
+        r[1] += w * ov.y;
+        r[2] += w * ov.z;
+        r[3] += w * ov.w;
+      }
+    }
+    const float iw = W > 0.f ? 1.f / W : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16x2(r[0] * iw, r[1] * iw);
+    pk.y = pack_bf16x2(r[2] * iw, r[3] * iw);
+    *reinterpret_cast<uint2 *>(p.out + row_h * kHeadDim + c0) = pk;
+    if (p.lse != nullptr && (tid & 15) == 0)
+      p.lse[row_h] = W > 0.f ? Mx + fast_log2(W) * kLn2 : -INFINITY;
+  }
+  if (tid == 0) p.counters[b * p.hkv + g] = 0u;  // ready for the next call / graph replay
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int max_seqlen_k, int window, int num_splits) {
+  int span = window > 0 ? (window < max_seqlen_k ? window : max_seqlen_k) : max_seqlen_k;
+  if (span < 1) span = 1;
+  long chunk;
+  if (num_splits > 0) {
+    chunk = (span + num_splits - 1) / num_splits;
+  } else {
+    // 512-token blocks keep a few thousand blocks in flight for typical
+    // batches; very long contexts grow the block so at most 64 splits exist.
+    chunk = 512;
+    const long cap = (span + 63) / 64;
+    if (chunk < cap) chunk = cap;
+  }
+  const long unit = kWarps * kSlab;
+  chunk = (chunk + unit - 1) / unit * unit;
+  DecodePlan plan;
+  plan.chunk = static_cast<int>(chunk);
+  plan.max_splits = static_cast<int>((span + chunk - 1) / chunk);
+  if (plan.max_splits < 1) plan.max_splits = 1;
+  return plan;
+}
+
+DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const DecodePlan &plan) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  DecodeWorkspace w;
+  const size_t rows = static_cast<size_t>(plan.max_splits) * batch * hq;
+  w.off_lse = up(rows * kHeadDim * sizeof(float));
+  w.off_counters = w.off_lse + up(rows * sizeof(float));
+  w.bytes = w.off_counters + up(static_cast<size_t>(batch) * hkv * sizeof(unsigned));
+  return w;
+}
+
+cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
+  Params p;
+  p.q = static_cast<const __nv_bfloat16 *>(a.q);
+  p.k = static_cast<const __nv_bfloat16 *>(a.k);
+  p.v = static_cast<const __nv_bfloat16 *>(a.v);
+  p.kv_indptr = a.kv_indptr;
+  p.block_table = a.block_table;
+  p.seqlens_k = a.seqlens_k;
+  p.max_pages = a.max_pages;
+  p.page_size = a.page_size;
+  p.batch = a.batch;
+  p.hq = a.hq;
+  p.hkv = a.hkv;
+  p.group = a.hq / a.hkv;
+  p.window = a.window;
+  p.chunk = a.plan.chunk;
+  p.sinks = a.sinks;
+  p.scale_log2 = a.scale * kLog2e;
+  p.out = static_cast<__nv_bfloat16 *>(a.out);
+  p.lse = a.lse;
+  const DecodeWorkspace w = decode_workspace_layout(a.batch, a.hq, a.hkv, a.plan);
+  uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+  p.part_o = reinterpret_cast<float *>(ws);
+  p.part_lse = reinterpret_cast<float *>(ws + w.off_lse);
+  p.counters = reinterpret_cast<unsigned int *>(ws + w.off_counters);
+
+  if (a.plan.max_splits > 1) {
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(a.batch) * a.hkv * 4, stream);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(a.plan.max_splits, a.hkv, a.batch);
+  if (a.block_table != nullptr) {
+    cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    decode_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  } else {
+    cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    decode_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sinkattn

@@ -1,0 +1,66 @@
+// Internal host interface between the C ABI (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sinkattn {
+
+constexpr int kHeadDim = 64;
+
+// ---- decode ----------------------------------------------------------------
+// Split plan: the visible KV range of every (sequence, KV head) is cut into
+// blocks of `chunk` tokens; max_splits bounds the block count of any sequence.
+struct DecodePlan {
+  int chunk;
+  int max_splits;
+};
+DecodePlan plan_decode(int max_seqlen_k, int window, int num_splits);
+// Workspace layout for a plan: [partial_o | partial_lse | counters].
+struct DecodeWorkspace {
+  size_t off_lse, off_counters, bytes;
+};
+DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const DecodePlan &plan);
+
+struct DecodeLaunch {
+  const void *q, *k, *v;
+  const int32_t *kv_indptr, *block_table, *seqlens_k;
+  int max_pages, page_size;
+  int batch, max_seqlen_k, hq, hkv, window;
+  const float *sinks;
+  float scale;
+  void *out;
+  float *lse;
+  void *workspace;
+  DecodePlan plan;
+};
+cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream);
+
+// ---- merge -----------------------------------------------------------------
+cudaError_t launch_merge(const float *partial_o, const float *partial_lse, int num_splits,
+                         int64_t rows, int hq, const float *sinks, void *out, float *lse,
+                         cudaStream_t stream);
+
+// ---- prefill ---------------------------------------------------------------
+struct PrefillLaunch {
+  const void *q, *k, *v;
+  const int32_t *cu_q, *cu_k;
+  int batch;
+  int64_t total_q, total_k;
+  int max_seqlen_q, max_seqlen_k, hq, hkv;
+  const float *sinks;
+  int causal, window;
+  float scale;
+  void *out;
+  float *lse;
+  void *v_f16;  // workspace: fp16 copy of v, prefill_workspace_bytes(total_k, hkv)
+};
+size_t prefill_workspace_bytes(int64_t total_k, int hkv);
+// Returns cudaSuccess, or the failing CUDA error; *encode_failed is set when
+// the tensor-map encoding (driver entry point) failed.
+cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed);
+// Reads and clears the prefill kernel's device error word (synchronises stream).
+cudaError_t prefill_read_error(cudaStream_t stream, int *code);
+
+}  // namespace sinkattn

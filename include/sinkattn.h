@@ -1,0 +1,180 @@
+/*
+ * sinkattn: grouped-query attention with learned per-head sinks, for NVIDIA
+ * GB300 (sm_103a). C ABI of libsinkattn.so.
+ *
+ * The operation. Page "GPT-OSS on day 0", section "Attention: GQA with
+ * Attention Sinks": several query heads share one KV head, and every query
+ * head owns one trained sink parameter that takes part in the softmax.
+ * Section "Kernels for GPT-OSS / Sink Attention": the sink is one extra logit
+ * beside the scaled Q.K products; it has no value row. For query row i of
+ * sequence b and query head h (KV head g = h / (hq / hkv)):
+ *
+ *   p   = (Lk_b - Lq_b) + i          query position; queries are the last
+ *                                     Lq_b of the Lk_b positions
+ *   J   = { j < Lk_b : (!causal || j <= p) && (window == 0 || j > p - window) }
+ *   s_j = scale * <q[i,h,:], k[j,g,:]>
+ *   out = sum_{j in J} e^{s_j} v[j,g,:] / (e^{sink_h} + sum_{j in J} e^{s_j})
+ *   lse = ln(e^{sink_h} + sum_{j in J} e^{s_j})
+ *
+ * The sink is not multiplied by `scale`. With sinks == NULL the sink term is
+ * absent. A row with an empty J gets out = 0 and lse = sink_h (or -inf with no
+ * sinks); it never produces NaN.
+ *
+ * The same section describes the online softmax (running maximum m and running
+ * denominator d) and how the sink enters it: m starts at the head's sink
+ * instead of -inf, with d = 1, and when the KV sequence is split into blocks
+ * the sink enters exactly one block. The kernels behind this header do that.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *    contiguous, 16-byte aligned. bf16 data is passed as `const void*`.
+ *  - The library allocates no device memory and never synchronises: every
+ *    call only enqueues work on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and returns. Device-side metadata (sequence offsets,
+ *    lengths, block tables) is never read by the host, so calls can be
+ *    captured in a CUDA graph.
+ *  - Host-side argument errors return before anything is enqueued. A failed
+ *    launch returns SINKATTN_ERR_CUDA. No C++ exception crosses the ABI.
+ *  - head_dim must be 64 (SINKATTN_ERR_UNSUPPORTED otherwise) and hq must be a
+ *    multiple of hkv.
+ *  - Outputs: `out` is bf16 (round to nearest even) with the query layout;
+ *    `lse` is float32, natural log, sink included; `lse` may be NULL.
+ *  - Inputs must be finite. Rows of K/V outside a sequence may be read but get
+ *    zero weight.
+ */
+#ifndef SINKATTN_H
+#define SINKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SINKATTN_OK = 0,
+  SINKATTN_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size */
+  SINKATTN_ERR_UNSUPPORTED = 2,      /* valid but not implemented (head_dim != 64, ...) */
+  SINKATTN_ERR_WORKSPACE_TOO_SMALL = 3,
+  SINKATTN_ERR_CUDA = 4              /* a CUDA runtime/driver call failed */
+} sinkattn_status_t;
+
+/* Mask of one call. The pages do not describe windows; this library reads a
+ * window of W as "the W most recent positions up to and including p". */
+typedef struct {
+  int causal;  /* nonzero: key j visible only if j <= p */
+  int window;  /* 0: no window; W > 0: key j visible only if j > p - W */
+  float scale; /* multiplies q.k; must be finite and > 0 */
+} sinkattn_mask_t;
+
+/* Human-readable name of a status code (static storage). */
+const char *sinkattn_status_string(sinkattn_status_t status);
+
+/*
+ * Prefill over packed variable-length sequences (page "Fast embeddings on
+ * GPUs", section "ROSE": attention over ragged inputs without padding).
+ *
+ *   q        bf16 [total_q, hq, 64]   sequence b owns rows cu_seqlens_q[b]..[b+1]
+ *   k, v     bf16 [total_k, hkv, 64]  sequence b owns rows cu_seqlens_k[b]..[b+1]
+ *   cu_seqlens_q, cu_seqlens_k  int32 [batch+1], device, non-decreasing,
+ *            starting at 0; the last entries equal total_q and total_k.
+ *   total_q, total_k            host copies of those last entries (bounds for
+ *            the tensor maps that stage Q/K/V tiles).
+ *   max_seqlen_q, max_seqlen_k  host upper bounds on any sequence's length
+ *            (grid sizing only; a smaller bound silently drops rows).
+ *   sinks    float32 [hq] or NULL.
+ *   out      bf16 [total_q, hq, 64];   lse  float32 [total_q, hq] or NULL.
+ *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
+ *            sinkattn_prefill_workspace_size(total_k, hkv, head_dim) bytes.
+ *            It receives an fp16 copy of v for the P.V product (values of
+ *            magnitude above 65504 are clamped to +-65504 there).
+ * A sequence with Lq_b > Lk_b is allowed: its first Lq_b - Lk_b queries see no
+ * key under a causal mask.
+ */
+size_t sinkattn_prefill_workspace_size(int64_t total_k, int hkv, int head_dim);
+
+sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
+                                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                   int batch, int64_t total_q, int64_t total_k,
+                                   int max_seqlen_q, int max_seqlen_k, int hq, int hkv,
+                                   int head_dim, const float *sinks, sinkattn_mask_t mask,
+                                   void *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
+ * Decode: one query token per sequence over a KV cache, split along the KV
+ * sequence (section "Kernels for GPT-OSS / Sink Attention": attention is
+ * parallelised over heads and over the KV length; the sink enters one block
+ * only). Block partials are merged by log-sum-exp inside the same launch: the
+ * last block of each (sequence, KV head) to finish merges them.
+ *
+ *   q        bf16 [batch, hq, 64]. The query sits at position Lk_b - 1.
+ * Contiguous cache (block_table == NULL):
+ *   k_cache, v_cache  bf16 [kv_rows, hkv, 64]; sequence b owns rows
+ *            kv_indptr[b]..kv_indptr[b+1]; kv_indptr int32 [batch+1], device,
+ *            starting at 0; kv_rows = kv_indptr[batch] (host copy).
+ *            seqlens_k must be NULL.
+ * Paged cache (page "Fast embeddings on GPUs", section "ROSE": paged decode):
+ *   k_cache, v_cache  bf16 [kv_rows, hkv, page_size, 64]; kv_rows = number of
+ *            pages. block_table int32 [batch, max_pages_per_seq], device:
+ *            key j of sequence b is slot j % page_size of page
+ *            block_table[b][j / page_size]. seqlens_k int32 [batch], device.
+ *            kv_indptr must be NULL. Any page_size >= 1 works; 16 is the
+ *            tested serving layout.
+ *   max_seqlen_k   host upper bound on Lk_b (sizes the split grid).
+ *   num_splits     0 = automatic; n > 0 = split the longest sequence into
+ *            about n blocks (shorter ones get proportionally fewer).
+ *   hq / hkv must be at most 8 (one KV head and all its query heads per block).
+ *   out      bf16 [batch, hq, 64];  lse float32 [batch, hq] or NULL.
+ *   workspace      device scratch of at least sinkattn_decode_workspace_size()
+ *            bytes for the same (batch, max_seqlen_k, hq, hkv, head_dim,
+ *            window, num_splits), 256-byte aligned; its contents need not be
+ *            initialised and are overwritten. When the plan has a single block
+ *            per sequence (short contexts or a short window) it is not touched
+ *            and may be NULL.
+ * mask.causal has no effect here (every cached key is at or before the query).
+ */
+size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int hkv, int head_dim,
+                                      int window, int num_splits);
+
+sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *kv_indptr, const int32_t *block_table,
+                                  const int32_t *seqlens_k, int64_t kv_rows,
+                                  int max_pages_per_seq, int page_size, int batch,
+                                  int max_seqlen_k, int hq, int hkv, int head_dim,
+                                  const float *sinks, sinkattn_mask_t mask, int num_splits,
+                                  void *out, float *lse, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * Merge of split-KV partials by log-sum-exp (section "Kernels for GPT-OSS /
+ * Sink Attention": when the KV sequence is split into blocks, the sink belongs
+ * to one block only; here it may enter as its own block, exactly once).
+ *
+ *   partial_o    float32 [num_splits, rows, hq, 64]: each block's normalised output
+ *   partial_lse  float32 [num_splits, rows, hq]: each block's natural-log lse;
+ *                -inf marks an empty block (its partial_o is ignored).
+ *   sinks        float32 [hq] or NULL; when given, the sink is one more block
+ *                with lse = sinks[h] and a zero output.
+ *   out          bf16 [rows, hq, 64];  lse float32 [rows, hq] or NULL.
+ * With M = max_k lse_k: out = sum_k e^{lse_k - M} o_k / sum_k e^{lse_k - M},
+ * lse = M + ln sum_k e^{lse_k - M}. All blocks empty: out = 0, lse = -inf.
+ */
+sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_lse,
+                                 int num_splits, int64_t rows, int hq, int head_dim,
+                                 const float *sinks, void *out, float *lse, void *stream);
+
+/*
+ * Device error word. Every wait inside the kernels is bounded; a wait that
+ * runs out records a nonzero code here and the kernel returns early instead of
+ * hanging. This call synchronises `stream`, copies the word to *code and
+ * resets it to 0. Codes: 0 none; 1 a pipeline barrier wait timed out.
+ */
+sinkattn_status_t sinkattn_get_device_error(void *stream, int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKATTN_H */

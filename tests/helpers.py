@@ -1,0 +1,73 @@
+"""Shared comparison helpers for the GPU-vs-oracle parity tests.
+
+Tolerances (floating point; bf16 inputs, fp32 accumulation, bf16 output):
+  |gpu - ref|                          <= max(1e-2, one bf16 spacing at |ref|)
+  sum |gpu - ref| / sum |ref|          <= 2e-3     on the output (L1 ratio)
+  max |lse_gpu - lse_ref|              <= 1e-3     on the natural-log lse
+
+The output is bf16. Below |ref| = 2 a bf16 spacing is at most 2^-7 < 1e-2, so
+the 1e-2 bar applies unchanged; at |ref| >= 2 the spacing (>= 2^-6) is itself
+above 1e-2 and no bf16 value can be within 1e-2 of every real number there,
+so the bar there is one spacing (the result must be one of the two bf16
+neighbours of the exact value).
+Rounding the exact output to bf16 alone gives an L1 ratio near 1.35e-3 (a
+quarter spacing on average over a significand uniform in [1, 2)); the kernels
+keep P at 11 (prefill, fp16) or 16 (decode, bf16 hi+lo) significant bits so
+that P adds well under the remaining 0.65e-3.
+Rows whose reference sees nothing (lse = -inf) must give out = 0, lse = -inf.
+
+Set SINKATTN_PARITY_LOG=<file> to append one line of error statistics per check.
+"""
+import json
+import os
+
+import numpy as np
+import torch
+
+ABS_FLOOR = 1e-2
+MEAN_REL = 2e-3
+LSE_ABS = 1e-3
+
+
+def to_np(t):
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
+    return t.detach().float().cpu().double().numpy()
+
+
+def bf16_spacing(x):
+    """Distance between consecutive bf16 values around |x| (8 significant bits)."""
+    a = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.ldexp(1.0, (np.floor(np.log2(a)) - 7).astype(np.int64))
+
+
+def check_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+    o = to_np(out_gpu).reshape(out_ref.shape)
+    assert np.all(np.isfinite(o)), what + ": non-finite output"
+    err = np.abs(o - out_ref)
+    bound = np.maximum(ABS_FLOOR, bf16_spacing(out_ref))
+    max_abs = float(err.max()) if err.size else 0.0
+    worst = float((err / bound).max()) if err.size else 0.0
+    denom = float(np.abs(out_ref).sum())
+    mean_rel = float(err.sum()) / denom if denom > 0 else float(err.sum())
+    stats = {"what": what, "max_abs": max_abs, "max_abs_over_bound": worst,
+             "mean_rel": mean_rel, "n": int(err.size)}
+    if lse_gpu is not None:
+        l = to_np(lse_gpu).reshape(lse_ref.shape)
+        empty = ~np.isfinite(lse_ref)
+        assert np.all(l[empty] == -np.inf), what + ": empty rows must give lse = -inf"
+        if np.any(~empty):
+            stats["lse_abs"] = float(np.abs(l[~empty] - lse_ref[~empty]).max())
+    log = os.environ.get("SINKATTN_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps(stats) + "\n")
+    assert worst <= 1.0, "%s: max_abs %.3g exceeds max(1e-2, bf16 spacing)" % (what, max_abs)
+    assert mean_rel <= MEAN_REL, "%s: mean_rel %.3g" % (what, mean_rel)
+    if "lse_abs" in stats:
+        assert stats["lse_abs"] <= LSE_ABS, "%s: lse err %.3g" % (what, stats["lse_abs"])
+    return stats
+
+
+def cuda(t):
+    return None if t is None else t.cuda()

@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/sinkattn.h declares, and rejects bad arguments before
+it touches the device (all cases below return before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_learned_sinks_gb300 as sa
+from attention_learned_sinks_gb300 import build as sbuild
+from attention_learned_sinks_gb300 import sinkattn as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sbuild.build()
+    return sa.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sinkattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sinkattn_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(B.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.sinkattn_status_string(code)
+    assert lib.sinkattn_status_string(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: every call below fails validation
+M = B.Mask(1, 0, 0.125)
+
+
+def prefill(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, cuq=FAKE, cuk=FAKE, batch=2, tq=10, tk=10, mq=5, mk=5,
+             hq=8, hkv=2, d=64, sinks=None, mask=M, out=FAKE, lse=None)
+    a.update(kw)
+    return lib.sinkattn_prefill(a["q"], a["k"], a["v"], a["cuq"], a["cuk"], a["batch"], a["tq"],
+                                a["tk"], a["mq"], a["mk"], a["hq"], a["hkv"], a["d"], a["sinks"],
+                                a["mask"], a["out"], a["lse"], a.get("ws"), a.get("wsb", 0), None)
+
+
+def decode(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, indptr=FAKE, table=None, seqlens=None, rows=100, maxp=0,
+             page=0, batch=2, mk=50, hq=8, hkv=2, d=64, sinks=None, mask=M, ns=0, out=FAKE,
+             lse=None, ws=None, wsb=0)
+    a.update(kw)
+    return lib.sinkattn_decode(a["q"], a["k"], a["v"], a["indptr"], a["table"], a["seqlens"],
+                               a["rows"], a["maxp"], a["page"], a["batch"], a["mk"], a["hq"],
+                               a["hkv"], a["d"], a["sinks"], a["mask"], a["ns"], a["out"],
+                               a["lse"], a["ws"], a["wsb"], None)
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert prefill(lib, d=128) == B.SINKATTN_ERR_UNSUPPORTED
+    assert prefill(lib, hq=6, hkv=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill(lib, hkv=0) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill(lib, mask=B.Mask(1, 0, 0.0)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill(lib, mask=B.Mask(1, -1, 0.1)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill(lib, mask=B.Mask(1, 0, float("nan"))) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill(lib, q=None) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill(lib, out=ctypes.c_void_p((1 << 20) + 2)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill(lib, batch=-1) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    need = lib.sinkattn_prefill_workspace_size(10, 2, 64)
+    assert need >= 10 * 2 * 64 * 2
+    assert prefill(lib) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert prefill(lib, ws=FAKE, wsb=need - 1) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert prefill(lib, ws=ctypes.c_void_p((1 << 20) + 16), wsb=need) == \
+        B.SINKATTN_ERR_INVALID_ARGUMENT
+    # nothing to do: returns before any launch
+    assert prefill(lib, batch=0) == B.SINKATTN_OK
+    assert prefill(lib, tq=0) == B.SINKATTN_OK
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert decode(lib, d=80) == B.SINKATTN_ERR_UNSUPPORTED
+    assert decode(lib, hq=32, hkv=2) == B.SINKATTN_ERR_UNSUPPORTED   # group of 16
+    assert decode(lib, hq=9, hkv=2) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert decode(lib, table=FAKE, seqlens=FAKE, page=16, maxp=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert decode(lib, indptr=None) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert decode(lib, indptr=None, table=FAKE, seqlens=None, page=16, maxp=4) == \
+        B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert decode(lib, seqlens=FAKE) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert decode(lib, ns=-1) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert decode(lib, mask=B.Mask(1, 0, -1.0)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    # long contexts are split: the workspace must be big enough
+    need = lib.sinkattn_decode_workspace_size(2, 5000, 8, 2, 64, 0, 0)
+    assert need > 0
+    assert decode(lib, mk=5000, ws=None, wsb=0) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert decode(lib, mk=5000, ws=FAKE, wsb=need - 1) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert decode(lib, batch=0) == B.SINKATTN_OK
+
+
+def test_merge_rejects_bad_arguments(lib):
+    f = lib.sinkattn_merge
+    assert f(FAKE, FAKE, 2, 4, 8, 32, None, FAKE, None, None) == B.SINKATTN_ERR_UNSUPPORTED
+    assert f(None, FAKE, 2, 4, 8, 64, None, FAKE, None, None) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, -1, 4, 8, 64, None, FAKE, None, None) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, 2, 0, 8, 64, None, FAKE, None, None) == B.SINKATTN_OK
+
+
+def test_workspace_sizes_follow_the_split_plan(lib):
+    ws = lambda b, mk, w=0, ns=0: lib.sinkattn_decode_workspace_size(b, mk, 64, 8, 64, w, ns)
+    assert ws(64, 8192) >= 16 * 64 * 64 * 64 * 4          # up to 16 blocks of 512
+    assert ws(64, 8192, ns=2) < ws(64, 8192)
+    assert ws(64, 8192, w=128) < ws(64, 8192)               # window: one block
+    assert lib.sinkattn_decode_workspace_size(0, 10, 8, 2, 64, 0, 0) == 0
+    assert lib.sinkattn_prefill_workspace_size(1000, 8, 64) == 1000 * 8 * 64 * 2
+    assert lib.sinkattn_prefill_workspace_size(1000, 8, 128) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(B, "_LIB", None)
+    with pytest.raises(RuntimeError):
+        B.load(str(tmp_path / "missing.so"))

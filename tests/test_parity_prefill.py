@@ -1,0 +1,120 @@
+"""GPU prefill (packed variable-length sequences) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import attention_learned_sinks_gb300 as sa
+from attention_learned_sinks_gb300 import synthetic as S
+from helpers import check_close, cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(c, device_tensors=False):
+    t = (lambda x: x) if device_tensors else cuda
+    return sa.sinkattn_prefill(t(c.q), t(c.k), t(c.v), c.cu_seqlens_q.cuda(),
+                               c.cu_seqlens_k.cuda(), c.max_seqlen_q, c.max_seqlen_k,
+                               sinks=cuda(c.sinks), causal=c.causal, window=c.window,
+                               scale=c.scale)
+
+
+def oracle_prefill(oracle, c):
+    return oracle.attention(c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k, hq=c.hq, hkv=c.hkv,
+                            head_dim=64, sinks=c.sinks, causal=c.causal, window=c.window,
+                            scale=c.scale)
+
+
+def test_prefill_tiny_config(oracle_lib):
+    """1 sequence of 64 tokens, causal, 4 q heads sharing 1 KV head, scale 1/8."""
+    c = S.tiny_prefill()
+    out, lse = run_prefill(c)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "tiny_prefill")
+
+
+# q/k lengths that span several 128-row tiles with ragged tails, chunked
+# queries (lq < lk), more queries than keys, and empty sequences
+SHAPES = [
+    ([1], [1]),
+    ([127], [127]),
+    ([128], [128]),
+    ([129], [129]),
+    ([300, 17, 256, 1], [300, 17, 256, 1]),
+    ([200], [700]),          # chunked: queries are the last 200 of 700 positions
+    ([130], [40]),           # more queries than keys: first 90 see nothing
+    ([0, 64, 0], [0, 64, 5]),
+    ([513], [513]),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
+@pytest.mark.parametrize("causal,window", [(True, 0), (False, 0), (True, 1), (True, 128),
+                                           (True, 129), (False, 50)])
+def test_prefill_shapes(oracle_lib, shape, causal, window):
+    lq, lk = shape
+    c = S.make_prefill("shape", lq, lk, 8, 2, seed=61 + sum(lq), causal=causal, window=window,
+                       sink_std=1.5)
+    out, lse = run_prefill(c)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "prefill %s causal=%s w=%d" % (shape, causal, window))
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (12, 3), (64, 8)])
+def test_prefill_groups_and_no_sink(oracle_lib, hq, hkv):
+    for with_sinks in (True, False):
+        c = S.make_prefill("grp", [190, 260], [190, 260], hq, hkv, seed=67 + hq,
+                           with_sinks=with_sinks)
+        out, lse = run_prefill(c)
+        ro, rl = oracle_prefill(oracle_lib, c)
+        check_close(out, lse, ro, rl, "hq=%d hkv=%d sinks=%s" % (hq, hkv, with_sinks))
+
+
+def test_prefill_large_sink(oracle_lib):
+    c = S.make_prefill("bigsink", [300], [300], 4, 1, seed=69)
+    c.sinks = torch.tensor([40.0, -40.0, 0.0, 12.0])
+    out, lse = run_prefill(c)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "large sink")
+
+
+def _sample_rows(c, per_seq, seed):
+    g = torch.Generator().manual_seed(seed)
+    rows = []
+    for b, lq in enumerate(c.seqlens_q):
+        if lq == 0:
+            continue
+        idx = set([0, lq - 1, min(lq - 1, 127), min(lq - 1, 128)])
+        idx |= set(torch.randint(0, lq, (per_seq,), generator=g).tolist())
+        for i in sorted(idx):
+            for h in torch.randint(0, c.hq, (2,), generator=g).tolist():
+                rows.append((b, h, i))
+    return np.array(rows, dtype=np.int32)
+
+
+def _check_rows(oracle, c, out, lse, rows, what):
+    ro, rl = oracle.attention_rows(rows, c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k, hq=c.hq,
+                                   hkv=c.hkv, head_dim=64, sinks=c.sinks, causal=c.causal,
+                                   window=c.window, scale=c.scale)
+    cu = c.cu_seqlens_q.tolist()
+    pr = torch.tensor([cu[b] + i for b, _, i in rows], device=out.device)
+    ph = torch.tensor([h for _, h, _ in rows], device=out.device)
+    check_close(out[pr, ph], lse[pr, ph], ro, rl, what)
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_prefill_varlen_full_config(oracle_lib, window):
+    """16 sequences, lengths uniform in [512, 4096], 64 q / 8 kv heads, causal;
+    full and sliding window 128. Sampled rows against the oracle."""
+    c = S.varlen_prefill(window=window)
+    out, lse = run_prefill(c)
+    torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 24, 71), "varlen_prefill w=%d" % window)
+
+
+def test_prefill_chunked_full_config(oracle_lib):
+    """4096 query tokens at positions 126976..131071 of a 131072-token causal
+    context. Sampled rows against the oracle."""
+    c = S.chunked_prefill()
+    out, lse = run_prefill(c)
+    torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 40, 73), "chunked_prefill")
