@@ -28,6 +28,9 @@
 // boundaries or local counters over grid-wide barriers).
 #include <math.h>
 
+#include <mutex>
+
+#include "../../include/sinkattn.h"
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -439,3 +442,102 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
 }
 
 }  // namespace sinkattn
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode entry point.
+//
+// Some callers cannot hand the library a scratch buffer: code that runs under
+// a memory planner owning every device byte, plugin hosts that forbid
+// allocation while enqueueing work, and latency-critical loops where
+// cudaMalloc/cudaFree may synchronise the device. For them,
+// sinkattn_decode_noalloc keeps the split-KV partials and the block counters
+// in the fixed array below instead of a caller workspace. The array is part
+// of the library image: every GPU that loads the library holds it until the
+// process exits. All calls on a device share it and it keeps the previous
+// call's contents; the counters are cleared on the stream at the start of
+// each call and the partials are always written before they are read. Two
+// calls whose kernels overlap on the GPU (different streams, no ordering
+// between them) race on this array and give wrong results.
+
+namespace sinkattn {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SINKATTN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch for one device, looked up once while
+// that device is current (the host-side symbol is not a device address).
+cudaError_t noalloc_scratch(int device, void **ptr) {
+  static std::mutex mu;
+  static void *addr[256] = {};
+  if (device < 0 || device >= 256) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[device] == nullptr) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[device] = p;
+  }
+  *ptr = addr[device];
+  return cudaSuccess;
+}
+
+bool is_aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace sinkattn
+
+extern "C" sinkattn_status_t sinkattn_decode_noalloc(
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_indptr,
+    const int32_t *block_table, const int32_t *seqlens_k, int64_t kv_rows, int max_pages_per_seq,
+    int page_size, int batch, int max_seqlen_k, int hq, int hkv, int head_dim, const float *sinks,
+    sinkattn_mask_t mask, int num_splits, void *out, float *lse, void *stream) {
+  using namespace sinkattn;
+  if (batch < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || num_splits < 0 ||
+      kv_rows < 0 || mask.window < 0 || !isfinite(mask.scale) || !(mask.scale > 0.f))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim || hq / hkv > 8) return SINKATTN_ERR_UNSUPPORTED;
+  const bool paged = block_table != nullptr;
+  if (paged == (kv_indptr != nullptr)) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (paged && (seqlens_k == nullptr || page_size <= 0 || max_pages_per_seq <= 0))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!paged && seqlens_k != nullptr) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch == 0) return SINKATTN_OK;
+  if (!q || !k_cache || !v_cache || !out) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!is_aligned(q, 16) || !is_aligned(k_cache, 16) || !is_aligned(v_cache, 16) ||
+      !is_aligned(out, 16) || (kv_indptr && !is_aligned(kv_indptr, 4)) ||
+      (block_table && !is_aligned(block_table, 4)) || (seqlens_k && !is_aligned(seqlens_k, 4)) ||
+      (sinks && !is_aligned(sinks, 4)) || (lse && !is_aligned(lse, 4)))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
+  const DecodePlan plan = plan_decode(max_seqlen_k, mask.window, num_splits);
+  // the plan's scratch must fit the fixed array
+  if (plan.max_splits > 1 &&
+      decode_workspace_layout(batch, hq, hkv, plan).bytes > SINKATTN_NOALLOC_SCRATCH_BYTES)
+    return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return SINKATTN_ERR_CUDA;
+  void *scratch = nullptr;
+  if (noalloc_scratch(device, &scratch) != cudaSuccess) return SINKATTN_ERR_CUDA;
+  DecodeLaunch a;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.kv_indptr = kv_indptr;
+  a.block_table = block_table;
+  a.seqlens_k = seqlens_k;
+  a.max_pages = max_pages_per_seq;
+  a.page_size = page_size;
+  a.batch = batch;
+  a.max_seqlen_k = max_seqlen_k;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.window = mask.window;
+  a.sinks = sinks;
+  a.scale = mask.scale;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = scratch;
+  a.plan = plan;
+  return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
+                                                                             : SINKATTN_ERR_CUDA;
+}

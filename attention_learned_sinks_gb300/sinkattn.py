@@ -26,6 +26,7 @@ EXPORTED = (
     "sinkattn_prefill",
     "sinkattn_decode_workspace_size",
     "sinkattn_decode",
+    "sinkattn_decode_noalloc",
     "sinkattn_merge",
     "sinkattn_get_device_error",
 )
@@ -66,6 +67,9 @@ def load(path: str = LIB_PATH):
     lib.sinkattn_decode.argtypes = [P, P, P, P, P, P, L, I, I, I, I, I, I, I, P, Mask, I,
                                     P, P, P, S, P]
     lib.sinkattn_decode.restype = I
+    lib.sinkattn_decode_noalloc.argtypes = [P, P, P, P, P, P, L, I, I, I, I, I, I, I, P, Mask,
+                                            I, P, P, P]
+    lib.sinkattn_decode_noalloc.restype = I
     lib.sinkattn_merge.argtypes = [P, P, I, L, I, I, P, P, P, P]
     lib.sinkattn_merge.restype = I
     lib.sinkattn_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
@@ -179,6 +183,28 @@ def sinkattn_decode(q, k_cache, v_cache, *, kv_indptr=None, block_table=None, se
                              int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
                              workspace.numel(), _stream(stream))
     _check(st, "sinkattn_decode")
+    return out, lse
+
+
+def sinkattn_decode_noalloc(q, k_cache, v_cache, *, kv_indptr=None, block_table=None,
+                            seqlens_k=None, max_seqlen_k, sinks=None, window=0, scale=None,
+                            num_splits=0, out, lse=None, stream=None):
+    """sinkattn_decode without a workspace: the library's fixed scratch array is
+    used instead (for callers that may not allocate device memory). `out` (and
+    `lse`, if wanted) must be given; nothing is allocated here."""
+    lib = load()
+    batch, hq, d = q.shape
+    hkv = k_cache.shape[1]
+    if block_table is not None:
+        kv_rows, page_size, max_pages = k_cache.shape[0], k_cache.shape[2], block_table.shape[1]
+    else:
+        kv_rows, page_size, max_pages = k_cache.shape[0], 0, 0
+    mask = Mask(1, int(window), float(d ** -0.5 if scale is None else scale))
+    st = lib.sinkattn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_indptr),
+                                     _ptr(block_table), _ptr(seqlens_k), kv_rows, max_pages,
+                                     page_size, batch, int(max_seqlen_k), hq, hkv, d, _ptr(sinks),
+                                     mask, int(num_splits), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "sinkattn_decode_noalloc")
     return out, lse
 
 

@@ -148,6 +148,38 @@ sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void
                                   size_t workspace_bytes, void *stream);
 
 /*
+ * Allocation-free decode. The pages have no counterpart to this entry point;
+ * it exists for callers that cannot give the library a scratch buffer:
+ * code running under a memory planner that owns all device memory, plugin
+ * hosts that forbid allocation while work is enqueued, and latency-critical
+ * loops in which cudaMalloc/cudaFree could synchronise the device.
+ *
+ * Same arguments and results as sinkattn_decode, without the workspace: the
+ * split-KV partials and counters live in a fixed device array of
+ * SINKATTN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits. The library still
+ * allocates nothing at call time; the caller passes all inputs and outputs.
+ *  - A plan whose scratch (sinkattn_decode_workspace_size for the same
+ *    arguments) exceeds SINKATTN_NOALLOC_SCRATCH_BYTES is rejected with
+ *    SINKATTN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (an
+ *    explicit, smaller num_splits shrinks the scratch a batch needs).
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (counters are cleared on the stream by each call). Calls whose
+ *    work can overlap on the GPU, e.g. on unordered streams, race on it.
+ */
+#define SINKATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+sinkattn_status_t sinkattn_decode_noalloc(const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *kv_indptr,
+                                          const int32_t *block_table, const int32_t *seqlens_k,
+                                          int64_t kv_rows, int max_pages_per_seq, int page_size,
+                                          int batch, int max_seqlen_k, int hq, int hkv,
+                                          int head_dim, const float *sinks, sinkattn_mask_t mask,
+                                          int num_splits, void *out, float *lse, void *stream);
+
+/*
  * Merge of split-KV partials by log-sum-exp (section "Kernels for GPT-OSS /
  * Sink Attention": when the KV sequence is split into blocks, the sink belongs
  * to one block only; here it may enter as its own block, exactly once).
