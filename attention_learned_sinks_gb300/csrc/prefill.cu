@@ -16,16 +16,27 @@
 // value of magnitude up to 65504; larger ones clamp to +-65504). Q K^T stays
 // in bf16.
 //
-// One CTA = 128 query rows of one (sequence, query head); 6 warps:
-//   warps 0-3  softmax: thread r owns row r (TMEM lane r)
-//   warp 4     TMA producer: Q once, then K_j / V_j into a 3-stage ring
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into TMEM (two S
-//              buffers), O += P_j V_j with P_j read from TMEM
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,320); P_j (bf16 pairs)
-// overwrites the first 64 columns of its S buffer after S_j has been read.
-// The running maximum is only moved (and O, d rescaled) when it grows by more
-// than 8 in log2 units; the final division uses the same reference maximum,
-// so the result is unchanged while most tiles skip the O round trip.
+// One CTA = 128 query rows x NT query heads (NT = 2 heads of one KV group
+// when the group size is even, else 1); every K/V tile is shared by the NT
+// tiles. Warps (NT = 2):
+//   warps 0-3, 4-7  softmax warpgroup t: thread r owns row r of tile t (TMEM lane r)
+//   warp 8          TMA producer: both Q tiles once, then K_j / V_j into a 3-stage ring
+//   warp 9          MMA issuer (one thread) and TMEM owner
+//   warps 10-11     idle; they complete the third warpgroup so that setmaxnreg
+//                   can hand its registers to the softmax warpgroups (208 each)
+// TMEM (512 columns): S_t at [128 t, 128 t + 128), O_t at [256 + 64 t, ...).
+// P_t (fp16 pairs) overwrites the first 64 columns of S_t once S_t has been
+// read, and feeds P V straight from TMEM. The MMA order
+//   QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...
+// lets softmax warpgroup 0 work on S_0(j+1) while the tensor core runs tile
+// 1's products, and the other way round (ping-pong).
+// Softmax: one read of the 128 scores of a row from TMEM, a range mask on
+// boundary tiles only, tree reductions (3-input max), packed f32x2 arithmetic, and one
+// exponential in four evaluated on the FMA pipe by a cubic (exp2_poly2) so the
+// special-function unit is not the only exp pipe. The running maximum is only
+// moved (and O, d rescaled) when it grows by more than 8 in log2 units; the
+// final division uses the same reference maximum, so the result is unchanged
+// while most tiles skip the O round trip.
 #include <math.h>
 
 #include <mutex>
@@ -36,25 +47,36 @@
 namespace sinkattn {
 namespace {
 
-constexpr int kBM = 128;  // query rows per CTA
+constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per KV tile
 constexpr int kStages = 3;
 constexpr int kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemO = 256;
+constexpr uint32_t kTmemO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+template <int NT>
+struct Cfg {
+  // NT = 2: three full warpgroups, so setmaxnreg can move registers from the
+  // producer/MMA warpgroup to the two softmax warpgroups.
+  static constexpr int kThreads = NT * 128 + (NT == 2 ? 128 : 64);
+  static constexpr int kLaunchRegs = NT == 2 ? 168 : 255;  // ptxas limit for kThreads
+  static constexpr int kRegsOther = 88;     // producer / MMA warpgroup after setmaxnreg
+  static constexpr int kRegsSoftmax = 208;  // each softmax warpgroup after setmaxnreg
+  static constexpr int kProducerWarp = NT * 4;
+  static constexpr int kMmaWarp = NT * 4 + 1;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + NT * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+};
+
+static_assert(Cfg<2>::kRegsOther * 128 + Cfg<2>::kRegsSoftmax * 256 <=
+                  Cfg<2>::kLaunchRegs * Cfg<2>::kThreads,
+              "register split must fit the registers the block is launched with");
 
 constexpr uint32_t kIdescQK = idesc_f32acc(kBM, kBN, /*bf16=*/true, false, false);
 constexpr uint32_t kIdescPV = idesc_f32acc(kBM, kHeadDim, /*bf16=*/false, false, true);
@@ -77,31 +99,107 @@ struct Barriers {
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(Barriers) <= 256, "barrier block");
 
-__global__ void __launch_bounds__(kThreads, 1)
+// 2^x for a pair, on the FMA pipe: x = n + f with n = round(x) (added to the
+// exponent field) and f in [-1/2, 1/2]; 2^f from a cubic fitted to minimise the
+// maximum relative error on that interval (Remez exchange, 7.5e-5). Inputs are
+// clamped at -126, so very negative arguments give about 1e-38 rather than 0:
+// callers use it only where some element of the row is at least 2^-8.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  const float2 magic = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -126.f);
+  x.y = fmaxf(x.y, -126.f);
+  const float2 t = __fadd2_rn(x, magic);  // round(x) sits in the low significand bits
+  const float2 n = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
+  const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
+  float2 p = __ffma2_rn(f, make_float2(0.0551716685f, 0.0551716685f),
+                        make_float2(0.2426111251f, 0.2426111251f));
+  p = __ffma2_rn(p, f, make_float2(0.6932609677f, 0.6932609677f));
+  p = __ffma2_rn(p, f, make_float2(0.9999280572f, 0.9999280572f));
+  float2 r;
+  r.x = __uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23));
+  r.y = __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23));
+  return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+#define F8(i) "=f"(v[i]), "=f"(v[i + 1]), "=f"(v[i + 2]), "=f"(v[i + 3]), \
+  "=f"(v[i + 4]), "=f"(v[i + 5]), "=f"(v[i + 6]), "=f"(v[i + 7])
+// 32 consecutive fp32 TMEM columns of this thread's lane, straight into floats.
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : F8(0), F8(8), F8(16), F8(24)
+      : "r"(taddr));
+}
+#undef F8
+
+// Columns outside this row's visible range [c_lo, c_lo + len) of the tile -> -inf.
+// col0 is the first tile column held in sv.
+__device__ __forceinline__ void mask32(float (&sv)[32], int col0, int c_lo, int len) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (static_cast<unsigned>(col0 + i - c_lo) >= static_cast<unsigned>(len)) sv[i] = -INFINITY;
+}
+
+__device__ __forceinline__ float row_max32(const float (&sv)[32]) {
+  float m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = max3(sv[8 * i], sv[8 * i + 1], sv[8 * i + 2]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = max3(m[i], sv[8 * i + 3], sv[8 * i + 4]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = max3(m[i], sv[8 * i + 5], sv[8 * i + 6]);
+  return max3(max3(m[0], m[1], m[2]), m[3], max3(sv[7], sv[15], max3(sv[23], sv[31], m[0])));
+}
+
+// 32 scores -> 2^(x c - m) as 16 fp16 pairs into pk[off..off+16); row sums into acc.
+template <bool kMasked>
+__device__ __forceinline__ void exp32(const float (&sv)[32], float2 c2, float2 nb2,
+                                      float2 (&acc)[4], uint32_t (&pk)[32], int off) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 a = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), c2, nb2);
+    const float2 e = (!kMasked && (i & 3) == 3) ? exp2_poly2(a)
+                                                 : make_float2(fast_exp2(a.x), fast_exp2(a.y));
+    acc[i & 3] = __fadd2_rn(acc[i & 3], e);
+    pk[off + i] = pack_f16x2(e.x, e.y);
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (sbase - raw);
-  Barriers *bars = reinterpret_cast<Barriers *>(smem + kOffBar);
+  Barriers *bars = reinterpret_cast<Barriers *>(smem + C::kOffBar);
   volatile int *abort = &bars->abort;
 
-  const int h = blockIdx.x;
+  const int h0 = blockIdx.x * NT;  // first query head of this CTA
   const int b = blockIdx.y;
   const int qt = p.max_qtiles - 1 - static_cast<int>(blockIdx.z);  // longest work first
   const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
   const int k0 = p.cu_k[b], lk = p.cu_k[b + 1] - k0;
   if (qt * kBM >= lq) return;  // CTA-uniform
   const int rows = min(kBM, lq - qt * kBM);
-  const int kvh = h / p.group;
+  const int kvh = h0 / p.group;
   const int p_min = lk - lq + qt * kBM;  // position of this tile's first query
   const int p_max = p_min + rows - 1;
   int key_hi = lk;
@@ -122,13 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], kBM);
+      mbar_init(&bars->o_done[i], 1);
     }
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -137,14 +235,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == kProducerWarp) {
+  if (warp >= C::kProducerWarp) {
+    if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsOther));
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, kTileBytes);
-      tma_load_3d(sbase + kOffQ, &tm_q, &bars->q_full, 0, h, q0 + qt * kBM);
+      mbar_arrive_expect_tx(&bars->q_full, NT * kTileBytes);
+      for (int t = 0; t < NT; ++t)
+        tma_load_3d(sbase + C::kOffQ + t * kTileBytes, &tm_q, &bars->q_full, 0, h0 + t,
+                    q0 + qt * kBM);
       int issued = 0;
       for (int j = 0; j < n; ++j) {
         const int st = j % kStages;
@@ -153,9 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         const int row = k0 + (kt_lo + j) * kBN;
         mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-        tma_load_3d(sbase + kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, kvh, row);
+        tma_load_3d(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, kvh, row);
         mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-        tma_load_3d(sbase + kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, kvh, row);
+        tma_load_3d(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, kvh, row);
         issued = j + 1;
       }
       if (*abort) {
@@ -168,91 +270,110 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && n > 0) {
-      const uint64_t qdesc = sdesc_sw128(sbase + kOffQ);
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, abort, &g_prefill_error)) return false;
-        if (!mbar_wait(&bars->v_full[i % kStages], (i / kStages) & 1, abort, &g_prefill_error))
-          return false;
-        tc_fence_after();
-        const uint64_t vdesc = sdesc_sw128(sbase + kOffV + (i % kStages) * kTileBytes);
-        const uint32_t pcol = tmem + kTmemS0 + (i & 1) * kBN;
+      auto qk = [&](int t, int j) {
+        const uint64_t qdesc = sdesc_sw128(sbase + C::kOffQ + t * kTileBytes);
+        const uint64_t kdesc = sdesc_sw128(sbase + C::kOffK + (j % kStages) * kTileBytes);
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          umma_ss(tmem + t * kBN, qdesc + ((ks * 32) >> 4), kdesc + ((ks * 32) >> 4), kIdescQK,
+                  ks > 0 ? 1u : 0u);
+        umma_commit(&bars->s_full[t]);
+      };
+      auto pv = [&](int t, int j) {
+        const uint64_t vdesc = sdesc_sw128(sbase + C::kOffV + (j % kStages) * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + kTmemO, pcol + kk * 8, vdesc + ((kk * 16 * 128) >> 4), kIdescPV,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->kv_empty[i % kStages]);
-        umma_commit(&bars->o_done);
-        return true;
+          umma_ts(tmem + kTmemO + t * kHeadDim, tmem + t * kBN + kk * 8,
+                  vdesc + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->o_done[t]);
       };
-      bool ok = mbar_wait(&bars->q_full, 0, abort, &g_prefill_error);
+      bool ok = mbar_wait(&bars->q_full, 0, abort, &g_prefill_error) &&
+                mbar_wait(&bars->k_full[0], 0, abort, &g_prefill_error);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < NT; ++t) qk(t, 0);
+      }
       for (int j = 0; ok && j < n; ++j) {
         const int st = j % kStages;
-        if (!mbar_wait(&bars->k_full[st], (j / kStages) & 1, abort, &g_prefill_error)) {
+        if (!mbar_wait(&bars->v_full[st], (j / kStages) & 1, abort, &g_prefill_error)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint64_t kdesc = sdesc_sw128(sbase + kOffK + st * kTileBytes);
-        const uint32_t sbuf = tmem + kTmemS0 + (j & 1) * kBN;
-#pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_ss(sbuf, qdesc + ((ks * 32) >> 4), kdesc + ((ks * 32) >> 4), kIdescQK,
-                  ks > 0 ? 1u : 0u);
-        umma_commit(&bars->s_full[j & 1]);
-        if (j > 0) ok = issue_pv(j - 1);
+        const bool next = j + 1 < n;
+        for (int t = 0; t < NT; ++t) {
+          if (!mbar_wait(&bars->p_full[t], j & 1, abort, &g_prefill_error)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          pv(t, j);
+          if (next) {
+            if (t == 0 && !mbar_wait(&bars->k_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
+                                     abort, &g_prefill_error)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            qk(t, j + 1);
+          }
+        }
+        if (!ok) break;
+        umma_commit(&bars->kv_empty[st]);
       }
-      if (ok) issue_pv(n - 1);
       // every MMA issued by this thread has finished before TMEM is released
       umma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, abort, &g_prefill_error, true);
     }
+  }
   } else {
+    if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsSoftmax));
     // -------------------------------------------------------------- softmax
-    const int r = threadIdx.x;  // row within the tile == TMEM lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int t = warp >> 2;             // which query tile (head h0 + t)
+    const int r = threadIdx.x & 127;     // row within the tile == TMEM lane
+    const int h = h0 + t;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_addr = lane_addr + t * kBN;
+    const uint32_t o_addr = lane_addr + kTmemO + t * kHeadDim;
     const bool has_sink = p.sinks != nullptr;
     float m_run = has_sink ? p.sinks[h] * kLog2e : -INFINITY;
     float d_run = has_sink ? 1.f : 0.f;
     const float c = p.scale_log2;
+    const float2 c2 = make_float2(c, c);
     const int pos = p_min + r;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const int buf = j & 1;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], (j >> 1) & 1, abort,
-                                             &g_prefill_error))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort, &g_prefill_error))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[kBN];
-#pragma unroll
-      for (int q = 0; q < kBN / 32; ++q)
-        tmem_ld32(lane_addr + kTmemS0 + buf * kBN + q * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(&sr[q * 32]));
-      tmem_wait_ld();
-      float s[kBN];
-#pragma unroll
-      for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sr[i]);
-
       const int key0 = (kt_lo + j) * kBN;
       const bool need_mask = (key0 + kBN > lk) || (p.causal && key0 + kBN - 1 > p_min) ||
                              (p.window > 0 && key0 <= p_max - p.window);
+      float s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32f(s_addr, s0);
+      tmem_ld32f(s_addr + 32, s1);
+      tmem_ld32f(s_addr + 64, s2);
+      tmem_ld32f(s_addr + 96, s3);
+      tmem_wait_ld();
       if (need_mask) {
-#pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          const int key = key0 + i;
-          const bool vis = key < lk && (!p.causal || key <= pos) &&
-                           (p.window == 0 || key > pos - p.window);
-          if (!vis) s[i] = -INFINITY;
-        }
+        // this row's visible keys form one range [lo, hi): sequence end, causal
+        // bound and window; as tile columns [c_lo, c_lo + len)
+        int hi = lk, lo = 0;
+        if (p.causal) hi = min(hi, pos + 1);
+        if (p.window > 0) lo = max(lo, pos - p.window + 1);
+        const int c_lo = min(max(lo - key0, 0), kBN);
+        const int len = max(min(hi - key0, kBN) - c_lo, 0);
+        mask32(s0, 0, c_lo, len);
+        mask32(s1, 32, c_lo, len);
+        mask32(s2, 64, c_lo, len);
+        mask32(s3, 96, c_lo, len);
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      const float mx = max3(fmaxf(row_max32(s0), row_max32(s1)), row_max32(s2), row_max32(s3));
       const float m_tile = mx * c;
       const float m_new = fmaxf(m_run, m_tile);
       float alpha = 1.f;
@@ -264,26 +385,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
       const float base = m_run == -INFINITY ? 0.f : m_run;
-      float sum = 0.f;
-      uint32_t pk[kBN / 2];
-#pragma unroll
-      for (int i = 0; i < kBN / 2; ++i) {
-        const float p0 = fast_exp2(fmaf(s[2 * i], c, -base));
-        const float p1 = fast_exp2(fmaf(s[2 * i + 1], c, -base));
-        sum += p0 + p1;
-        pk[i] = pack_f16x2(p0, p1);
+      const float2 nb2 = make_float2(-base, -base);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
+      // Pass 2: re-read each half, exponentiate, and store it as 32 columns of
+      // fp16 pairs over the half's first columns (already consumed).
+      {
+        uint32_t pk[32];
+        if (need_mask) {
+          exp32<true>(s0, c2, nb2, acc, pk, 0);
+          exp32<true>(s1, c2, nb2, acc, pk, 16);
+        } else {
+          exp32<false>(s0, c2, nb2, acc, pk, 0);
+          exp32<false>(s1, c2, nb2, acc, pk, 16);
+        }
+        tmem_st32(s_addr, pk);
+        if (need_mask) {
+          exp32<true>(s2, c2, nb2, acc, pk, 0);
+          exp32<true>(s3, c2, nb2, acc, pk, 16);
+        } else {
+          exp32<false>(s2, c2, nb2, acc, pk, 0);
+          exp32<false>(s3, c2, nb2, acc, pk, 16);
+        }
+        tmem_st32(s_addr + 32, pk);
       }
-      d_run += sum;
-#pragma unroll
-      for (int q = 0; q < kBN / 64; ++q)
-        tmem_st32(lane_addr + kTmemS0 + buf * kBN + q * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(&pk[q * 32]));
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a03 = __fadd2_rn(a01, a23);
+      d_run += a03.x + a03.y;
       tmem_wait_st();
       if (j > 0) {
-        // O holds P_0..P_{j-1} V; it must be complete before it is rescaled,
+        // O_t holds P_0..P_{j-1} V; it must be complete before it is rescaled,
         // and waiting for every phase in order keeps the parity unambiguous.
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&bars->o_done, (j - 1) & 1, abort, &g_prefill_error))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort,
+                                               &g_prefill_error))) {
           ok = false;
           break;
         }
@@ -294,56 +428,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < kHeadDim / 32; ++q) {
             uint32_t ov[32];
-            tmem_ld32(lane_addr + kTmemO + q * 32, ov);
+            tmem_ld32(o_addr + q * 32, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(lane_addr + kTmemO + q * 32, ov);
+            tmem_st32(o_addr + q * 32, ov);
           }
           tmem_wait_st();
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->p_full[buf]);
+      mbar_arrive(&bars->p_full[t]);
     }
 
     // ------------------------------------------------------------- epilogue
-    float o[kHeadDim];
+    const bool have_o = __all_sync(0xffffffffu, ok && n > 0 &&
+                                                   mbar_wait(&bars->o_done[t], (n - 1) & 1,
+                                                             abort, &g_prefill_error));
+    const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
+    const size_t row_h = static_cast<size_t>(q0 + qt * kBM + r) * p.hq + h;
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + row_h * kHeadDim);
+    if (have_o) tc_fence_after();
 #pragma unroll
-    for (int i = 0; i < kHeadDim; ++i) o[i] = 0.f;
-    if (__all_sync(0xffffffffu,
-                   ok && n > 0 && mbar_wait(&bars->o_done, (n - 1) & 1, abort, &g_prefill_error))) {
-      tc_fence_after();
-#pragma unroll
-      for (int q = 0; q < kHeadDim / 32; ++q) {
-        uint32_t ov[32];
-        tmem_ld32(lane_addr + kTmemO + q * 32, ov);
+    for (int q = 0; q < kHeadDim / 32; ++q) {
+      uint32_t ov[32];
+      if (have_o) {
+        tmem_ld32(o_addr + q * 32, ov);
         tmem_wait_ld();
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[q * 32 + i] = __uint_as_float(ov[i]);
+        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+      }
+      if (r < rows) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float *o = reinterpret_cast<const float *>(&ov[8 * i]);
+          uint4 v;
+          v.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+          v.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+          v.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+          v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+          dst[q * 4 + i] = v;
+        }
       }
     }
-    if (r < rows) {
-      const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
-      const size_t row_h = static_cast<size_t>(q0 + qt * kBM + r) * p.hq + h;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + row_h * kHeadDim);
-#pragma unroll
-      for (int i = 0; i < kHeadDim / 8; ++i) {
-        uint4 v;
-        v.x = pack_bf16x2(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
-        v.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
-        v.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
-        v.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
-        dst[i] = v;
-      }
-      if (p.lse != nullptr)
-        p.lse[row_h] = d_run > 0.f ? (m_run + fast_log2(d_run)) * kLn2 : -INFINITY;
-    }
+    if (r < rows && p.lse != nullptr)
+      p.lse[row_h] = d_run > 0.f ? (m_run + fast_log2(d_run)) * kLn2 : -INFINITY;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -441,11 +576,31 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
   p.scale_log2 = a.scale * kLog2e;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.lse = a.lse;
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.hq, a.batch, max_qtiles);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  cudaError_t e;
+  if (p.group % 2 == 0) {
+    e = cudaFuncSetAttribute(prefill_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<2>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits until the registers exist: the block must be launched
+    // with at least the split's total, or the softmax warps would never start.
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, prefill_kernel<2>);
+      if (e != cudaSuccess) return e;
+      launch_regs = attr.numRegs;
+    }
+    if (launch_regs * Cfg<2>::kThreads < Cfg<2>::kRegsOther * 128 + Cfg<2>::kRegsSoftmax * 256)
+      return cudaErrorNotSupported;
+    dim3 grid(a.hq / 2, a.batch, max_qtiles);
+    prefill_kernel<2><<<grid, Cfg<2>::kThreads, Cfg<2>::kSmemBytes, stream>>>(tq, tk, tv, p);
+  } else {
+    e = cudaFuncSetAttribute(prefill_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<1>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.hq, a.batch, max_qtiles);
+    prefill_kernel<1><<<grid, Cfg<1>::kThreads, Cfg<1>::kSmemBytes, stream>>>(tq, tk, tv, p);
+  }
   return cudaGetLastError();
 }
 
