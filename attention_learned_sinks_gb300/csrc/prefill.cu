@@ -23,13 +23,14 @@
 //   warp 8          TMA producer: both Q tiles once, then K_j / V_j into a 3-stage ring
 //   warp 9          MMA issuer (one thread) and TMEM owner
 //   warps 10-11     idle; they complete the third warpgroup so that setmaxnreg
-//                   can hand its registers to the softmax warpgroups (208 each)
-// TMEM (512 columns): S_t at [128 t, 128 t + 128), O_t at [256 + 64 t, ...).
-// P_t (fp16 pairs) overwrites the first 64 columns of S_t once S_t has been
-// read, and feeds P V straight from TMEM. The MMA order
-//   QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...
-// lets softmax warpgroup 0 work on S_0(j+1) while the tensor core runs tile
-// 1's products, and the other way round (ping-pong).
+//                   can hand its registers to the softmax warpgroups (200 each)
+// TMEM (512 columns): three 128-column S buffers shared round-robin by the
+// work items k = NT j + t (KV tile j, query tile t) and O_t at [384 + 64 t, ...).
+// P_k (fp16 pairs) overwrites the first 64 columns of its S buffer once S_k
+// has been read, and feeds P V straight from TMEM. With three buffers the MMA
+// warp computes S for up to two items ahead of the softmax, so a softmax
+// warpgroup rarely waits for its next scores, and the two warpgroups' softmax
+// phases overlap the tensor core's P V and Q K^T work.
 // Softmax: one read of the 128 scores of a row from TMEM, a range mask on
 // boundary tiles only, tree reductions (3-input max), packed f32x2 arithmetic, and one
 // exponential in four evaluated on the FMA pipe by a cubic (exp2_poly2) so the
@@ -52,7 +53,8 @@ constexpr int kBN = 128;  // keys per KV tile
 constexpr int kStages = 3;
 constexpr int kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;
+constexpr int kSBufs = 3;                        // S buffers shared round-robin by the tiles
+constexpr uint32_t kTmemO = kSBufs * 128;        // O_t at 384 + 64 t
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -63,8 +65,8 @@ struct Cfg {
   // producer/MMA warpgroup to the two softmax warpgroups.
   static constexpr int kThreads = NT * 128 + (NT == 2 ? 128 : 64);
   static constexpr int kLaunchRegs = NT == 2 ? 168 : 255;  // ptxas limit for kThreads
-  static constexpr int kRegsOther = 88;     // producer / MMA warpgroup after setmaxnreg
-  static constexpr int kRegsSoftmax = 208;  // each softmax warpgroup after setmaxnreg
+  static constexpr int kRegsOther = 104;    // producer / MMA warpgroup after setmaxnreg
+  static constexpr int kRegsSoftmax = 200;  // each softmax warpgroup after setmaxnreg
   static constexpr int kProducerWarp = NT * 4;
   static constexpr int kMmaWarp = NT * 4 + 1;
   static constexpr int kOffQ = 0;
@@ -97,8 +99,8 @@ struct Barriers {
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t s_full[kSBufs];
+  uint64_t p_full[kSBufs];
   uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -217,11 +219,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], kBM);
-      mbar_init(&bars->o_done[i], 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&bars->o_done[i], 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -237,97 +239,106 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 
   if (warp >= C::kProducerWarp) {
     if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsOther));
-  if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    if (warp == C::kProducerWarp && n > 0) {
+      // ---------------------------------------------------------- producer
+      // The whole warp runs this loop; one elected lane issues each copy.
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, NT * kTileBytes);
+      mbar_arrive_expect_tx_elect(&bars->q_full, NT * kTileBytes);
       for (int t = 0; t < NT; ++t)
-        tma_load_3d(sbase + C::kOffQ + t * kTileBytes, &tm_q, &bars->q_full, 0, h0 + t,
-                    q0 + qt * kBM);
+        tma_load_3d_elect(sbase + C::kOffQ + t * kTileBytes, &tm_q, &bars->q_full, 0, h0 + t,
+                          q0 + qt * kBM);
       int issued = 0;
       for (int j = 0; j < n; ++j) {
         const int st = j % kStages;
-        if (j >= kStages &&
-            !mbar_wait(&bars->kv_empty[st], ((j / kStages) - 1) & 1, abort, &g_prefill_error))
+        if (j >= kStages && !mbar_wait_warp(&bars->kv_empty[st], ((j / kStages) - 1) & 1, abort,
+                                            &g_prefill_error))
           break;
         const int row = k0 + (kt_lo + j) * kBN;
-        mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-        tma_load_3d(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, kvh, row);
-        mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-        tma_load_3d(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, kvh, row);
+        mbar_arrive_expect_tx_elect(&bars->k_full[st], kTileBytes);
+        tma_load_3d_elect(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, kvh,
+                          row);
+        mbar_arrive_expect_tx_elect(&bars->v_full[st], kTileBytes);
+        tma_load_3d_elect(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, kvh,
+                          row);
         issued = j + 1;
       }
       if (*abort) {
         // Copies already issued still land in this CTA's shared memory: wait
         // for them (bounded) before the CTA may exit.
-        mbar_wait(&bars->q_full, 0, abort, &g_prefill_error, true);
+        mbar_wait_warp(&bars->q_full, 0, abort, &g_prefill_error, true);
         for (int j = max(0, issued - kStages); j < issued; ++j) {
-          mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, abort, &g_prefill_error, true);
-          mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, abort, &g_prefill_error, true);
+          mbar_wait_warp(&bars->k_full[j % kStages], (j / kStages) & 1, abort, &g_prefill_error,
+                         true);
+          mbar_wait_warp(&bars->v_full[j % kStages], (j / kStages) & 1, abort, &g_prefill_error,
+                         true);
         }
       }
-    }
-  } else if (warp == C::kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && n > 0) {
-      auto qk = [&](int t, int j) {
-        const uint64_t qdesc = sdesc_sw128(sbase + C::kOffQ + t * kTileBytes);
-        const uint64_t kdesc = sdesc_sw128(sbase + C::kOffK + (j % kStages) * kTileBytes);
+    } else if (warp == C::kMmaWarp && n > 0) {
+      // -------------------------------------------------------- MMA issuer
+      // Work items k = NT j + t (KV tile j, query tile t), in order. Item k's
+      // scores go to S buffer k % 3; QK(k + 3) may reuse that buffer once PV(k)
+      // (which reads P_k from it) has been issued, so QK runs up to two items
+      // ahead of the softmax. The whole warp runs the loop (uniform operands);
+      // one elected lane issues each MMA and commit.
+      const int items = NT * n;
+      const uint64_t qdesc0 = sdesc_sw128(sbase + C::kOffQ);
+      const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
+      const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV);
+      constexpr uint64_t kTileDesc = kTileBytes >> 4;  // one tile, in descriptor address units
+      bool ok = mbar_wait_warp(&bars->q_full, 0, abort, &g_prefill_error);
+      int next_qk = 0;
+      // issue QK for items below `limit`, waiting for each new K tile
+      auto issue_qk = [&](int limit) -> bool {
+        if (limit > items) limit = items;
+        for (; next_qk < limit; ++next_qk) {
+          const int t = next_qk % NT, jj = next_qk / NT;
+          if (t == 0) {
+            if (!mbar_wait_warp(&bars->k_full[jj % kStages], (jj / kStages) & 1, abort,
+                                &g_prefill_error))
+              return false;
+            tc_fence_after();
+          }
+          const uint64_t qd = qdesc0 + t * kTileDesc;
+          const uint64_t kd = kdesc0 + (jj % kStages) * kTileDesc;
+          const uint32_t sbuf = tmem + (next_qk % kSBufs) * kBN;
 #pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_ss(tmem + t * kBN, qdesc + ((ks * 32) >> 4), kdesc + ((ks * 32) >> 4), kIdescQK,
-                  ks > 0 ? 1u : 0u);
-        umma_commit(&bars->s_full[t]);
+          for (int ks = 0; ks < kHeadDim / 16; ++ks)
+            umma_ss_elect(sbuf, qd + 2 * ks, kd + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+          umma_commit_elect(&bars->s_full[next_qk % kSBufs]);
+        }
+        return true;
       };
-      auto pv = [&](int t, int j) {
-        const uint64_t vdesc = sdesc_sw128(sbase + C::kOffV + (j % kStages) * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + kTmemO + t * kHeadDim, tmem + t * kBN + kk * 8,
-                  vdesc + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->o_done[t]);
-      };
-      bool ok = mbar_wait(&bars->q_full, 0, abort, &g_prefill_error) &&
-                mbar_wait(&bars->k_full[0], 0, abort, &g_prefill_error);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < NT; ++t) qk(t, 0);
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait(&bars->v_full[st], (j / kStages) & 1, abort, &g_prefill_error)) {
+      if (ok) ok = issue_qk(kSBufs);
+      for (int k = 0; ok && k < items; ++k) {
+        const int t = k % NT, jj = k / NT;
+        if (t == 0 && !mbar_wait_warp(&bars->v_full[jj % kStages], (jj / kStages) & 1, abort,
+                                      &g_prefill_error)) {
           ok = false;
           break;
         }
-        const bool next = j + 1 < n;
-        for (int t = 0; t < NT; ++t) {
-          if (!mbar_wait(&bars->p_full[t], j & 1, abort, &g_prefill_error)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          pv(t, j);
-          if (next) {
-            if (t == 0 && !mbar_wait(&bars->k_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
-                                     abort, &g_prefill_error)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            qk(t, j + 1);
-          }
+        if (!mbar_wait_warp(&bars->p_full[k % kSBufs], (k / kSBufs) & 1, abort,
+                            &g_prefill_error)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        umma_commit(&bars->kv_empty[st]);
+        tc_fence_after();
+        const uint64_t vd = vdesc0 + (jj % kStages) * kTileDesc;
+        const uint32_t pbuf = tmem + (k % kSBufs) * kBN;
+        const uint32_t obuf = tmem + kTmemO + t * kHeadDim;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts_elect(obuf, pbuf + kk * 8, vd + kk * (16 * 128 / 16), kIdescPV,
+                        (jj > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_elect(&bars->o_done[t]);
+        if (t == NT - 1) umma_commit_elect(&bars->kv_empty[jj % kStages]);
+        ok = issue_qk(k + 1 + kSBufs);
       }
-      // every MMA issued by this thread has finished before TMEM is released
-      umma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, abort, &g_prefill_error, true);
+      // every MMA issued by this warp has finished before TMEM is released
+      umma_commit_elect(&bars->drain);
+      mbar_wait_warp(&bars->drain, 0, abort, &g_prefill_error, true);
     }
-  }
   } else {
     if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsSoftmax));
     // -------------------------------------------------------------- softmax
@@ -335,7 +346,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int r = threadIdx.x & 127;     // row within the tile == TMEM lane
     const int h = h0 + t;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t s_addr = lane_addr + t * kBN;
     const uint32_t o_addr = lane_addr + kTmemO + t * kHeadDim;
     const bool has_sink = p.sinks != nullptr;
     float m_run = has_sink ? p.sinks[h] * kLog2e : -INFINITY;
@@ -345,8 +355,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int pos = p_min + r;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
+      const int k = j * NT + t;  // work item: S buffer k % 3, its (k / 3)-th use
+      const uint32_t s_addr = lane_addr + (k % kSBufs) * kBN;
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort, &g_prefill_error))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[k % kSBufs], (k / kSBufs) & 1, abort,
+                                             &g_prefill_error))) {
         ok = false;
         break;
       }
@@ -438,7 +451,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
+      mbar_arrive(&bars->p_full[k % kSBufs]);
     }
 
     // ------------------------------------------------------------- epilogue
