@@ -21,8 +21,9 @@
 // tiles. Warps (NT = 2):
 //   warps 0-3, 4-7  softmax warpgroup t: thread r owns row r of tile t (TMEM lane r)
 //   warp 8          TMA producer: both Q tiles once, then K_j / V_j into a 3-stage ring
-//   warp 9          MMA issuer (one thread) and TMEM owner
-//   warps 10-11     idle; they complete the third warpgroup so that setmaxnreg
+//   warp 9          P V issuer and TMEM owner
+//   warp 10         Q K^T issuer
+//   warp 11         idle; it completes the third warpgroup so that setmaxnreg
 //                   can hand its registers to the softmax warpgroups (200 each)
 // TMEM (512 columns): three 128-column S buffers shared round-robin by the
 // work items k = NT j + t (KV tile j, query tile t) and O_t at [384 + 64 t, ...).
@@ -63,12 +64,13 @@ template <int NT>
 struct Cfg {
   // NT = 2: three full warpgroups, so setmaxnreg can move registers from the
   // producer/MMA warpgroup to the two softmax warpgroups.
-  static constexpr int kThreads = NT * 128 + (NT == 2 ? 128 : 64);
-  static constexpr int kLaunchRegs = NT == 2 ? 168 : 255;  // ptxas limit for kThreads
+  static constexpr int kThreads = NT * 128 + (NT == 2 ? 128 : 96);
+  static constexpr int kLaunchRegs = NT == 2 ? 168 : 224;  // ptxas limit for kThreads
   static constexpr int kRegsOther = 104;    // producer / MMA warpgroup after setmaxnreg
   static constexpr int kRegsSoftmax = 200;  // each softmax warpgroup after setmaxnreg
   static constexpr int kProducerWarp = NT * 4;
-  static constexpr int kMmaWarp = NT * 4 + 1;
+  static constexpr int kMmaWarp = NT * 4 + 1;    // P V issuer, TMEM owner
+  static constexpr int kQkWarp = NT * 4 + 2;     // Q K^T issuer
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + NT * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
@@ -102,7 +104,8 @@ struct Barriers {
   uint64_t s_full[kSBufs];
   uint64_t p_full[kSBufs];
   uint64_t o_done[2];
-  uint64_t drain;
+  uint64_t pv_done[kSBufs];  // P V of the item in this S buffer has completed
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -222,9 +225,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], kBM);
+      mbar_init(&bars->pv_done[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&bars->o_done[i], 1);
-    mbar_init(&bars->drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->o_done[i], 1);
+      mbar_init(&bars->drain[i], 1);
+    }
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -275,69 +281,75 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                          true);
         }
       }
-    } else if (warp == C::kMmaWarp && n > 0) {
-      // -------------------------------------------------------- MMA issuer
-      // Work items k = NT j + t (KV tile j, query tile t), in order. Item k's
-      // scores go to S buffer k % 3; QK(k + 3) may reuse that buffer once PV(k)
-      // (which reads P_k from it) has been issued, so QK runs up to two items
-      // ahead of the softmax. The whole warp runs the loop (uniform operands);
-      // one elected lane issues each MMA and commit.
+    } else if ((warp == C::kMmaWarp || warp == C::kQkWarp) && n > 0) {
+      // ------------------------------------------------------- MMA issuers
+      // Work items k = NT j + t (KV tile j, query tile t). Item k's scores go
+      // to S buffer k % 3. The Q K^T warp issues QK(k) once PV(k - 3) (which
+      // read P_{k-3} from that buffer) has completed; the P V warp issues PV(k)
+      // once the softmax has written P_k. With three buffers Q K^T runs up to
+      // two items ahead of the softmax, and either warp can feed the tensor
+      // core while the other waits. Each warp runs its loop whole (uniform
+      // operands); one elected lane issues each MMA and commit.
       const int items = NT * n;
-      const uint64_t qdesc0 = sdesc_sw128(sbase + C::kOffQ);
-      const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
-      const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV);
       constexpr uint64_t kTileDesc = kTileBytes >> 4;  // one tile, in descriptor address units
-      bool ok = mbar_wait_warp(&bars->q_full, 0, abort, &g_prefill_error);
-      int next_qk = 0;
-      // issue QK for items below `limit`, waiting for each new K tile
-      auto issue_qk = [&](int limit) -> bool {
-        if (limit > items) limit = items;
-        for (; next_qk < limit; ++next_qk) {
-          const int t = next_qk % NT, jj = next_qk / NT;
-          if (t == 0) {
-            if (!mbar_wait_warp(&bars->k_full[jj % kStages], (jj / kStages) & 1, abort,
-                                &g_prefill_error))
-              return false;
-            tc_fence_after();
+      bool ok = true;
+      const int role = warp == C::kMmaWarp ? 0 : 1;
+      if (role == 1) {
+        const uint64_t qdesc0 = sdesc_sw128(sbase + C::kOffQ);
+        const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
+        ok = mbar_wait_warp(&bars->q_full, 0, abort, &g_prefill_error);
+        for (int k = 0; ok && k < items; ++k) {
+          const int t = k % NT, jj = k / NT, b = k % kSBufs;
+          if (k >= kSBufs && !mbar_wait_warp(&bars->pv_done[b], ((k - kSBufs) / kSBufs) & 1, abort,
+                                             &g_prefill_error)) {
+            ok = false;
+            break;
           }
+          if (t == 0 && !mbar_wait_warp(&bars->k_full[jj % kStages], (jj / kStages) & 1, abort,
+                                        &g_prefill_error)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const uint64_t qd = qdesc0 + t * kTileDesc;
           const uint64_t kd = kdesc0 + (jj % kStages) * kTileDesc;
-          const uint32_t sbuf = tmem + (next_qk % kSBufs) * kBN;
+          const uint32_t sbuf = tmem + b * kBN;
 #pragma unroll
           for (int ks = 0; ks < kHeadDim / 16; ++ks)
             umma_ss_elect(sbuf, qd + 2 * ks, kd + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
-          umma_commit_elect(&bars->s_full[next_qk % kSBufs]);
+          umma_commit_elect(&bars->s_full[b]);
         }
-        return true;
-      };
-      if (ok) ok = issue_qk(kSBufs);
-      for (int k = 0; ok && k < items; ++k) {
-        const int t = k % NT, jj = k / NT;
-        if (t == 0 && !mbar_wait_warp(&bars->v_full[jj % kStages], (jj / kStages) & 1, abort,
-                                      &g_prefill_error)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait_warp(&bars->p_full[k % kSBufs], (k / kSBufs) & 1, abort,
-                            &g_prefill_error)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t vd = vdesc0 + (jj % kStages) * kTileDesc;
-        const uint32_t pbuf = tmem + (k % kSBufs) * kBN;
-        const uint32_t obuf = tmem + kTmemO + t * kHeadDim;
+      } else {
+        const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV);
+        for (int k = 0; ok && k < items; ++k) {
+          const int t = k % NT, jj = k / NT, b = k % kSBufs;
+          if (t == 0 && !mbar_wait_warp(&bars->v_full[jj % kStages], (jj / kStages) & 1, abort,
+                                        &g_prefill_error)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_warp(&bars->p_full[b], (k / kSBufs) & 1, abort, &g_prefill_error)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = vdesc0 + (jj % kStages) * kTileDesc;
+          const uint32_t pbuf = tmem + b * kBN;
+          const uint32_t obuf = tmem + kTmemO + t * kHeadDim;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts_elect(obuf, pbuf + kk * 8, vd + kk * (16 * 128 / 16), kIdescPV,
-                        (jj > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_elect(&bars->o_done[t]);
-        if (t == NT - 1) umma_commit_elect(&bars->kv_empty[jj % kStages]);
-        ok = issue_qk(k + 1 + kSBufs);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts_elect(obuf, pbuf + kk * 8, vd + kk * (16 * 128 / 16), kIdescPV,
+                          (jj > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_elect(&bars->o_done[t]);
+          umma_commit_elect(&bars->pv_done[b]);
+          // PV(k) completing implies QK of every item of tile j completed (it
+          // preceded P_k), so the K/V stage is free after the last item of j.
+          if (t == NT - 1) umma_commit_elect(&bars->kv_empty[jj % kStages]);
+        }
       }
       // every MMA issued by this warp has finished before TMEM is released
-      umma_commit_elect(&bars->drain);
-      mbar_wait_warp(&bars->drain, 0, abort, &g_prefill_error, true);
+      umma_commit_elect(&bars->drain[role]);
+      mbar_wait_warp(&bars->drain[role], 0, abort, &g_prefill_error, true);
     }
   } else {
     if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsSoftmax));
