@@ -101,7 +101,7 @@ size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int h
   if (batch <= 0 || hq <= 0 || hkv <= 0 || head_dim != kHeadDim || max_seqlen_k < 0 ||
       window < 0 || num_splits < 0)
     return 0;
-  const DecodePlan plan = plan_decode(max_seqlen_k, window, num_splits);
+  const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, window, num_splits);
   return decode_workspace_layout(batch, hq, hkv, plan).bytes;
 }
 
@@ -130,7 +130,7 @@ sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void
       (lse && !aligned(lse, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
-  const DecodePlan plan = plan_decode(max_seqlen_k, mask.window, num_splits);
+  const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
   if (plan.max_splits > 1) {
     const size_t need = decode_workspace_layout(batch, hq, hkv, plan).bytes;
     if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;

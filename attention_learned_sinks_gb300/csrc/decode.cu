@@ -54,6 +54,7 @@ struct Params {
   const __nv_bfloat16 *q, *k, *v;
   const int32_t *kv_indptr, *block_table, *seqlens_k;
   int max_pages, page_size;
+  int page_shift;  // log2(page_size) when it is a power of two, else -1
   int batch, hq, hkv, group, window, chunk;
   const float *sinks;
   float scale_log2;
@@ -63,12 +64,28 @@ struct Params {
   unsigned int *counters;
 };
 
+// Page ids of one block's token range are staged in shared memory once per
+// block (one coalesced read of the block table) so the per-row address needs
+// no dependent global load; ranges longer than this read the table directly.
+constexpr int kMaxBlockPages = 1024;
+
+__device__ __forceinline__ int page_index(const Params &p, int j) {
+  return p.page_shift >= 0 ? j >> p.page_shift : j / p.page_size;
+}
+__device__ __forceinline__ int page_slot(const Params &p, int j) {
+  return p.page_shift >= 0 ? j & (p.page_size - 1) : j % p.page_size;
+}
+
 // Element offset of row (token j, KV head g) of sequence b in the K/V cache.
+// Paged: pages[] holds the ids of pages pg0.. when `staged`.
 template <bool kPaged>
-__device__ __forceinline__ size_t kv_row(const Params &p, int b, int kv_base, int j, int g) {
+__device__ __forceinline__ size_t kv_row(const Params &p, int b, int kv_base, int j, int g,
+                                         const int *pages, int pg0, bool staged) {
   if (kPaged) {
-    const int page = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + j / p.page_size);
-    return ((static_cast<size_t>(page) * p.hkv + g) * p.page_size + (j % p.page_size)) * kHeadDim;
+    const int pi = page_index(p, j);
+    const int page = staged ? pages[pi - pg0]
+                            : __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pi);
+    return ((static_cast<size_t>(page) * p.hkv + g) * p.page_size + page_slot(p, j)) * kHeadDim;
   }
   return (static_cast<size_t>(kv_base + j) * p.hkv + g) * kHeadDim;
 }
@@ -107,6 +124,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
   const int t0 = lo + split * chunk;
   const int t1 = min(L, t0 + chunk);
   const int nslab = (max(0, t1 - t0) + kSlab - 1) / kSlab;
+
+  __shared__ int s_pages[kPaged ? kMaxBlockPages : 1];
+  int pg0 = 0;
+  bool staged = false;
+  if (kPaged) {
+    pg0 = page_index(p, t0);
+    const int npg = t1 > t0 ? page_index(p, t1 - 1) - pg0 + 1 : 0;
+    staged = npg <= kMaxBlockPages;
+    if (staged)
+      for (int i = threadIdx.x; i < npg; i += kThreads)
+        s_pages[i] = p.block_table[static_cast<size_t>(b) * p.max_pages + pg0 + i];
+    __syncthreads();
+  }
   const int my_slabs = warp < nslab ? (nslab - warp + kWarps - 1) / kWarps : 0;
 
   // Q^T as the B operand of S^T = K Q^T: lane (lr, lc) holds head lr,
@@ -151,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
       const int col = lane & 7;
       const int j = slab0 + row;
       const bool ok = j < t1;
-      const size_t off = ok ? kv_row<kPaged>(p, b, kv_base, j, g) + col * 8 : 0;
+      const size_t off = ok ? kv_row<kPaged>(p, b, kv_base, j, g, s_pages, pg0, staged) + col * 8 : 0;
       cp_async_16(kdst + swz(row, col), p.k + off, ok ? 16u : 0u);
       cp_async_16(vdst + swz(row, col), p.v + off, ok ? 16u : 0u);
     }
@@ -368,17 +398,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
 
 }  // namespace
 
-DecodePlan plan_decode(int max_seqlen_k, int window, int num_splits) {
+DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num_splits) {
   int span = window > 0 ? (window < max_seqlen_k ? window : max_seqlen_k) : max_seqlen_k;
   if (span < 1) span = 1;
   long chunk;
   if (num_splits > 0) {
     chunk = (span + num_splits - 1) / num_splits;
   } else {
-    // 512-token blocks keep a few thousand blocks in flight for typical
-    // batches; very long contexts grow the block so at most 64 splits exist.
-    chunk = 512;
-    const long cap = (span + 63) / 64;
+    // About three blocks per (sequence, KV head) for contexts spread up to
+    // `span` (mean taken as span / 2), and at least ~4 waves of two blocks per
+    // SM on a 152-SM GB300 for small batches. Measured on GB300: larger blocks
+    // cut the per-block prologue and merge traffic, and three per pair keep
+    // the waves balanced.
+    const long pairs = static_cast<long>(batch > 0 ? batch : 1) * (hkv > 0 ? hkv : 1);
+    const long est = span / 2 > 0 ? span / 2 : 1;
+    long blocks = 3 * pairs;
+    if (blocks < 4 * 2 * 152) blocks = 4 * 2 * 152;
+    chunk = (pairs * est + blocks - 1) / blocks;
+    const long cap = (span + 63) / 64;  // at most 64 splits
     if (chunk < cap) chunk = cap;
   }
   const long unit = kWarps * kSlab;
@@ -410,6 +447,11 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   p.seqlens_k = a.seqlens_k;
   p.max_pages = a.max_pages;
   p.page_size = a.page_size;
+  p.page_shift = -1;
+  if (a.page_size > 0 && (a.page_size & (a.page_size - 1)) == 0) {
+    p.page_shift = 0;
+    while ((1 << p.page_shift) < a.page_size) ++p.page_shift;
+  }
   p.batch = a.batch;
   p.hq = a.hq;
   p.hkv = a.hkv;
@@ -509,7 +551,7 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
       (sinks && !is_aligned(sinks, 4)) || (lse && !is_aligned(lse, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
-  const DecodePlan plan = plan_decode(max_seqlen_k, mask.window, num_splits);
+  const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
   // the plan's scratch must fit the fixed array
   if (plan.max_splits > 1 &&
       decode_workspace_layout(batch, hq, hkv, plan).bytes > SINKATTN_NOALLOC_SCRATCH_BYTES)

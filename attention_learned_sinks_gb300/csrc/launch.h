@@ -16,7 +16,7 @@ struct DecodePlan {
   int chunk;
   int max_splits;
 };
-DecodePlan plan_decode(int max_seqlen_k, int window, int num_splits);
+DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num_splits);
 // Workspace layout for a plan: [partial_o | partial_lse | counters].
 struct DecodeWorkspace {
   size_t off_lse, off_counters, bytes;

@@ -113,8 +113,9 @@ def test_merge_rejects_bad_arguments(lib):
 
 def test_workspace_sizes_follow_the_split_plan(lib):
     ws = lambda b, mk, w=0, ns=0: lib.sinkattn_decode_workspace_size(b, mk, 64, 8, 64, w, ns)
-    assert ws(64, 8192) >= 16 * 64 * 64 * 64 * 4          # up to 16 blocks of 512
-    assert ws(64, 8192, ns=2) < ws(64, 8192)
+    assert ws(64, 8192, ns=16) >= 16 * 64 * 64 * 64 * 4    # 16 blocks of 512
+    assert ws(64, 8192) > 0
+    assert ws(64, 8192, ns=2) < ws(64, 8192, ns=16)
     assert ws(64, 8192, w=128) < ws(64, 8192)               # window: one block
     assert lib.sinkattn_decode_workspace_size(0, 10, 8, 2, 64, 0, 0) == 0
     assert lib.sinkattn_prefill_workspace_size(1000, 8, 64) == 1000 * 8 * 64 * 2

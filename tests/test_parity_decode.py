@@ -76,7 +76,7 @@ def test_decode_large_sink_and_empty(oracle_lib):
 
 
 @pytest.mark.parametrize("window", [0, 16, 200])
-@pytest.mark.parametrize("page_size", [16, 32])
+@pytest.mark.parametrize("page_size", [16, 32, 24])
 def test_decode_paged_small(oracle_lib, window, page_size):
     c = S.make_decode("paged", LENS, 64, 8, seed=49 + window, window=window, paged=True,
                       page_size=page_size, sink_std=2.0)

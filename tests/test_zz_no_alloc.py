@@ -66,8 +66,8 @@ def test_noalloc_decode_matches_workspace_decode_twice():
 def test_noalloc_rejects_plans_beyond_its_scratch():
     lib = sa.load()
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the call is rejected first
-    need = lib.sinkattn_decode_workspace_size(256, 32768, 64, 8, 64, 0, 0)
+    need = lib.sinkattn_decode_workspace_size(256, 32768, 64, 8, 64, 0, 64)
     assert need > (32 << 20)
     st = lib.sinkattn_decode_noalloc(fake, fake, fake, fake, None, None, 1000, 0, 0, 256, 32768,
-                                     64, 8, 64, None, B.Mask(1, 0, 0.125), 0, fake, None, None)
+                                     64, 8, 64, None, B.Mask(1, 0, 0.125), 64, fake, None, None)
     assert st == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
