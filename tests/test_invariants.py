@@ -1,0 +1,118 @@
+"""GPU-only invariants of the sink-attention kernels (no oracle needed).
+
+- paged and contiguous decode of the same tokens are bitwise equal under the
+  same split plan (the layout changes addresses only);
+- permuting the pages (and the block table with them) changes nothing;
+- decode of a sequence's last token equals the last row of its prefill
+  (within the parity tolerance: different kernels, same definition);
+- the decode result does not depend on the number of KV splits (tolerance);
+- repeated calls are bitwise identical (no floating-point atomics).
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_learned_sinks_gb300 as sa
+from attention_learned_sinks_gb300 import synthetic as S
+from helpers import check_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+LENS = [700, 1, 2049, 333, 4096, 17]
+
+
+def _paged_from_contig(c, page_size, seed):
+    """The same tokens as a contiguous case, scattered over randomly ordered pages."""
+    g = torch.Generator().manual_seed(seed)
+    npages = [(l + page_size - 1) // page_size for l in c.seqlens_k]
+    total = sum(npages)
+    perm = torch.randperm(total, generator=g)
+    kc = torch.zeros((total, c.hkv, page_size, 64), dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    table = torch.zeros((c.batch, max(npages)), dtype=torch.int32)
+    at = 0
+    for b, L in enumerate(c.seqlens_k):
+        k0 = int(c.kv_indptr[b])
+        for i in range(npages[b]):
+            page = int(perm[at + i])
+            table[b, i] = page
+            lo, hi = i * page_size, min(L, (i + 1) * page_size)
+            kc[page, :, : hi - lo] = c.k[k0 + lo:k0 + hi].transpose(0, 1)
+            vc[page, :, : hi - lo] = c.v[k0 + lo:k0 + hi].transpose(0, 1)
+        at += npages[b]
+    return kc, vc, table
+
+
+def _decode_contig(c, ns=0, window=0):
+    return sa.sinkattn_decode(c.q.cuda(), c.k.cuda(), c.v.cuda(), kv_indptr=c.kv_indptr.cuda(),
+                              max_seqlen_k=c.max_seqlen_k, sinks=c.sinks.cuda(), window=window,
+                              num_splits=ns)
+
+
+@pytest.mark.parametrize("window", [0, 300])
+@pytest.mark.parametrize("ns", [0, 3])
+def test_paged_equals_contiguous_bitwise(ns, window):
+    c = S.make_decode("inv", LENS, 64, 8, seed=301)
+    out_c, lse_c = _decode_contig(c, ns, window)
+    kc, vc, table = _paged_from_contig(c, 16, seed=302)
+    out_p, lse_p = sa.sinkattn_decode(c.q.cuda(), kc.cuda(), vc.cuda(), block_table=table.cuda(),
+                                      seqlens_k=torch.tensor(LENS, dtype=torch.int32).cuda(),
+                                      max_seqlen_k=c.max_seqlen_k, sinks=c.sinks.cuda(),
+                                      window=window, num_splits=ns)
+    assert torch.equal(out_c, out_p)
+    assert torch.equal(lse_c, lse_p)
+
+
+def test_page_permutation_invariance():
+    c = S.make_decode("perm", LENS, 64, 8, seed=303)
+    kc, vc, table = _paged_from_contig(c, 16, seed=304)
+    kc2, vc2, table2 = _paged_from_contig(c, 16, seed=305)
+    assert not torch.equal(table, table2)
+    sl = torch.tensor(LENS, dtype=torch.int32).cuda()
+    a = sa.sinkattn_decode(c.q.cuda(), kc.cuda(), vc.cuda(), block_table=table.cuda(),
+                           seqlens_k=sl, max_seqlen_k=c.max_seqlen_k, sinks=c.sinks.cuda())
+    b = sa.sinkattn_decode(c.q.cuda(), kc2.cuda(), vc2.cuda(), block_table=table2.cuda(),
+                           seqlens_k=sl, max_seqlen_k=c.max_seqlen_k, sinks=c.sinks.cuda())
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_decode_equals_last_prefill_row(window):
+    lens = [130, 1000, 4097, 64]
+    p = S.make_prefill("pf", lens, lens, 64, 8, seed=306, window=window)
+    out_p, lse_p = sa.sinkattn_prefill(p.q.cuda(), p.k.cuda(), p.v.cuda(),
+                                       p.cu_seqlens_q.cuda(), p.cu_seqlens_k.cuda(),
+                                       p.max_seqlen_q, p.max_seqlen_k, sinks=p.sinks.cuda(),
+                                       causal=True, window=window)
+    last = (p.cu_seqlens_q[1:] - 1).long()
+    q_last = p.q[last].contiguous()
+    out_d, lse_d = sa.sinkattn_decode(q_last.cuda(), p.k.cuda(), p.v.cuda(),
+                                      kv_indptr=p.cu_seqlens_k.cuda(), max_seqlen_k=max(lens),
+                                      sinks=p.sinks.cuda(), window=window)
+    check_close(out_d, lse_d, to_np(out_p[last.cuda()]), to_np(lse_p[last.cuda()]),
+                "decode vs last prefill row w=%d" % window)
+
+
+def test_decode_independent_of_split_count():
+    c = S.make_decode("ns", LENS, 64, 8, seed=307)
+    ref_o, ref_l = _decode_contig(c, 1)
+    for ns in (2, 5, 17, 64):
+        o, l = _decode_contig(c, ns)
+        check_close(o, l, to_np(ref_o), to_np(ref_l), "splits %d vs 1" % ns)
+
+
+def test_repeated_calls_are_bitwise_identical():
+    c = S.make_decode("det", LENS, 64, 8, seed=308)
+    a = _decode_contig(c, 7)
+    b = _decode_contig(c, 7)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    p = S.make_prefill("detp", [300, 1200], [300, 1200], 64, 8, seed=309)
+    args = (p.q.cuda(), p.k.cuda(), p.v.cuda(), p.cu_seqlens_q.cuda(), p.cu_seqlens_k.cuda(),
+            p.max_seqlen_q, p.max_seqlen_k)
+    x = sa.sinkattn_prefill(*args, sinks=p.sinks.cuda())
+    y = sa.sinkattn_prefill(*args, sinks=p.sinks.cuda())
+    assert torch.equal(x[0], y[0]) and torch.equal(x[1], y[1])
+
+
+def test_no_device_error_after_the_suite():
+    assert sa.sinkattn_get_device_error() == 0
