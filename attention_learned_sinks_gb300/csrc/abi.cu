@@ -42,9 +42,10 @@ const char *sinkattn_status_string(sinkattn_status_t s) {
   return "unknown status";
 }
 
-size_t sinkattn_prefill_workspace_size(int64_t total_k, int hkv, int head_dim) {
-  if (total_k < 0 || hkv <= 0 || head_dim != kHeadDim) return 0;
-  return prefill_workspace_bytes(total_k, hkv);
+size_t sinkattn_prefill_workspace_size(int batch, int64_t total_q, int64_t total_k, int hkv,
+                                       int head_dim) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || hkv <= 0 || head_dim != kHeadDim) return 0;
+  return prefill_workspace_bytes(batch, total_q, total_k, hkv);
 }
 
 sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
@@ -66,10 +67,9 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
   if (batch > 65535 || total_q > INT32_MAX || total_k > INT32_MAX ||
       (max_seqlen_q + 127) / 128 > 65535)
     return SINKATTN_ERR_UNSUPPORTED;
-  const size_t need = prefill_workspace_bytes(total_k, hkv);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need))
-    return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
-  if (need > 0 && !aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
+  const size_t need = prefill_workspace_bytes(batch, total_q, total_k, hkv);
+  if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
   PrefillLaunch a;
   a.q = q;
   a.k = k;

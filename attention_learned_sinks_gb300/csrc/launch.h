@@ -54,9 +54,10 @@ struct PrefillLaunch {
   float scale;
   void *out;
   float *lse;
-  void *v_f16;  // workspace: fp16 copy of v, prefill_workspace_bytes(total_k, hkv)
+  void *v_f16;  // workspace (prefill_workspace_bytes): fp16 copy of v, tile counter, work list
 };
-size_t prefill_workspace_bytes(int64_t total_k, int hkv);
+size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hkv);
+size_t prefill_counter_offset(int64_t total_k, int hkv);
 // Returns cudaSuccess, or the failing CUDA error; *encode_failed is set when
 // the tensor-map encoding (driver entry point) failed.
 cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed);

@@ -71,11 +71,11 @@ struct Cfg {
   static constexpr int kProducerWarp = NT * 4;
   static constexpr int kMmaWarp = NT * 4 + 1;    // P V issuer, TMEM owner
   static constexpr int kQkWarp = NT * 4 + 2;     // Q K^T issuer
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + NT * kTileBytes;
+  static constexpr int kOffQ = 0;                                  // 2 buffers x NT tiles
+  static constexpr int kOffK = kOffQ + 2 * NT * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + control block + alignment slack
 };
 
 static_assert(Cfg<2>::kRegsOther * 128 + Cfg<2>::kRegsSoftmax * 256 <=
@@ -89,27 +89,39 @@ __device__ int g_prefill_error;
 
 struct Params {
   const int32_t *cu_q, *cu_k;
-  int hq, group, causal, window, max_qtiles;
+  int batch, hq, group, causal, window, max_qtiles;
   const float *sinks;
   float scale_log2;
   __nv_bfloat16 *out;
   float *lse;
+  unsigned int *work_counter;  // zeroed by build_worklist_kernel
+  const unsigned *work_pairs;  // longest-first (sequence, query tile) list, packed b << 16 | qt
+  const int *num_pairs;        // its length
+};
+
+// One unit of work: 128 query rows of sequence b for the NT heads h0...
+struct Tile {
+  int valid;  // 0: no more work
+  int h0, b, qt, q0, lq, k0, lk, rows, kvh, p_min, p_max, kt_lo, n;
 };
 
 struct Barriers {
-  uint64_t q_full;
+  uint64_t q_full[2], q_empty[2];       // double-buffered Q tiles
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[kSBufs];
   uint64_t p_full[kSBufs];
-  uint64_t o_done[2];
-  uint64_t pv_done[kSBufs];  // P V of the item in this S buffer has completed
+  uint64_t pv_done[kSBufs];             // P V of the item in this S buffer has completed
+  uint64_t o_done[2];                   // one phase per P V into O_t
+  uint64_t o_free[2];                   // one phase per tile: epilogue has read O_t
+  uint64_t tile_full[2], tile_empty[2]; // tile descriptor ring
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
+  Tile tiles[2];
 };
-static_assert(sizeof(Barriers) <= 256, "barrier block");
+static_assert(sizeof(Barriers) <= 1024, "control block");
 
 // 2^x for a pair, on the FMA pipe: x = n + f with n = round(x) (added to the
 // exponent field) and f in [-1/2, 1/2]; 2^f from a cubic fitted to minimise the
@@ -185,6 +197,130 @@ __device__ __forceinline__ void exp32(const float (&sv)[32], float2 c2, float2 n
   }
 }
 
+// Work index w -> tile: list entry w / groups gives (sequence, query tile),
+// w % groups the head group. n = 0 for a tile that sees no key.
+__device__ __forceinline__ void decode_work(const Params &p, int NT, int w, Tile &t) {
+  const int groups = p.hq / NT;
+  const unsigned e = p.work_pairs[w / groups];
+  const int b = static_cast<int>(e >> 16), qt = static_cast<int>(e & 0xffffu);
+  const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
+  t.valid = 1;
+  t.h0 = (w % groups) * NT;
+  t.b = b;
+  t.qt = qt;
+  t.q0 = q0;
+  t.lq = lq;
+  t.k0 = p.cu_k[b];
+  t.lk = p.cu_k[b + 1] - t.k0;
+  t.rows = min(kBM, lq - qt * kBM);
+  t.kvh = t.h0 / p.group;
+  t.p_min = t.lk - lq + qt * kBM;  // position of the tile's first query
+  t.p_max = t.p_min + t.rows - 1;
+  int key_hi = t.lk, key_lo = 0;
+  if (p.causal) key_hi = min(key_hi, t.p_max + 1);
+  if (p.window > 0) key_lo = max(0, t.p_min - p.window + 1);
+  t.kt_lo = key_lo / kBN;
+  t.n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - t.kt_lo : 0;
+}
+
+// One block: the list of non-empty (sequence b, query tile qt) pairs, ordered
+// by qt descending (the tiles with the most keys first under a causal mask),
+// and the zeroed work counter. Levels (one per qt) are counted with a
+// histogram of tiles per sequence, offset by a scan, then filled.
+constexpr int kMaxLevels = 4096;  // longer sequences: pairs in sequence order
+
+// Exclusive scan of one int per thread across a block of blockDim.x (a
+// multiple of 32, at most 1024) threads; returns this thread's prefix and the
+// block total.
+__device__ __forceinline__ int block_exclusive_scan(int x, int *total) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = blockDim.x >> 5;
+    int v = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_sums[lane] = v;  // inclusive prefix over warps
+  }
+  __syncthreads();
+  const int warp_off = wid > 0 ? warp_sums[wid - 1] : 0;
+  *total = warp_sums[(blockDim.x >> 5) - 1];
+  return warp_off + incl - x;
+}
+
+// One block: the list of non-empty (sequence b, query tile qt) pairs, ordered
+// by qt descending (the tiles with the most keys first under a causal mask),
+// and the zeroed work counter. Levels (one per qt) are counted, offset by a
+// block scan, then filled. Sequences longer than max_qtiles tiles are cut to
+// that bound (the host passes an upper bound on every length).
+__global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_q, int batch,
+                                                               int max_qtiles, unsigned *pairs,
+                                                               int *num_pairs,
+                                                               unsigned int *counter) {
+  __shared__ int level_start[kMaxLevels];
+  __shared__ int level_fill[kMaxLevels];
+  const int tid = threadIdx.x;
+  if (tid == 0) *counter = 0u;
+  if (max_qtiles <= kMaxLevels) {
+    // level z holds qt = max_qtiles - 1 - z; count tiles per level
+    for (int z = tid; z < max_qtiles; z += blockDim.x) {
+      level_start[z] = 0;
+      level_fill[z] = 0;
+    }
+    __syncthreads();
+    for (int b = tid; b < batch; b += blockDim.x) {
+      const int nq = min((cu_q[b + 1] - cu_q[b] + kBM - 1) / kBM, max_qtiles);
+      for (int qt = 0; qt < nq; ++qt) atomicAdd(&level_start[max_qtiles - 1 - qt], 1);
+    }
+    __syncthreads();
+    // exclusive scan over the levels: each thread owns a run of `per` levels
+    const int per = (max_qtiles + blockDim.x - 1) / blockDim.x;
+    const int z0 = min(tid * per, max_qtiles), z1 = min(z0 + per, max_qtiles);
+    int local = 0;
+    for (int z = z0; z < z1; ++z) local += level_start[z];
+    int total = 0;
+    int run = block_exclusive_scan(local, &total);
+    for (int z = z0; z < z1; ++z) {
+      const int c = level_start[z];
+      level_start[z] = run;
+      run += c;
+    }
+    if (tid == 0) *num_pairs = total;
+    __syncthreads();
+    for (int b = tid; b < batch; b += blockDim.x) {
+      const int nq = min((cu_q[b + 1] - cu_q[b] + kBM - 1) / kBM, max_qtiles);
+      for (int qt = 0; qt < nq; ++qt) {
+        const int z = max_qtiles - 1 - qt;
+        pairs[level_start[z] + atomicAdd(&level_fill[z], 1)] =
+            (static_cast<unsigned>(b) << 16) | static_cast<unsigned>(qt);
+      }
+    }
+  } else if (tid == 0) {
+    int run = 0;
+    for (int b = 0; b < batch; ++b) {
+      const int nq = min((cu_q[b + 1] - cu_q[b] + kBM - 1) / kBM, max_qtiles);
+      for (int qt = nq - 1; qt >= 0; --qt)
+        pairs[run++] = (static_cast<unsigned>(b) << 16) | static_cast<unsigned>(qt);
+    }
+    *num_pairs = run;
+  }
+}
+
+// Persistent: one CTA per SM takes tiles from a global counter until the list
+// is exhausted. Every role keeps running counters (S buffer items, K/V stages,
+// Q buffers, tiles) across tiles, so the next tile's loads and Q K^T overlap
+// the current tile's softmax and epilogue.
 template <int NT>
 __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -197,26 +333,17 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   Barriers *bars = reinterpret_cast<Barriers *>(smem + C::kOffBar);
   volatile int *abort = &bars->abort;
 
-  const int h0 = blockIdx.x * NT;  // first query head of this CTA
-  const int b = blockIdx.y;
-  const int qt = p.max_qtiles - 1 - static_cast<int>(blockIdx.z);  // longest work first
-  const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
-  const int k0 = p.cu_k[b], lk = p.cu_k[b + 1] - k0;
-  if (qt * kBM >= lq) return;  // CTA-uniform
-  const int rows = min(kBM, lq - qt * kBM);
-  const int kvh = h0 / p.group;
-  const int p_min = lk - lq + qt * kBM;  // position of this tile's first query
-  const int p_max = p_min + rows - 1;
-  int key_hi = lk;
-  if (p.causal) key_hi = min(key_hi, p_max + 1);
-  int key_lo = 0;
-  if (p.window > 0) key_lo = max(0, p_min - p.window + 1);
-  const int kt_lo = key_lo / kBN;
-  const int n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - kt_lo : 0;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->o_done[i], 1);
+      mbar_init(&bars->o_free[i], kBM);
+      mbar_init(&bars->tile_full[i], 1);
+      mbar_init(&bars->tile_empty[i], NT * kBM + 2);
+      mbar_init(&bars->drain[i], 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
@@ -226,10 +353,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], kBM);
       mbar_init(&bars->pv_done[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->o_done[i], 1);
-      mbar_init(&bars->drain[i], 1);
     }
     bars->abort = 0;
     fence_mbar_init();
@@ -245,107 +368,159 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 
   if (warp >= C::kProducerWarp) {
     if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsOther));
-    if (warp == C::kProducerWarp && n > 0) {
+    if (warp == C::kProducerWarp) {
       // ---------------------------------------------------------- producer
-      // The whole warp runs this loop; one elected lane issues each copy.
+      // Fetches tiles, publishes them in the 2-slot ring, and streams each
+      // tile's Q (double-buffered) and K/V tiles (3-stage ring). The whole warp
+      // runs the loop; lane 0 fetches and publishes, one elected lane issues
+      // each copy.
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx_elect(&bars->q_full, NT * kTileBytes);
-      for (int t = 0; t < NT; ++t)
-        tma_load_3d_elect(sbase + C::kOffQ + t * kTileBytes, &tm_q, &bars->q_full, 0, h0 + t,
-                          q0 + qt * kBM);
-      int issued = 0;
-      for (int j = 0; j < n; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait_warp(&bars->kv_empty[st], ((j / kStages) - 1) & 1, abort,
-                                            &g_prefill_error))
+      int J = 0;  // K/V stage uses so far
+      int q_loads = 0;
+      const int num_work = *p.num_pairs * (p.hq / NT);
+      for (int nt = 0;; ++nt) {
+        const int slot = nt & 1;
+        if (nt >= 2 && !mbar_wait_warp(&bars->tile_empty[slot], ((nt >> 1) - 1) & 1, abort,
+                                       &g_prefill_error))
           break;
-        const int row = k0 + (kt_lo + j) * kBN;
-        mbar_arrive_expect_tx_elect(&bars->k_full[st], kTileBytes);
-        tma_load_3d_elect(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, kvh,
-                          row);
-        mbar_arrive_expect_tx_elect(&bars->v_full[st], kTileBytes);
-        tma_load_3d_elect(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, kvh,
-                          row);
-        issued = j + 1;
+        if (lane == 0) {
+          Tile t;
+          t.valid = 0;
+          const int w = static_cast<int>(atomicAdd(p.work_counter, 1u));
+          if (w < num_work) decode_work(p, NT, w, t);
+          bars->tiles[slot] = t;
+          mbar_arrive(&bars->tile_full[slot]);
+        }
+        __syncwarp();
+        const Tile t = bars->tiles[slot];
+        if (!t.valid) break;
+        const int qb = nt & 1;
+        if (nt >= 2 && !mbar_wait_warp(&bars->q_empty[qb], ((nt >> 1) - 1) & 1, abort,
+                                       &g_prefill_error))
+          break;
+        mbar_arrive_expect_tx_elect(&bars->q_full[qb], NT * kTileBytes);
+        ++q_loads;
+        for (int i = 0; i < NT; ++i)
+          tma_load_3d_elect(sbase + C::kOffQ + (qb * NT + i) * kTileBytes, &tm_q, &bars->q_full[qb],
+                            0, t.h0 + i, t.q0 + t.qt * kBM);
+        bool ok = true;
+        for (int j = 0; j < t.n; ++j, ++J) {
+          const int st = J % kStages;
+          if (J >= kStages && !mbar_wait_warp(&bars->kv_empty[st], ((J / kStages) - 1) & 1, abort,
+                                              &g_prefill_error)) {
+            ok = false;
+            break;
+          }
+          const int row = t.k0 + (t.kt_lo + j) * kBN;
+          mbar_arrive_expect_tx_elect(&bars->k_full[st], kTileBytes);
+          tma_load_3d_elect(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, t.kvh,
+                            row);
+          mbar_arrive_expect_tx_elect(&bars->v_full[st], kTileBytes);
+          tma_load_3d_elect(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, t.kvh,
+                            row);
+        }
+        if (!ok) break;
       }
       if (*abort) {
         // Copies already issued still land in this CTA's shared memory: wait
-        // for them (bounded) before the CTA may exit.
-        mbar_wait_warp(&bars->q_full, 0, abort, &g_prefill_error, true);
-        for (int j = max(0, issued - kStages); j < issued; ++j) {
-          mbar_wait_warp(&bars->k_full[j % kStages], (j / kStages) & 1, abort, &g_prefill_error,
+        // for the last ones of each ring (bounded) before the CTA may exit.
+        for (int i = max(0, q_loads - 2); i < q_loads; ++i)
+          mbar_wait_warp(&bars->q_full[i & 1], (i >> 1) & 1, abort, &g_prefill_error, true);
+        for (int i = max(0, J - kStages); i < J; ++i) {
+          mbar_wait_warp(&bars->k_full[i % kStages], (i / kStages) & 1, abort, &g_prefill_error,
                          true);
-          mbar_wait_warp(&bars->v_full[j % kStages], (j / kStages) & 1, abort, &g_prefill_error,
+          mbar_wait_warp(&bars->v_full[i % kStages], (i / kStages) & 1, abort, &g_prefill_error,
                          true);
         }
       }
-    } else if ((warp == C::kMmaWarp || warp == C::kQkWarp) && n > 0) {
+    } else if (warp == C::kMmaWarp || warp == C::kQkWarp) {
       // ------------------------------------------------------- MMA issuers
-      // Work items k = NT j + t (KV tile j, query tile t). Item k's scores go
-      // to S buffer k % 3. The Q K^T warp issues QK(k) once PV(k - 3) (which
-      // read P_{k-3} from that buffer) has completed; the P V warp issues PV(k)
-      // once the softmax has written P_k. With three buffers Q K^T runs up to
-      // two items ahead of the softmax, and either warp can feed the tensor
-      // core while the other waits. Each warp runs its loop whole (uniform
+      // Work items k = NT j + t of a tile (KV tile j, query tile t), counted
+      // globally across tiles (K). Item K's scores go to S buffer K % 3. The
+      // Q K^T warp issues QK(K) once PV(K - 3) (which read P from that buffer)
+      // has completed; the P V warp issues PV(K) once the softmax has written
+      // P. With three buffers Q K^T runs up to two items ahead of the softmax,
+      // also across tile boundaries. Each warp runs its loop whole (uniform
       // operands); one elected lane issues each MMA and commit.
-      const int items = NT * n;
       constexpr uint64_t kTileDesc = kTileBytes >> 4;  // one tile, in descriptor address units
-      bool ok = true;
       const int role = warp == C::kMmaWarp ? 0 : 1;
-      if (role == 1) {
-        const uint64_t qdesc0 = sdesc_sw128(sbase + C::kOffQ);
-        const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
-        ok = mbar_wait_warp(&bars->q_full, 0, abort, &g_prefill_error);
-        for (int k = 0; ok && k < items; ++k) {
-          const int t = k % NT, jj = k / NT, b = k % kSBufs;
-          if (k >= kSBufs && !mbar_wait_warp(&bars->pv_done[b], ((k - kSBufs) / kSBufs) & 1, abort,
-                                             &g_prefill_error)) {
-            ok = false;
-            break;
-          }
-          if (t == 0 && !mbar_wait_warp(&bars->k_full[jj % kStages], (jj / kStages) & 1, abort,
-                                        &g_prefill_error)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t qd = qdesc0 + t * kTileDesc;
-          const uint64_t kd = kdesc0 + (jj % kStages) * kTileDesc;
-          const uint32_t sbuf = tmem + b * kBN;
+      const uint64_t qdesc0 = sdesc_sw128(sbase + C::kOffQ);
+      const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
+      const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV);
+      int K = 0, J = 0;
+      for (int nt = 0;; ++nt) {
+        const int slot = nt & 1;
+        if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, &g_prefill_error))
+          break;
+        const Tile t = bars->tiles[slot];
+        if (!t.valid) break;
+        const int items = NT * t.n;
+        bool ok = true;
+        if (role == 1) {
+          const int qb = nt & 1;
+          ok = mbar_wait_warp(&bars->q_full[qb], (nt >> 1) & 1, abort, &g_prefill_error);
+          for (int k = 0; ok && k < items; ++k) {
+            const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % kSBufs;
+            if (KK >= kSBufs && !mbar_wait_warp(&bars->pv_done[b], ((KK - kSBufs) / kSBufs) & 1,
+                                                abort, &g_prefill_error)) {
+              ok = false;
+              break;
+            }
+            const int Jc = J + jj;
+            if (tt == 0 && !mbar_wait_warp(&bars->k_full[Jc % kStages], (Jc / kStages) & 1, abort,
+                                           &g_prefill_error)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t qd = qdesc0 + (qb * NT + tt) * kTileDesc;
+            const uint64_t kd = kdesc0 + (Jc % kStages) * kTileDesc;
+            const uint32_t sbuf = tmem + b * kBN;
 #pragma unroll
-          for (int ks = 0; ks < kHeadDim / 16; ++ks)
-            umma_ss_elect(sbuf, qd + 2 * ks, kd + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
-          umma_commit_elect(&bars->s_full[b]);
-        }
-      } else {
-        const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV);
-        for (int k = 0; ok && k < items; ++k) {
-          const int t = k % NT, jj = k / NT, b = k % kSBufs;
-          if (t == 0 && !mbar_wait_warp(&bars->v_full[jj % kStages], (jj / kStages) & 1, abort,
-                                        &g_prefill_error)) {
-            ok = false;
-            break;
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+              umma_ss_elect(sbuf, qd + 2 * ks, kd + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+            umma_commit_elect(&bars->s_full[b]);
           }
-          if (!mbar_wait_warp(&bars->p_full[b], (k / kSBufs) & 1, abort, &g_prefill_error)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t vd = vdesc0 + (jj % kStages) * kTileDesc;
-          const uint32_t pbuf = tmem + b * kBN;
-          const uint32_t obuf = tmem + kTmemO + t * kHeadDim;
+          if (ok) umma_commit_elect(&bars->q_empty[qb]);  // Q buffer free once these QK finish
+        } else {
+          // O_t of the previous tile must have been read by its epilogue
+          for (int tt = 0; ok && tt < NT; ++tt)
+            if (nt > 0 && !mbar_wait_warp(&bars->o_free[tt], (nt - 1) & 1, abort,
+                                          &g_prefill_error))
+              ok = false;
+          for (int k = 0; ok && k < items; ++k) {
+            const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % kSBufs, Jc = J + jj;
+            if (tt == 0 && !mbar_wait_warp(&bars->v_full[Jc % kStages], (Jc / kStages) & 1, abort,
+                                           &g_prefill_error)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait_warp(&bars->p_full[b], (KK / kSBufs) & 1, abort, &g_prefill_error)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vd = vdesc0 + (Jc % kStages) * kTileDesc;
+            const uint32_t pbuf = tmem + b * kBN;
+            const uint32_t obuf = tmem + kTmemO + tt * kHeadDim;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts_elect(obuf, pbuf + kk * 8, vd + kk * (16 * 128 / 16), kIdescPV,
-                          (jj > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_elect(&bars->o_done[t]);
-          umma_commit_elect(&bars->pv_done[b]);
-          // PV(k) completing implies QK of every item of tile j completed (it
-          // preceded P_k), so the K/V stage is free after the last item of j.
-          if (t == NT - 1) umma_commit_elect(&bars->kv_empty[jj % kStages]);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_ts_elect(obuf, pbuf + kk * 8, vd + kk * (16 * 128 / 16), kIdescPV,
+                            (jj > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elect(&bars->o_done[tt]);
+            umma_commit_elect(&bars->pv_done[b]);
+            // PV(K) completing implies QK of every item of this KV tile
+            // completed (it preceded P), so the K/V stage is free after the
+            // tile's last item.
+            if (tt == NT - 1) umma_commit_elect(&bars->kv_empty[Jc % kStages]);
+          }
         }
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
+        K += items;
+        J += t.n;
       }
       // every MMA issued by this warp has finished before TMEM is released
       umma_commit_elect(&bars->drain[role]);
@@ -354,151 +529,171 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   } else {
     if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsSoftmax));
     // -------------------------------------------------------------- softmax
-    const int t = warp >> 2;             // which query tile (head h0 + t)
-    const int r = threadIdx.x & 127;     // row within the tile == TMEM lane
-    const int h = h0 + t;
+    const int t = warp >> 2;          // which query tile (head h0 + t)
+    const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t o_addr = lane_addr + kTmemO + t * kHeadDim;
-    const bool has_sink = p.sinks != nullptr;
-    float m_run = has_sink ? p.sinks[h] * kLog2e : -INFINITY;
-    float d_run = has_sink ? 1.f : 0.f;
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
-    const int pos = p_min + r;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int k = j * NT + t;  // work item: S buffer k % 3, its (k / 3)-th use
-      const uint32_t s_addr = lane_addr + (k % kSBufs) * kBN;
-      // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[k % kSBufs], (k / kSBufs) & 1, abort,
-                                             &g_prefill_error))) {
-        ok = false;
+    int K = 0;        // items of earlier tiles
+    int o_waits = 0;  // o_done[t] phases consumed
+    for (int nt = 0;; ++nt) {
+      const int slot = nt & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->tile_full[slot], (nt >> 1) & 1, abort,
+                                             &g_prefill_error)))
         break;
-      }
-      tc_fence_after();
-      const int key0 = (kt_lo + j) * kBN;
-      const bool need_mask = (key0 + kBN > lk) || (p.causal && key0 + kBN - 1 > p_min) ||
-                             (p.window > 0 && key0 <= p_max - p.window);
-      float s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32f(s_addr, s0);
-      tmem_ld32f(s_addr + 32, s1);
-      tmem_ld32f(s_addr + 64, s2);
-      tmem_ld32f(s_addr + 96, s3);
-      tmem_wait_ld();
-      if (need_mask) {
-        // this row's visible keys form one range [lo, hi): sequence end, causal
-        // bound and window; as tile columns [c_lo, c_lo + len)
-        int hi = lk, lo = 0;
-        if (p.causal) hi = min(hi, pos + 1);
-        if (p.window > 0) lo = max(lo, pos - p.window + 1);
-        const int c_lo = min(max(lo - key0, 0), kBN);
-        const int len = max(min(hi - key0, kBN) - c_lo, 0);
-        mask32(s0, 0, c_lo, len);
-        mask32(s1, 32, c_lo, len);
-        mask32(s2, 64, c_lo, len);
-        mask32(s3, 96, c_lo, len);
-      }
-      const float mx = max3(fmaxf(row_max32(s0), row_max32(s1)), row_max32(s2), row_max32(s3));
-      const float m_tile = mx * c;
-      const float m_new = fmaxf(m_run, m_tile);
-      float alpha = 1.f;
-      bool rescale = false;
-      if (m_new > m_run + kRescaleThreshold) {
-        alpha = fast_exp2(m_run - m_new);
-        d_run *= alpha;
-        m_run = m_new;
-        rescale = true;
-      }
-      const float base = m_run == -INFINITY ? 0.f : m_run;
-      const float2 nb2 = make_float2(-base, -base);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-      // Pass 2: re-read each half, exponentiate, and store it as 32 columns of
-      // fp16 pairs over the half's first columns (already consumed).
-      {
-        uint32_t pk[32];
-        if (need_mask) {
-          exp32<true>(s0, c2, nb2, acc, pk, 0);
-          exp32<true>(s1, c2, nb2, acc, pk, 16);
-        } else {
-          exp32<false>(s0, c2, nb2, acc, pk, 0);
-          exp32<false>(s1, c2, nb2, acc, pk, 16);
-        }
-        tmem_st32(s_addr, pk);
-        if (need_mask) {
-          exp32<true>(s2, c2, nb2, acc, pk, 0);
-          exp32<true>(s3, c2, nb2, acc, pk, 16);
-        } else {
-          exp32<false>(s2, c2, nb2, acc, pk, 0);
-          exp32<false>(s3, c2, nb2, acc, pk, 16);
-        }
-        tmem_st32(s_addr + 32, pk);
-      }
-      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
-      const float2 a03 = __fadd2_rn(a01, a23);
-      d_run += a03.x + a03.y;
-      tmem_wait_st();
-      if (j > 0) {
-        // O_t holds P_0..P_{j-1} V; it must be complete before it is rescaled,
-        // and waiting for every phase in order keeps the parity unambiguous.
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort,
-                                               &g_prefill_error))) {
+      const Tile ti = bars->tiles[slot];
+      if (!ti.valid) break;
+      const int h = ti.h0 + t;
+      const bool has_sink = p.sinks != nullptr;
+      float m_run = has_sink ? p.sinks[h] * kLog2e : -INFINITY;
+      float d_run = has_sink ? 1.f : 0.f;
+      const int pos = ti.p_min + r;
+      const int n = ti.n;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int k = K + j * NT + t;  // work item: S buffer k % 3, its (k / 3)-th use
+        const uint32_t s_addr = lane_addr + (k % kSBufs) * kBN;
+        // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[k % kSBufs], (k / kSBufs) & 1,
+                                               abort, &g_prefill_error))) {
           ok = false;
           break;
         }
-        // one lane's rescale makes the whole warp run the (collective) O round
-        // trip; lanes that did not move their maximum multiply by alpha = 1
-        if (__any_sync(0xffffffffu, rescale)) {
-          tc_fence_after();
-#pragma unroll
-          for (int q = 0; q < kHeadDim / 32; ++q) {
-            uint32_t ov[32];
-            tmem_ld32(o_addr + q * 32, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(o_addr + q * 32, ov);
-          }
-          tmem_wait_st();
+        tc_fence_after();
+        const int key0 = (ti.kt_lo + j) * kBN;
+        const bool need_mask = (key0 + kBN > ti.lk) || (p.causal && key0 + kBN - 1 > ti.p_min) ||
+                               (p.window > 0 && key0 <= ti.p_max - p.window);
+        float s0[32], s1[32], s2[32], s3[32];
+        tmem_ld32f(s_addr, s0);
+        tmem_ld32f(s_addr + 32, s1);
+        tmem_ld32f(s_addr + 64, s2);
+        tmem_ld32f(s_addr + 96, s3);
+        tmem_wait_ld();
+        if (need_mask) {
+          // this row's visible keys form one range [lo, hi): sequence end, causal
+          // bound and window; as tile columns [c_lo, c_lo + len)
+          int hi = ti.lk, lo = 0;
+          if (p.causal) hi = min(hi, pos + 1);
+          if (p.window > 0) lo = max(lo, pos - p.window + 1);
+          const int c_lo = min(max(lo - key0, 0), kBN);
+          const int len = max(min(hi - key0, kBN) - c_lo, 0);
+          mask32(s0, 0, c_lo, len);
+          mask32(s1, 32, c_lo, len);
+          mask32(s2, 64, c_lo, len);
+          mask32(s3, 96, c_lo, len);
         }
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[k % kSBufs]);
-    }
-
-    // ------------------------------------------------------------- epilogue
-    const bool have_o = __all_sync(0xffffffffu, ok && n > 0 &&
-                                                   mbar_wait(&bars->o_done[t], (n - 1) & 1,
-                                                             abort, &g_prefill_error));
-    const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
-    const size_t row_h = static_cast<size_t>(q0 + qt * kBM + r) * p.hq + h;
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out + row_h * kHeadDim);
-    if (have_o) tc_fence_after();
+        const float mx = max3(fmaxf(row_max32(s0), row_max32(s1)), row_max32(s2), row_max32(s3));
+        const float m_tile = mx * c;
+        const float m_new = fmaxf(m_run, m_tile);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_new > m_run + kRescaleThreshold) {
+          alpha = fast_exp2(m_run - m_new);
+          d_run *= alpha;
+          m_run = m_new;
+          rescale = true;
+        }
+        const float base = m_run == -INFINITY ? 0.f : m_run;
+        const float2 nb2 = make_float2(-base, -base);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        {
+          uint32_t pk[32];
+          if (need_mask) {
+            exp32<true>(s0, c2, nb2, acc, pk, 0);
+            exp32<true>(s1, c2, nb2, acc, pk, 16);
+          } else {
+            exp32<false>(s0, c2, nb2, acc, pk, 0);
+            exp32<false>(s1, c2, nb2, acc, pk, 16);
+          }
+          tmem_st32(s_addr, pk);
+          if (need_mask) {
+            exp32<true>(s2, c2, nb2, acc, pk, 0);
+            exp32<true>(s3, c2, nb2, acc, pk, 16);
+          } else {
+            exp32<false>(s2, c2, nb2, acc, pk, 0);
+            exp32<false>(s3, c2, nb2, acc, pk, 16);
+          }
+          tmem_st32(s_addr + 32, pk);
+        }
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a03 = __fadd2_rn(a01, a23);
+        d_run += a03.x + a03.y;
+        tmem_wait_st();
+        if (j > 0) {
+          // O_t holds P_0..P_{j-1} V; it must be complete before it is rescaled,
+          // and waiting for every phase in order keeps the parity unambiguous.
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], o_waits & 1, abort,
+                                                 &g_prefill_error))) {
+            ok = false;
+            break;
+          }
+          ++o_waits;
+          // one lane's rescale makes the whole warp run the (collective) O round
+          // trip; lanes that did not move their maximum multiply by alpha = 1
+          if (__any_sync(0xffffffffu, rescale)) {
+            tc_fence_after();
 #pragma unroll
-    for (int q = 0; q < kHeadDim / 32; ++q) {
-      uint32_t ov[32];
+            for (int q = 0; q < kHeadDim / 32; ++q) {
+              uint32_t ov[32];
+              tmem_ld32(o_addr + q * 32, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(o_addr + q * 32, ov);
+            }
+            tmem_wait_st();
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[k % kSBufs]);
+      }
+      if (!ok) break;
+
+      // ----------------------------------------------------------- epilogue
+      bool have_o = false;
+      if (n > 0) {
+        have_o = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], o_waits & 1, abort,
+                                                   &g_prefill_error));
+        ++o_waits;
+        if (!have_o) break;
+      }
+      const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
+      const size_t row_h = static_cast<size_t>(ti.q0 + ti.qt * kBM + r) * p.hq + h;
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + row_h * kHeadDim);
+      uint32_t ov[2][32];
       if (have_o) {
-        tmem_ld32(o_addr + q * 32, ov);
+        tc_fence_after();
+        tmem_ld32(o_addr, ov[0]);
+        tmem_ld32(o_addr + 32, ov[1]);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        for (int i = 0; i < 32; ++i) ov[0][i] = ov[1][i] = 0u;
       }
-      if (r < rows) {
+      // O_t may now be overwritten by the next tile's first P V
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+      if (r < ti.rows) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float *o = reinterpret_cast<const float *>(&ov[8 * i]);
-          uint4 v;
-          v.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-          v.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-          v.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-          v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-          dst[q * 4 + i] = v;
-        }
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float *o = reinterpret_cast<const float *>(&ov[q][8 * i]);
+            uint4 v;
+            v.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+            v.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+            v.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+            v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+            dst[q * 4 + i] = v;
+          }
+        if (p.lse != nullptr)
+          p.lse[row_h] = d_run > 0.f ? (m_run + fast_log2(d_run)) * kLn2 : -INFINITY;
       }
+      mbar_arrive(&bars->tile_empty[slot]);
+      K += NT * n;
     }
-    if (r < rows && p.lse != nullptr)
-      p.lse[row_h] = d_run > 0.f ? (m_run + fast_log2(d_run)) * kLn2 : -INFINITY;
   }
 
   tc_fence_before();
@@ -562,9 +757,15 @@ bool encode_rows_heads(EncodeTiledFn fn, CUtensorMap *map, const void *base, int
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int64_t total_k, int hkv) {
+// Workspace: fp16 copy of V, then the tile counter of the persistent grid.
+size_t prefill_counter_offset(int64_t total_k, int hkv) {
   const size_t bytes = static_cast<size_t>(total_k) * hkv * kHeadDim * 2;
   return (bytes + 255) / 256 * 256;
+}
+
+size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hkv) {
+  const size_t pairs = static_cast<size_t>(total_q / kBM + batch) * 4;
+  return prefill_counter_offset(total_k, hkv) + 256 + (pairs + 255) / 256 * 256;
 }
 
 cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed) {
@@ -592,6 +793,7 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
   Params p;
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
+  p.batch = a.batch;
   p.hq = a.hq;
   p.group = a.hq / a.hkv;
   p.causal = a.causal ? 1 : 0;
@@ -601,8 +803,30 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
   p.scale_log2 = a.scale * kLog2e;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.lse = a.lse;
-  cudaError_t e;
-  if (p.group % 2 == 0) {
+  uint8_t *ws = static_cast<uint8_t *>(a.v_f16);
+  const size_t off = prefill_counter_offset(a.total_k, a.hkv);
+  p.work_counter = reinterpret_cast<unsigned int *>(ws + off);
+  int *num_pairs = reinterpret_cast<int *>(ws + off + 4);
+  unsigned *pairs = reinterpret_cast<unsigned *>(ws + off + 256);
+  p.work_pairs = pairs;
+  p.num_pairs = num_pairs;
+  const int nt = p.group % 2 == 0 ? 2 : 1;
+  build_worklist_kernel<<<1, 1024, 0, stream>>>(a.cu_q, a.batch, max_qtiles, pairs, num_pairs,
+                                                p.work_counter);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // upper bound on the number of work items, for the grid size
+  const int64_t max_pairs = a.total_q / kBM + a.batch;
+  const int64_t max_work = max_pairs * (a.hq / nt);
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
+  const unsigned grid = static_cast<unsigned>(max_work < num_sms ? max_work : num_sms);
+  if (nt == 2) {
     e = cudaFuncSetAttribute(prefill_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<2>::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -617,13 +841,11 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
     }
     if (launch_regs * Cfg<2>::kThreads < Cfg<2>::kRegsOther * 128 + Cfg<2>::kRegsSoftmax * 256)
       return cudaErrorNotSupported;
-    dim3 grid(a.hq / 2, a.batch, max_qtiles);
     prefill_kernel<2><<<grid, Cfg<2>::kThreads, Cfg<2>::kSmemBytes, stream>>>(tq, tk, tv, p);
   } else {
     e = cudaFuncSetAttribute(prefill_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<1>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.hq, a.batch, max_qtiles);
     prefill_kernel<1><<<grid, Cfg<1>::kThreads, Cfg<1>::kSmemBytes, stream>>>(tq, tk, tv, p);
   }
   return cudaGetLastError();

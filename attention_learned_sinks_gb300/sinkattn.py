@@ -57,7 +57,7 @@ def load(path: str = LIB_PATH):
     P, I, L, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.sinkattn_status_string.argtypes = [I]
     lib.sinkattn_status_string.restype = ctypes.c_char_p
-    lib.sinkattn_prefill_workspace_size.argtypes = [L, I, I]
+    lib.sinkattn_prefill_workspace_size.argtypes = [I, L, L, I, I]
     lib.sinkattn_prefill_workspace_size.restype = S
     lib.sinkattn_prefill.argtypes = [P, P, P, P, P, I, L, L, I, I, I, I, I, P, Mask,
                                      P, P, P, S, P]
@@ -105,8 +105,9 @@ def _req(t, dtype, name):
         raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
 
 
-def sinkattn_prefill_workspace_size(total_k, hkv, head_dim=64):
-    return load().sinkattn_prefill_workspace_size(int(total_k), hkv, head_dim)
+def sinkattn_prefill_workspace_size(batch, total_q, total_k, hkv, head_dim=64):
+    return load().sinkattn_prefill_workspace_size(int(batch), int(total_q), int(total_k), hkv,
+                                                  head_dim)
 
 
 def sinkattn_decode_workspace_size(batch, max_seqlen_k, hq, hkv, head_dim=64, window=0,
@@ -136,7 +137,8 @@ def sinkattn_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
         _req(sinks, torch.float32, "sinks")
     tk_ = tk if total_k is None else total_k
     if workspace is None:
-        need = lib.sinkattn_prefill_workspace_size(tk_, hkv, d)
+        need = lib.sinkattn_prefill_workspace_size(cu_seqlens_q.numel() - 1,
+                                                   tq if total_q is None else total_q, tk_, hkv, d)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     mask = Mask(1 if causal else 0, int(window), float(d ** -0.5 if scale is None else scale))
     st = lib.sinkattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),

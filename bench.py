@@ -438,8 +438,8 @@ def extras(sa, S, dev, stream, pk, pk_kind):
         sk = c.sinks.to(dev)
         out = torch.empty_like(c.q)
         lse = torch.empty((c.q.shape[0], c.hq), dtype=torch.float32, device=dev)
-        ws = torch.empty(sa.sinkattn_prefill_workspace_size(c.k.shape[0], c.hkv), dtype=torch.uint8,
-                         device=dev)
+        ws = torch.empty(sa.sinkattn_prefill_workspace_size(c.batch, c.q.shape[0], c.k.shape[0],
+                                                            c.hkv), dtype=torch.uint8, device=dev)
 
         def call():
             sa.sinkattn_prefill(c.q, c.k, c.v, cq, ck, c.max_seqlen_q, c.max_seqlen_k, sinks=sk,

@@ -86,13 +86,16 @@ const char *sinkattn_status_string(sinkattn_status_t status);
  *   sinks    float32 [hq] or NULL.
  *   out      bf16 [total_q, hq, 64];   lse  float32 [total_q, hq] or NULL.
  *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
- *            sinkattn_prefill_workspace_size(total_k, hkv, head_dim) bytes.
- *            It receives an fp16 copy of v for the P.V product (values of
- *            magnitude above 65504 are clamped to +-65504 there).
+ *            sinkattn_prefill_workspace_size(batch, total_q, total_k, hkv,
+ *            head_dim) bytes; contents need not be initialised. It receives
+ *            an fp16 copy of v for the P.V product (values of magnitude above
+ *            65504 are clamped to +-65504 there) and the list of query tiles
+ *            that the persistent kernel works through, longest first.
  * A sequence with Lq_b > Lk_b is allowed: its first Lq_b - Lk_b queries see no
  * key under a causal mask.
  */
-size_t sinkattn_prefill_workspace_size(int64_t total_k, int hkv, int head_dim);
+size_t sinkattn_prefill_workspace_size(int batch, int64_t total_q, int64_t total_k, int hkv,
+                                       int head_dim);
 
 sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
                                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,

@@ -73,7 +73,7 @@ def test_prefill_rejects_bad_arguments(lib):
     assert prefill(lib, q=None) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill(lib, out=ctypes.c_void_p((1 << 20) + 2)) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill(lib, batch=-1) == B.SINKATTN_ERR_INVALID_ARGUMENT
-    need = lib.sinkattn_prefill_workspace_size(10, 2, 64)
+    need = lib.sinkattn_prefill_workspace_size(2, 10, 10, 2, 64)
     assert need >= 10 * 2 * 64 * 2
     assert prefill(lib) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
     assert prefill(lib, ws=FAKE, wsb=need - 1) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
@@ -118,8 +118,8 @@ def test_workspace_sizes_follow_the_split_plan(lib):
     assert ws(64, 8192, ns=2) < ws(64, 8192, ns=16)
     assert ws(64, 8192, w=128) < ws(64, 8192)               # window: one block
     assert lib.sinkattn_decode_workspace_size(0, 10, 8, 2, 64, 0, 0) == 0
-    assert lib.sinkattn_prefill_workspace_size(1000, 8, 64) == 1000 * 8 * 64 * 2
-    assert lib.sinkattn_prefill_workspace_size(1000, 8, 128) == 0
+    assert lib.sinkattn_prefill_workspace_size(3, 1000, 1000, 8, 64) >= 1000 * 8 * 64 * 2 + 256
+    assert lib.sinkattn_prefill_workspace_size(3, 1000, 1000, 8, 128) == 0
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
