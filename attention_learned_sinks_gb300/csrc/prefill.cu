@@ -33,9 +33,8 @@
 // warpgroup rarely waits for its next scores, and the two warpgroups' softmax
 // phases overlap the tensor core's P V and Q K^T work.
 // Softmax: one read of the 128 scores of a row from TMEM, a range mask on
-// boundary tiles only, tree reductions (3-input max), packed f32x2 arithmetic, and one
-// exponential in four evaluated on the FMA pipe by a cubic (exp2_poly2) so the
-// special-function unit is not the only exp pipe. The running maximum is only
+// boundary tiles only, tree reductions (3-input max), packed f32x2 arithmetic
+// and hardware ex2. The running maximum is only
 // moved (and O, d rescaled) when it grows by more than 8 in log2 units; the
 // final division uses the same reference maximum, so the result is unchanged
 // while most tiles skip the O round trip.
@@ -123,28 +122,6 @@ struct Barriers {
 };
 static_assert(sizeof(Barriers) <= 1024, "control block");
 
-// 2^x for a pair, on the FMA pipe: x = n + f with n = round(x) (added to the
-// exponent field) and f in [-1/2, 1/2]; 2^f from a cubic fitted to minimise the
-// maximum relative error on that interval (Remez exchange, 7.5e-5). Inputs are
-// clamped at -126, so very negative arguments give about 1e-38 rather than 0:
-// callers use it only where some element of the row is at least 2^-8.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  const float2 magic = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -126.f);
-  x.y = fmaxf(x.y, -126.f);
-  const float2 t = __fadd2_rn(x, magic);  // round(x) sits in the low significand bits
-  const float2 n = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
-  const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
-  float2 p = __ffma2_rn(f, make_float2(0.0551716685f, 0.0551716685f),
-                        make_float2(0.2426111251f, 0.2426111251f));
-  p = __ffma2_rn(p, f, make_float2(0.6932609677f, 0.6932609677f));
-  p = __ffma2_rn(p, f, make_float2(0.9999280572f, 0.9999280572f));
-  float2 r;
-  r.x = __uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23));
-  r.y = __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23));
-  return r;
-}
-
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -184,14 +161,15 @@ __device__ __forceinline__ float row_max32(const float (&sv)[32]) {
 }
 
 // 32 scores -> 2^(x c - m) as 16 fp16 pairs into pk[off..off+16); row sums into acc.
-template <bool kMasked>
+// Exponentials on the special-function unit (ex2(-inf) = 0 for masked keys).
+// Measured on GB300: moving a share of them to an FMA-pipe polynomial made
+// this kernel slower (the softmax is bound by ALU/FMA issue, not by ex2).
 __device__ __forceinline__ void exp32(const float (&sv)[32], float2 c2, float2 nb2,
                                       float2 (&acc)[4], uint32_t (&pk)[32], int off) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float2 a = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), c2, nb2);
-    const float2 e = (!kMasked && (i & 3) == 3) ? exp2_poly2(a)
-                                                 : make_float2(fast_exp2(a.x), fast_exp2(a.y));
+    const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
     acc[i & 3] = __fadd2_rn(acc[i & 3], e);
     pk[off + i] = pack_f16x2(e.x, e.y);
   }
@@ -600,21 +578,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                          make_float2(0.f, 0.f)};
         {
           uint32_t pk[32];
-          if (need_mask) {
-            exp32<true>(s0, c2, nb2, acc, pk, 0);
-            exp32<true>(s1, c2, nb2, acc, pk, 16);
-          } else {
-            exp32<false>(s0, c2, nb2, acc, pk, 0);
-            exp32<false>(s1, c2, nb2, acc, pk, 16);
-          }
+          exp32(s0, c2, nb2, acc, pk, 0);
+          exp32(s1, c2, nb2, acc, pk, 16);
           tmem_st32(s_addr, pk);
-          if (need_mask) {
-            exp32<true>(s2, c2, nb2, acc, pk, 0);
-            exp32<true>(s3, c2, nb2, acc, pk, 16);
-          } else {
-            exp32<false>(s2, c2, nb2, acc, pk, 0);
-            exp32<false>(s3, c2, nb2, acc, pk, 16);
-          }
+          exp32(s2, c2, nb2, acc, pk, 0);
+          exp32(s3, c2, nb2, acc, pk, 16);
           tmem_st32(s_addr + 32, pk);
         }
         const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
