@@ -113,7 +113,7 @@ struct Barriers {
   uint64_t p_full[kSBufs];
   uint64_t pv_done[kSBufs];             // P V of the item in this S buffer has completed
   uint64_t o_done[2];                   // one phase per P V into O_t
-  uint64_t o_free[2];                   // one phase per tile: epilogue has read O_t
+  uint64_t o_free[2];                   // one phase per tile with keys: epilogue has read O_t
   uint64_t tile_full[2], tile_empty[2]; // tile descriptor ring
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -428,6 +428,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
       const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV);
       int K = 0, J = 0;
+      int o_free_waits[2] = {0, 0};  // P V warp: o_free phases consumed per tile slot t
+      bool o_used = false;           // an earlier tile wrote O (had keys)
       for (int nt = 0;; ++nt) {
         const int slot = nt & 1;
         if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, &g_prefill_error))
@@ -463,13 +465,17 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           }
           if (ok) umma_commit_elect(&bars->q_empty[qb]);  // Q buffer free once these QK finish
         } else {
-          // O_t of the previous tile must have been read by its epilogue
-          for (int tt = 0; ok && tt < NT; ++tt)
-            if (nt > 0 && !mbar_wait_warp(&bars->o_free[tt], (nt - 1) & 1, abort,
-                                          &g_prefill_error))
-              ok = false;
           for (int k = 0; ok && k < items; ++k) {
             const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % kSBufs, Jc = J + jj;
+            // the first P V of a tile into O_t waits until the epilogue of the
+            // last tile that used O_t (same softmax warpgroup) has read it; only
+            // tiles with keys use O_t and signal o_free, so the phases pair up
+            if (jj == 0 && o_used && !mbar_wait_warp(&bars->o_free[tt], o_free_waits[tt] & 1,
+                                                     abort, &g_prefill_error)) {
+              ok = false;
+              break;
+            }
+            if (jj == 0 && o_used) ++o_free_waits[tt];
             if (tt == 0 && !mbar_wait_warp(&bars->v_full[Jc % kStages], (Jc / kStages) & 1, abort,
                                            &g_prefill_error)) {
               ok = false;
@@ -496,6 +502,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           }
         }
         if (!ok) break;
+        if (t.n > 0) o_used = true;
         if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
         K += items;
         J += t.n;
@@ -640,9 +647,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) ov[0][i] = ov[1][i] = 0u;
       }
-      // O_t may now be overwritten by the next tile's first P V
-      tc_fence_before();
-      mbar_arrive(&bars->o_free[t]);
+      // O_t may now be overwritten by the next tile's first P V (only tiles
+      // with keys wrote O_t, and only they signal)
+      if (have_o) {
+        tc_fence_before();
+        mbar_arrive(&bars->o_free[t]);
+      }
       if (r < ti.rows) {
 #pragma unroll
         for (int q = 0; q < 2; ++q)

@@ -69,6 +69,18 @@ def test_prefill_groups_and_no_sink(oracle_lib, hq, hkv):
         check_close(out, lse, ro, rl, "hq=%d hkv=%d sinks=%s" % (hq, hkv, with_sinks))
 
 
+def test_prefill_keyless_tiles_between_others(oracle_lib):
+    """Many sequences whose first query tiles see no key (more queries than keys,
+    causal) mixed with long ones: the persistent grid then meets tiles without
+    keys between tiles with keys on the same CTA."""
+    lq = [400] * 20 + [1000] * 20
+    lk = [100] * 20 + [2000] * 20
+    c = S.make_prefill("keyless", lq, lk, 8, 2, seed=75)
+    out, lse = run_prefill(c)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "keyless tiles")
+
+
 def test_prefill_large_sink(oracle_lib):
     c = S.make_prefill("bigsink", [300], [300], 4, 1, seed=69)
     c.sinks = torch.tensor([40.0, -40.0, 0.0, 12.0])
