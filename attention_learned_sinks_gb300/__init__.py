@@ -12,6 +12,9 @@ from .sinkattn import (  # noqa: F401
     sinkattn_decode_workspace_size,
     sinkattn_get_device_error,
     sinkattn_merge,
+    sinkattn_decode_noalloc,
     sinkattn_prefill,
+    sinkattn_prefill_paged,
+    sinkattn_prefill_paged_workspace_size,
     sinkattn_prefill_workspace_size,
 )

@@ -96,6 +96,75 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
   return from_cuda(e);
 }
 
+size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max_seqlen_k,
+                                             int hkv, int head_dim) {
+  if (batch < 0 || total_q < 0 || max_seqlen_k < 0 || hkv <= 0 || head_dim != kHeadDim) return 0;
+  return prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hkv);
+}
+
+sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q,
+                                         const void *k_cache, const void *v_cache,
+                                         const int32_t *block_table, const int32_t *seqlens_k,
+                                         int num_pages, int max_pages_per_seq, int page_size,
+                                         int batch, int64_t total_q, int max_seqlen_q,
+                                         int max_seqlen_k, int hq, int hkv, int head_dim,
+                                         const float *sinks, sinkattn_mask_t mask, void *out,
+                                         float *lse, void *workspace, size_t workspace_bytes,
+                                         void *stream) {
+  if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 ||
+      hq % hkv != 0 || num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0 || !mask_ok(mask))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_seqlen_k) > static_cast<int64_t>(max_pages_per_seq) * page_size)
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return SINKATTN_OK;
+  if (!q || !cu_seqlens_q || !seqlens_k || !out) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (max_seqlen_k > 0 && (!k_cache || !v_cache || !block_table || num_pages == 0))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(block_table, 4) || !aligned(seqlens_k, 4) ||
+      (sinks && !aligned(sinks, 4)) || (lse && !aligned(lse, 4)))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch > 65535 || total_q > INT32_MAX || (max_seqlen_q + 127) / 128 > 65535 ||
+      static_cast<int64_t>(batch) * max_seqlen_k + 128 > INT32_MAX)
+    return SINKATTN_ERR_UNSUPPORTED;
+  const size_t need = prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hkv);
+  if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
+  PrefillPagedLaunch a;
+  a.base.q = q;
+  a.base.k = nullptr;
+  a.base.v = nullptr;
+  a.base.cu_q = cu_seqlens_q;
+  a.base.cu_k = nullptr;
+  a.base.batch = batch;
+  a.base.total_q = total_q;
+  a.base.total_k = 0;
+  a.base.max_seqlen_q = max_seqlen_q;
+  a.base.max_seqlen_k = max_seqlen_k;
+  a.base.hq = hq;
+  a.base.hkv = hkv;
+  a.base.sinks = sinks;
+  a.base.causal = mask.causal != 0;
+  a.base.window = mask.window;
+  a.base.scale = mask.scale;
+  a.base.out = out;
+  a.base.lse = lse;
+  a.base.v_f16 = nullptr;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seqlens_k = seqlens_k;
+  a.max_pages = max_pages_per_seq;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.workspace = workspace;
+  bool encode_failed = false;
+  cudaError_t e = launch_prefill_paged(a, static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return SINKATTN_ERR_CUDA;
+  return from_cuda(e);
+}
+
 size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int hkv, int head_dim,
                                       int window, int num_splits) {
   if (batch <= 0 || hq <= 0 || hkv <= 0 || head_dim != kHeadDim || max_seqlen_k < 0 ||

@@ -61,6 +61,19 @@ size_t prefill_counter_offset(int64_t total_k, int hkv);
 // Returns cudaSuccess, or the failing CUDA error; *encode_failed is set when
 // the tensor-map encoding (driver entry point) failed.
 cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed);
+// Prefill over a paged K/V cache: the referenced pages are gathered into
+// contiguous staging (K bf16, V fp16) in the workspace, then the same kernel
+// runs. base.k/v/cu_k/total_k/v_f16 are unused.
+struct PrefillPagedLaunch {
+  PrefillLaunch base;
+  const void *k_cache, *v_cache;  // [num_pages, hkv, page_size, 64] bf16
+  const int32_t *block_table, *seqlens_k;
+  int max_pages, page_size, num_pages;
+  void *workspace;
+};
+size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hkv);
+cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,
+                                 bool *encode_failed);
 // Reads and clears the prefill kernel's device error word (synchronises stream).
 cudaError_t prefill_read_error(cudaStream_t stream, int *code);
 

@@ -682,20 +682,23 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   }
 }
 
+// 8 bf16 -> 8 fp16, magnitudes above the fp16 range clamped to +-65504.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
+  const float lim = 65504.f;
+  uint4 y;
+  y.x = pack_f16x2(fminf(fmaxf(bf16_lo(x.x), -lim), lim), fminf(fmaxf(bf16_hi(x.x), -lim), lim));
+  y.y = pack_f16x2(fminf(fmaxf(bf16_lo(x.y), -lim), lim), fminf(fmaxf(bf16_hi(x.y), -lim), lim));
+  y.z = pack_f16x2(fminf(fmaxf(bf16_lo(x.z), -lim), lim), fminf(fmaxf(bf16_hi(x.z), -lim), lim));
+  y.w = pack_f16x2(fminf(fmaxf(bf16_lo(x.w), -lim), lim), fminf(fmaxf(bf16_hi(x.w), -lim), lim));
+  return y;
+}
+
 // bf16 V -> fp16 copy for the P V product (8 elements per thread per step).
 __global__ void __launch_bounds__(256) convert_v_kernel(const uint4 *__restrict__ src,
                                                         uint4 *__restrict__ dst, int64_t n8) {
-  const float lim = 65504.f;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 x = src[i];
-    uint4 y;
-    y.x = pack_f16x2(fminf(fmaxf(bf16_lo(x.x), -lim), lim), fminf(fmaxf(bf16_hi(x.x), -lim), lim));
-    y.y = pack_f16x2(fminf(fmaxf(bf16_lo(x.y), -lim), lim), fminf(fmaxf(bf16_hi(x.y), -lim), lim));
-    y.z = pack_f16x2(fminf(fmaxf(bf16_lo(x.z), -lim), lim), fminf(fmaxf(bf16_hi(x.z), -lim), lim));
-    y.w = pack_f16x2(fminf(fmaxf(bf16_lo(x.w), -lim), lim), fminf(fmaxf(bf16_hi(x.w), -lim), lim));
-    dst[i] = y;
-  }
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = bf16x8_to_f16x8(src[i]);
 }
 
 // ---------------------------------------------------------------- host side
@@ -741,36 +744,142 @@ size_t prefill_counter_offset(int64_t total_k, int hkv) {
   return (bytes + 255) / 256 * 256;
 }
 
+namespace {
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+// tile counter + work list for the persistent grid
+size_t schedule_bytes(int batch, int64_t total_q) {
+  return 256 + round256(static_cast<size_t>(total_q / kBM + batch) * 4);
+}
+}  // namespace
+
 size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hkv) {
-  const size_t pairs = static_cast<size_t>(total_q / kBM + batch) * 4;
-  return prefill_counter_offset(total_k, hkv) + 256 + (pairs + 255) / 256 * 256;
+  return prefill_counter_offset(total_k, hkv) + schedule_bytes(batch, total_q);
 }
 
-cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed) {
-  *encode_failed = false;
+// Paged prefill workspace: contiguous K (bf16) and V (fp16) staging of up to
+// batch * max_seqlen_k rows plus a zeroed 128-row tail, the sequence offsets,
+// then the schedule.
+namespace {
+int64_t paged_stage_rows(int batch, int max_seqlen_k) {
+  return static_cast<int64_t>(batch) * max_seqlen_k + kBM;
+}
+size_t paged_stage_bytes(int batch, int max_seqlen_k, int hkv) {
+  return round256(static_cast<size_t>(paged_stage_rows(batch, max_seqlen_k)) * hkv * kHeadDim * 2);
+}
+}  // namespace
+
+size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hkv) {
+  return 2 * paged_stage_bytes(batch, max_seqlen_k, hkv) +
+         round256(static_cast<size_t>(batch + 1) * 4) + schedule_bytes(batch, total_q);
+}
+
+namespace {
+
+// cu_k[b] = sum of min(seqlens_k[i], max_seqlen_k) over i < b (one block).
+__global__ void __launch_bounds__(1024) seqlen_offsets_kernel(const int32_t *seqlens_k, int batch,
+                                                               int max_seqlen_k, int32_t *cu_k) {
+  int carry = 0;
+  for (int base = 0; base < batch; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int len = 0;
+    if (b < batch) {
+      len = seqlens_k[b];
+      if (len < 0 || len > max_seqlen_k) {
+        atomicExch(&g_prefill_error, kErrBadLength);
+        len = min(max(len, 0), max_seqlen_k);
+      }
+    }
+    int total = 0;
+    const int ex = block_exclusive_scan(len, &total);
+    if (b < batch) cu_k[b] = carry + ex;
+    carry += total;
+    __syncthreads();  // warp_sums is reused by the next chunk
+  }
+  if (threadIdx.x == 0) cu_k[batch] = carry;
+}
+
+// Paged K/V -> contiguous staging, one warp per token (all KV heads): K as
+// bf16, V converted to fp16 (clamped to +-65504) for the P V product. Rows
+// [total, total + 128) are zeroed so that a tile running past the last
+// sequence reads zeros.
+__global__ void __launch_bounds__(256) gather_paged_kernel(
+    const __nv_bfloat16 *__restrict__ kc, const __nv_bfloat16 *__restrict__ vc,
+    const int32_t *__restrict__ block_table, const int32_t *__restrict__ cu_k, int batch,
+    int max_pages, int page_size, int num_pages, int hkv, int64_t cap_rows,
+    __nv_bfloat16 *__restrict__ k_out,
+    __half *__restrict__ v_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t total = cu_k[batch];
+  const int64_t end = total + kBM < cap_rows ? total + kBM : cap_rows;
+  const int chunks = hkv * (kHeadDim / 8);  // 16-byte chunks per token row of all heads
+  for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; r < end;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
+    uint4 *kd = reinterpret_cast<uint4 *>(k_out + r * hkv * kHeadDim);
+    uint4 *vd = reinterpret_cast<uint4 *>(v_out + r * hkv * kHeadDim);
+    int page = -1, slot = 0;
+    if (r < total) {
+      int lo = 0, hi = batch;  // sequence b with cu_k[b] <= r < cu_k[b + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu_k[mid] <= r) lo = mid; else hi = mid;
+      }
+      const int j = static_cast<int>(r - cu_k[lo]);
+      page = block_table[static_cast<size_t>(lo) * max_pages + j / page_size];
+      slot = j % page_size;
+      if (page < 0 || page >= num_pages) {
+        if (lane == 0) atomicExch(&g_prefill_error, kErrBadPage);
+        page = -1;
+      }
+    }
+    if (page < 0) {
+      for (int c = lane; c < chunks; c += 32) {
+        kd[c] = make_uint4(0u, 0u, 0u, 0u);
+        vd[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      continue;
+    }
+    for (int c = lane; c < chunks; c += 32) {
+      const int h = c / (kHeadDim / 8), e = c % (kHeadDim / 8);
+      const size_t src = ((static_cast<size_t>(page) * hkv + h) * page_size + slot) * kHeadDim;
+      kd[c] = reinterpret_cast<const uint4 *>(kc + src)[e];
+      vd[c] = bf16x8_to_f16x8(reinterpret_cast<const uint4 *>(vc + src)[e]);
+    }
+  }
+}
+
+int sm_count() {
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
+  return num_sms;
+}
+
+// Everything after the K/V staging: tensor maps, the work list, the kernel.
+// k (bf16) and v16 (fp16) are [k_rows, hkv, 64]; cu_k may live on the device
+// only; sched is the schedule area (tile counter + work list).
+cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, int64_t k_rows,
+                        const int32_t *cu_k, uint8_t *sched, cudaStream_t stream,
+                        bool *encode_failed) {
   const int max_qtiles = (a.max_seqlen_q + kBM - 1) / kBM;
-  if (a.batch == 0 || a.total_q == 0 || max_qtiles == 0) return cudaSuccess;
   EncodeTiledFn fn = get_encode_fn();
   CUtensorMap tq, tk, tv;
   const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   // With no keys at all nothing reads K or V; the maps then point at q.
-  const void *kbase = a.total_k > 0 ? a.k : a.q;
-  const void *vbase = a.total_k > 0 ? a.v_f16 : a.q;
+  const void *kbase = k_rows > 0 ? k : a.q;
+  const void *vbase = k_rows > 0 ? v16 : a.q;
   if (fn == nullptr || !encode_rows_heads(fn, &tq, a.q, a.total_q, a.hq, bf16) ||
-      !encode_rows_heads(fn, &tk, kbase, a.total_k, a.hkv, bf16) ||
-      !encode_rows_heads(fn, &tv, vbase, a.total_k, a.hkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) {
+      !encode_rows_heads(fn, &tk, kbase, k_rows, a.hkv, bf16) ||
+      !encode_rows_heads(fn, &tv, vbase, k_rows, a.hkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
-  const int64_t n8 = a.total_k * a.hkv * kHeadDim / 8;
-  if (n8 > 0) {
-    const int64_t blocks = (n8 + 255) / 256;
-    convert_v_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
-        static_cast<const uint4 *>(a.v), static_cast<uint4 *>(a.v_f16), n8);
-  }
   Params p;
   p.cu_q = a.cu_q;
-  p.cu_k = a.cu_k;
+  p.cu_k = cu_k;
   p.batch = a.batch;
   p.hq = a.hq;
   p.group = a.hq / a.hkv;
@@ -781,11 +890,9 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
   p.scale_log2 = a.scale * kLog2e;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.lse = a.lse;
-  uint8_t *ws = static_cast<uint8_t *>(a.v_f16);
-  const size_t off = prefill_counter_offset(a.total_k, a.hkv);
-  p.work_counter = reinterpret_cast<unsigned int *>(ws + off);
-  int *num_pairs = reinterpret_cast<int *>(ws + off + 4);
-  unsigned *pairs = reinterpret_cast<unsigned *>(ws + off + 256);
+  p.work_counter = reinterpret_cast<unsigned int *>(sched);
+  int *num_pairs = reinterpret_cast<int *>(sched + 4);
+  unsigned *pairs = reinterpret_cast<unsigned *>(sched + 256);
   p.work_pairs = pairs;
   p.num_pairs = num_pairs;
   const int nt = p.group % 2 == 0 ? 2 : 1;
@@ -796,13 +903,7 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
   // upper bound on the number of work items, for the grid size
   const int64_t max_pairs = a.total_q / kBM + a.batch;
   const int64_t max_work = max_pairs * (a.hq / nt);
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      num_sms = 148;
-  }
+  const int num_sms = sm_count();
   const unsigned grid = static_cast<unsigned>(max_work < num_sms ? max_work : num_sms);
   if (nt == 2) {
     e = cudaFuncSetAttribute(prefill_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -827,6 +928,47 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
     prefill_kernel<1><<<grid, Cfg<1>::kThreads, Cfg<1>::kSmemBytes, stream>>>(tq, tk, tv, p);
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed) {
+  *encode_failed = false;
+  const int max_qtiles = (a.max_seqlen_q + kBM - 1) / kBM;
+  if (a.batch == 0 || a.total_q == 0 || max_qtiles == 0) return cudaSuccess;
+  const int64_t n8 = a.total_k * a.hkv * kHeadDim / 8;
+  if (n8 > 0) {
+    const int64_t blocks = (n8 + 255) / 256;
+    convert_v_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+        static_cast<const uint4 *>(a.v), static_cast<uint4 *>(a.v_f16), n8);
+  }
+  uint8_t *ws = static_cast<uint8_t *>(a.v_f16);
+  return launch_core(a, a.k, a.v_f16, a.total_k, a.cu_k,
+                     ws + prefill_counter_offset(a.total_k, a.hkv), stream, encode_failed);
+}
+
+cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,
+                                 bool *encode_failed) {
+  *encode_failed = false;
+  const PrefillLaunch &c = a.base;
+  const int max_qtiles = (c.max_seqlen_q + kBM - 1) / kBM;
+  if (c.batch == 0 || c.total_q == 0 || max_qtiles == 0) return cudaSuccess;
+  uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+  const size_t stage = paged_stage_bytes(c.batch, c.max_seqlen_k, c.hkv);
+  __nv_bfloat16 *k_st = reinterpret_cast<__nv_bfloat16 *>(ws);
+  __half *v_st = reinterpret_cast<__half *>(ws + stage);
+  int32_t *cu_k = reinterpret_cast<int32_t *>(ws + 2 * stage);
+  uint8_t *sched = ws + 2 * stage + round256(static_cast<size_t>(c.batch + 1) * 4);
+  seqlen_offsets_kernel<<<1, 1024, 0, stream>>>(a.seqlens_k, c.batch, c.max_seqlen_k, cu_k);
+  const int64_t cap = paged_stage_rows(c.batch, c.max_seqlen_k);
+  const int64_t warps = cap < sm_count() * 64 ? cap : sm_count() * 64;
+  gather_paged_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(a.k_cache), static_cast<const __nv_bfloat16 *>(a.v_cache),
+      a.block_table, cu_k, c.batch, a.max_pages, a.page_size, a.num_pages, c.hkv, cap, k_st,
+      v_st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_core(c, k_st, v_st, cap, cu_k, sched, stream, encode_failed);
 }
 
 cudaError_t prefill_read_error(cudaStream_t stream, int *code) {

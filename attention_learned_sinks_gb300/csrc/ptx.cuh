@@ -17,6 +17,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 // A bounded wait that runs out stores this code into the kernel's error word
 // (read back by sinkattn_get_device_error).
 constexpr int kErrWaitTimeout = 1;
+// The paged prefill gather met a block-table entry outside [0, num_pages)
+// (the row is staged as zeros) or a key length outside [0, max_seqlen_k]
+// (clamped into that range).
+constexpr int kErrBadPage = 2;
+constexpr int kErrBadLength = 3;
 // A single pipeline wait is microseconds in a working kernel; give up after
 // one second of wall-clock time so a broken pipeline cannot hang the GPU.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

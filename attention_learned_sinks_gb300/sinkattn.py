@@ -24,6 +24,8 @@ EXPORTED = (
     "sinkattn_status_string",
     "sinkattn_prefill_workspace_size",
     "sinkattn_prefill",
+    "sinkattn_prefill_paged_workspace_size",
+    "sinkattn_prefill_paged",
     "sinkattn_decode_workspace_size",
     "sinkattn_decode",
     "sinkattn_decode_noalloc",
@@ -62,6 +64,11 @@ def load(path: str = LIB_PATH):
     lib.sinkattn_prefill.argtypes = [P, P, P, P, P, I, L, L, I, I, I, I, I, P, Mask,
                                      P, P, P, S, P]
     lib.sinkattn_prefill.restype = I
+    lib.sinkattn_prefill_paged_workspace_size.argtypes = [I, L, I, I, I]
+    lib.sinkattn_prefill_paged_workspace_size.restype = S
+    lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, L, I, I, I, I, I, P,
+                                           Mask, P, P, P, S, P]
+    lib.sinkattn_prefill_paged.restype = I
     lib.sinkattn_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.sinkattn_decode_workspace_size.restype = S
     lib.sinkattn_decode.argtypes = [P, P, P, P, P, P, L, I, I, I, I, I, I, I, P, Mask, I,
@@ -147,6 +154,48 @@ def sinkattn_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
                               _ptr(sinks), mask, _ptr(out), _ptr(lse), _ptr(workspace),
                               workspace.numel(), _stream(stream))
     _check(st, "sinkattn_prefill")
+    return out, lse
+
+
+def sinkattn_prefill_paged_workspace_size(batch, total_q, max_seqlen_k, hkv, head_dim=64):
+    return load().sinkattn_prefill_paged_workspace_size(int(batch), int(total_q),
+                                                        int(max_seqlen_k), hkv, head_dim)
+
+
+def sinkattn_prefill_paged(q, cu_seqlens_q, k_cache, v_cache, block_table, seqlens_k,
+                           max_seqlen_q, max_seqlen_k, *, sinks=None, causal=True, window=0,
+                           scale=None, out=None, lse=None, return_lse=True, workspace=None,
+                           stream=None):
+    """Sink-attention prefill of packed queries against a paged KV cache
+    [num_pages, hkv, page_size, 64] addressed by block_table / seqlens_k.
+    Returns (out, lse)."""
+    lib = load()
+    _req(q, torch.bfloat16, "q")
+    _req(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _req(k_cache, torch.bfloat16, "k_cache")
+    _req(v_cache, torch.bfloat16, "v_cache")
+    _req(block_table, torch.int32, "block_table")
+    _req(seqlens_k, torch.int32, "seqlens_k")
+    tq, hq, d = q.shape
+    num_pages, hkv, page_size, _ = k_cache.shape
+    batch = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((tq, hq), dtype=torch.float32, device=q.device)
+    if sinks is not None:
+        _req(sinks, torch.float32, "sinks")
+    if workspace is None:
+        need = lib.sinkattn_prefill_paged_workspace_size(batch, tq, int(max_seqlen_k), hkv, d)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    mask = Mask(1 if causal else 0, int(window), float(d ** -0.5 if scale is None else scale))
+    st = lib.sinkattn_prefill_paged(_ptr(q), _ptr(cu_seqlens_q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_table), _ptr(seqlens_k), num_pages,
+                                    block_table.shape[1], page_size, batch, tq,
+                                    int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
+                                    _ptr(sinks), mask, _ptr(out), _ptr(lse), _ptr(workspace),
+                                    workspace.numel(), _stream(stream))
+    _check(st, "sinkattn_prefill_paged")
     return out, lse
 
 

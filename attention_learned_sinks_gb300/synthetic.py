@@ -16,6 +16,10 @@ are not available here, so seeded normal values stand in for them):
                    randomly permuted block table, sinks ~N(0, 2), full or window 128
   chunked_prefill  4096 new query tokens at positions 126976..131071 of a
                    131072-token causal context
+  paged_chunked_prefill  the same, with K/V in 16-token pages and a randomly
+                   permuted block table
+  paged_prefill_batch    16 sequences, new chunks uniform in [256, 2048] after
+                   cached contexts uniform in [1024, 32768], 16-token pages
 
 Conventions: "uniform in [a, b]" draws integers with both ends included; values
 are float32 normal samples rounded to bf16 (round to nearest even); sinks stay
@@ -93,10 +97,20 @@ class PrefillCase:
     window: int
     scale: float
     head_dim: int = HEAD_DIM
+    # paged K/V (k, v and cu_seqlens_k are None then)
+    k_cache: Optional[torch.Tensor] = None      # bf16 [num_pages, hkv, page, D]
+    v_cache: Optional[torch.Tensor] = None
+    block_table: Optional[torch.Tensor] = None  # int32 [batch, max_pages]
+    seqlens_k_t: Optional[torch.Tensor] = None  # int32 [batch]
+    page_size: int = PAGE_SIZE
 
     @property
     def batch(self):
         return len(self.seqlens_q)
+
+    @property
+    def paged(self):
+        return self.block_table is not None
 
     @property
     def max_seqlen_q(self):
@@ -161,6 +175,47 @@ def make_prefill(name, seqlens_q, seqlens_k, hq, hkv, *, seed, causal=True,
                        head_dim=head_dim)
 
 
+def _page_table(seqlens_k, page_size, seed, spare_pages=0):
+    """Block table over randomly permuted pages: sequence b gets
+    ceil(Lk_b / page_size) pages; spare_pages extra pages are never referenced."""
+    pages_per_seq = [(l + page_size - 1) // page_size for l in seqlens_k]
+    num_pages = max(1, sum(pages_per_seq) + spare_pages)
+    max_pages = max(1, max(pages_per_seq) if pages_per_seq else 1)
+    g = _gen(seed, "cpu")
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    table = torch.zeros((len(seqlens_k), max_pages), dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(pages_per_seq):
+        table[b, :n] = perm[at:at + n]
+        at += n
+    return table, num_pages
+
+
+def make_prefill_paged(name, seqlens_q, seqlens_k, hq, hkv, *, seed, causal=True,
+                       window=0, sink_std=1.0, with_sinks=True, scale=None,
+                       page_size=PAGE_SIZE, spare_pages=0, device="cpu",
+                       head_dim=HEAD_DIM) -> PrefillCase:
+    """Packed queries against K/V in pages; the queries of sequence b are the
+    last Lq_b of its Lk_b positions."""
+    tq = sum(seqlens_q)
+    q = bf16_normal((tq, hq, head_dim), seed * 10 + 1, device=device)
+    table, num_pages = _page_table(seqlens_k, page_size, seed * 10 + 5, spare_pages)
+    sinks = normal_f32(hq, seed * 10 + 4, sink_std) if with_sinks else None
+    return PrefillCase(name=name, q=q, k=None, v=None, cu_seqlens_q=offsets(seqlens_q),
+                       cu_seqlens_k=None, seqlens_q=list(seqlens_q),
+                       seqlens_k=list(seqlens_k), hq=hq, hkv=hkv, sinks=sinks,
+                       causal=causal, window=window,
+                       scale=scale if scale is not None else head_dim ** -0.5,
+                       head_dim=head_dim,
+                       k_cache=bf16_normal((num_pages, hkv, page_size, head_dim),
+                                           seed * 10 + 2, device=device),
+                       v_cache=bf16_normal((num_pages, hkv, page_size, head_dim),
+                                           seed * 10 + 3, device=device),
+                       block_table=table,
+                       seqlens_k_t=torch.tensor(seqlens_k, dtype=torch.int32),
+                       page_size=page_size)
+
+
 def make_decode(name, seqlens_k, hq, hkv, *, seed, window=0, sink_std=1.0,
                 with_sinks=True, paged=False, page_size=PAGE_SIZE, scale=None,
                 device="cpu", head_dim=HEAD_DIM) -> DecodeCase:
@@ -177,16 +232,7 @@ def make_decode(name, seqlens_k, hq, hkv, *, seed, window=0, sink_std=1.0,
         case.v = bf16_normal((tk, hkv, head_dim), seed * 10 + 3, device=device)
         case.kv_indptr = offsets(seqlens_k)
         return case
-    pages_per_seq = [(l + page_size - 1) // page_size for l in seqlens_k]
-    num_pages = max(1, sum(pages_per_seq))
-    max_pages = max(1, max(pages_per_seq) if pages_per_seq else 1)
-    g = _gen(seed * 10 + 5, "cpu")
-    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
-    table = torch.zeros((batch, max_pages), dtype=torch.int32)
-    at = 0
-    for b, n in enumerate(pages_per_seq):
-        table[b, :n] = perm[at:at + n]
-        at += n
+    table, num_pages = _page_table(seqlens_k, page_size, seed * 10 + 5)
     case.k_cache = bf16_normal((num_pages, hkv, page_size, head_dim),
                                seed * 10 + 2, device=device)
     case.v_cache = bf16_normal((num_pages, hkv, page_size, head_dim),
@@ -227,10 +273,25 @@ def chunked_prefill(device="cpu", lq=4096, lk=131072) -> PrefillCase:
                         causal=True, device=device)
 
 
+def paged_chunked_prefill(device="cpu", lq=4096, lk=131072) -> PrefillCase:
+    return make_prefill_paged("paged_chunked_prefill", [lq], [lk], 64, 8, seed=6,
+                              causal=True, device=device)
+
+
+def paged_prefill_batch(device="cpu", nseq=16) -> PrefillCase:
+    new = uniform_lengths(nseq, 256, 2048, seed=6000)
+    cached = uniform_lengths(nseq, 1024, 32768, seed=6001)
+    return make_prefill_paged("paged_prefill_batch", new,
+                              [n + c for n, c in zip(new, cached)], 64, 8, seed=7,
+                              causal=True, device=device)
+
+
 WORKLOADS = {
     "tiny_prefill": tiny_prefill,
     "decode_contig": decode_contig,
     "varlen_prefill": varlen_prefill,
     "paged_decode": paged_decode,
     "chunked_prefill": chunked_prefill,
+    "paged_chunked_prefill": paged_chunked_prefill,
+    "paged_prefill_batch": paged_prefill_batch,
 }

@@ -12,7 +12,10 @@ Extras on the same run (reported, not the headline): varlen prefill (16
 sequences, lengths uniform in [512, 4096], causal; full and window 128) and
 4096-query chunked prefill over a 131072-token context in TFLOP/s of visible
 (q, k) pairs (4 * 64 flops per pair), and paged decode (batch 256, contexts
-uniform in [1024, 32768], 16-token pages; full and window 128) in GB/s.
+uniform in [1024, 32768], 16-token pages; full and window 128) in GB/s, and
+prefill against a 16-token paged cache (the chunked workload above, and 16
+sequences with new chunks of 256..2048 tokens after 1k..32k cached ones) in
+TFLOP/s.
 
 --impl reference times the float64 CPU oracle instead, on the same workload
 and metric, one sequence (all heads) per step.
@@ -452,7 +455,37 @@ def extras(sa, S, dev, stream, pk, pk_kind):
         res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3, "tokens_per_s": tokens / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,
                      "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)",
-                     "flops": fl, "launches_per_call": 2}
+                     "flops": fl, "launches_per_call": 3}
+        del c, out, lse, ws
+        torch.cuda.empty_cache()
+
+    # prefill against the paged cache: gather of the pages into contiguous
+    # staging, then the same kernel; timed as one call (4 launches)
+    for name, mk in (("paged_chunked_prefill", lambda: S.paged_chunked_prefill(device="cuda")),
+                     ("paged_prefill_batch", lambda: S.paged_prefill_batch(device="cuda"))):
+        c = mk()
+        cq, bt, sl = c.cu_seqlens_q.to(dev), c.block_table.to(dev), c.seqlens_k_t.to(dev)
+        sk = c.sinks.to(dev)
+        out = torch.empty_like(c.q)
+        lse = torch.empty((c.q.shape[0], c.hq), dtype=torch.float32, device=dev)
+        ws = torch.empty(sa.sinkattn_prefill_paged_workspace_size(c.batch, c.q.shape[0],
+                                                                  c.max_seqlen_k, c.hkv),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            sa.sinkattn_prefill_paged(c.q, cq, c.k_cache, c.v_cache, bt, sl, c.max_seqlen_q,
+                                      c.max_seqlen_k, sinks=sk, causal=c.causal,
+                                      window=c.window, out=out, lse=lse, workspace=ws)
+        for _ in range(3):
+            call()
+        t = time_calls(call, 10, stream, flush)
+        fl = prefill_flops(c)
+        kv = sum(c.seqlens_k) * c.hkv * 64 * 2 * 2
+        res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3,
+                     "tokens_per_s": sum(c.seqlens_q) / t,
+                     "frac_of_bf16_peak": fl / t / 1e12 / burst,
+                     "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)",
+                     "flops": fl, "kv_bytes": kv, "launches_per_call": 4}
         del c, out, lse, ws
         torch.cuda.empty_cache()
 

@@ -106,6 +106,50 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
                                    size_t workspace_bytes, void *stream);
 
 /*
+ * Prefill over a paged KV cache: chunked prefill of new query tokens against
+ * keys and values that live in fixed-size pages (page "Fast embeddings on
+ * GPUs", section "ROSE": paged KV for serving; ragged sequences without
+ * padding). Same operation, mask and outputs as sinkattn_prefill; only the
+ * key/value addressing differs.
+ *
+ *   q        bf16 [total_q, hq, 64]   sequence b owns rows cu_seqlens_q[b]..[b+1]
+ *   cu_seqlens_q  int32 [batch+1], device, non-decreasing, starting at 0,
+ *            last entry total_q.
+ *   k_cache, v_cache  bf16 [num_pages, hkv, page_size, 64]. Key j of sequence
+ *            b is slot j % page_size of page block_table[b][j / page_size].
+ *   block_table   int32 [batch, max_pages_per_seq], device.
+ *   seqlens_k     int32 [batch], device: Lk_b, which counts the cached keys and
+ *            the new tokens' own keys (already written into the pages). The
+ *            queries are the last Lq_b of the Lk_b positions.
+ *   max_seqlen_q  host upper bound on Lq_b (grid sizing).
+ *   max_seqlen_k  host upper bound on Lk_b; must not exceed
+ *            max_pages_per_seq * page_size. It sizes the workspace.
+ *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
+ *            sinkattn_prefill_paged_workspace_size(batch, total_q,
+ *            max_seqlen_k, hkv, head_dim) bytes (about
+ *            batch * max_seqlen_k * hkv * 256 bytes); contents need not be
+ *            initialised. The call first gathers every sequence's pages into
+ *            contiguous rows there (K as bf16, V as fp16 for the P.V product,
+ *            clamped to +-65504), then runs the prefill kernel on them.
+ * A block-table entry outside [0, num_pages) or an Lk_b outside
+ * [0, max_seqlen_k] is not read through: the key row is staged as zeros, or
+ * the length clamped, and the device error word (sinkattn_get_device_error)
+ * records code 2 or 3.
+ */
+size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max_seqlen_k,
+                                             int hkv, int head_dim);
+
+sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q,
+                                         const void *k_cache, const void *v_cache,
+                                         const int32_t *block_table, const int32_t *seqlens_k,
+                                         int num_pages, int max_pages_per_seq, int page_size,
+                                         int batch, int64_t total_q, int max_seqlen_q,
+                                         int max_seqlen_k, int hq, int hkv, int head_dim,
+                                         const float *sinks, sinkattn_mask_t mask, void *out,
+                                         float *lse, void *workspace, size_t workspace_bytes,
+                                         void *stream);
+
+/*
  * Decode: one query token per sequence over a KV cache, split along the KV
  * sequence (section "Kernels for GPT-OSS / Sink Attention": attention is
  * parallelised over heads and over the KV length; the sink enters one block
@@ -204,7 +248,9 @@ sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_ls
  * Device error word. Every wait inside the kernels is bounded; a wait that
  * runs out records a nonzero code here and the kernel returns early instead of
  * hanging. This call synchronises `stream`, copies the word to *code and
- * resets it to 0. Codes: 0 none; 1 a pipeline barrier wait timed out.
+ * resets it to 0. Codes: 0 none; 1 a pipeline barrier wait timed out;
+ * 2 a paged-prefill block-table entry was outside [0, num_pages); 3 a
+ * paged-prefill key length was outside [0, max_seqlen_k].
  */
 sinkattn_status_t sinkattn_get_device_error(void *stream, int *code);
 

@@ -84,6 +84,42 @@ def test_prefill_rejects_bad_arguments(lib):
     assert prefill(lib, tq=0) == B.SINKATTN_OK
 
 
+def prefill_paged(lib, **kw):
+    a = dict(q=FAKE, cuq=FAKE, k=FAKE, v=FAKE, table=FAKE, seqlens=FAKE, npages=8, maxp=4,
+             page=16, batch=2, tq=10, mq=5, mk=64, hq=8, hkv=2, d=64, sinks=None, mask=M,
+             out=FAKE, lse=None)
+    a.update(kw)
+    return lib.sinkattn_prefill_paged(a["q"], a["cuq"], a["k"], a["v"], a["table"], a["seqlens"],
+                                      a["npages"], a["maxp"], a["page"], a["batch"], a["tq"],
+                                      a["mq"], a["mk"], a["hq"], a["hkv"], a["d"], a["sinks"],
+                                      a["mask"], a["out"], a["lse"], a.get("ws"), a.get("wsb", 0),
+                                      None)
+
+
+def test_prefill_paged_rejects_bad_arguments(lib):
+    assert prefill_paged(lib, d=128) == B.SINKATTN_ERR_UNSUPPORTED
+    assert prefill_paged(lib, hq=6, hkv=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill_paged(lib, page=0) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    # the block table must be able to address max_seqlen_k keys
+    assert prefill_paged(lib, mk=65) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill_paged(lib, table=None) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill_paged(lib, seqlens=None) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill_paged(lib, npages=0) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill_paged(lib, k=ctypes.c_void_p((1 << 20) + 8)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill_paged(lib, mask=B.Mask(0, -3, 0.1)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    need = lib.sinkattn_prefill_paged_workspace_size(2, 10, 64, 2, 64)
+    # K and V staging for batch * max_seqlen_k rows plus a 128-row tail
+    assert need >= 2 * (2 * 64 + 128) * 2 * 64 * 2
+    assert prefill_paged(lib) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert prefill_paged(lib, ws=FAKE, wsb=need - 1) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert prefill_paged(lib, ws=ctypes.c_void_p((1 << 20) + 16), wsb=need) == \
+        B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert prefill_paged(lib, batch=0) == B.SINKATTN_OK
+    assert prefill_paged(lib, tq=0) == B.SINKATTN_OK
+    assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 64, 2, 96) == 0
+    assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 128, 2, 64) > need
+
+
 def test_decode_rejects_bad_arguments(lib):
     assert decode(lib, d=80) == B.SINKATTN_ERR_UNSUPPORTED
     assert decode(lib, hq=32, hkv=2) == B.SINKATTN_ERR_UNSUPPORTED   # group of 16
