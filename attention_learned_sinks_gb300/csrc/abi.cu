@@ -42,20 +42,27 @@ const char *sinkattn_status_string(sinkattn_status_t s) {
   return "unknown status";
 }
 
-size_t sinkattn_prefill_workspace_size(int batch, int64_t total_q, int64_t total_k, int hkv,
-                                       int head_dim) {
-  if (batch < 0 || total_q < 0 || total_k < 0 || hkv <= 0 || head_dim != kHeadDim) return 0;
-  return prefill_workspace_bytes(batch, total_q, total_k, hkv);
+size_t sinkattn_prefill_workspace_size(int batch, int64_t total_q, int64_t total_k,
+                                       int max_seqlen_q, int max_seqlen_k, int hq, int hkv,
+                                       int head_dim, int window, int num_splits) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+      hq <= 0 || hkv <= 0 || hq % hkv != 0 || head_dim != kHeadDim || window < 0 ||
+      num_splits < 0)
+    return 0;
+  const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
+                                         hq, hkv, window);
+  return prefill_workspace_bytes(batch, total_q, total_k, hq, hkv, splits);
 }
 
 sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
                                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                    int batch, int64_t total_q, int64_t total_k, int max_seqlen_q,
                                    int max_seqlen_k, int hq, int hkv, int head_dim,
-                                   const float *sinks, sinkattn_mask_t mask, void *out, float *lse,
-                                   void *workspace, size_t workspace_bytes, void *stream) {
+                                   const float *sinks, sinkattn_mask_t mask, int num_splits,
+                                   void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
   if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 ||
-      hkv <= 0 || hq % hkv != 0 || !mask_ok(mask))
+      hkv <= 0 || hq % hkv != 0 || num_splits < 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return SINKATTN_OK;
@@ -67,7 +74,11 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
   if (batch > 65535 || total_q > INT32_MAX || total_k > INT32_MAX ||
       (max_seqlen_q + 127) / 128 > 65535)
     return SINKATTN_ERR_UNSUPPORTED;
-  const size_t need = prefill_workspace_bytes(batch, total_q, total_k, hkv);
+  const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
+                                         hq, hkv, mask.window);
+  if (splits > 1 && static_cast<int64_t>(splits) * total_q * hq > INT32_MAX)
+    return SINKATTN_ERR_UNSUPPORTED;
+  const size_t need = prefill_workspace_bytes(batch, total_q, total_k, hq, hkv, splits);
   if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
   PrefillLaunch a;
@@ -89,6 +100,7 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
   a.scale = mask.scale;
   a.out = out;
   a.lse = lse;
+  a.num_splits = splits;
   a.v_f16 = workspace;
   bool encode_failed = false;
   cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream), &encode_failed);
@@ -96,10 +108,15 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
   return from_cuda(e);
 }
 
-size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max_seqlen_k,
-                                             int hkv, int head_dim) {
-  if (batch < 0 || total_q < 0 || max_seqlen_k < 0 || hkv <= 0 || head_dim != kHeadDim) return 0;
-  return prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hkv);
+size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max_seqlen_q,
+                                             int max_seqlen_k, int hq, int hkv, int head_dim,
+                                             int window, int num_splits) {
+  if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 ||
+      hq % hkv != 0 || head_dim != kHeadDim || window < 0 || num_splits < 0)
+    return 0;
+  const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
+                                         hq, hkv, window);
+  return prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hq, hkv, splits);
 }
 
 sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q,
@@ -108,11 +125,12 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
                                          int num_pages, int max_pages_per_seq, int page_size,
                                          int batch, int64_t total_q, int max_seqlen_q,
                                          int max_seqlen_k, int hq, int hkv, int head_dim,
-                                         const float *sinks, sinkattn_mask_t mask, void *out,
-                                         float *lse, void *workspace, size_t workspace_bytes,
-                                         void *stream) {
+                                         const float *sinks, sinkattn_mask_t mask,
+                                         int num_splits, void *out, float *lse, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
   if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 ||
-      hq % hkv != 0 || num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0 || !mask_ok(mask))
+      hq % hkv != 0 || num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0 ||
+      num_splits < 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_seqlen_k) > static_cast<int64_t>(max_pages_per_seq) * page_size)
@@ -128,7 +146,11 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
   if (batch > 65535 || total_q > INT32_MAX || (max_seqlen_q + 127) / 128 > 65535 ||
       static_cast<int64_t>(batch) * max_seqlen_k + 128 > INT32_MAX)
     return SINKATTN_ERR_UNSUPPORTED;
-  const size_t need = prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hkv);
+  const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
+                                         hq, hkv, mask.window);
+  if (splits > 1 && static_cast<int64_t>(splits) * total_q * hq > INT32_MAX)
+    return SINKATTN_ERR_UNSUPPORTED;
+  const size_t need = prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hq, hkv, splits);
   if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
   PrefillPagedLaunch a;
@@ -150,6 +172,7 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
   a.base.scale = mask.scale;
   a.base.out = out;
   a.base.lse = lse;
+  a.base.num_splits = splits;
   a.base.v_f16 = nullptr;
   a.k_cache = k_cache;
   a.v_cache = v_cache;

@@ -54,10 +54,19 @@ struct PrefillLaunch {
   float scale;
   void *out;
   float *lse;
-  void *v_f16;  // workspace (prefill_workspace_bytes): fp16 copy of v, tile counter, work list
+  int num_splits;  // key-range splits per work item (>= 1), from prefill_plan_splits
+  // workspace (prefill_workspace_bytes): fp16 copy of v, tile counter, work
+  // list, split partials
+  void *v_f16;
 };
-size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hkv);
-size_t prefill_counter_offset(int64_t total_k, int hkv);
+// Key-range splits for a prefill call: requested > 0 is taken as is (capped at
+// kMaxPrefillSplits); 0 picks a count from the host bounds so that calls with
+// few (query tile, head) items over long contexts fill the GPU.
+constexpr int kMaxPrefillSplits = 64;
+int prefill_plan_splits(int requested, int batch, int64_t total_q, int max_seqlen_q,
+                        int max_seqlen_k, int hq, int hkv, int window);
+size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv,
+                               int splits);
 // Returns cudaSuccess, or the failing CUDA error; *encode_failed is set when
 // the tensor-map encoding (driver entry point) failed.
 cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed);
@@ -71,7 +80,8 @@ struct PrefillPagedLaunch {
   int max_pages, page_size, num_pages;
   void *workspace;
 };
-size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hkv);
+size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hq,
+                                     int hkv, int splits);
 cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,
                                  bool *encode_failed);
 // Reads and clears the prefill kernel's device error word (synchronises stream).

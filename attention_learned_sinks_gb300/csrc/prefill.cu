@@ -40,6 +40,7 @@
 // while most tiles skip the O round trip.
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "launch.h"
@@ -96,12 +97,18 @@ struct Params {
   unsigned int *work_counter;  // zeroed by build_worklist_kernel
   const unsigned *work_pairs;  // longest-first (sequence, query tile) list, packed b << 16 | qt
   const int *num_pairs;        // its length
+  // Split-KV: with num_splits > 1 every (tile, heads) item is cut into that
+  // many key ranges; split s writes its normalised partial output and lse to
+  // part_o [s][total_q][hq][64] / part_lse [s][total_q][hq] (fp32) instead of
+  // out/lse, and only split 0 starts from the sink.
+  int num_splits, total_q;
+  float *part_o, *part_lse;
 };
 
 // One unit of work: 128 query rows of sequence b for the NT heads h0...
 struct Tile {
   int valid;  // 0: no more work
-  int h0, b, qt, q0, lq, k0, lk, rows, kvh, p_min, p_max, kt_lo, n;
+  int h0, b, qt, q0, lq, k0, lk, rows, kvh, p_min, p_max, kt_lo, n, split;
 };
 
 struct Barriers {
@@ -175,14 +182,19 @@ __device__ __forceinline__ void exp32(const float (&sv)[32], float2 c2, float2 n
   }
 }
 
-// Work index w -> tile: list entry w / groups gives (sequence, query tile),
-// w % groups the head group. n = 0 for a tile that sees no key.
-__device__ __forceinline__ void decode_work(const Params &p, int NT, int w, Tile &t) {
+// Work index w -> tile. Splits are outermost (items that run at the same time
+// share a key range, which keeps it in L2); within a split, list entry
+// (w / groups) gives (sequence, query tile) and w % groups the head group.
+// n = 0 for a tile that sees no key (in this split).
+__device__ __forceinline__ void decode_work(const Params &p, int NT, int npairs, int w, Tile &t) {
   const int groups = p.hq / NT;
+  const int split = w / (npairs * groups);
+  w -= split * npairs * groups;
   const unsigned e = p.work_pairs[w / groups];
   const int b = static_cast<int>(e >> 16), qt = static_cast<int>(e & 0xffffu);
   const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
   t.valid = 1;
+  t.split = split;
   t.h0 = (w % groups) * NT;
   t.b = b;
   t.qt = qt;
@@ -199,6 +211,12 @@ __device__ __forceinline__ void decode_work(const Params &p, int NT, int w, Tile
   if (p.window > 0) key_lo = max(0, t.p_min - p.window + 1);
   t.kt_lo = key_lo / kBN;
   t.n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - t.kt_lo : 0;
+  if (p.num_splits > 1) {  // this split's share of the key tiles
+    const int lo = static_cast<int>(static_cast<int64_t>(t.n) * split / p.num_splits);
+    const int hi = static_cast<int>(static_cast<int64_t>(t.n) * (split + 1) / p.num_splits);
+    t.kt_lo += lo;
+    t.n = hi - lo;
+  }
 }
 
 // One block: the list of non-empty (sequence b, query tile qt) pairs, ordered
@@ -357,7 +375,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       tma_prefetch_desc(&tm_v);
       int J = 0;  // K/V stage uses so far
       int q_loads = 0;
-      const int num_work = *p.num_pairs * (p.hq / NT);
+      const int npairs = *p.num_pairs;
+      const int num_work = npairs * (p.hq / NT) * p.num_splits;
       for (int nt = 0;; ++nt) {
         const int slot = nt & 1;
         if (nt >= 2 && !mbar_wait_warp(&bars->tile_empty[slot], ((nt >> 1) - 1) & 1, abort,
@@ -367,7 +386,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           Tile t;
           t.valid = 0;
           const int w = static_cast<int>(atomicAdd(p.work_counter, 1u));
-          if (w < num_work) decode_work(p, NT, w, t);
+          if (w < num_work) decode_work(p, NT, npairs, w, t);
           bars->tiles[slot] = t;
           mbar_arrive(&bars->tile_full[slot]);
         }
@@ -530,7 +549,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       const Tile ti = bars->tiles[slot];
       if (!ti.valid) break;
       const int h = ti.h0 + t;
-      const bool has_sink = p.sinks != nullptr;
+      const bool has_sink = p.sinks != nullptr && ti.split == 0;
       float m_run = has_sink ? p.sinks[h] * kLog2e : -INFINITY;
       float d_run = has_sink ? 1.f : 0.f;
       const int pos = ti.p_min + r;
@@ -636,7 +655,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       }
       const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
       const size_t row_h = static_cast<size_t>(ti.q0 + ti.qt * kBM + r) * p.hq + h;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + row_h * kHeadDim);
       uint32_t ov[2][32];
       if (have_o) {
         tc_fence_after();
@@ -653,7 +671,20 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars->o_free[t]);
       }
-      if (r < ti.rows) {
+      const float lse = d_run > 0.f ? (m_run + fast_log2(d_run)) * kLn2 : -INFINITY;
+      if (r < ti.rows && p.num_splits > 1) {
+        const size_t at = static_cast<size_t>(ti.split) * p.total_q * p.hq + row_h;
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + at * kHeadDim);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float *o = reinterpret_cast<const float *>(&ov[q][4 * i]);
+            dst[q * 8 + i] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+          }
+        p.part_lse[at] = lse;
+      } else if (r < ti.rows) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + row_h * kHeadDim);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -666,8 +697,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
             dst[q * 4 + i] = v;
           }
-        if (p.lse != nullptr)
-          p.lse[row_h] = d_run > 0.f ? (m_run + fast_log2(d_run)) * kLn2 : -INFINITY;
+        if (p.lse != nullptr) p.lse[row_h] = lse;
       }
       mbar_arrive(&bars->tile_empty[slot]);
       K += NT * n;
@@ -739,38 +769,90 @@ bool encode_rows_heads(EncodeTiledFn fn, CUtensorMap *map, const void *base, int
 }  // namespace
 
 // Workspace: fp16 copy of V, then the tile counter of the persistent grid.
-size_t prefill_counter_offset(int64_t total_k, int hkv) {
-  const size_t bytes = static_cast<size_t>(total_k) * hkv * kHeadDim * 2;
-  return (bytes + 255) / 256 * 256;
+namespace {
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+int sm_count() {
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
+  return num_sms;
 }
 
-namespace {
-size_t round256(size_t x) { return (x + 255) / 256 * 256; }
-// tile counter + work list for the persistent grid
-size_t schedule_bytes(int batch, int64_t total_q) {
+// Workspace pieces. Every piece starts on a 256-byte boundary.
+size_t vcopy_bytes(int64_t total_k, int hkv) {  // fp16 copy of V
+  return round256(static_cast<size_t>(total_k) * hkv * kHeadDim * 2);
+}
+size_t schedule_bytes(int batch, int64_t total_q) {  // tile counter + work list
   return 256 + round256(static_cast<size_t>(total_q / kBM + batch) * 4);
 }
-}  // namespace
-
-size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hkv) {
-  return prefill_counter_offset(total_k, hkv) + schedule_bytes(batch, total_q);
+size_t partial_o_bytes(int64_t total_q, int hq, int splits) {
+  return splits > 1 ? round256(static_cast<size_t>(splits) * total_q * hq * kHeadDim * 4) : 0;
 }
-
-// Paged prefill workspace: contiguous K (bf16) and V (fp16) staging of up to
-// batch * max_seqlen_k rows plus a zeroed 128-row tail, the sequence offsets,
-// then the schedule.
-namespace {
+size_t partials_bytes(int64_t total_q, int hq, int splits) {  // o, then lse
+  return splits > 1 ? partial_o_bytes(total_q, hq, splits) +
+                          round256(static_cast<size_t>(splits) * total_q * hq * 4)
+                    : 0;
+}
+// Paged staging: K (bf16) or V (fp16) of up to batch * max_seqlen_k rows plus
+// a zeroed 128-row tail.
 int64_t paged_stage_rows(int batch, int max_seqlen_k) {
   return static_cast<int64_t>(batch) * max_seqlen_k + kBM;
 }
 size_t paged_stage_bytes(int batch, int max_seqlen_k, int hkv) {
   return round256(static_cast<size_t>(paged_stage_rows(batch, max_seqlen_k)) * hkv * kHeadDim * 2);
 }
+
 }  // namespace
 
-size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hkv) {
+int prefill_plan_splits(int requested, int batch, int64_t total_q, int max_seqlen_q,
+                        int max_seqlen_k, int hq, int hkv, int window) {
+  if (requested > 0) return requested < kMaxPrefillSplits ? requested : kMaxPrefillSplits;
+  const int nt = (hq / hkv) % 2 == 0 ? 2 : 1;
+  const int64_t qtiles = (max_seqlen_q + kBM - 1) / kBM;
+  const int64_t pairs = std::min<int64_t>(total_q / kBM + batch, batch * qtiles);
+  const int64_t items = pairs * (hq / nt);
+  int64_t kv_tiles = (max_seqlen_k + kBN - 1) / kBN;
+  if (window > 0)
+    kv_tiles = std::min<int64_t>(kv_tiles, (static_cast<int64_t>(window) + kBM - 1) / kBN + 2);
+  const int64_t sms = sm_count();
+  // Enough items already, or too few keys to be worth cutting.
+  if (items <= 0 || items >= 2 * sms || kv_tiles < 32) return 1;
+  // Cost model: the items run in waves over the SMs; an item costs its share
+  // of key tiles plus about 4 tiles of fixed work (Q load, pipeline fill and
+  // drain, epilogue). The merge pass is small next to that.
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  const int64_t max_s = std::min<int64_t>(kMaxPrefillSplits, kv_tiles / 16);
+  for (int64_t s = 1; s <= max_s; ++s) {
+    const int64_t waves = (items * s + sms - 1) / sms;
+    const int64_t cost = waves * ((kv_tiles + s - 1) / s + 4);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = static_cast<int>(s);
+    }
+  }
+  return best;
+}
+
+size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv,
+                               int splits) {
+  return vcopy_bytes(total_k, hkv) + schedule_bytes(batch, total_q) +
+         partials_bytes(total_q, hq, splits);
+}
+
+// Paged prefill workspace: K staging, V staging, the sequence offsets, the
+// schedule, the split partials.
+size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hq,
+                                     int hkv, int splits) {
   return 2 * paged_stage_bytes(batch, max_seqlen_k, hkv) +
-         round256(static_cast<size_t>(batch + 1) * 4) + schedule_bytes(batch, total_q);
+         round256(static_cast<size_t>(batch + 1) * 4) + schedule_bytes(batch, total_q) +
+         partials_bytes(total_q, hq, splits);
 }
 
 namespace {
@@ -847,20 +929,10 @@ __global__ void __launch_bounds__(256) gather_paged_kernel(
   }
 }
 
-int sm_count() {
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      num_sms = 148;
-  }
-  return num_sms;
-}
-
-// Everything after the K/V staging: tensor maps, the work list, the kernel.
-// k (bf16) and v16 (fp16) are [k_rows, hkv, 64]; cu_k may live on the device
-// only; sched is the schedule area (tile counter + work list).
+// Everything after the K/V staging: tensor maps, the work list, the kernel
+// and, with splits, the merge. k (bf16) and v16 (fp16) are [k_rows, hkv, 64];
+// cu_k may live on the device only; sched is the schedule area (tile counter +
+// work list), followed by the split partials.
 cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, int64_t k_rows,
                         const int32_t *cu_k, uint8_t *sched, cudaStream_t stream,
                         bool *encode_failed) {
@@ -895,6 +967,13 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   unsigned *pairs = reinterpret_cast<unsigned *>(sched + 256);
   p.work_pairs = pairs;
   p.num_pairs = num_pairs;
+  const int splits = a.num_splits > 1 ? a.num_splits : 1;
+  p.num_splits = splits;
+  p.total_q = static_cast<int>(a.total_q);
+  uint8_t *part = sched + schedule_bytes(a.batch, a.total_q);
+  p.part_o = splits > 1 ? reinterpret_cast<float *>(part) : nullptr;
+  p.part_lse = splits > 1 ? reinterpret_cast<float *>(part + partial_o_bytes(a.total_q, a.hq, splits))
+                          : nullptr;
   const int nt = p.group % 2 == 0 ? 2 : 1;
   build_worklist_kernel<<<1, 1024, 0, stream>>>(a.cu_q, a.batch, max_qtiles, pairs, num_pairs,
                                                 p.work_counter);
@@ -902,7 +981,7 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   if (e != cudaSuccess) return e;
   // upper bound on the number of work items, for the grid size
   const int64_t max_pairs = a.total_q / kBM + a.batch;
-  const int64_t max_work = max_pairs * (a.hq / nt);
+  const int64_t max_work = max_pairs * (a.hq / nt) * splits;
   const int num_sms = sm_count();
   const unsigned grid = static_cast<unsigned>(max_work < num_sms ? max_work : num_sms);
   if (nt == 2) {
@@ -927,7 +1006,11 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
     if (e != cudaSuccess) return e;
     prefill_kernel<1><<<grid, Cfg<1>::kThreads, Cfg<1>::kSmemBytes, stream>>>(tq, tk, tv, p);
   }
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  // split 0 carried the sink: the merge adds no sink of its own
+  return launch_merge(p.part_o, p.part_lse, splits, a.total_q, a.hq, nullptr, a.out, a.lse,
+                      stream);
 }
 
 }  // namespace
@@ -943,8 +1026,8 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
         static_cast<const uint4 *>(a.v), static_cast<uint4 *>(a.v_f16), n8);
   }
   uint8_t *ws = static_cast<uint8_t *>(a.v_f16);
-  return launch_core(a, a.k, a.v_f16, a.total_k, a.cu_k,
-                     ws + prefill_counter_offset(a.total_k, a.hkv), stream, encode_failed);
+  return launch_core(a, a.k, a.v_f16, a.total_k, a.cu_k, ws + vcopy_bytes(a.total_k, a.hkv),
+                     stream, encode_failed);
 }
 
 cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,

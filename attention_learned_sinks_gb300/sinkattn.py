@@ -59,15 +59,15 @@ def load(path: str = LIB_PATH):
     P, I, L, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.sinkattn_status_string.argtypes = [I]
     lib.sinkattn_status_string.restype = ctypes.c_char_p
-    lib.sinkattn_prefill_workspace_size.argtypes = [I, L, L, I, I]
+    lib.sinkattn_prefill_workspace_size.argtypes = [I, L, L, I, I, I, I, I, I, I]
     lib.sinkattn_prefill_workspace_size.restype = S
-    lib.sinkattn_prefill.argtypes = [P, P, P, P, P, I, L, L, I, I, I, I, I, P, Mask,
+    lib.sinkattn_prefill.argtypes = [P, P, P, P, P, I, L, L, I, I, I, I, I, P, Mask, I,
                                      P, P, P, S, P]
     lib.sinkattn_prefill.restype = I
-    lib.sinkattn_prefill_paged_workspace_size.argtypes = [I, L, I, I, I]
+    lib.sinkattn_prefill_paged_workspace_size.argtypes = [I, L, I, I, I, I, I, I, I]
     lib.sinkattn_prefill_paged_workspace_size.restype = S
     lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, L, I, I, I, I, I, P,
-                                           Mask, P, P, P, S, P]
+                                           Mask, I, P, P, P, S, P]
     lib.sinkattn_prefill_paged.restype = I
     lib.sinkattn_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.sinkattn_decode_workspace_size.restype = S
@@ -112,9 +112,11 @@ def _req(t, dtype, name):
         raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
 
 
-def sinkattn_prefill_workspace_size(batch, total_q, total_k, hkv, head_dim=64):
-    return load().sinkattn_prefill_workspace_size(int(batch), int(total_q), int(total_k), hkv,
-                                                  head_dim)
+def sinkattn_prefill_workspace_size(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, hq,
+                                    hkv, head_dim=64, window=0, num_splits=0):
+    return load().sinkattn_prefill_workspace_size(int(batch), int(total_q), int(total_k),
+                                                  int(max_seqlen_q), int(max_seqlen_k), hq, hkv,
+                                                  head_dim, int(window), int(num_splits))
 
 
 def sinkattn_decode_workspace_size(batch, max_seqlen_k, hq, hkv, head_dim=64, window=0,
@@ -124,8 +126,8 @@ def sinkattn_decode_workspace_size(batch, max_seqlen_k, hq, hkv, head_dim=64, wi
 
 
 def sinkattn_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *,
-                     sinks=None, causal=True, window=0, scale=None, out=None, lse=None,
-                     return_lse=True, workspace=None, total_q=None, total_k=None,
+                     sinks=None, causal=True, window=0, scale=None, num_splits=0, out=None,
+                     lse=None, return_lse=True, workspace=None, total_q=None, total_k=None,
                      stream=None):
     """Sink-attention prefill over packed sequences. Returns (out, lse)."""
     lib = load()
@@ -143,29 +145,34 @@ def sinkattn_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     if sinks is not None:
         _req(sinks, torch.float32, "sinks")
     tk_ = tk if total_k is None else total_k
+    tq_ = tq if total_q is None else total_q
+    batch = cu_seqlens_q.numel() - 1
     if workspace is None:
-        need = lib.sinkattn_prefill_workspace_size(cu_seqlens_q.numel() - 1,
-                                                   tq if total_q is None else total_q, tk_, hkv, d)
+        need = lib.sinkattn_prefill_workspace_size(batch, tq_, tk_, int(max_seqlen_q),
+                                                   int(max_seqlen_k), hq, hkv, d, int(window),
+                                                   int(num_splits))
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     mask = Mask(1 if causal else 0, int(window), float(d ** -0.5 if scale is None else scale))
     st = lib.sinkattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                              cu_seqlens_q.numel() - 1, tq if total_q is None else total_q,
-                              tk_, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
-                              _ptr(sinks), mask, _ptr(out), _ptr(lse), _ptr(workspace),
-                              workspace.numel(), _stream(stream))
+                              batch, tq_, tk_, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
+                              _ptr(sinks), mask, int(num_splits), _ptr(out), _ptr(lse),
+                              _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "sinkattn_prefill")
     return out, lse
 
 
-def sinkattn_prefill_paged_workspace_size(batch, total_q, max_seqlen_k, hkv, head_dim=64):
+def sinkattn_prefill_paged_workspace_size(batch, total_q, max_seqlen_q, max_seqlen_k, hq, hkv,
+                                          head_dim=64, window=0, num_splits=0):
     return load().sinkattn_prefill_paged_workspace_size(int(batch), int(total_q),
-                                                        int(max_seqlen_k), hkv, head_dim)
+                                                        int(max_seqlen_q), int(max_seqlen_k), hq,
+                                                        hkv, head_dim, int(window),
+                                                        int(num_splits))
 
 
 def sinkattn_prefill_paged(q, cu_seqlens_q, k_cache, v_cache, block_table, seqlens_k,
                            max_seqlen_q, max_seqlen_k, *, sinks=None, causal=True, window=0,
-                           scale=None, out=None, lse=None, return_lse=True, workspace=None,
-                           stream=None):
+                           scale=None, num_splits=0, out=None, lse=None, return_lse=True,
+                           workspace=None, stream=None):
     """Sink-attention prefill of packed queries against a paged KV cache
     [num_pages, hkv, page_size, 64] addressed by block_table / seqlens_k.
     Returns (out, lse)."""
@@ -186,15 +193,17 @@ def sinkattn_prefill_paged(q, cu_seqlens_q, k_cache, v_cache, block_table, seqle
     if sinks is not None:
         _req(sinks, torch.float32, "sinks")
     if workspace is None:
-        need = lib.sinkattn_prefill_paged_workspace_size(batch, tq, int(max_seqlen_k), hkv, d)
+        need = lib.sinkattn_prefill_paged_workspace_size(batch, tq, int(max_seqlen_q),
+                                                         int(max_seqlen_k), hq, hkv, d,
+                                                         int(window), int(num_splits))
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     mask = Mask(1 if causal else 0, int(window), float(d ** -0.5 if scale is None else scale))
     st = lib.sinkattn_prefill_paged(_ptr(q), _ptr(cu_seqlens_q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(block_table), _ptr(seqlens_k), num_pages,
                                     block_table.shape[1], page_size, batch, tq,
                                     int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
-                                    _ptr(sinks), mask, _ptr(out), _ptr(lse), _ptr(workspace),
-                                    workspace.numel(), _stream(stream))
+                                    _ptr(sinks), mask, int(num_splits), _ptr(out), _ptr(lse),
+                                    _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "sinkattn_prefill_paged")
     return out, lse
 

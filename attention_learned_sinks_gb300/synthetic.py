@@ -16,7 +16,9 @@ are not available here, so seeded normal values stand in for them):
                    randomly permuted block table, sinks ~N(0, 2), full or window 128
   chunked_prefill  4096 new query tokens at positions 126976..131071 of a
                    131072-token causal context
-  paged_chunked_prefill  the same, with K/V in 16-token pages and a randomly
+  long_context_prefill   256 new query tokens at the end of a 131072-token
+                   causal context (few query tiles: the split-KV case)
+  paged_chunked_prefill  the same as chunked_prefill, with K/V in 16-token pages and a randomly
                    permuted block table
   paged_prefill_batch    16 sequences, new chunks uniform in [256, 2048] after
                    cached contexts uniform in [1024, 32768], 16-token pages
@@ -273,6 +275,11 @@ def chunked_prefill(device="cpu", lq=4096, lk=131072) -> PrefillCase:
                         causal=True, device=device)
 
 
+def long_context_prefill(device="cpu", lq=256, lk=131072) -> PrefillCase:
+    return make_prefill("long_context_prefill", [lq], [lk], 64, 8, seed=8, causal=True,
+                        device=device)
+
+
 def paged_chunked_prefill(device="cpu", lq=4096, lk=131072) -> PrefillCase:
     return make_prefill_paged("paged_chunked_prefill", [lq], [lk], 64, 8, seed=6,
                               causal=True, device=device)
@@ -292,6 +299,7 @@ WORKLOADS = {
     "varlen_prefill": varlen_prefill,
     "paged_decode": paged_decode,
     "chunked_prefill": chunked_prefill,
+    "long_context_prefill": long_context_prefill,
     "paged_chunked_prefill": paged_chunked_prefill,
     "paged_prefill_batch": paged_prefill_batch,
 }

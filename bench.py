@@ -15,7 +15,8 @@ sequences, lengths uniform in [512, 4096], causal; full and window 128) and
 uniform in [1024, 32768], 16-token pages; full and window 128) in GB/s, and
 prefill against a 16-token paged cache (the chunked workload above, and 16
 sequences with new chunks of 256..2048 tokens after 1k..32k cached ones) in
-TFLOP/s.
+TFLOP/s, and 256 queries over a 131072-token context with the automatic
+split-KV plan and without splits.
 
 --impl reference times the float64 CPU oracle instead, on the same workload
 and metric, one sequence (all heads) per step.
@@ -433,20 +434,27 @@ def extras(sa, S, dev, stream, pk, pk_kind):
     def flush():
         flush_buf.zero_()
 
-    for name, mk in (("varlen_prefill", lambda: S.varlen_prefill(device="cuda")),
-                     ("varlen_prefill_w128", lambda: S.varlen_prefill(window=128, device="cuda")),
-                     ("chunked_prefill", lambda: S.chunked_prefill(device="cuda"))):
+    for name, mk, ns in (
+            ("varlen_prefill", lambda: S.varlen_prefill(device="cuda"), 0),
+            ("varlen_prefill_w128", lambda: S.varlen_prefill(window=128, device="cuda"), 0),
+            ("chunked_prefill", lambda: S.chunked_prefill(device="cuda"), 0),
+            ("long_context_prefill", lambda: S.long_context_prefill(device="cuda"), 0),
+            ("long_context_prefill_unsplit", lambda: S.long_context_prefill(device="cuda"), 1)):
         c = mk()
         cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
         sk = c.sinks.to(dev)
         out = torch.empty_like(c.q)
         lse = torch.empty((c.q.shape[0], c.hq), dtype=torch.float32, device=dev)
         ws = torch.empty(sa.sinkattn_prefill_workspace_size(c.batch, c.q.shape[0], c.k.shape[0],
-                                                            c.hkv), dtype=torch.uint8, device=dev)
+                                                            c.max_seqlen_q, c.max_seqlen_k, c.hq,
+                                                            c.hkv, window=c.window,
+                                                            num_splits=ns),
+                         dtype=torch.uint8, device=dev)
 
         def call():
             sa.sinkattn_prefill(c.q, c.k, c.v, cq, ck, c.max_seqlen_q, c.max_seqlen_k, sinks=sk,
-                                causal=c.causal, window=c.window, out=out, lse=lse, workspace=ws)
+                                causal=c.causal, window=c.window, num_splits=ns, out=out, lse=lse,
+                                workspace=ws)
         for _ in range(3):
             call()
         t = time_calls(call, 10, stream, flush)
@@ -455,7 +463,7 @@ def extras(sa, S, dev, stream, pk, pk_kind):
         res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3, "tokens_per_s": tokens / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,
                      "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)",
-                     "flops": fl, "launches_per_call": 3}
+                     "flops": fl, "num_splits": "auto" if ns == 0 else ns}
         del c, out, lse, ws
         torch.cuda.empty_cache()
 
@@ -469,7 +477,8 @@ def extras(sa, S, dev, stream, pk, pk_kind):
         out = torch.empty_like(c.q)
         lse = torch.empty((c.q.shape[0], c.hq), dtype=torch.float32, device=dev)
         ws = torch.empty(sa.sinkattn_prefill_paged_workspace_size(c.batch, c.q.shape[0],
-                                                                  c.max_seqlen_k, c.hkv),
+                                                                  c.max_seqlen_q, c.max_seqlen_k,
+                                                                  c.hq, c.hkv, window=c.window),
                          dtype=torch.uint8, device=dev)
 
         def call():
@@ -485,7 +494,7 @@ def extras(sa, S, dev, stream, pk, pk_kind):
                      "tokens_per_s": sum(c.seqlens_q) / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,
                      "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)",
-                     "flops": fl, "kv_bytes": kv, "launches_per_call": 4}
+                     "flops": fl, "kv_bytes": kv}
         del c, out, lse, ws
         torch.cuda.empty_cache()
 

@@ -84,25 +84,37 @@ const char *sinkattn_status_string(sinkattn_status_t status);
  *   max_seqlen_q, max_seqlen_k  host upper bounds on any sequence's length
  *            (grid sizing only; a smaller bound silently drops rows).
  *   sinks    float32 [hq] or NULL.
+ *   num_splits     key-range splits (section "Kernels for GPT-OSS / Sink
+ *            Attention": the KV sequence split into blocks, the sink in one
+ *            block only). 1 = none; n > 1 = every (query tile, head) item is
+ *            cut into n key ranges, each writing a normalised partial output
+ *            and lse (the first range alone starting from the sink), which a
+ *            log-sum-exp merge then combines; at most 64. 0 = automatic: splits
+ *            only when the call has too few (query tile, head) items to fill
+ *            the GPU's SMs and long key ranges (e.g. a few hundred new tokens
+ *            over a long context); the choice depends on the current device's
+ *            SM count.
  *   out      bf16 [total_q, hq, 64];   lse  float32 [total_q, hq] or NULL.
  *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
- *            sinkattn_prefill_workspace_size(batch, total_q, total_k, hkv,
- *            head_dim) bytes; contents need not be initialised. It receives
- *            an fp16 copy of v for the P.V product (values of magnitude above
- *            65504 are clamped to +-65504 there) and the list of query tiles
- *            that the persistent kernel works through, longest first.
+ *            sinkattn_prefill_workspace_size() bytes for the same arguments;
+ *            contents need not be initialised. It receives an fp16 copy of v
+ *            for the P.V product (values of magnitude above 65504 are clamped
+ *            to +-65504 there), the list of query tiles that the persistent
+ *            kernel works through, longest first, and with splits the fp32
+ *            partials (splits * total_q * hq * 260 bytes).
  * A sequence with Lq_b > Lk_b is allowed: its first Lq_b - Lk_b queries see no
  * key under a causal mask.
  */
-size_t sinkattn_prefill_workspace_size(int batch, int64_t total_q, int64_t total_k, int hkv,
-                                       int head_dim);
+size_t sinkattn_prefill_workspace_size(int batch, int64_t total_q, int64_t total_k,
+                                       int max_seqlen_q, int max_seqlen_k, int hq, int hkv,
+                                       int head_dim, int window, int num_splits);
 
 sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
                                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                    int batch, int64_t total_q, int64_t total_k,
                                    int max_seqlen_q, int max_seqlen_k, int hq, int hkv,
                                    int head_dim, const float *sinks, sinkattn_mask_t mask,
-                                   void *out, float *lse, void *workspace,
+                                   int num_splits, void *out, float *lse, void *workspace,
                                    size_t workspace_bytes, void *stream);
 
 /*
@@ -124,20 +136,22 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
  *   max_seqlen_q  host upper bound on Lq_b (grid sizing).
  *   max_seqlen_k  host upper bound on Lk_b; must not exceed
  *            max_pages_per_seq * page_size. It sizes the workspace.
+ *   num_splits    as for sinkattn_prefill.
  *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
- *            sinkattn_prefill_paged_workspace_size(batch, total_q,
- *            max_seqlen_k, hkv, head_dim) bytes (about
- *            batch * max_seqlen_k * hkv * 256 bytes); contents need not be
- *            initialised. The call first gathers every sequence's pages into
- *            contiguous rows there (K as bf16, V as fp16 for the P.V product,
- *            clamped to +-65504), then runs the prefill kernel on them.
+ *            sinkattn_prefill_paged_workspace_size() bytes for the same
+ *            arguments (about batch * max_seqlen_k * hkv * 256 bytes, plus
+ *            the split partials); contents need not be initialised. The call
+ *            first gathers every sequence's pages into contiguous rows there
+ *            (K as bf16, V as fp16 for the P.V product, clamped to +-65504),
+ *            then runs the prefill kernel on them.
  * A block-table entry outside [0, num_pages) or an Lk_b outside
  * [0, max_seqlen_k] is not read through: the key row is staged as zeros, or
  * the length clamped, and the device error word (sinkattn_get_device_error)
  * records code 2 or 3.
  */
-size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max_seqlen_k,
-                                             int hkv, int head_dim);
+size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max_seqlen_q,
+                                             int max_seqlen_k, int hq, int hkv, int head_dim,
+                                             int window, int num_splits);
 
 sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q,
                                          const void *k_cache, const void *v_cache,
@@ -145,9 +159,9 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
                                          int num_pages, int max_pages_per_seq, int page_size,
                                          int batch, int64_t total_q, int max_seqlen_q,
                                          int max_seqlen_k, int hq, int hkv, int head_dim,
-                                         const float *sinks, sinkattn_mask_t mask, void *out,
-                                         float *lse, void *workspace, size_t workspace_bytes,
-                                         void *stream);
+                                         const float *sinks, sinkattn_mask_t mask,
+                                         int num_splits, void *out, float *lse, void *workspace,
+                                         size_t workspace_bytes, void *stream);
 
 /*
  * Decode: one query token per sequence over a KV cache, split along the KV

@@ -45,11 +45,12 @@ M = B.Mask(1, 0, 0.125)
 
 def prefill(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, cuq=FAKE, cuk=FAKE, batch=2, tq=10, tk=10, mq=5, mk=5,
-             hq=8, hkv=2, d=64, sinks=None, mask=M, out=FAKE, lse=None)
+             hq=8, hkv=2, d=64, sinks=None, mask=M, ns=0, out=FAKE, lse=None)
     a.update(kw)
     return lib.sinkattn_prefill(a["q"], a["k"], a["v"], a["cuq"], a["cuk"], a["batch"], a["tq"],
                                 a["tk"], a["mq"], a["mk"], a["hq"], a["hkv"], a["d"], a["sinks"],
-                                a["mask"], a["out"], a["lse"], a.get("ws"), a.get("wsb", 0), None)
+                                a["mask"], a["ns"], a["out"], a["lse"], a.get("ws"),
+                                a.get("wsb", 0), None)
 
 
 def decode(lib, **kw):
@@ -73,7 +74,8 @@ def test_prefill_rejects_bad_arguments(lib):
     assert prefill(lib, q=None) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill(lib, out=ctypes.c_void_p((1 << 20) + 2)) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill(lib, batch=-1) == B.SINKATTN_ERR_INVALID_ARGUMENT
-    need = lib.sinkattn_prefill_workspace_size(2, 10, 10, 2, 64)
+    assert prefill(lib, ns=-1) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    need = lib.sinkattn_prefill_workspace_size(2, 10, 10, 5, 5, 8, 2, 64, 0, 0)
     assert need >= 10 * 2 * 64 * 2
     assert prefill(lib) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
     assert prefill(lib, ws=FAKE, wsb=need - 1) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
@@ -86,14 +88,14 @@ def test_prefill_rejects_bad_arguments(lib):
 
 def prefill_paged(lib, **kw):
     a = dict(q=FAKE, cuq=FAKE, k=FAKE, v=FAKE, table=FAKE, seqlens=FAKE, npages=8, maxp=4,
-             page=16, batch=2, tq=10, mq=5, mk=64, hq=8, hkv=2, d=64, sinks=None, mask=M,
+             page=16, batch=2, tq=10, mq=5, mk=64, hq=8, hkv=2, d=64, sinks=None, mask=M, ns=0,
              out=FAKE, lse=None)
     a.update(kw)
     return lib.sinkattn_prefill_paged(a["q"], a["cuq"], a["k"], a["v"], a["table"], a["seqlens"],
                                       a["npages"], a["maxp"], a["page"], a["batch"], a["tq"],
                                       a["mq"], a["mk"], a["hq"], a["hkv"], a["d"], a["sinks"],
-                                      a["mask"], a["out"], a["lse"], a.get("ws"), a.get("wsb", 0),
-                                      None)
+                                      a["mask"], a["ns"], a["out"], a["lse"], a.get("ws"),
+                                      a.get("wsb", 0), None)
 
 
 def test_prefill_paged_rejects_bad_arguments(lib):
@@ -107,7 +109,8 @@ def test_prefill_paged_rejects_bad_arguments(lib):
     assert prefill_paged(lib, npages=0) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill_paged(lib, k=ctypes.c_void_p((1 << 20) + 8)) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill_paged(lib, mask=B.Mask(0, -3, 0.1)) == B.SINKATTN_ERR_INVALID_ARGUMENT
-    need = lib.sinkattn_prefill_paged_workspace_size(2, 10, 64, 2, 64)
+    assert prefill_paged(lib, ns=-2) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    need = lib.sinkattn_prefill_paged_workspace_size(2, 10, 5, 64, 8, 2, 64, 0, 0)
     # K and V staging for batch * max_seqlen_k rows plus a 128-row tail
     assert need >= 2 * (2 * 64 + 128) * 2 * 64 * 2
     assert prefill_paged(lib) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
@@ -116,8 +119,8 @@ def test_prefill_paged_rejects_bad_arguments(lib):
         B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill_paged(lib, batch=0) == B.SINKATTN_OK
     assert prefill_paged(lib, tq=0) == B.SINKATTN_OK
-    assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 64, 2, 96) == 0
-    assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 128, 2, 64) > need
+    assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 5, 64, 8, 2, 96, 0, 0) == 0
+    assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 5, 128, 8, 2, 64, 0, 0) > need
 
 
 def test_decode_rejects_bad_arguments(lib):
@@ -154,8 +157,21 @@ def test_workspace_sizes_follow_the_split_plan(lib):
     assert ws(64, 8192, ns=2) < ws(64, 8192, ns=16)
     assert ws(64, 8192, w=128) < ws(64, 8192)               # window: one block
     assert lib.sinkattn_decode_workspace_size(0, 10, 8, 2, 64, 0, 0) == 0
-    assert lib.sinkattn_prefill_workspace_size(3, 1000, 1000, 8, 64) >= 1000 * 8 * 64 * 2 + 256
-    assert lib.sinkattn_prefill_workspace_size(3, 1000, 1000, 8, 128) == 0
+    pws = lambda *a: lib.sinkattn_prefill_workspace_size(*a)
+    assert pws(3, 1000, 1000, 500, 500, 64, 8, 64, 0, 1) >= 1000 * 8 * 64 * 2 + 256
+    assert pws(3, 1000, 1000, 500, 500, 64, 8, 128, 0, 1) == 0
+    assert pws(3, 1000, 1000, 500, 500, 64, 8, 64, -1, 0) == 0
+    # explicit splits add fp32 partials: splits * total_q * hq * (64 + 1) * 4 bytes
+    one = pws(3, 1000, 1000, 500, 500, 64, 8, 64, 0, 1)
+    assert pws(3, 1000, 1000, 500, 500, 64, 8, 64, 0, 4) >= one + 4 * 1000 * 64 * 260
+    # automatic: a few hundred queries over a long context are split ...
+    long_ctx = pws(1, 256, 131072, 256, 131072, 64, 8, 64, 0, 0)
+    assert long_ctx > pws(1, 256, 131072, 256, 131072, 64, 8, 64, 0, 1)
+    # ... many query tiles or short contexts are not
+    assert pws(1, 4096, 131072, 4096, 131072, 64, 8, 64, 0, 0) == \
+        pws(1, 4096, 131072, 4096, 131072, 64, 8, 64, 0, 1)
+    assert pws(1, 256, 2048, 256, 2048, 64, 8, 64, 0, 0) == \
+        pws(1, 256, 2048, 256, 2048, 64, 8, 64, 0, 1)
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

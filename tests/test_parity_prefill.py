@@ -10,12 +10,12 @@ from helpers import check_close, cuda
 pytestmark = pytest.mark.gpu
 
 
-def run_prefill(c, device_tensors=False):
+def run_prefill(c, device_tensors=False, num_splits=0):
     t = (lambda x: x) if device_tensors else cuda
     return sa.sinkattn_prefill(t(c.q), t(c.k), t(c.v), c.cu_seqlens_q.cuda(),
                                c.cu_seqlens_k.cuda(), c.max_seqlen_q, c.max_seqlen_k,
                                sinks=cuda(c.sinks), causal=c.causal, window=c.window,
-                               scale=c.scale)
+                               scale=c.scale, num_splits=num_splits)
 
 
 def oracle_prefill(oracle, c):
@@ -89,6 +89,49 @@ def test_prefill_large_sink(oracle_lib):
     check_close(out, lse, ro, rl, "large sink")
 
 
+# split-KV: every (query tile, heads) item cut into n key ranges, merged by
+# log-sum-exp, the sink counted in the first range only
+SPLIT_SHAPES = [
+    ([129], [129]),
+    ([200], [1500]),
+    ([300, 17, 256, 1], [300, 900, 256, 40]),
+    ([130], [40]),
+    ([0, 64, 0], [0, 64, 5]),
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=[str(i) for i in range(len(SPLIT_SHAPES))])
+@pytest.mark.parametrize("num_splits", [2, 3, 7, 64])
+@pytest.mark.parametrize("causal,window", [(True, 0), (False, 0), (True, 200)])
+def test_prefill_explicit_splits(oracle_lib, shape, num_splits, causal, window):
+    lq, lk = shape
+    c = S.make_prefill("split", lq, lk, 8, 2, seed=101 + sum(lk) + num_splits, causal=causal,
+                       window=window, sink_std=1.5)
+    out, lse = run_prefill(c, num_splits=num_splits)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "prefill %s splits=%d causal=%s w=%d"
+                % (shape, num_splits, causal, window))
+
+
+@pytest.mark.parametrize("with_sinks", [True, False])
+def test_prefill_splits_sink_counted_once(oracle_lib, with_sinks):
+    """Large sinks make a double-counted (or dropped) sink visible at once."""
+    c = S.make_prefill("split_sink", [300], [2000], 4, 1, seed=103, with_sinks=with_sinks)
+    if with_sinks:
+        c.sinks = torch.tensor([9.0, -30.0, 0.0, 4.0])
+    out, lse = run_prefill(c, num_splits=5)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "split sink once (sinks=%s)" % with_sinks)
+
+
+def test_prefill_splits_odd_group(oracle_lib):
+    """Groups of 3 query heads per KV head run one head per item."""
+    c = S.make_prefill("split_odd", [250, 90], [1300, 600], 12, 4, seed=105)
+    out, lse = run_prefill(c, num_splits=6)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "split odd group")
+
+
 def _sample_rows(c, per_seq, seed):
     g = torch.Generator().manual_seed(seed)
     rows = []
@@ -121,6 +164,28 @@ def test_prefill_varlen_full_config(oracle_lib, window):
     out, lse = run_prefill(c)
     torch.cuda.synchronize()
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 24, 71), "varlen_prefill w=%d" % window)
+
+
+def test_prefill_long_context_auto_splits(oracle_lib):
+    """256 queries at the end of a 131072-token context: too few query tiles to
+    fill the SMs, so the automatic plan splits the keys. Sampled rows against
+    the oracle, and the whole output against the unsplit call."""
+    c = S.long_context_prefill()
+    ws_auto = sa.sinkattn_prefill_workspace_size(1, 256, 131072, 256, 131072, 64, 8)
+    ws_one = sa.sinkattn_prefill_workspace_size(1, 256, 131072, 256, 131072, 64, 8,
+                                                num_splits=1)
+    assert ws_auto > ws_one  # the plan did split
+    q, k, v = c.q.cuda(), c.k.cuda(), c.v.cuda()
+    args = (q, k, v, c.cu_seqlens_q.cuda(), c.cu_seqlens_k.cuda(), 256, 131072)
+    out, lse = sa.sinkattn_prefill(*args, sinks=c.sinks.cuda())
+    torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 60, 107), "long_context_prefill")
+    o1, l1 = sa.sinkattn_prefill(*args, sinks=c.sinks.cuda(), num_splits=1)
+    # both are within the oracle's tolerance; between them, bf16 rounding only
+    d = (out.float() - o1.float()).abs()
+    assert float(d.max()) <= 2e-2
+    assert float(d.sum() / o1.float().abs().sum()) <= 2e-3
+    assert float((lse - l1).abs().max()) <= 1e-3
 
 
 def test_prefill_chunked_full_config(oracle_lib):
