@@ -14,6 +14,8 @@ from .sinkattn import (  # noqa: F401
     sinkattn_merge,
     sinkattn_decode_noalloc,
     sinkattn_prefill,
+    sinkattn_prefill_backward,
+    sinkattn_prefill_backward_workspace_size,
     sinkattn_prefill_paged,
     sinkattn_prefill_paged_workspace_size,
     sinkattn_prefill_workspace_size,

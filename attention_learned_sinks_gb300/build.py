@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsinkattn.so")
-SOURCES = ["abi.cu", "decode.cu", "merge.cu", "prefill.cu"]
+SOURCES = ["abi.cu", "backward.cu", "decode.cu", "merge.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -266,10 +266,79 @@ sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_ls
                                 static_cast<cudaStream_t>(stream)));
 }
 
+size_t sinkattn_prefill_backward_workspace_size(int batch, int64_t total_q, int64_t total_k,
+                                                int hq, int hkv, int head_dim) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 ||
+      head_dim != kHeadDim)
+    return 0;
+  return backward_workspace_bytes(batch, total_q, total_k, hq, hkv);
+}
+
+sinkattn_status_t sinkattn_prefill_backward(
+    const void *q, const void *k, const void *v, const void *out, const void *dout,
+    const float *lse, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int batch,
+    int64_t total_q, int64_t total_k, int max_seqlen_q, int max_seqlen_k, int hq, int hkv,
+    int head_dim, const float *sinks, sinkattn_mask_t mask, void *dq, void *dk, void *dv,
+    float *dsinks, void *workspace, size_t workspace_bytes, void *stream) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 ||
+      hkv <= 0 || hq % hkv != 0 || !mask_ok(mask))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (batch == 0 || (total_q == 0 && total_k == 0)) return SINKATTN_OK;
+  if (!q || !k || !v || !out || !dout || !lse || !cu_seqlens_q || !cu_seqlens_k || !dq || !dk ||
+      !dv)
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) ||
+      (sinks && !aligned(sinks, 4)) || (dsinks && !aligned(dsinks, 4)))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (batch > 65535 || total_q > INT32_MAX || total_k > INT32_MAX ||
+      (max_seqlen_q + 127) / 128 > 65535 || (max_seqlen_k + 127) / 128 > 65535 ||
+      (total_q / 128 + batch) * hq > INT32_MAX || (total_k / 128 + batch) * hkv > INT32_MAX)
+    return SINKATTN_ERR_UNSUPPORTED;
+  const size_t need = backward_workspace_bytes(batch, total_q, total_k, hq, hkv);
+  if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
+  BackwardLaunch a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.sinks = sinks;
+  a.causal = mask.causal != 0;
+  a.window = mask.window;
+  a.scale = mask.scale;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dsinks = dsinks;
+  a.workspace = workspace;
+  bool encode_failed = false;
+  cudaError_t e = launch_backward(a, static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return SINKATTN_ERR_CUDA;
+  return from_cuda(e);
+}
+
 sinkattn_status_t sinkattn_get_device_error(void *stream, int *code) {
   if (code == nullptr) return SINKATTN_ERR_INVALID_ARGUMENT;
   *code = 0;
-  return from_cuda(prefill_read_error(static_cast<cudaStream_t>(stream), code));
+  int other = 0;
+  cudaError_t e = prefill_read_error(static_cast<cudaStream_t>(stream), code);
+  if (e == cudaSuccess) e = backward_read_error(static_cast<cudaStream_t>(stream), &other);
+  if (*code == 0) *code = other;
+  return from_cuda(e);
 }
 
 }  // extern "C"

@@ -1,0 +1,811 @@
+// Backward pass of sink attention over packed variable-length sequences.
+//
+// The pages give the forward only (page "GPT-OSS on day 0", sections
+// "Attention: GQA with Attention Sinks" and "Kernels for GPT-OSS / Sink
+// Attention": one learned logit per head inside the softmax denominator, no
+// value row). Its gradients, for row i of head h with P_j = e^{s_j - lse_i}
+// (lse includes the sink) and P_c = e^{c_h - lse_i}:
+//
+//   D_i  = dO_i . O_i            dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - D_i)
+//   dq_i = scale sum_j dS_ij k_j     dk_j = scale sum_i dS_ij q_i
+//   dv_j = sum_i P_ij dO_i           dc_h = -sum_i P_c,i D_i
+//
+// dk and dv of a KV head sum over its query heads. Launches, in order:
+//  1. bwd_prep_q_kernel: fp16 copies of q and dO, D from the bf16 forward
+//     output and lse in log2 units (head-major, so one tile's rows of one
+//     head are contiguous);
+//  2. bwd_prep_kv_kernel: fp16 copies of k and v;
+//  3. two tile lists (query tiles, key tiles);
+//  4. bwd_dq_kernel: one CTA per (query tile, head); per key tile S = Q K^T
+//     and dP = dO V^T on tcgen05 into TMEM, P and dS in registers, dQ += dS K
+//     (dS as the TMEM A operand) and Y += P K; it also forms the exact
+//     D = sum_j P_j dP_j and corrects dQ with it;
+//  5. bwd_dsink_kernel: dc_h, one block per head, fixed summation order;
+//  6. bwd_dkdv_kernel: one CTA per (key tile, KV head); per (query head,
+//     query tile) S^T = K Q^T and dP^T = V dO^T, P^T and dS^T in registers,
+//     dV += P^T dO and dK += dS^T Q with P^T / dS^T as TMEM A operands.
+// Every gradient element is written by exactly one CTA (no atomics), so the
+// results are deterministic. All MMA operands are fp16 (bf16 inputs convert
+// exactly except below 2^-14, and P, dS in fp16 keep 11 significant bits);
+// accumulation is fp32. Every mbarrier wait is bounded.
+#include <math.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace sinkattn {
+namespace {
+
+constexpr int kBM = 128;                        // query rows per tile
+constexpr int kBN = 128;                        // keys per tile
+constexpr int kTileBytes = 128 * kHeadDim * 2;  // 16 KB
+constexpr int kStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+// Dynamic shared memory requested by the two MMA kernels: more than half of
+// the SM's, so one CTA per SM holds all 512 TMEM columns without contention.
+constexpr int kSmemRequest = 120 * 1024;
+
+// ss: both operands K-major in shared memory (S = Q K^T, dP = dO V^T, ...);
+// ts: A from TMEM, B MN-major in shared memory (dQ += dS K, ...). fp16 inputs.
+constexpr uint32_t kIdescSS = idesc_f32acc(128, 128, /*bf16=*/false, false, false);
+constexpr uint32_t kIdescTS = idesc_f32acc(128, kHeadDim, /*bf16=*/false, false, true);
+constexpr uint64_t kTileDesc = kTileBytes >> 4;        // one tile in descriptor units
+constexpr uint64_t kRows16Desc = (16 * 128) >> 4;      // 16 rows of 128 B
+
+__device__ int g_backward_error;
+
+struct BwdParams {
+  const int32_t *cu_q, *cu_k;
+  int batch, hq, hkv, group, causal, window;
+  int total_q;
+  float scale, scale_log2;
+  const float *lse2t;  // [hq][total_q]: lse * log2(e) (+inf: row with no key and no sink)
+  float *dt;           // [hq][total_q]: D, from the forward output, then exact (dQ kernel)
+  const unsigned *q_pairs, *k_pairs;
+  const int *num_q_pairs, *num_k_pairs;
+  __nv_bfloat16 *dq, *dk, *dv;
+};
+
+// ----------------------------------------------------------------- prep ---
+// Thread = 8 consecutive elements of one (row, head). Every iteration of the
+// block loop is uniform across the block, so the 8-lane shuffles always see
+// full warps.
+__global__ void __launch_bounds__(256) bwd_prep_q_kernel(
+    const uint4 *__restrict__ q, const uint4 *__restrict__ dout, const uint4 *__restrict__ out,
+    const float *__restrict__ lse, int64_t total_q, int hq, uint4 *__restrict__ q16,
+    uint4 *__restrict__ do16, float *__restrict__ lse2t, float *__restrict__ dt) {
+  const int64_t n = total_q * hq * 8;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < n;
+       base += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = base + threadIdx.x;
+    float part = 0.f;
+    if (i < n) {
+      q16[i] = bf16x8_to_f16x8(q[i]);
+      const uint4 g = dout[i], o = out[i];
+      do16[i] = bf16x8_to_f16x8(g);
+      part = bf16_lo(g.x) * bf16_lo(o.x) + bf16_hi(g.x) * bf16_hi(o.x) +
+             bf16_lo(g.y) * bf16_lo(o.y) + bf16_hi(g.y) * bf16_hi(o.y) +
+             bf16_lo(g.z) * bf16_lo(o.z) + bf16_hi(g.z) * bf16_hi(o.z) +
+             bf16_lo(g.w) * bf16_lo(o.w) + bf16_hi(g.w) * bf16_hi(o.w);
+    }
+    part += __shfl_xor_sync(0xffffffffu, part, 4);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    if (i < n && (i & 7) == 0) {
+      const int64_t rh = i >> 3;
+      const int64_t row = rh / hq;
+      const int h = static_cast<int>(rh % hq);
+      const float l = lse[rh];
+      lse2t[h * total_q + row] = l == -INFINITY ? INFINITY : l * kLog2e;
+      dt[h * total_q + row] = part;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) bwd_prep_kv_kernel(const uint4 *__restrict__ k,
+                                                          const uint4 *__restrict__ v,
+                                                          uint4 *__restrict__ k16,
+                                                          uint4 *__restrict__ v16, int64_t n8) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    k16[i] = bf16x8_to_f16x8(k[i]);
+    v16[i] = bf16x8_to_f16x8(v[i]);
+  }
+}
+
+// dc_h = -sum_i e^{c_h - lse_i} D_i over every row of head h; double
+// accumulation in a fixed order (per-thread strides, then a fixed tree).
+__global__ void __launch_bounds__(256) bwd_dsink_kernel(const float *__restrict__ sinks,
+                                                        const float *__restrict__ lse2t,
+                                                        const float *__restrict__ dt,
+                                                        int64_t total_q, float *__restrict__ dsinks) {
+  __shared__ double part[256];
+  const int h = blockIdx.x;
+  const float c2 = sinks[h] * kLog2e;
+  double acc = 0.0;
+  for (int64_t r = threadIdx.x; r < total_q; r += blockDim.x) {
+    const float l2 = lse2t[h * total_q + r];
+    if (l2 != INFINITY) acc -= static_cast<double>(exp2f(c2 - l2)) * dt[h * total_q + r];
+  }
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) part[threadIdx.x] += part[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dsinks[h] = static_cast<float>(part[0]);
+}
+
+// 32 columns of scores s (raw q.k) and dP -> P = 2^(s c - l2) (0 outside the
+// visible range) and dS = P (dP - D), both packed as fp16 pairs. The per-row
+// variant (dQ) takes l2 and D as scalars and also sums P dP into acc; the
+// per-column one (dK/dV) takes them per column.
+__device__ __forceinline__ void p_ds_row(float (&s)[32], const float (&dp)[32], float c, float l2,
+                                         float d, uint32_t (&p16)[16], uint32_t (&ds16)[16],
+                                         float2 &acc) {
+  const float2 c2 = make_float2(c, c), nl = make_float2(-l2, -l2), nd = make_float2(-d, -d);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 a = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2, nl);
+    const float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+    const float2 x = make_float2(dp[2 * i], dp[2 * i + 1]);
+    const float2 ds = __fmul2_rn(p, __fadd2_rn(x, nd));
+    acc = __ffma2_rn(p, x, acc);
+    p16[i] = pack_f16x2(p.x, p.y);
+    ds16[i] = pack_f16x2(ds.x, ds.y);
+  }
+}
+
+__device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], float c,
+                                         const float *l2, const float *d, uint32_t (&p16)[16],
+                                         uint32_t (&ds16)[16]) {
+  const float2 c2 = make_float2(c, c);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 l = *reinterpret_cast<const float2 *>(l2 + 2 * i);
+    const float2 dd = *reinterpret_cast<const float2 *>(d + 2 * i);
+    const float2 a = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2,
+                                make_float2(-l.x, -l.y));
+    const float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+    const float2 g = __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]), make_float2(-dd.x, -dd.y));
+    const float2 ds = __fmul2_rn(p, g);
+    p16[i] = pack_f16x2(p.x, p.y);
+    ds16[i] = pack_f16x2(ds.x, ds.y);
+  }
+}
+
+// 64 fp32 TMEM columns (a row of dQ, dK or dV) times `mul` -> 64 bf16 in global.
+__device__ __forceinline__ void store_row64(uint32_t taddr, float mul, __nv_bfloat16 *dst,
+                                            bool write) {
+  uint32_t a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_wait_ld();
+  if (!write) return;
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float *x = reinterpret_cast<const float *>(&a[8 * i]);
+    d4[i] = make_uint4(pack_bf16x2(x[0] * mul, x[1] * mul), pack_bf16x2(x[2] * mul, x[3] * mul),
+                       pack_bf16x2(x[4] * mul, x[5] * mul), pack_bf16x2(x[6] * mul, x[7] * mul));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float *x = reinterpret_cast<const float *>(&b[8 * i]);
+    d4[4 + i] = make_uint4(pack_bf16x2(x[0] * mul, x[1] * mul), pack_bf16x2(x[2] * mul, x[3] * mul),
+                           pack_bf16x2(x[4] * mul, x[5] * mul), pack_bf16x2(x[6] * mul, x[7] * mul));
+  }
+}
+
+__device__ __forceinline__ void zero_row64(__nv_bfloat16 *dst) {
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d4[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ---------------------------------------------------------------- dQ -------
+// Warps 0-3: one query row per thread (TMEM lane); warp 4: TMA; warp 5: MMA
+// issue and TMEM owner. TMEM columns: S [0,128), dP [128,256), dS fp16
+// [256,320), P fp16 [320,384), dQ [384,448), Y [448,512). S and dP of the next
+// key tile are written only by MMAs issued after the previous tile's dQ / Y
+// MMAs, and dS / P only by the softmax warps after the commit that follows
+// them, so no MMA reads TMEM that a later write may clobber before it
+// completes.
+//
+// D from the bf16 forward output (D_a) carries the output's rounding, and
+// dP - D cancels when one key dominates a row. This kernel therefore also
+// sums the exact D_e = sum_j P_j dP_j (fp32) and Y = sum_j P_j k_j (one more
+// product), and corrects: dq = scale (sum_j P_j (dP_j - D_a) k_j
+// - (D_e - D_a) Y). The correction is small, so its own fp16 rounding does
+// not matter. D_e replaces D_a in the workspace for the dK/dV kernel and the
+// sink gradient, which run after this one.
+struct DqBars {
+  uint64_t qd_full;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full, ds_full, dq_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr int kDqOffQ = 0, kDqOffDo = kTileBytes, kDqOffK = 2 * kTileBytes,
+              kDqOffV = kDqOffK + kStages * kTileBytes, kDqOffBar = kDqOffV + kStages * kTileBytes;
+static_assert(kDqOffBar + 1024 + 1024 <= kSmemRequest, "dQ shared memory");
+
+__global__ void __launch_bounds__(192, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const BwdParams p) {
+  const int w = blockIdx.x;
+  if (w >= *p.num_q_pairs * p.hq) return;
+  const unsigned e = p.q_pairs[w / p.hq];
+  const int h = w % p.hq, g = h / p.group;
+  const int b = static_cast<int>(e >> 16), qt = static_cast<int>(e & 0xffffu);
+  const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
+  const int k0 = p.cu_k[b], lk = p.cu_k[b + 1] - k0;
+  const int rows = min(kBM, lq - qt * kBM);
+  const int p_min = lk - lq + qt * kBM, p_max = p_min + rows - 1;
+  int key_hi = lk, key_lo = 0;
+  if (p.causal) key_hi = min(key_hi, p_max + 1);
+  if (p.window > 0) key_lo = max(0, p_min - p.window + 1);
+  const int kt_lo = key_lo / kBN;
+  const int n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - kt_lo : 0;
+  const int r = threadIdx.x & 127;
+  const int warp = threadIdx.x >> 5;
+  __nv_bfloat16 *dq_row = p.dq + (static_cast<size_t>(q0 + qt * kBM + r) * p.hq + h) * kHeadDim;
+  const size_t lidx = static_cast<size_t>(h) * p.total_q + q0 + qt * kBM + r;
+  if (n == 0) {  // no row of this tile sees a key: dq = 0, D = 0
+    if (warp < 4 && r < rows) {
+      zero_row64(dq_row);
+      p.dt[lidx] = 0.f;
+    }
+    return;
+  }
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  DqBars *bars = reinterpret_cast<DqBars *>(smem_raw + (sbase - raw) + kDqOffBar);
+  volatile int *abort = &bars->abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->qd_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->ds_full, 128);
+    mbar_init(&bars->dq_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int *err = &g_backward_error;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    mbar_arrive_expect_tx_elect(&bars->qd_full, 2 * kTileBytes);
+    tma_load_3d_elect(sbase + kDqOffQ, &tm_q, &bars->qd_full, 0, h, q0 + qt * kBM);
+    tma_load_3d_elect(sbase + kDqOffDo, &tm_do, &bars->qd_full, 0, h, q0 + qt * kBM);
+    int j = 0;
+    for (; j < n; ++j) {
+      const int st = j % kStages;
+      if (j >= kStages &&
+          !mbar_wait_warp(&bars->kv_empty[st], ((j / kStages) - 1) & 1, abort, err))
+        break;
+      const int row = k0 + (kt_lo + j) * kBN;
+      mbar_arrive_expect_tx_elect(&bars->kv_full[st], 2 * kTileBytes);
+      tma_load_3d_elect(sbase + kDqOffK + st * kTileBytes, &tm_k, &bars->kv_full[st], 0, g, row);
+      tma_load_3d_elect(sbase + kDqOffV + st * kTileBytes, &tm_v, &bars->kv_full[st], 0, g, row);
+    }
+    if (*abort) {  // copies already issued still land here: wait for them (bounded)
+      mbar_wait_warp(&bars->qd_full, 0, abort, err, true);
+      for (int i = max(0, j - kStages); i < j; ++i)
+        mbar_wait_warp(&bars->kv_full[i % kStages], (i / kStages) & 1, abort, err, true);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA
+    const uint64_t qdesc = sdesc_sw128(sbase + kDqOffQ);
+    const uint64_t dodesc = sdesc_sw128(sbase + kDqOffDo);
+    const uint64_t kdesc0 = sdesc_sw128(sbase + kDqOffK);
+    const uint64_t vdesc0 = sdesc_sw128(sbase + kDqOffV);
+    const uint32_t t_s = tmem, t_dp = tmem + 128, t_ds = tmem + 256, t_p = tmem + 320;
+    const uint32_t t_dq = tmem + 384, t_y = tmem + 448;
+    bool ok = mbar_wait_warp(&bars->qd_full, 0, abort, err) &&
+              mbar_wait_warp(&bars->kv_full[0], 0, abort, err);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kHeadDim / 16; ++ks)
+        umma_ss_elect(t_s, qdesc + 2 * ks, kdesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < kHeadDim / 16; ++ks)
+        umma_ss_elect(t_dp, dodesc + 2 * ks, vdesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
+      umma_commit_elect(&bars->s_full);
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      if (!mbar_wait_warp(&bars->ds_full, j & 1, abort, err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int st = j % kStages;
+      const uint64_t kd = kdesc0 + st * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        umma_ts_elect(t_dq, t_ds + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        umma_ts_elect(t_y, t_p + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_elect(&bars->kv_empty[st]);
+      if (j + 1 < n) {
+        const int s1 = (j + 1) % kStages;
+        if (!mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kStages) & 1, abort, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          umma_ss_elect(t_s, qdesc + 2 * ks, kdesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
+                        ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          umma_ss_elect(t_dp, dodesc + 2 * ks, vdesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
+                        ks > 0 ? 1u : 0u);
+        umma_commit_elect(&bars->s_full);
+      }
+    }
+    if (ok) umma_commit_elect(&bars->dq_done);
+    // every MMA issued here has finished before TMEM is released
+    umma_commit_elect(&bars->drain);
+    mbar_wait_warp(&bars->drain, 0, abort, err, true);
+  } else {
+    // -------------------------------------------------- dS (one row / thread)
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = t_s + 128, t_ds = t_s + 256, t_p = t_s + 320;
+    const uint32_t t_dq = t_s + 384, t_y = t_s + 448;
+    const float l2 = r < rows ? p.lse2t[lidx] : INFINITY;
+    const float d = r < rows ? p.dt[lidx] : 0.f;
+    const int pos = p_min + r;
+    int hi = lk, lo = 0;
+    if (p.causal) hi = min(hi, pos + 1);
+    if (p.window > 0) lo = max(lo, pos - p.window + 1);
+    if (r >= rows) hi = lo = 0;
+    bool ok = true;
+    float2 dsum = make_float2(0.f, 0.f);  // sum_j P_j dP_j
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait_warp(&bars->s_full, j & 1, abort, err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int key0 = (kt_lo + j) * kBN;
+      const int c_lo = min(max(lo - key0, 0), kBN);
+      const int len = max(min(hi - key0, kBN) - c_lo, 0);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float s[32], dp[32];
+        tmem_ld32f(t_s + 32 * c, s);
+        tmem_ld32f(t_dp + 32 * c, dp);
+        tmem_wait_ld();
+        mask32(s, 32 * c, c_lo, len);
+        uint32_t p16[16], ds16[16];
+        p_ds_row(s, dp, p.scale_log2, l2, d, p16, ds16, dsum);
+        tmem_st16(t_ds + 16 * c, ds16);
+        tmem_st16(t_p + 16 * c, p16);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full);
+    }
+    if (ok && mbar_wait_warp(&bars->dq_done, 0, abort, err)) {
+      tc_fence_after();
+      const float d_e = dsum.x + dsum.y;
+      const float corr = d_e - d;
+      for (int half = 0; half < 2; ++half) {
+        float a[32], y[32];
+        tmem_ld32f(t_dq + 32 * half, a);
+        tmem_ld32f(t_y + 32 * half, y);
+        tmem_wait_ld();
+        if (r < rows) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dq_row) + 4 * half;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float o[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) o[t] = p.scale * fmaf(-corr, y[8 * i + t], a[8 * i + t]);
+            d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                               pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+          }
+        }
+      }
+      if (r < rows) p.dt[lidx] = d_e;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- dK / dV -----
+// Warps 0-3: one key row per thread (TMEM lane); warp 4: TMA and the per-
+// query-tile lse / D vectors; warp 5: MMA issue and TMEM owner. TMEM columns:
+// S^T [0,128), dP^T [128,256), P^T fp16 [256,320), dS^T fp16 [320,384),
+// dV [384,448), dK [448,512). Steps run over (query head of the group, query
+// tile that sees the key tile); Q, dO, lse and D are double-buffered.
+struct DkvBars {
+  uint64_t kv_full;
+  uint64_t qd_full[kStages], qd_empty[kStages];
+  uint64_t st_full, ew_done, done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr int kKvOffK = 0, kKvOffV = kTileBytes, kKvOffQ = 2 * kTileBytes,
+              kKvOffDo = kKvOffQ + kStages * kTileBytes,
+              kKvOffVec = kKvOffDo + kStages * kTileBytes,  // per stage: lse2[128], D[128]
+    kKvOffBar = kKvOffVec + kStages * 1024;
+static_assert(kKvOffBar + 1024 + 1024 <= kSmemRequest, "dK/dV shared memory");
+
+__global__ void __launch_bounds__(192, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
+  const int w = blockIdx.x;
+  const int npairs = *p.num_k_pairs;
+  if (w >= npairs * p.hkv) return;
+  // the list holds key tiles of higher index first; under a causal mask the
+  // low tiles have the most queries, so walk it backwards (longest first)
+  const unsigned e = p.k_pairs[npairs - 1 - w / p.hkv];
+  const int g = w % p.hkv;
+  const int b = static_cast<int>(e >> 16), kt = static_cast<int>(e & 0xffffu);
+  const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
+  const int k0 = p.cu_k[b], lk = p.cu_k[b + 1] - k0;
+  const int krows = min(kBN, lk - kt * kBN);
+  const int base = lk - lq;  // position of query 0
+  const int jmin = kt * kBN, jmax = jmin + krows - 1;
+  int iq_lo = 0, iq_hi = lq;  // queries that see at least one key of the tile
+  if (p.causal) iq_lo = max(0, jmin - base);
+  if (p.window > 0) iq_hi = min(iq_hi, jmax + p.window - base);
+  const int qt_lo = iq_lo / kBM;
+  const int nqt = iq_hi > iq_lo ? (iq_hi + kBM - 1) / kBM - qt_lo : 0;
+  const int steps = nqt * p.group;
+  const int r = threadIdx.x & 127;
+  const int warp = threadIdx.x >> 5;
+  const size_t krow = (static_cast<size_t>(k0 + kt * kBN + r) * p.hkv + g) * kHeadDim;
+  if (steps == 0) {  // no query sees this key tile
+    if (warp < 4 && r < krows) {
+      zero_row64(p.dk + krow);
+      zero_row64(p.dv + krow);
+    }
+    return;
+  }
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (sbase - raw);
+  DkvBars *bars = reinterpret_cast<DkvBars *>(smem + kKvOffBar);
+  volatile int *abort = &bars->abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->qd_full[s], 1);
+      mbar_init(&bars->qd_empty[s], 1);
+    }
+    mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->ew_done, 128);
+    mbar_init(&bars->done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int *err = &g_backward_error;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    const int lane = threadIdx.x & 31;
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    mbar_arrive_expect_tx_elect(&bars->kv_full, 2 * kTileBytes);
+    tma_load_3d_elect(sbase + kKvOffK, &tm_k, &bars->kv_full, 0, g, k0 + kt * kBN);
+    tma_load_3d_elect(sbase + kKvOffV, &tm_v, &bars->kv_full, 0, g, k0 + kt * kBN);
+    int s = 0;
+    for (; s < steps; ++s) {
+      const int st = s % kStages;
+      const int h = g * p.group + s / nqt, qt = qt_lo + s % nqt;
+      if (s >= kStages &&
+          !mbar_wait_warp(&bars->qd_empty[st], ((s / kStages) - 1) & 1, abort, err))
+        break;
+      // lse2 / D of the tile's 128 query rows (rows past the sequence: empty)
+      float *vec = reinterpret_cast<float *>(smem + kKvOffVec + st * 1024);
+      const int valid = lq - qt * kBM;
+      const size_t at = static_cast<size_t>(h) * p.total_q + q0 + qt * kBM;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = lane + 32 * i;
+        vec[row] = row < valid ? p.lse2t[at + row] : INFINITY;
+        vec[128 + row] = row < valid ? p.dt[at + row] : 0.f;
+      }
+      __syncwarp();
+      mbar_arrive_expect_tx_elect(&bars->qd_full[st], 2 * kTileBytes);
+      tma_load_3d_elect(sbase + kKvOffQ + st * kTileBytes, &tm_q, &bars->qd_full[st], 0, h,
+                        q0 + qt * kBM);
+      tma_load_3d_elect(sbase + kKvOffDo + st * kTileBytes, &tm_do, &bars->qd_full[st], 0, h,
+                        q0 + qt * kBM);
+    }
+    if (*abort) {
+      mbar_wait_warp(&bars->kv_full, 0, abort, err, true);
+      for (int i = max(0, s - kStages); i < s; ++i)
+        mbar_wait_warp(&bars->qd_full[i % kStages], (i / kStages) & 1, abort, err, true);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA
+    const uint64_t kdesc = sdesc_sw128(sbase + kKvOffK);
+    const uint64_t vdesc = sdesc_sw128(sbase + kKvOffV);
+    const uint64_t qdesc0 = sdesc_sw128(sbase + kKvOffQ);
+    const uint64_t dodesc0 = sdesc_sw128(sbase + kKvOffDo);
+    const uint32_t t_st = tmem, t_dpt = tmem + 128, t_pt = tmem + 256, t_dst = tmem + 320;
+    const uint32_t t_dv = tmem + 384, t_dk = tmem + 448;
+    bool ok = mbar_wait_warp(&bars->kv_full, 0, abort, err) &&
+              mbar_wait_warp(&bars->qd_full[0], 0, abort, err);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kHeadDim / 16; ++ks)
+        umma_ss_elect(t_st, kdesc + 2 * ks, qdesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < kHeadDim / 16; ++ks)
+        umma_ss_elect(t_dpt, vdesc + 2 * ks, dodesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
+      umma_commit_elect(&bars->st_full);
+    }
+    for (int s = 0; ok && s < steps; ++s) {
+      if (!mbar_wait_warp(&bars->ew_done, s & 1, abort, err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int st = s % kStages;
+      const uint64_t qd = qdesc0 + st * kTileDesc, dod = dodesc0 + st * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < kBM / 16; ++kk)
+        umma_ts_elect(t_dv, t_pt + kk * 8, dod + kk * kRows16Desc, kIdescTS,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < kBM / 16; ++kk)
+        umma_ts_elect(t_dk, t_dst + kk * 8, qd + kk * kRows16Desc, kIdescTS,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_elect(&bars->qd_empty[st]);
+      if (s + 1 < steps) {
+        const int s1 = (s + 1) % kStages;
+        if (!mbar_wait_warp(&bars->qd_full[s1], ((s + 1) / kStages) & 1, abort, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          umma_ss_elect(t_st, kdesc + 2 * ks, qdesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
+                        ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          umma_ss_elect(t_dpt, vdesc + 2 * ks, dodesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
+                        ks > 0 ? 1u : 0u);
+        umma_commit_elect(&bars->st_full);
+      }
+    }
+    if (ok) umma_commit_elect(&bars->done);
+    umma_commit_elect(&bars->drain);
+    mbar_wait_warp(&bars->drain, 0, abort, err, true);
+  } else {
+    // ------------------------------------------- P^T, dS^T (one key / thread)
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_st = tmem + lane_off, t_dpt = t_st + 128, t_pt = t_st + 256,
+                   t_dst = t_st + 320, t_dv = t_st + 384, t_dk = t_st + 448;
+    const int jk = kt * kBN + r;  // this thread's key
+    bool ok = true;
+    for (int s = 0; s < steps; ++s) {
+      const int st = s % kStages;
+      const int qt = qt_lo + s % nqt;
+      // the lse / D vectors are plain shared-memory stores: wait on their
+      // barrier directly, then on the MMAs
+      if (!mbar_wait_warp(&bars->qd_full[st], (s / kStages) & 1, abort, err) ||
+          !mbar_wait_warp(&bars->st_full, s & 1, abort, err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // visible query columns of this key: [c_lo, c_hi)
+      const int qb = base + qt * kBM;  // position of the tile's query 0
+      int c_lo = 0, c_hi = min(kBM, lq - qt * kBM);
+      if (p.causal) c_lo = min(max(jk - qb, 0), kBM);
+      if (p.window > 0) c_hi = min(c_hi, max(jk - qb + p.window, 0));
+      const int len = r < krows ? max(c_hi - c_lo, 0) : 0;
+      const float *vec = reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float sv[32], dp[32];
+        tmem_ld32f(t_st + 32 * c, sv);
+        tmem_ld32f(t_dpt + 32 * c, dp);
+        tmem_wait_ld();
+        mask32(sv, 32 * c, c_lo, len);
+        uint32_t p16[16], ds16[16];
+        p_ds_col(sv, dp, p.scale_log2, vec + 32 * c, vec + 128 + 32 * c, p16, ds16);
+        tmem_st16(t_pt + 16 * c, p16);
+        tmem_st16(t_dst + 16 * c, ds16);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->ew_done);
+    }
+    if (ok && mbar_wait_warp(&bars->done, 0, abort, err)) {
+      tc_fence_after();
+      store_row64(t_dv, 1.f, p.dv + krow, r < krows);
+      store_row64(t_dk, p.scale, p.dk + krow, r < krows);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+size_t list_bytes(int batch, int64_t total) {  // counter + pairs of one tile list
+  return 256 + round256(static_cast<size_t>(total / kBM + batch) * 4);
+}
+
+}  // namespace
+
+// Workspace: q16, do16 [total_q, hq, 64] fp16; k16, v16 [total_k, hkv, 64]
+// fp16; lse2t, dt [hq, total_q] fp32; the query-tile and key-tile lists.
+size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv) {
+  const size_t qb = round256(static_cast<size_t>(total_q) * hq * kHeadDim * 2);
+  const size_t kb = round256(static_cast<size_t>(total_k) * hkv * kHeadDim * 2);
+  const size_t vb = round256(static_cast<size_t>(total_q) * hq * 4);
+  return 2 * qb + 2 * kb + 2 * vb + list_bytes(batch, total_q) + list_bytes(batch, total_k);
+}
+
+cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed) {
+  *encode_failed = false;
+  if (a.batch == 0) return cudaSuccess;
+  uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+  const size_t qb = round256(static_cast<size_t>(a.total_q) * a.hq * kHeadDim * 2);
+  const size_t kb = round256(static_cast<size_t>(a.total_k) * a.hkv * kHeadDim * 2);
+  const size_t vb = round256(static_cast<size_t>(a.total_q) * a.hq * 4);
+  uint8_t *q16 = ws, *do16 = ws + qb, *k16 = ws + 2 * qb, *v16 = ws + 2 * qb + kb;
+  float *lse2t = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb);
+  float *dt = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb + vb);
+  uint8_t *qlist = ws + 2 * qb + 2 * kb + 2 * vb;
+  uint8_t *klist = qlist + list_bytes(a.batch, a.total_q);
+
+  cudaError_t e;
+  if (a.total_q > 0) {
+    const int64_t n = a.total_q * a.hq * 8;
+    const int64_t blocks = (n + 255) / 256;
+    bwd_prep_q_kernel<<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
+        static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.dout),
+        static_cast<const uint4 *>(a.out), a.lse, a.total_q, a.hq, reinterpret_cast<uint4 *>(q16),
+        reinterpret_cast<uint4 *>(do16), lse2t, dt);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.total_k > 0) {
+    const int64_t n8 = a.total_k * a.hkv * 8;
+    const int64_t blocks = (n8 + 255) / 256;
+    bwd_prep_kv_kernel<<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
+        static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
+        reinterpret_cast<uint4 *>(k16), reinterpret_cast<uint4 *>(v16), n8);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const int max_qtiles = (a.max_seqlen_q + kBM - 1) / kBM;
+  const int max_ktiles = (a.max_seqlen_k + kBN - 1) / kBN;
+  BwdParams p;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.batch = a.batch;
+  p.hq = a.hq;
+  p.hkv = a.hkv;
+  p.group = a.hq / a.hkv;
+  p.causal = a.causal ? 1 : 0;
+  p.window = a.window;
+  p.total_q = static_cast<int>(a.total_q);
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  p.lse2t = lse2t;
+  p.dt = dt;
+  p.q_pairs = reinterpret_cast<const unsigned *>(qlist + 256);
+  p.num_q_pairs = reinterpret_cast<const int *>(qlist + 4);
+  p.k_pairs = reinterpret_cast<const unsigned *>(klist + 256);
+  p.num_k_pairs = reinterpret_cast<const int *>(klist + 4);
+  p.dq = static_cast<__nv_bfloat16 *>(a.dq);
+  p.dk = static_cast<__nv_bfloat16 *>(a.dk);
+  p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+  if ((e = launch_tile_list(a.cu_q, a.batch, max_qtiles, reinterpret_cast<unsigned *>(qlist + 256),
+                            reinterpret_cast<int *>(qlist + 4), reinterpret_cast<unsigned *>(qlist),
+                            stream)) != cudaSuccess)
+    return e;
+  if ((e = launch_tile_list(a.cu_k, a.batch, max_ktiles, reinterpret_cast<unsigned *>(klist + 256),
+                            reinterpret_cast<int *>(klist + 4), reinterpret_cast<unsigned *>(klist),
+                            stream)) != cudaSuccess)
+    return e;
+
+  EncodeTiledFn fn = get_encode_fn();
+  CUtensorMap tq, tdo, tk, tv;
+  const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // with no keys (or queries) nothing reads those maps; they then point at q16
+  const void *kbase = a.total_k > 0 ? static_cast<const void *>(k16) : q16;
+  const void *vbase = a.total_k > 0 ? static_cast<const void *>(v16) : q16;
+  if (fn == nullptr || !encode_rows_heads(fn, &tq, q16, a.total_q, a.hq, f16) ||
+      !encode_rows_heads(fn, &tdo, do16, a.total_q, a.hq, f16) ||
+      !encode_rows_heads(fn, &tk, kbase, a.total_k, a.hkv, f16) ||
+      !encode_rows_heads(fn, &tv, vbase, a.total_k, a.hkv, f16)) {
+    *encode_failed = true;
+    return cudaErrorInvalidValue;
+  }
+  if ((e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemRequest)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemRequest)) != cudaSuccess)
+    return e;
+  if (a.total_q > 0) {
+    const int64_t items = (a.total_q / kBM + a.batch) * a.hq;
+    bwd_dq_kernel<<<static_cast<unsigned>(items), 192, kSmemRequest, stream>>>(tq, tdo, tk, tv, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.sinks != nullptr && a.dsinks != nullptr) {  // after dQ: D is exact by now
+    bwd_dsink_kernel<<<a.hq, 256, 0, stream>>>(a.sinks, lse2t, dt, a.total_q, a.dsinks);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.total_k > 0) {
+    const int64_t items = (a.total_k / kBN + a.batch) * a.hkv;
+    bwd_dkdv_kernel<<<static_cast<unsigned>(items), 192, kSmemRequest, stream>>>(tq, tdo, tk, tv,
+                                                                                p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t backward_read_error(cudaStream_t stream, int *code) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(code, g_backward_error, sizeof(int));
+  const int zero = 0;
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_backward_error, &zero, sizeof(int));
+  return e;
+}
+
+}  // namespace sinkattn

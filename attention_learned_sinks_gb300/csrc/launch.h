@@ -42,6 +42,14 @@ cudaError_t launch_merge(const float *partial_o, const float *partial_lse, int n
                          int64_t rows, int hq, const float *sinks, void *out, float *lse,
                          cudaStream_t stream);
 
+// ---- tile lists ------------------------------------------------------------
+// One block on `stream`: the non-empty (sequence b, 128-row tile t) pairs of
+// the ragged layout cu[0..batch], packed b << 16 | t, tiles of higher index
+// first (at most max_tiles per sequence); their count in *num_pairs; *counter
+// zeroed. `pairs` holds up to cu[batch] / 128 + batch entries.
+cudaError_t launch_tile_list(const int32_t *cu, int batch, int max_tiles, unsigned *pairs,
+                             int *num_pairs, unsigned *counter, cudaStream_t stream);
+
 // ---- prefill ---------------------------------------------------------------
 struct PrefillLaunch {
   const void *q, *k, *v;
@@ -84,6 +92,25 @@ size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_
                                      int hkv, int splits);
 cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,
                                  bool *encode_failed);
+// ---- backward --------------------------------------------------------------
+struct BackwardLaunch {
+  const void *q, *k, *v, *out, *dout;  // bf16
+  const float *lse;                    // [total_q, hq], natural log, sink included
+  const int32_t *cu_q, *cu_k;
+  int batch;
+  int64_t total_q, total_k;
+  int max_seqlen_q, max_seqlen_k, hq, hkv;
+  const float *sinks;
+  int causal, window;
+  float scale;
+  void *dq, *dk, *dv;  // bf16
+  float *dsinks;       // [hq] or null
+  void *workspace;     // backward_workspace_bytes
+};
+size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv);
+cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed);
+cudaError_t backward_read_error(cudaStream_t stream, int *code);
+
 // Reads and clears the prefill kernel's device error word (synchronises stream).
 cudaError_t prefill_read_error(cudaStream_t stream, int *code);
 

@@ -45,6 +45,7 @@
 
 #include "launch.h"
 #include "ptx.cuh"
+#include "tma_host.h"
 
 namespace sinkattn {
 namespace {
@@ -133,27 +134,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-#define F8(i) "=f"(v[i]), "=f"(v[i + 1]), "=f"(v[i + 2]), "=f"(v[i + 3]), \
-  "=f"(v[i + 4]), "=f"(v[i + 5]), "=f"(v[i + 6]), "=f"(v[i + 7])
-// 32 consecutive fp32 TMEM columns of this thread's lane, straight into floats.
-__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : F8(0), F8(8), F8(16), F8(24)
-      : "r"(taddr));
-}
-#undef F8
-
-// Columns outside this row's visible range [c_lo, c_lo + len) of the tile -> -inf.
-// col0 is the first tile column held in sv.
-__device__ __forceinline__ void mask32(float (&sv)[32], int col0, int c_lo, int len) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (static_cast<unsigned>(col0 + i - c_lo) >= static_cast<unsigned>(len)) sv[i] = -INFINITY;
 }
 
 __device__ __forceinline__ float row_max32(const float (&sv)[32]) {
@@ -712,17 +692,6 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   }
 }
 
-// 8 bf16 -> 8 fp16, magnitudes above the fp16 range clamped to +-65504.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
-  const float lim = 65504.f;
-  uint4 y;
-  y.x = pack_f16x2(fminf(fmaxf(bf16_lo(x.x), -lim), lim), fminf(fmaxf(bf16_hi(x.x), -lim), lim));
-  y.y = pack_f16x2(fminf(fmaxf(bf16_lo(x.y), -lim), lim), fminf(fmaxf(bf16_hi(x.y), -lim), lim));
-  y.z = pack_f16x2(fminf(fmaxf(bf16_lo(x.z), -lim), lim), fminf(fmaxf(bf16_hi(x.z), -lim), lim));
-  y.w = pack_f16x2(fminf(fmaxf(bf16_lo(x.w), -lim), lim), fminf(fmaxf(bf16_hi(x.w), -lim), lim));
-  return y;
-}
-
 // bf16 V -> fp16 copy for the P V product (8 elements per thread per step).
 __global__ void __launch_bounds__(256) convert_v_kernel(const uint4 *__restrict__ src,
                                                         uint4 *__restrict__ dst, int64_t n8) {
@@ -731,58 +700,19 @@ __global__ void __launch_bounds__(256) convert_v_kernel(const uint4 *__restrict_
     dst[i] = bf16x8_to_f16x8(src[i]);
 }
 
-// ---------------------------------------------------------------- host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// [rows, heads, 64] 16-bit tensor; a box is 128 rows of one head, 128-byte swizzle.
-bool encode_rows_heads(EncodeTiledFn fn, CUtensorMap *map, const void *base, int64_t rows,
-                       int heads, CUtensorMapDataType dtype) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(heads),
-                              static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
-                                 static_cast<cuuint64_t>(heads) * kHeadDim * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1, static_cast<cuuint32_t>(kBM)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, dtype, 3, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
-// Workspace: fp16 copy of V, then the tile counter of the persistent grid.
+// ---------------------------------------------------------------- host side
+
+cudaError_t launch_tile_list(const int32_t *cu, int batch, int max_tiles, unsigned *pairs,
+                             int *num_pairs, unsigned *counter, cudaStream_t stream) {
+  build_worklist_kernel<<<1, 1024, 0, stream>>>(cu, batch, max_tiles, pairs, num_pairs, counter);
+  return cudaGetLastError();
+}
+
 namespace {
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
-
-int sm_count() {
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      num_sms = 148;
-  }
-  return num_sms;
-}
 
 // Workspace pieces. Every piece starts on a 256-byte boundary.
 size_t vcopy_bytes(int64_t total_k, int hkv) {  // fp16 copy of V

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <math.h>
 #include <stdint.h>
 
 namespace sinkattn {
@@ -142,6 +143,18 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // The two bf16 halves of a packed pair, as fp32 (exact).
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// 8 bf16 -> 8 fp16 (round to nearest even), magnitudes above the fp16 range
+// clamped to +-65504.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
+  const float lim = 65504.f;
+  uint4 y;
+  y.x = pack_f16x2(fminf(fmaxf(bf16_lo(x.x), -lim), lim), fminf(fmaxf(bf16_hi(x.x), -lim), lim));
+  y.y = pack_f16x2(fminf(fmaxf(bf16_lo(x.y), -lim), lim), fminf(fmaxf(bf16_hi(x.y), -lim), lim));
+  y.z = pack_f16x2(fminf(fmaxf(bf16_lo(x.z), -lim), lim), fminf(fmaxf(bf16_hi(x.z), -lim), lim));
+  y.w = pack_f16x2(fminf(fmaxf(bf16_lo(x.w), -lim), lim), fminf(fmaxf(bf16_hi(x.w), -lim), lim));
+  return y;
+}
 
 // 2^x on the special-function unit (PTX ex2.approx; ex2(-inf) = +0).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -296,6 +309,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
           taddr),
       SINKATTN_W8(0), SINKATTN_W8(8), SINKATTN_W8(16), SINKATTN_W8(24)
+      : "memory");
+}
+#define F8(i) "=f"(v[i]), "=f"(v[i + 1]), "=f"(v[i + 2]), "=f"(v[i + 3]), \
+  "=f"(v[i + 4]), "=f"(v[i + 5]), "=f"(v[i + 6]), "=f"(v[i + 7])
+// 32 consecutive fp32 TMEM columns of this thread's lane, straight into floats.
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : F8(0), F8(8), F8(16), F8(24)
+      : "r"(taddr));
+}
+#undef F8
+
+// Columns outside this row's visible range [c_lo, c_lo + len) of the tile -> -inf.
+// col0 is the first tile column held in sv.
+__device__ __forceinline__ void mask32(float (&sv)[32], int col0, int c_lo, int len) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (static_cast<unsigned>(col0 + i - c_lo) >= static_cast<unsigned>(len)) sv[i] = -INFINITY;
+}
+
+// registers -> 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      SINKATTN_W8(0), SINKATTN_W8(8)
       : "memory");
 }
 #undef SINKATTN_R8

@@ -1,0 +1,62 @@
+// Host helpers shared by the kernel files: the driver's tensor-map encoder
+// (looked up once through the runtime, so the library needs no -lcuda), the
+// [rows, heads, 64] 16-bit tile map the tcgen05 kernels load with TMA, and the
+// device's SM count.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "launch.h"
+
+namespace sinkattn {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [rows, heads, 64] 16-bit tensor; a box is 128 rows of one head, 128-byte
+// swizzle. Rows past the end read as zeros.
+inline bool encode_rows_heads(EncodeTiledFn fn, CUtensorMap *map, const void *base, int64_t rows,
+                              int heads, CUtensorMapDataType dtype) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
+                                 static_cast<cuuint64_t>(heads) * kHeadDim * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count() {
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
+  return num_sms;
+}
+
+}  // namespace sinkattn

@@ -26,6 +26,8 @@ EXPORTED = (
     "sinkattn_prefill",
     "sinkattn_prefill_paged_workspace_size",
     "sinkattn_prefill_paged",
+    "sinkattn_prefill_backward_workspace_size",
+    "sinkattn_prefill_backward",
     "sinkattn_decode_workspace_size",
     "sinkattn_decode",
     "sinkattn_decode_noalloc",
@@ -69,6 +71,11 @@ def load(path: str = LIB_PATH):
     lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, L, I, I, I, I, I, P,
                                            Mask, I, P, P, P, S, P]
     lib.sinkattn_prefill_paged.restype = I
+    lib.sinkattn_prefill_backward_workspace_size.argtypes = [I, L, L, I, I, I]
+    lib.sinkattn_prefill_backward_workspace_size.restype = S
+    lib.sinkattn_prefill_backward.argtypes = [P, P, P, P, P, P, P, P, I, L, L, I, I, I, I, I, P,
+                                              Mask, P, P, P, P, P, S, P]
+    lib.sinkattn_prefill_backward.restype = I
     lib.sinkattn_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.sinkattn_decode_workspace_size.restype = S
     lib.sinkattn_decode.argtypes = [P, P, P, P, P, P, L, I, I, I, I, I, I, I, P, Mask, I,
@@ -206,6 +213,48 @@ def sinkattn_prefill_paged(q, cu_seqlens_q, k_cache, v_cache, block_table, seqle
                                     _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "sinkattn_prefill_paged")
     return out, lse
+
+
+def sinkattn_prefill_backward_workspace_size(batch, total_q, total_k, hq, hkv, head_dim=64):
+    return load().sinkattn_prefill_backward_workspace_size(int(batch), int(total_q),
+                                                           int(total_k), hq, hkv, head_dim)
+
+
+def sinkattn_prefill_backward(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                              max_seqlen_k, *, sinks=None, causal=True, window=0, scale=None,
+                              dq=None, dk=None, dv=None, dsinks=None, workspace=None,
+                              stream=None):
+    """Gradients of sinkattn_prefill with respect to q, k, v and the sinks,
+    given the forward's out and lse and the output gradient dout.
+    Returns (dq, dk, dv, dsinks); dsinks is None without sinks."""
+    lib = load()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _req(t, torch.bfloat16, name)
+    _req(lse, torch.float32, "lse")
+    _req(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _req(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    tq, hq, d = q.shape
+    tk, hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    if sinks is not None:
+        _req(sinks, torch.float32, "sinks")
+        if dsinks is None:
+            dsinks = torch.empty(hq, dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        need = lib.sinkattn_prefill_backward_workspace_size(batch, tq, tk, hq, hkv, d)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    mask = Mask(1 if causal else 0, int(window), float(d ** -0.5 if scale is None else scale))
+    st = lib.sinkattn_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                       _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch,
+                                       tq, tk, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
+                                       _ptr(sinks), mask, _ptr(dq), _ptr(dk), _ptr(dv),
+                                       _ptr(dsinks if sinks is not None else None),
+                                       _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sinkattn_prefill_backward")
+    return dq, dk, dv, (dsinks if sinks is not None else None)
 
 
 def sinkattn_decode(q, k_cache, v_cache, *, kv_indptr=None, block_table=None, seqlens_k=None,

@@ -498,6 +498,35 @@ def extras(sa, S, dev, stream, pk, pk_kind):
         del c, out, lse, ws
         torch.cuda.empty_cache()
 
+    # backward of the varlen prefill (dq, dk, dv, dsinks), forward outputs
+    # precomputed; algorithmic flops: 5 products of 2 * 64 per visible pair
+    for name, w in (("varlen_backward", 0), ("varlen_backward_w128", 128)):
+        c = S.varlen_prefill(window=w, device="cuda")
+        cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
+        sk = c.sinks.to(dev)
+        out, lse = sa.sinkattn_prefill(c.q, c.k, c.v, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
+                                       sinks=sk, causal=True, window=w)
+        dout = S.bf16_normal(tuple(c.q.shape), 19, device="cuda")
+        dq, dk, dv = torch.empty_like(c.q), torch.empty_like(c.k), torch.empty_like(c.v)
+        dsk = torch.empty_like(sk)
+        ws = torch.empty(sa.sinkattn_prefill_backward_workspace_size(c.batch, c.q.shape[0],
+                                                                     c.k.shape[0], c.hq, c.hkv),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            sa.sinkattn_prefill_backward(c.q, c.k, c.v, out, lse, dout, cq, ck, c.max_seqlen_q,
+                                         c.max_seqlen_k, sinks=sk, causal=True, window=w, dq=dq,
+                                         dk=dk, dv=dv, dsinks=dsk, workspace=ws)
+        for _ in range(3):
+            call()
+        t = time_calls(call, 10, stream, flush)
+        fl = 10 * 64 * prefill_pairs(c) * c.hq
+        res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3, "tokens_per_s": sum(c.seqlens_q) / t,
+                     "frac_of_bf16_peak": fl / t / 1e12 / burst,
+                     "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)", "flops": fl}
+        del c, out, lse, dout, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+
     for name, w in (("paged_decode", 0), ("paged_decode_w128", 128)):
         c = S.paged_decode(window=w, device="cuda")
         bt, sl, sk = c.block_table.to(dev), c.seqlens_k_t.to(dev), c.sinks.to(dev)

@@ -259,7 +259,48 @@ sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_ls
                                  const float *sinks, void *out, float *lse, void *stream);
 
 /*
- * Device error word. Every wait inside the kernels is bounded; a wait that
+ * Backward of sinkattn_prefill (packed sequences, contiguous K/V). The pages
+ * give the forward only; the gradients follow from its definition (section
+ * "Kernels for GPT-OSS / Sink Attention": one sink logit per head in the
+ * softmax denominator, no value row). With P_ij = e^{s_ij - lse_i},
+ * P_sink,i = e^{sink_h - lse_i}, D_i = dO_i . O_i and
+ * dS_ij = P_ij (dO_i . v_j - D_i):
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,
+ *   dv_j = sum_i P_ij dO_i,         dsink_h = -sum_i P_sink,i D_i,
+ * with dk, dv summed over the query heads sharing a KV head and dsink over
+ * every row of head h.
+ *
+ *   q, k, v, cu_seqlens_*, total_*, max_seqlen_*, hq, hkv, head_dim, sinks,
+ *            mask   exactly as passed to the forward call.
+ *   out, lse       the forward's outputs for the same inputs (bf16
+ *            [total_q, hq, 64]; float32 [total_q, hq], required).
+ *   dout     bf16 [total_q, hq, 64]: gradient of the loss with respect to out.
+ *   dq       bf16 [total_q, hq, 64];  dk, dv  bf16 [total_k, hkv, 64].
+ *            Every element is written (rows that see no key get 0).
+ *   dsinks   float32 [hq] or NULL; written when both sinks and dsinks are
+ *            given.
+ *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
+ *            sinkattn_prefill_backward_workspace_size() bytes for the same
+ *            sizes (fp16 copies of q, k, v and dout, two float32 values per
+ *            (row, head), two tile lists); contents need not be initialised.
+ * The products run on fp16 copies of the inputs (values of magnitude above
+ * 65504 are clamped) with fp32 accumulation; P and dS enter the second
+ * products as fp16. Every output element is written by one CTA, so repeated
+ * calls give bitwise identical results.
+ */
+size_t sinkattn_prefill_backward_workspace_size(int batch, int64_t total_q, int64_t total_k,
+                                                int hq, int hkv, int head_dim);
+
+sinkattn_status_t sinkattn_prefill_backward(
+    const void *q, const void *k, const void *v, const void *out, const void *dout,
+    const float *lse, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int batch,
+    int64_t total_q, int64_t total_k, int max_seqlen_q, int max_seqlen_k, int hq, int hkv,
+    int head_dim, const float *sinks, sinkattn_mask_t mask, void *dq, void *dk, void *dv,
+    float *dsinks, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Device error word (prefill, paged prefill and backward kernels). Every
+ * wait inside the kernels is bounded; a wait that
  * runs out records a nonzero code here and the kernel returns early instead of
  * hanging. This call synchronises `stream`, copies the word to *code and
  * resets it to 0. Codes: 0 none; 1 a pipeline barrier wait timed out;

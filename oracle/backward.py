@@ -101,11 +101,13 @@ def forward(q, k, v, cu_seqlens_q, cu_seqlens_k, *, hq, hkv, sinks=None, causal=
 
 
 def backward(q, k, v, cu_seqlens_q, cu_seqlens_k, dout, *, hq, hkv, sinks=None, causal=True,
-             window=0, scale):
+             window=0, scale, seqs=None):
     """Gradients of sum(dout * out) with respect to q, k, v and the sinks.
 
     Returns float64 (dq [total_q, hq, d], dk [total_k, hkv, d],
-    dv [total_k, hkv, d], dsinks [hq] or None without sinks).
+    dv [total_k, hkv, d], dsinks [hq] or None without sinks). `seqs` limits
+    the work to those sequences: their rows of dq/dk/dv are exact, other rows
+    stay zero, and dsinks sums over those sequences only.
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
     cq, ck = _i64(cu_seqlens_q), _i64(cu_seqlens_k)
@@ -115,7 +117,7 @@ def backward(q, k, v, cu_seqlens_q, cu_seqlens_k, dout, *, hq, hkv, sinks=None, 
     dk = np.zeros(k.shape, dtype=np.float64)
     dv = np.zeros(v.shape, dtype=np.float64)
     dsink = np.zeros(hq, dtype=np.float64)
-    for b in range(len(cq) - 1):
+    for b in (range(len(cq) - 1) if seqs is None else seqs):
         q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
         lq, lk = q1 - q0, k1 - k0
         if lq == 0:

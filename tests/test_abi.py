@@ -123,6 +123,37 @@ def test_prefill_paged_rejects_bad_arguments(lib):
     assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 5, 128, 8, 2, 64, 0, 0) > need
 
 
+def backward(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, dout=FAKE, lse=FAKE, cuq=FAKE, cuk=FAKE, batch=2,
+             tq=10, tk=10, mq=5, mk=5, hq=8, hkv=2, d=64, sinks=None, mask=M, dq=FAKE, dk=FAKE,
+             dv=FAKE, dsinks=None)
+    a.update(kw)
+    return lib.sinkattn_prefill_backward(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"],
+                                         a["cuq"], a["cuk"], a["batch"], a["tq"], a["tk"],
+                                         a["mq"], a["mk"], a["hq"], a["hkv"], a["d"], a["sinks"],
+                                         a["mask"], a["dq"], a["dk"], a["dv"], a["dsinks"],
+                                         a.get("ws"), a.get("wsb", 0), None)
+
+
+def test_backward_rejects_bad_arguments(lib):
+    assert backward(lib, d=128) == B.SINKATTN_ERR_UNSUPPORTED
+    assert backward(lib, hq=6, hkv=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert backward(lib, lse=None) == B.SINKATTN_ERR_INVALID_ARGUMENT   # lse is required
+    assert backward(lib, out=None) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert backward(lib, dv=ctypes.c_void_p((1 << 20) + 4)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert backward(lib, mask=B.Mask(1, 0, -2.0)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    need = lib.sinkattn_prefill_backward_workspace_size(2, 10, 10, 8, 2, 64)
+    # fp16 copies of q, dout (10 x 8 x 64) and k, v (10 x 2 x 64), two fp32 per (row, head)
+    assert need >= 2 * 10 * 8 * 128 + 2 * 10 * 2 * 128 + 2 * 10 * 8 * 4
+    assert backward(lib) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert backward(lib, ws=FAKE, wsb=need - 1) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert backward(lib, ws=ctypes.c_void_p((1 << 20) + 64), wsb=need) == \
+        B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert backward(lib, batch=0) == B.SINKATTN_OK
+    assert backward(lib, tq=0, tk=0) == B.SINKATTN_OK
+    assert lib.sinkattn_prefill_backward_workspace_size(2, 10, 10, 8, 2, 96) == 0
+
+
 def test_decode_rejects_bad_arguments(lib):
     assert decode(lib, d=80) == B.SINKATTN_ERR_UNSUPPORTED
     assert decode(lib, hq=32, hkv=2) == B.SINKATTN_ERR_UNSUPPORTED   # group of 16
