@@ -18,6 +18,8 @@ are not available here, so seeded normal values stand in for them):
                    131072-token causal context
   long_context_prefill   256 new query tokens at the end of a 131072-token
                    causal context (few query tiles: the split-KV case)
+  decode_contig_fp8  decode_contig's lengths and geometry over an fp8 e4m3 KV
+                   cache with per-KV-head scales 2^-4 * U(0.5, 2)
   paged_chunked_prefill  the same as chunked_prefill, with K/V in 16-token pages and a randomly
                    permuted block table
   paged_prefill_batch    16 sequences, new chunks uniform in [256, 2048] after
@@ -144,6 +146,11 @@ class DecodeCase:
     seqlens_k_t: Optional[torch.Tensor] = None  # int32 [batch]
     page_size: int = PAGE_SIZE
     head_dim: int = HEAD_DIM
+    # fp8 cache: k/v (or k_cache/v_cache) hold e4m3 codes as uint8; the value
+    # of a code c of KV head g is k_scale[g] * e4m3(c)
+    kv_dtype: str = "bf16"
+    k_scale: Optional[torch.Tensor] = None  # f32 [hkv]
+    v_scale: Optional[torch.Tensor] = None
 
     @property
     def batch(self):
@@ -218,27 +225,59 @@ def make_prefill_paged(name, seqlens_q, seqlens_k, hq, hkv, *, seed, causal=True
                        page_size=page_size)
 
 
+def fp8_scales(hkv: int, seed: int) -> torch.Tensor:
+    """Per-KV-head fp8 scales 2^-4 * U(0.5, 2): codes of N(0, 1) values then
+    reach magnitudes near 2^4 * 4 sigma, well inside e4m3's 448."""
+    g = _gen(seed, "cpu")
+    return (torch.rand(hkv, generator=g, dtype=torch.float32) * 1.5 + 0.5) / 16.0
+
+
+def e4m3_codes(shape, seed: int, scale: torch.Tensor, head_axis: int,
+               device="cpu") -> torch.Tensor:
+    """uint8 e4m3 codes of N(0, 1) samples divided by the per-head scale
+    (rounded to nearest even by torch's float8_e4m3fn conversion)."""
+    x = torch.empty(shape, dtype=torch.float32, device=device)
+    g = _gen(seed, device)
+    flat = x.view(-1)
+    step = 1 << 26
+    for s in range(0, flat.numel(), step):
+        e = min(flat.numel(), s + step)
+        flat[s:e].copy_(torch.randn(e - s, generator=g, dtype=torch.float32, device=device))
+    view = [1] * len(shape)
+    view[head_axis] = shape[head_axis]
+    x.div_(scale.to(device).view(view))
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 def make_decode(name, seqlens_k, hq, hkv, *, seed, window=0, sink_std=1.0,
                 with_sinks=True, paged=False, page_size=PAGE_SIZE, scale=None,
-                device="cpu", head_dim=HEAD_DIM) -> DecodeCase:
+                device="cpu", head_dim=HEAD_DIM, kv_dtype="bf16") -> DecodeCase:
     batch = len(seqlens_k)
     q = bf16_normal((batch, hq, head_dim), seed * 10 + 1, device=device)
     sinks = normal_f32(hq, seed * 10 + 4, sink_std) if with_sinks else None
     case = DecodeCase(name=name, q=q, seqlens_k=list(seqlens_k), hq=hq,
                       hkv=hkv, sinks=sinks, window=window,
                       scale=scale if scale is not None else head_dim ** -0.5,
-                      page_size=page_size, head_dim=head_dim)
+                      page_size=page_size, head_dim=head_dim, kv_dtype=kv_dtype)
+    if kv_dtype == "fp8":
+        case.k_scale = fp8_scales(hkv, seed * 10 + 6)
+        case.v_scale = fp8_scales(hkv, seed * 10 + 7)
+
+        def values(shape, s, which):
+            sc = case.k_scale if which == "k" else case.v_scale
+            return e4m3_codes(shape, s, sc, 1, device=device)
+    else:
+        def values(shape, s, which):
+            return bf16_normal(shape, s, device=device)
     if not paged:
         tk = sum(seqlens_k)
-        case.k = bf16_normal((tk, hkv, head_dim), seed * 10 + 2, device=device)
-        case.v = bf16_normal((tk, hkv, head_dim), seed * 10 + 3, device=device)
+        case.k = values((tk, hkv, head_dim), seed * 10 + 2, "k")
+        case.v = values((tk, hkv, head_dim), seed * 10 + 3, "v")
         case.kv_indptr = offsets(seqlens_k)
         return case
     table, num_pages = _page_table(seqlens_k, page_size, seed * 10 + 5)
-    case.k_cache = bf16_normal((num_pages, hkv, page_size, head_dim),
-                               seed * 10 + 2, device=device)
-    case.v_cache = bf16_normal((num_pages, hkv, page_size, head_dim),
-                               seed * 10 + 3, device=device)
+    case.k_cache = values((num_pages, hkv, page_size, head_dim), seed * 10 + 2, "k")
+    case.v_cache = values((num_pages, hkv, page_size, head_dim), seed * 10 + 3, "v")
     case.block_table = table
     case.seqlens_k_t = torch.tensor(seqlens_k, dtype=torch.int32)
     return case
@@ -261,6 +300,11 @@ def varlen_prefill(window=0, device="cpu", nseq=16) -> PrefillCase:
     return make_prefill("varlen_prefill" + ("_w%d" % window if window else ""),
                         lens, lens, 64, 8, seed=3, causal=True, window=window,
                         device=device)
+
+
+def decode_contig_fp8(device="cpu", batch=64) -> DecodeCase:
+    lens = uniform_lengths(batch, 1024, 8192, seed=2000)
+    return make_decode("decode_contig_fp8", lens, 64, 8, seed=9, device=device, kv_dtype="fp8")
 
 
 def paged_decode(window=0, device="cpu", batch=256) -> DecodeCase:
@@ -298,6 +342,7 @@ WORKLOADS = {
     "decode_contig": decode_contig,
     "varlen_prefill": varlen_prefill,
     "paged_decode": paged_decode,
+    "decode_contig_fp8": decode_contig_fp8,
     "chunked_prefill": chunked_prefill,
     "long_context_prefill": long_context_prefill,
     "paged_chunked_prefill": paged_chunked_prefill,
