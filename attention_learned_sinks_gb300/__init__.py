@@ -9,6 +9,7 @@ from .sinkattn import (  # noqa: F401
     SinkAttnError,
     load,
     sinkattn_decode,
+    sinkattn_decode_fp8,
     sinkattn_decode_workspace_size,
     sinkattn_get_device_error,
     sinkattn_merge,

@@ -197,13 +197,18 @@ size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int h
   return decode_workspace_layout(batch, hq, hkv, plan).bytes;
 }
 
-sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
-                                  const int32_t *kv_indptr, const int32_t *block_table,
-                                  const int32_t *seqlens_k, int64_t kv_rows, int max_pages_per_seq,
-                                  int page_size, int batch, int max_seqlen_k, int hq, int hkv,
-                                  int head_dim, const float *sinks, sinkattn_mask_t mask,
-                                  int num_splits, void *out, float *lse, void *workspace,
-                                  size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+sinkattn_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache, bool fp8,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *kv_indptr, const int32_t *block_table,
+                              const int32_t *seqlens_k, int64_t kv_rows, int max_pages_per_seq,
+                              int page_size, int batch, int max_seqlen_k, int hq, int hkv,
+                              int head_dim, const float *sinks, sinkattn_mask_t mask,
+                              int num_splits, void *out, float *lse, void *workspace,
+                              size_t workspace_bytes, void *stream) {
   if (batch < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || num_splits < 0 ||
       kv_rows < 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
@@ -219,7 +224,8 @@ sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       (kv_indptr && !aligned(kv_indptr, 4)) || (block_table && !aligned(block_table, 4)) ||
       (seqlens_k && !aligned(seqlens_k, 4)) || (sinks && !aligned(sinks, 4)) ||
-      (lse && !aligned(lse, 4)))
+      (lse && !aligned(lse, 4)) || (k_scale && !aligned(k_scale, 4)) ||
+      (v_scale && !aligned(v_scale, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
   const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
@@ -248,7 +254,42 @@ sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void
   a.lse = lse;
   a.workspace = workspace;
   a.plan = plan;
+  a.fp8 = fp8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *kv_indptr, const int32_t *block_table,
+                                  const int32_t *seqlens_k, int64_t kv_rows, int max_pages_per_seq,
+                                  int page_size, int batch, int max_seqlen_k, int hq, int hkv,
+                                  int head_dim, const float *sinks, sinkattn_mask_t mask,
+                                  int num_splits, void *out, float *lse, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+  return decode_impl(q, k_cache, v_cache, false, nullptr, nullptr, kv_indptr, block_table,
+                     seqlens_k, kv_rows, max_pages_per_seq, page_size, batch, max_seqlen_k, hq,
+                     hkv, head_dim, sinks, mask, num_splits, out, lse, workspace,
+                     workspace_bytes, stream);
+}
+
+sinkattn_status_t sinkattn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *kv_indptr, const int32_t *block_table,
+                                      const int32_t *seqlens_k, int64_t kv_rows,
+                                      int max_pages_per_seq, int page_size, int batch,
+                                      int max_seqlen_k, int hq, int hkv, int head_dim,
+                                      const float *sinks, sinkattn_mask_t mask, int num_splits,
+                                      void *out, float *lse, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+  return decode_impl(q, k_cache, v_cache, true, k_scale, v_scale, kv_indptr, block_table,
+                     seqlens_k, kv_rows, max_pages_per_seq, page_size, batch, max_seqlen_k, hq,
+                     hkv, head_dim, sinks, mask, num_splits, out, lse, workspace,
+                     workspace_bytes, stream);
 }
 
 sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_lse, int num_splits,

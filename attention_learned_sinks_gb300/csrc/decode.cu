@@ -1,5 +1,6 @@
 // Split-KV decode for sink attention: one query token per sequence over a
-// contiguous or paged bf16 KV cache.
+// contiguous or paged KV cache in bf16, or in fp8 e4m3 with per-KV-head
+// scales.
 //
 // Page "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention":
 // the online softmax keeps a running maximum m and a running denominator d;
@@ -19,6 +20,12 @@
 //   O^T[64 dims x 8 heads]  += V^T . P^T          (P^T re-used as the B operand
 //                                                  after an in-register 8x8
 //                                                  transpose, movmatrix)
+//
+// fp8 cache (page "GPT-OSS on day 0": FP8 serving): the ring holds e4m3 slabs
+// (half the bytes); after each slab lands the warp widens it to fp16 in a
+// per-warp shared-memory slab with the bf16 layout (e4m3 -> fp16 is exact),
+// and the MMAs run in fp16 (q converted once, P as one fp16 term). The K scale
+// folds into the softmax scale, the V scale into the final normalisation.
 //
 // The per-warp states (m, d, O) are combined in shared memory; a sequence with
 // one block writes the final bf16 output directly, otherwise each block writes
@@ -46,12 +53,24 @@ constexpr int kSlabBytes = kSlab * kRowBytes;   // 4 KB of K (or of V)
 constexpr int kStageBytes = 2 * kSlabBytes;     // K + V
 constexpr int kWarpBytes = kStages * kStageBytes;
 constexpr int kSmemBytes = kWarps * kWarpBytes;  // 96 KB -> two blocks per SM
+// fp8: 64-byte rows in a 2-stage ring, plus one fp16 slab per warp that holds
+// the widened K slab, then the widened V slab (48 KB per block: four per SM;
+// the fp8 kernel is bound by latency inside each warp, so more warps beat a
+// deeper ring)
+constexpr int kRowBytes8 = kHeadDim;
+constexpr int kSlabBytes8 = kSlab * kRowBytes8;  // 2 KB
+constexpr int kStageBytes8 = 2 * kSlabBytes8;
+constexpr int kStages8 = 2;
+constexpr int kWarpBytes8 = kStages8 * kStageBytes8 + kSlabBytes;
+constexpr int kSmemBytes8 = kWarps * kWarpBytes8;
 constexpr int kMaxGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct Params {
   const __nv_bfloat16 *q, *k, *v;
+  const uint8_t *k8, *v8;            // fp8 cache
+  const float *k_scale, *v_scale;    // fp8: per KV head, or null
   const int32_t *kv_indptr, *block_table, *seqlens_k;
   int max_pages, page_size;
   int page_shift;  // log2(page_size) when it is a power of two, else -1
@@ -96,8 +115,33 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
 }
 
-template <bool kPaged>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
+// One 32-row fp8 slab (64-byte rows, unswizzled) -> fp16 with the swizzled
+// 128-byte-row layout that ldmatrix reads. Lane: rows lane/4 + 8i, 16-byte
+// chunk lane%4, so each access of the warp covers 512 contiguous bytes.
+__device__ __forceinline__ void widen_slab(uint32_t src, uint32_t dst, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = i * 8 + (lane >> 2), c = lane & 3;
+    uint32_t x0, x1, x2, x3;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                 : "r"(src + row * kRowBytes8 + c * 16));
+    uint32_t y[8];
+    e4m3x4_to_f16x4(x0, y[0], y[1]);
+    e4m3x4_to_f16x4(x1, y[2], y[3]);
+    e4m3x4_to_f16x4(x2, y[4], y[5]);
+    e4m3x4_to_f16x4(x3, y[6], y[7]);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(row, 2 * c)),
+                 "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3])
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(row, 2 * c + 1)),
+                 "r"(y[4]), "r"(y[5]), "r"(y[6]), "r"(y[7])
+                 : "memory");
+  }
+}
+
+template <bool kPaged, bool kFp8>
+__global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -140,18 +184,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
   const int my_slabs = warp < nslab ? (nslab - warp + kWarps - 1) / kWarps : 0;
 
   // Q^T as the B operand of S^T = K Q^T: lane (lr, lc) holds head lr,
-  // dims ks*16 + 2lc + {0,1} and + 8.
+  // dims ks*16 + 2lc + {0,1} and + 8 (fp8 cache: as fp16, clamped to its range).
   uint32_t qf[4][2];
   {
     const bool valid = lr < p.group;
     const __nv_bfloat16 *qrow =
         p.q + (static_cast<size_t>(b) * p.hq + g * p.group + (valid ? lr : 0)) * kHeadDim;
+    auto frag = [&](int at) -> uint32_t {
+      if (!valid) return 0u;
+      const uint32_t x = *reinterpret_cast<const uint32_t *>(qrow + at);
+      if (!kFp8) return x;
+      const float lim = 65504.f;
+      return pack_f16x2(fminf(fmaxf(bf16_lo(x), -lim), lim), fminf(fmaxf(bf16_hi(x), -lim), lim));
+    };
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      qf[ks][0] = valid ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * lc) : 0u;
-      qf[ks][1] = valid ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * lc + 8) : 0u;
+      qf[ks][0] = frag(ks * 16 + 2 * lc);
+      qf[ks][1] = frag(ks * 16 + 2 * lc + 8);
     }
   }
+  // fp8: the K scale multiplies every score, the V scale every output
+  const float score_log2 = kFp8 && p.k_scale != nullptr ? p.scale_log2 * p.k_scale[g]
+                                                         : p.scale_log2;
+  const float out_scale = kFp8 && p.v_scale != nullptr ? p.v_scale[g] : 1.f;
 
   // Online-softmax state for heads 2lc and 2lc+1 (log2 domain). The sink
   // initialises block 0, warp 0: m = sink, d = 1 (d kept by lane row 0 only,
@@ -169,10 +224,26 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
 
-  const uint32_t wbase = smem_u32(smem) + warp * kWarpBytes;
+  const uint32_t wbase = smem_u32(smem) + warp * (kFp8 ? kWarpBytes8 : kWarpBytes);
 
   auto load_slab = [&](int i) {
     const int slab0 = t0 + (warp + i * kWarps) * kSlab;
+    if (kFp8) {
+      const uint32_t kdst = wbase + (i % kStages8) * kStageBytes8;
+      const uint32_t vdst = kdst + kSlabBytes8;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = r * 8 + (lane >> 2);
+        const int col = lane & 3;
+        const int j = slab0 + row;
+        const bool ok = j < t1;
+        const size_t off =
+            ok ? kv_row<kPaged>(p, b, kv_base, j, g, s_pages, pg0, staged) + col * 16 : 0;
+        cp_async_16(kdst + row * kRowBytes8 + col * 16, p.k8 + off, ok ? 16u : 0u);
+        cp_async_16(vdst + row * kRowBytes8 + col * 16, p.v8 + off, ok ? 16u : 0u);
+      }
+      return;
+    }
     const uint32_t kdst = wbase + (i % kStages) * kStageBytes;
     const uint32_t vdst = kdst + kSlabBytes;
 #pragma unroll
@@ -187,21 +258,32 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     }
   };
 
+  constexpr int kRing = kFp8 ? kStages8 : kStages;
 #pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
+  for (int i = 0; i < kRing - 1; ++i) {
     if (i < my_slabs) load_slab(i);
     cp_async_commit();
   }
 
   for (int it = 0; it < my_slabs; ++it) {
-    cp_async_wait<kStages - 2>();
+    cp_async_wait<kRing - 2>();
     __syncwarp();
-    if (it + kStages - 1 < my_slabs) load_slab(it + kStages - 1);
+    if (it + kRing - 1 < my_slabs) load_slab(it + kRing - 1);
     cp_async_commit();
 
     const int slab0 = t0 + (warp + it * kWarps) * kSlab;
-    const uint32_t kb = wbase + (it % kStages) * kStageBytes;
-    const uint32_t vb = kb + kSlabBytes;
+    uint32_t kb, vb;
+    const uint32_t k8 = wbase + (it % kStages8) * kStageBytes8;
+    if (kFp8) {
+      // widen the K slab into the warp's fp16 slab (the previous iteration's
+      // reads of it are complete: __syncwarp above); V follows after the scores
+      kb = vb = wbase + kStages8 * kStageBytes8;
+      widen_slab(k8, kb, lane);
+      __syncwarp();
+    } else {
+      kb = wbase + (it % kStages) * kStageBytes;
+      vb = kb + kSlabBytes;
+    }
     const int mi = lane >> 3, mr = lane & 7;
 
     // scores: two 16-token m-tiles
@@ -215,7 +297,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
         uint32_t a[4];
         const int row = mt * 16 + (mi & 1) * 8 + mr;
         ldmatrix_x4(kb + swz(row, ks * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
-        mma_bf16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
+        if (kFp8)
+          mma_f16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
+        else
+          mma_bf16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
       }
     }
     // scale to log2 units, mask the ragged end of the chunk, tile maximum
@@ -225,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = slab0 + mt * 16 + lr + ((e & 2) ? 8 : 0);
-        const float x = j < t1 ? s[mt][e] * p.scale_log2 : -INFINITY;
+        const float x = j < t1 ? s[mt][e] * score_log2 : -INFINITY;
         s[mt][e] = x;
         if (e & 1)
           mx1 = fmaxf(mx1, x);
@@ -246,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     float sum0 = 0.f, sum1 = 0.f;
     // P enters the tensor core as two bf16 terms, hi + lo, which together
     // carry 16 significant bits: a single bf16 P (8 bits) alone would add
-    // about 1.6e-3 rms relative error to the output.
+    // about 1.6e-3 rms relative error to the output. With the fp16 MMAs of
+    // the fp8 cache P is one fp16 term (11 bits).
     uint32_t pb[2][2], pl[2][2];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
@@ -254,6 +340,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
       const float p2 = fast_exp2(s[mt][2] - base0), p3 = fast_exp2(s[mt][3] - base1);
       sum0 += p0 + p2;
       sum1 += p1 + p3;
+      if (kFp8) {
+        pb[mt][0] = movmatrix_trans(pack_f16x2(p0, p1));
+        pb[mt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+        continue;
+      }
       const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
       const uint32_t l01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
       const uint32_t l23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
@@ -272,6 +363,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
       o[dt][2] *= al0;
       o[dt][3] *= al1;
     }
+    if (kFp8) {  // the scores are in registers: the fp16 slab now takes V
+      __syncwarp();
+      widen_slab(k8 + kSlabBytes8, vb, lane);
+      __syncwarp();
+    }
     // O^T += V^T P^T
 #pragma unroll
     for (int dt = 0; dt < 4; ++dt)
@@ -280,8 +376,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
         uint32_t a[4];
         const int row = mt * 16 + (mi >> 1) * 8 + mr;
         ldmatrix_x4_trans(vb + swz(row, dt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
-        mma_bf16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
-        mma_bf16_16816(o[dt], a, pl[mt][0], pl[mt][1]);
+        if (kFp8) {
+          mma_f16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
+        } else {
+          mma_bf16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
+          mma_bf16_16816(o[dt], a, pl[mt][0], pl[mt][1]);
+        }
       }
   }
   cp_async_wait<0>();
@@ -331,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     acc[2] += f * ov.z;
     acc[3] += f * ov.w;
   }
-  const float inv = Dn > 0.f ? 1.f / Dn : 0.f;
+  const float inv = Dn > 0.f ? out_scale / Dn : 0.f;
   // block lse in natural log (-inf when nothing is visible and no sink)
   const float blse = Dn > 0.f ? (M + fast_log2(Dn)) * kLn2 : -INFINITY;
   const bool head_ok = hh < p.group;
@@ -442,6 +542,10 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.k = static_cast<const __nv_bfloat16 *>(a.k);
   p.v = static_cast<const __nv_bfloat16 *>(a.v);
+  p.k8 = static_cast<const uint8_t *>(a.k);
+  p.v8 = static_cast<const uint8_t *>(a.v);
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   p.kv_indptr = a.kv_indptr;
   p.block_table = a.block_table;
   p.seqlens_k = a.seqlens_k;
@@ -473,12 +577,21 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   dim3 grid(a.plan.max_splits, a.hkv, a.batch);
-  if (a.block_table != nullptr) {
-    cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    decode_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  auto go = [&](auto kernel, int smem) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kernel<<<grid, kThreads, smem, stream>>>(p);
+  };
+  const bool paged = a.block_table != nullptr;
+  if (a.fp8) {
+    if (paged)
+      go(decode_kernel<true, true>, kSmemBytes8);
+    else
+      go(decode_kernel<false, true>, kSmemBytes8);
   } else {
-    cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    decode_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    if (paged)
+      go(decode_kernel<true, false>, kSmemBytes);
+    else
+      go(decode_kernel<false, false>, kSmemBytes);
   }
   return cudaGetLastError();
 }

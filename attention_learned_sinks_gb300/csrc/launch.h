@@ -24,7 +24,9 @@ struct DecodeWorkspace {
 DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const DecodePlan &plan);
 
 struct DecodeLaunch {
-  const void *q, *k, *v;
+  const void *q, *k, *v;  // k, v: bf16, or fp8 e4m3 bytes when fp8
+  bool fp8 = false;
+  const float *k_scale = nullptr, *v_scale = nullptr;  // fp8: per KV head (null = 1)
   const int32_t *kv_indptr, *block_table, *seqlens_k;
   int max_pages, page_size;
   int batch, max_seqlen_k, hq, hkv, window;

@@ -30,6 +30,7 @@ EXPORTED = (
     "sinkattn_prefill_backward",
     "sinkattn_decode_workspace_size",
     "sinkattn_decode",
+    "sinkattn_decode_fp8",
     "sinkattn_decode_noalloc",
     "sinkattn_merge",
     "sinkattn_get_device_error",
@@ -81,6 +82,9 @@ def load(path: str = LIB_PATH):
     lib.sinkattn_decode.argtypes = [P, P, P, P, P, P, L, I, I, I, I, I, I, I, P, Mask, I,
                                     P, P, P, S, P]
     lib.sinkattn_decode.restype = I
+    lib.sinkattn_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, L, I, I, I, I, I, I, I, P, Mask,
+                                        I, P, P, P, S, P]
+    lib.sinkattn_decode_fp8.restype = I
     lib.sinkattn_decode_noalloc.argtypes = [P, P, P, P, P, P, L, I, I, I, I, I, I, I, P, Mask,
                                             I, P, P, P]
     lib.sinkattn_decode_noalloc.restype = I
@@ -292,6 +296,47 @@ def sinkattn_decode(q, k_cache, v_cache, *, kv_indptr=None, block_table=None, se
                              int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
                              workspace.numel(), _stream(stream))
     _check(st, "sinkattn_decode")
+    return out, lse
+
+
+def sinkattn_decode_fp8(q, k_cache, v_cache, *, k_scale=None, v_scale=None, kv_indptr=None,
+                        block_table=None, seqlens_k=None, max_seqlen_k, sinks=None, window=0,
+                        scale=None, num_splits=0, out=None, lse=None, return_lse=True,
+                        workspace=None, stream=None):
+    """sinkattn_decode over an fp8 e4m3 cache (uint8 codes, same layouts) with
+    optional per-KV-head scales. Returns (out, lse)."""
+    lib = load()
+    _req(q, torch.bfloat16, "q")
+    _req(k_cache, torch.uint8, "k_cache")
+    _req(v_cache, torch.uint8, "v_cache")
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale"), (sinks, "sinks")):
+        if t is not None:
+            _req(t, torch.float32, name)
+    batch, hq, d = q.shape
+    hkv = k_cache.shape[1]
+    if block_table is not None:
+        _req(block_table, torch.int32, "block_table")
+        _req(seqlens_k, torch.int32, "seqlens_k")
+        kv_rows, page_size, max_pages = k_cache.shape[0], k_cache.shape[2], block_table.shape[1]
+    else:
+        _req(kv_indptr, torch.int32, "kv_indptr")
+        kv_rows, page_size, max_pages = k_cache.shape[0], 0, 0
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((batch, hq), dtype=torch.float32, device=q.device)
+    need = lib.sinkattn_decode_workspace_size(batch, int(max_seqlen_k), hq, hkv, d, int(window),
+                                              int(num_splits))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    mask = Mask(1, int(window), float(d ** -0.5 if scale is None else scale))
+    st = lib.sinkattn_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                 _ptr(v_scale), _ptr(kv_indptr), _ptr(block_table),
+                                 _ptr(seqlens_k), kv_rows, max_pages, page_size, batch,
+                                 int(max_seqlen_k), hq, hkv, d, _ptr(sinks), mask,
+                                 int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(st, "sinkattn_decode_fp8")
     return out, lse
 
 

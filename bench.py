@@ -67,9 +67,11 @@ def decode_visible(lens, window):
 
 
 def decode_bytes(case):
-    """Algorithmic bytes of one decode call: every visible K and V row once,
-    plus q, out (bf16), lse and sinks (fp32)."""
-    kv = sum(decode_visible(case.seqlens_k, case.window)) * case.hkv * 64 * 2 * 2
+    """Algorithmic bytes of one decode call: every visible K and V row once
+    (2 bytes per element, 1 for an fp8 cache), plus q, out (bf16), lse and
+    sinks (fp32)."""
+    elem = 1 if getattr(case, "kv_dtype", "bf16") == "fp8" else 2
+    kv = sum(decode_visible(case.seqlens_k, case.window)) * case.hkv * 64 * elem * 2
     return kv + case.batch * case.hq * (64 * 2 * 2 + 4) + case.hq * 4
 
 
@@ -525,6 +527,43 @@ def extras(sa, S, dev, stream, pk, pk_kind):
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,
                      "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)", "flops": fl}
         del c, out, lse, dout, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+
+    # fp8 e4m3 cache with per-KV-head scales: contiguous (decode_contig's
+    # lengths) and paged (paged_decode's lengths, 16-token pages)
+    for name, mk in (("decode_contig_fp8", lambda: S.decode_contig_fp8(device="cuda")),
+                     ("paged_decode_fp8", lambda: S.make_decode(
+                         "paged_decode_fp8", S.uniform_lengths(256, 1024, 32768, seed=4000), 64,
+                         8, seed=4, sink_std=2.0, paged=True, device="cuda", kv_dtype="fp8"))):
+        c = mk()
+        sk, ks, vs = c.sinks.to(dev), c.k_scale.to(dev), c.v_scale.to(dev)
+        out = torch.empty_like(c.q)
+        lse = torch.empty((c.batch, c.hq), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(1, sa.sinkattn_decode_workspace_size(c.batch, c.max_seqlen_k, c.hq,
+                                                                   c.hkv)),
+                         dtype=torch.uint8, device=dev)
+        if c.paged:
+            bt, sl = c.block_table.to(dev), c.seqlens_k_t.to(dev)
+
+            def call():
+                sa.sinkattn_decode_fp8(c.q, c.k_cache, c.v_cache, k_scale=ks, v_scale=vs,
+                                       block_table=bt, seqlens_k=sl, max_seqlen_k=c.max_seqlen_k,
+                                       sinks=sk, out=out, lse=lse, workspace=ws)
+        else:
+            ind = c.kv_indptr.to(dev)
+
+            def call():
+                sa.sinkattn_decode_fp8(c.q, c.k, c.v, k_scale=ks, v_scale=vs, kv_indptr=ind,
+                                       max_seqlen_k=c.max_seqlen_k, sinks=sk, out=out, lse=lse,
+                                       workspace=ws)
+        for _ in range(3):
+            call()
+        t = time_calls(call, 10, stream, flush)
+        nb = decode_bytes(c)
+        res[name] = {"gbs": nb / t / 1e9, "ms": t * 1e3, "tokens_per_s": c.batch / t,
+                     "frac_of_hbm_peak": nb / t / 1e9 / float(pk["hbm_gbs"]),
+                     "kv_bytes": nb, "l2": "flushed before each call (256 MB write)"}
+        del c, out, lse, ws
         torch.cuda.empty_cache()
 
     for name, w in (("paged_decode", 0), ("paged_decode_w128", 128)):

@@ -209,6 +209,29 @@ sinkattn_status_t sinkattn_decode(const void *q, const void *k_cache, const void
                                   size_t workspace_bytes, void *stream);
 
 /*
+ * Decode over an fp8 KV cache (page "GPT-OSS on day 0": the model is served
+ * with FP8). Same arguments, layouts, plan, workspace
+ * (sinkattn_decode_workspace_size) and results as sinkattn_decode, except:
+ *   k_cache, v_cache  fp8 e4m3 (OCP "E4M3": 1 sign, 4 exponent bits with
+ *            bias 7, 3 mantissa bits; 0x7F / 0xFF are NaN), one byte per
+ *            element, with the same [rows, hkv, 64] or [pages, hkv, page, 64]
+ *            layout; rows are 64 bytes.
+ *   k_scale, v_scale  float32 [hkv] or NULL (= 1): key j of KV head g stands
+ *            for k_scale[g] * e4m3(k_cache[...]), likewise for v.
+ * The products run in fp16 (every e4m3 value is exact in fp16; q is rounded
+ * to fp16, clamped to +-65504) with fp32 accumulation.
+ */
+sinkattn_status_t sinkattn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *kv_indptr, const int32_t *block_table,
+                                      const int32_t *seqlens_k, int64_t kv_rows,
+                                      int max_pages_per_seq, int page_size, int batch,
+                                      int max_seqlen_k, int hq, int hkv, int head_dim,
+                                      const float *sinks, sinkattn_mask_t mask, int num_splits,
+                                      void *out, float *lse, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/*
  * Allocation-free decode. The pages have no counterpart to this entry point;
  * it exists for callers that cannot give the library a scratch buffer:
  * code running under a memory planner that owns all device memory, plugin
