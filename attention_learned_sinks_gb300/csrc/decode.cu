@@ -22,10 +22,14 @@
 //                                                  transpose, movmatrix)
 //
 // fp8 cache (page "GPT-OSS on day 0": FP8 serving): the ring holds e4m3 slabs
-// (half the bytes); after each slab lands the warp widens it to fp16 in a
-// per-warp shared-memory slab with the bf16 layout (e4m3 -> fp16 is exact),
-// and the MMAs run in fp16 (q converted once, P as one fp16 term). The K scale
-// folds into the softmax scale, the V scale into the final normalisation.
+// (half the bytes, 64-byte rows) and the MMA fragments are built straight
+// from them in registers (e4m3 -> fp16 is exact); the MMAs run in fp16 (q
+// converted once, P as one fp16 term). Two relabelings make every fragment a
+// plain load: the 64 dims of q and K are visited in the order that puts a
+// thread's four K bytes of one k-step side by side (a dot product does not
+// care about the order), and V^T's MMA rows stand for dims 2r and 2r+1 of each
+// 16-dim tile (undone when O is stored). The K scale folds into the softmax
+// scale, the V scale into the final normalisation.
 //
 // The per-warp states (m, d, O) are combined in shared memory; a sequence with
 // one block writes the final bf16 output directly, otherwise each block writes
@@ -53,15 +57,12 @@ constexpr int kSlabBytes = kSlab * kRowBytes;   // 4 KB of K (or of V)
 constexpr int kStageBytes = 2 * kSlabBytes;     // K + V
 constexpr int kWarpBytes = kStages * kStageBytes;
 constexpr int kSmemBytes = kWarps * kWarpBytes;  // 96 KB -> two blocks per SM
-// fp8: 64-byte rows in a 2-stage ring, plus one fp16 slab per warp that holds
-// the widened K slab, then the widened V slab (48 KB per block: four per SM;
-// the fp8 kernel is bound by latency inside each warp, so more warps beat a
-// deeper ring)
+// fp8: 64-byte rows in a 3-stage ring (48 KB per block: four per SM)
 constexpr int kRowBytes8 = kHeadDim;
 constexpr int kSlabBytes8 = kSlab * kRowBytes8;  // 2 KB
 constexpr int kStageBytes8 = 2 * kSlabBytes8;
-constexpr int kStages8 = 2;
-constexpr int kWarpBytes8 = kStages8 * kStageBytes8 + kSlabBytes;
+constexpr int kStages8 = 3;
+constexpr int kWarpBytes8 = kStages8 * kStageBytes8;
 constexpr int kSmemBytes8 = kWarps * kWarpBytes8;
 constexpr int kMaxGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -115,29 +116,10 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
 }
 
-// One 32-row fp8 slab (64-byte rows, unswizzled) -> fp16 with the swizzled
-// 128-byte-row layout that ldmatrix reads. Lane: rows lane/4 + 8i, 16-byte
-// chunk lane%4, so each access of the warp covers 512 contiguous bytes.
-__device__ __forceinline__ void widen_slab(uint32_t src, uint32_t dst, int lane) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int row = i * 8 + (lane >> 2), c = lane & 3;
-    uint32_t x0, x1, x2, x3;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                 : "r"(src + row * kRowBytes8 + c * 16));
-    uint32_t y[8];
-    e4m3x4_to_f16x4(x0, y[0], y[1]);
-    e4m3x4_to_f16x4(x1, y[2], y[3]);
-    e4m3x4_to_f16x4(x2, y[4], y[5]);
-    e4m3x4_to_f16x4(x3, y[6], y[7]);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(row, 2 * c)),
-                 "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3])
-                 : "memory");
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(row, 2 * c + 1)),
-                 "r"(y[4]), "r"(y[5]), "r"(y[6]), "r"(y[7])
-                 : "memory");
-  }
+// fp8 slab rows are 64 bytes; their four 16-byte chunks are XOR-swizzled by
+// row / 2, which makes the fragment loads below free of bank conflicts.
+__device__ __forceinline__ int swz8(int row, int chunk) {
+  return row * kRowBytes8 + ((chunk ^ ((row >> 1) & 3)) << 4);
 }
 
 template <bool kPaged, bool kFp8>
@@ -199,8 +181,10 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     };
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      qf[ks][0] = frag(ks * 16 + 2 * lc);
-      qf[ks][1] = frag(ks * 16 + 2 * lc + 8);
+      // fp8: k positions 2lc, 2lc+1 / 2lc+8, 2lc+9 of the k-step stand for
+      // dims 4lc, 4lc+1 / 4lc+2, 4lc+3 (the K fragments use the same order)
+      qf[ks][0] = frag(ks * 16 + (kFp8 ? 4 * lc : 2 * lc));
+      qf[ks][1] = frag(ks * 16 + (kFp8 ? 4 * lc + 2 : 2 * lc + 8));
     }
   }
   // fp8: the K scale multiplies every score, the V scale every output
@@ -239,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
         const bool ok = j < t1;
         const size_t off =
             ok ? kv_row<kPaged>(p, b, kv_base, j, g, s_pages, pg0, staged) + col * 16 : 0;
-        cp_async_16(kdst + row * kRowBytes8 + col * 16, p.k8 + off, ok ? 16u : 0u);
-        cp_async_16(vdst + row * kRowBytes8 + col * 16, p.v8 + off, ok ? 16u : 0u);
+        cp_async_16(kdst + swz8(row, col), p.k8 + off, ok ? 16u : 0u);
+        cp_async_16(vdst + swz8(row, col), p.v8 + off, ok ? 16u : 0u);
       }
       return;
     }
@@ -272,18 +256,11 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     cp_async_commit();
 
     const int slab0 = t0 + (warp + it * kWarps) * kSlab;
-    uint32_t kb, vb;
-    const uint32_t k8 = wbase + (it % kStages8) * kStageBytes8;
-    if (kFp8) {
-      // widen the K slab into the warp's fp16 slab (the previous iteration's
-      // reads of it are complete: __syncwarp above); V follows after the scores
-      kb = vb = wbase + kStages8 * kStageBytes8;
-      widen_slab(k8, kb, lane);
-      __syncwarp();
-    } else {
-      kb = wbase + (it % kStages) * kStageBytes;
-      vb = kb + kSlabBytes;
-    }
+    const uint32_t kb = wbase + (it % kRing) * (kFp8 ? kStageBytes8 : kStageBytes);
+    const uint32_t vb = kb + (kFp8 ? kSlabBytes8 : kSlabBytes);
+    // generic pointers to the same fp8 slabs, for the fragment loads
+    const uint8_t *k8 = smem + (kb - smem_u32(smem));
+    const uint8_t *v8 = k8 + kSlabBytes8;
     const int mi = lane >> 3, mr = lane & 7;
 
     // scores: two 16-token m-tiles
@@ -295,12 +272,19 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         uint32_t a[4];
-        const int row = mt * 16 + (mi & 1) * 8 + mr;
-        ldmatrix_x4(kb + swz(row, ks * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
-        if (kFp8)
+        if (kFp8) {
+          // rows lr and lr + 8: dims 4lc..4lc+3 of the k-step, one word each
+          const int r0 = mt * 16 + lr, r1 = r0 + 8;
+          const uint32_t x0 = *reinterpret_cast<const uint32_t *>(k8 + swz8(r0, ks) + 4 * lc);
+          const uint32_t x1 = *reinterpret_cast<const uint32_t *>(k8 + swz8(r1, ks) + 4 * lc);
+          e4m3x4_to_f16x4(x0, a[0], a[2]);
+          e4m3x4_to_f16x4(x1, a[1], a[3]);
           mma_f16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
-        else
+        } else {
+          const int row = mt * 16 + (mi & 1) * 8 + mr;
+          ldmatrix_x4(kb + swz(row, ks * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
           mma_bf16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
+        }
       }
     }
     // scale to log2 units, mask the ragged end of the chunk, tile maximum
@@ -363,22 +347,28 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
       o[dt][2] *= al0;
       o[dt][3] *= al1;
     }
-    if (kFp8) {  // the scores are in registers: the fp16 slab now takes V
-      __syncwarp();
-      widen_slab(k8 + kSlabBytes8, vb, lane);
-      __syncwarp();
-    }
     // O^T += V^T P^T
 #pragma unroll
     for (int dt = 0; dt < 4; ++dt)
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         uint32_t a[4];
-        const int row = mt * 16 + (mi >> 1) * 8 + mr;
-        ldmatrix_x4_trans(vb + swz(row, dt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
         if (kFp8) {
+          // MMA rows lr / lr + 8 are dims 2lr / 2lr + 1 of the 16-dim tile:
+          // one 16-bit load per token (tokens t, t+1, t+8, t+9), bytes paired
+          // across tokens with a byte permute
+          const int t = mt * 16 + 2 * lc;
+          const int off = 2 * lr;
+          const uint32_t w0 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t, dt) + off);
+          const uint32_t w1 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t + 1, dt) + off);
+          const uint32_t w2 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t + 8, dt) + off);
+          const uint32_t w3 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t + 9, dt) + off);
+          e4m3x4_to_f16x4(__byte_perm(w0, w1, 0x5140), a[0], a[1]);
+          e4m3x4_to_f16x4(__byte_perm(w2, w3, 0x5140), a[2], a[3]);
           mma_f16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
         } else {
+          const int row = mt * 16 + (mi >> 1) * 8 + mr;
+          ldmatrix_x4_trans(vb + swz(row, dt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
           mma_bf16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
           mma_bf16_16816(o[dt], a, pl[mt][0], pl[mt][1]);
         }
@@ -403,13 +393,16 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     sm_d[warp * 8 + 2 * lc] = d0;
     sm_d[warp * 8 + 2 * lc + 1] = d1;
   }
+  // O^T rows lr / lr + 8 of dim tile dt are dims dt*16 + lr / + 8 (bf16),
+  // dt*16 + 2lr / + 1 (fp8)
+  const int dr0 = kFp8 ? 2 * lr : lr, dr1 = kFp8 ? 2 * lr + 1 : lr + 8;
 #pragma unroll
   for (int dt = 0; dt < 4; ++dt) {
     float *ow = sm_o + warp * 512;
-    ow[(2 * lc) * 64 + dt * 16 + lr] = o[dt][0];
-    ow[(2 * lc + 1) * 64 + dt * 16 + lr] = o[dt][1];
-    ow[(2 * lc) * 64 + dt * 16 + lr + 8] = o[dt][2];
-    ow[(2 * lc + 1) * 64 + dt * 16 + lr + 8] = o[dt][3];
+    ow[(2 * lc) * 64 + dt * 16 + dr0] = o[dt][0];
+    ow[(2 * lc + 1) * 64 + dt * 16 + dr0] = o[dt][1];
+    ow[(2 * lc) * 64 + dt * 16 + dr1] = o[dt][2];
+    ow[(2 * lc + 1) * 64 + dt * 16 + dr1] = o[dt][3];
   }
   __syncthreads();
 
