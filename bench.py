@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="run one extra workload by name and print its numbers only "
+                         "(for profiling one kernel)")
     return ap.parse_args()
 
 
@@ -299,6 +302,12 @@ def run_ours(args):
     sa.load()
     stream = torch.cuda.current_stream()
     pk, pk_kind = peaks()
+    if args.only:
+        res = extras(sa, S, dev, stream, pk, pk_kind, only=args.only)
+        if args.only not in res:
+            raise SystemExit("unknown workload: " + args.only)
+        print(json.dumps({"only": args.only, **res[args.only]}))
+        return 0
 
     # ---- headline: contiguous decode, inputs resident in HBM ----
     case = S.decode_contig(device="cuda")
@@ -426,7 +435,7 @@ def run_ours(args):
     return 0
 
 
-def extras(sa, S, dev, stream, pk, pk_kind):
+def extras(sa, S, dev, stream, pk, pk_kind, only=None):
     """Prefill TFLOP/s and paged-decode GB/s on the other workloads."""
     import torch
     res = {}
@@ -445,6 +454,8 @@ def extras(sa, S, dev, stream, pk, pk_kind):
             ("chunked_prefill", lambda: S.chunked_prefill(device="cuda"), 0),
             ("long_context_prefill", lambda: S.long_context_prefill(device="cuda"), 0),
             ("long_context_prefill_unsplit", lambda: S.long_context_prefill(device="cuda"), 1)):
+        if only is not None and name != only:
+            continue
         c = mk()
         cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
         sk = c.sinks.to(dev)
@@ -476,6 +487,8 @@ def extras(sa, S, dev, stream, pk, pk_kind):
     # staging, then the same kernel; timed as one call (4 launches)
     for name, mk in (("paged_chunked_prefill", lambda: S.paged_chunked_prefill(device="cuda")),
                      ("paged_prefill_batch", lambda: S.paged_prefill_batch(device="cuda"))):
+        if only is not None and name != only:
+            continue
         c = mk()
         cq, bt, sl = c.cu_seqlens_q.to(dev), c.block_table.to(dev), c.seqlens_k_t.to(dev)
         sk = c.sinks.to(dev)
@@ -506,6 +519,8 @@ def extras(sa, S, dev, stream, pk, pk_kind):
     # backward of the varlen prefill (dq, dk, dv, dsinks), forward outputs
     # precomputed; algorithmic flops: 5 products of 2 * 64 per visible pair
     for name, w in (("varlen_backward", 0), ("varlen_backward_w128", 128)):
+        if only is not None and name != only:
+            continue
         c = S.varlen_prefill(window=w, device="cuda")
         cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
         sk = c.sinks.to(dev)
@@ -538,6 +553,8 @@ def extras(sa, S, dev, stream, pk, pk_kind):
                      ("paged_decode_fp8", lambda: S.make_decode(
                          "paged_decode_fp8", S.uniform_lengths(256, 1024, 32768, seed=4000), 64,
                          8, seed=4, sink_std=2.0, paged=True, device="cuda", kv_dtype="fp8"))):
+        if only is not None and name != only:
+            continue
         c = mk()
         sk, ks, vs = c.sinks.to(dev), c.k_scale.to(dev), c.v_scale.to(dev)
         out = torch.empty_like(c.q)
@@ -570,6 +587,8 @@ def extras(sa, S, dev, stream, pk, pk_kind):
         torch.cuda.empty_cache()
 
     for name, w in (("paged_decode", 0), ("paged_decode_w128", 128)):
+        if only is not None and name != only:
+            continue
         c = S.paged_decode(window=w, device="cuda")
         bt, sl, sk = c.block_table.to(dev), c.seqlens_k_t.to(dev), c.sinks.to(dev)
         out = torch.empty_like(c.q)
