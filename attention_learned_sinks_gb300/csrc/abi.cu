@@ -190,11 +190,11 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
 
 size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int hkv, int head_dim,
                                       int window, int num_splits) {
-  if (batch <= 0 || hq <= 0 || hkv <= 0 || head_dim != kHeadDim || max_seqlen_k < 0 ||
+  if (batch <= 0 || hq <= 0 || hkv <= 0 || !decode_head_dim_ok(head_dim) || max_seqlen_k < 0 ||
       window < 0 || num_splits < 0)
     return 0;
   const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, window, num_splits);
-  return decode_workspace_layout(batch, hq, hkv, plan).bytes;
+  return decode_workspace_layout(batch, hq, hkv, plan, head_dim).bytes;
 }
 
 }  // extern "C"
@@ -212,7 +212,7 @@ sinkattn_status_t decode_impl(const void *q, const void *k_cache, const void *v_
   if (batch < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || num_splits < 0 ||
       kv_rows < 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (!decode_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   if (hq / hkv > 8) return SINKATTN_ERR_UNSUPPORTED;
   const bool paged = block_table != nullptr;
   if (paged == (kv_indptr != nullptr)) return SINKATTN_ERR_INVALID_ARGUMENT;
@@ -230,7 +230,7 @@ sinkattn_status_t decode_impl(const void *q, const void *k_cache, const void *v_
   if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
   const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
   if (plan.max_splits > 1) {
-    const size_t need = decode_workspace_layout(batch, hq, hkv, plan).bytes;
+    const size_t need = decode_workspace_layout(batch, hq, hkv, plan, head_dim).bytes;
     if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
   }
@@ -255,6 +255,7 @@ sinkattn_status_t decode_impl(const void *q, const void *k_cache, const void *v_
   a.workspace = workspace;
   a.plan = plan;
   a.fp8 = fp8;
+  a.head_dim = head_dim;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));

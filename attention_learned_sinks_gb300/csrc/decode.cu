@@ -40,6 +40,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/sinkattn.h"
 #include "launch.h"
@@ -50,23 +51,30 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlab = 32;                       // tokens per warp step
-constexpr int kStages = 3;                      // per-warp pipeline depth
-constexpr int kRowBytes = kHeadDim * 2;         // one K or V row: 128 B
-constexpr int kSlabBytes = kSlab * kRowBytes;   // 4 KB of K (or of V)
-constexpr int kStageBytes = 2 * kSlabBytes;     // K + V
-constexpr int kWarpBytes = kStages * kStageBytes;
-constexpr int kSmemBytes = kWarps * kWarpBytes;  // 96 KB -> two blocks per SM
-// fp8: 64-byte rows in a 3-stage ring (48 KB per block: four per SM)
-constexpr int kRowBytes8 = kHeadDim;
-constexpr int kSlabBytes8 = kSlab * kRowBytes8;  // 2 KB
-constexpr int kStageBytes8 = 2 * kSlabBytes8;
-constexpr int kStages8 = 3;
-constexpr int kWarpBytes8 = kStages8 * kStageBytes8;
-constexpr int kSmemBytes8 = kWarps * kWarpBytes8;
+constexpr int kStages = 3;  // per-warp pipeline depth (both caches)
 constexpr int kMaxGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// Shapes for head dimension D (64 or 128). A warp step covers kSlab tokens:
+// 32 at D = 64, 16 at D = 128, so that a slab of K and V is the same number
+// of bytes for both and the shared memory per block stays at 96 KB (bf16,
+// two blocks per SM) or 48 KB (fp8, four per SM).
+template <int D>
+struct DCfg {
+  static constexpr int kSlab = D == 64 ? 32 : 16;
+  static constexpr int kMT = kSlab / 16;         // 16-token m-tiles per slab
+  static constexpr int kKS = D / 16;             // k-steps of Q K^T, dim tiles of P V
+  static constexpr int kRowBytes = D * 2;        // bf16 row
+  static constexpr int kSlabBytes = kSlab * kRowBytes;
+  static constexpr int kStageBytes = 2 * kSlabBytes;
+  static constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kRowBytes8 = D;           // fp8 row
+  static constexpr int kSlabBytes8 = kSlab * kRowBytes8;
+  static constexpr int kStageBytes8 = 2 * kSlabBytes8;
+  static constexpr int kSmemBytes8 = kWarps * kStages * kStageBytes8;
+  static constexpr int kOutPer = D / 16;         // output dims per thread in the epilogue
+};
 
 struct Params {
   const __nv_bfloat16 *q, *k, *v;
@@ -98,32 +106,38 @@ __device__ __forceinline__ int page_slot(const Params &p, int j) {
 
 // Element offset of row (token j, KV head g) of sequence b in the K/V cache.
 // Paged: pages[] holds the ids of pages pg0.. when `staged`.
-template <bool kPaged>
+template <int D, bool kPaged>
 __device__ __forceinline__ size_t kv_row(const Params &p, int b, int kv_base, int j, int g,
                                          const int *pages, int pg0, bool staged) {
   if (kPaged) {
     const int pi = page_index(p, j);
     const int page = staged ? pages[pi - pg0]
                             : __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pi);
-    return ((static_cast<size_t>(page) * p.hkv + g) * p.page_size + page_slot(p, j)) * kHeadDim;
+    return ((static_cast<size_t>(page) * p.hkv + g) * p.page_size + page_slot(p, j)) * D;
   }
-  return (static_cast<size_t>(kv_base + j) * p.hkv + g) * kHeadDim;
+  return (static_cast<size_t>(kv_base + j) * p.hkv + g) * D;
 }
 
-// 128-byte rows, 16-byte chunks XOR-swizzled by row so that ldmatrix of 8 rows
-// of one chunk column touches 8 different bank groups.
+// bf16 rows (128 or 256 bytes): 16-byte chunks XOR-swizzled by row so that
+// ldmatrix of 8 rows of one chunk column touches 8 different bank groups.
+template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return static_cast<uint32_t>(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
+  return static_cast<uint32_t>(row * DCfg<D>::kRowBytes + ((chunk ^ (row & 7)) << 4));
 }
 
-// fp8 slab rows are 64 bytes; their four 16-byte chunks are XOR-swizzled by
-// row / 2, which makes the fragment loads below free of bank conflicts.
+// fp8 rows (64 or 128 bytes): chunks XOR-swizzled by row / 2 (four chunks) or
+// by row (eight chunks), which makes the fragment loads below free of bank
+// conflicts.
+template <int D>
 __device__ __forceinline__ int swz8(int row, int chunk) {
-  return row * kRowBytes8 + ((chunk ^ ((row >> 1) & 3)) << 4);
+  const int x = D == 64 ? ((row >> 1) & 3) : (row & 7);
+  return row * DCfg<D>::kRowBytes8 + ((chunk ^ x) << 4);
 }
 
-template <bool kPaged, bool kFp8>
+template <int D, bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Params p) {
+  using C = DCfg<D>;
+  constexpr int kSlab = C::kSlab, kMT = C::kMT, kKS = C::kKS;
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,11 +181,11 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
 
   // Q^T as the B operand of S^T = K Q^T: lane (lr, lc) holds head lr,
   // dims ks*16 + 2lc + {0,1} and + 8 (fp8 cache: as fp16, clamped to its range).
-  uint32_t qf[4][2];
+  uint32_t qf[kKS][2];
   {
     const bool valid = lr < p.group;
     const __nv_bfloat16 *qrow =
-        p.q + (static_cast<size_t>(b) * p.hq + g * p.group + (valid ? lr : 0)) * kHeadDim;
+        p.q + (static_cast<size_t>(b) * p.hq + g * p.group + (valid ? lr : 0)) * D;
     auto frag = [&](int at) -> uint32_t {
       if (!valid) return 0u;
       const uint32_t x = *reinterpret_cast<const uint32_t *>(qrow + at);
@@ -180,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
       return pack_f16x2(fminf(fmaxf(bf16_lo(x), -lim), lim), fminf(fmaxf(bf16_hi(x), -lim), lim));
     };
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
+    for (int ks = 0; ks < kKS; ++ks) {
       // fp8: k positions 2lc, 2lc+1 / 2lc+8, 2lc+9 of the k-step stand for
       // dims 4lc, 4lc+1 / 4lc+2, 4lc+3 (the K fragments use the same order)
       qf[ks][0] = frag(ks * 16 + (kFp8 ? 4 * lc : 2 * lc));
@@ -202,87 +216,92 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     m1 = p.sinks[g * p.group + h1] * kLog2e;
     if (lr == 0) d0 = d1 = 1.f;
   }
-  float o[4][4];
+  float o[kKS][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kKS; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
 
-  const uint32_t wbase = smem_u32(smem) + warp * (kFp8 ? kWarpBytes8 : kWarpBytes);
+  const uint32_t wbase =
+      smem_u32(smem) + warp * kStages * (kFp8 ? C::kStageBytes8 : C::kStageBytes);
 
   auto load_slab = [&](int i) {
     const int slab0 = t0 + (warp + i * kWarps) * kSlab;
     if (kFp8) {
-      const uint32_t kdst = wbase + (i % kStages8) * kStageBytes8;
-      const uint32_t vdst = kdst + kSlabBytes8;
+      // kSlab rows of D/16 chunks: 128 chunks, four per lane
+      constexpr int kCols = D / 16;
+      const uint32_t kdst = wbase + (i % kStages) * C::kStageBytes8;
+      const uint32_t vdst = kdst + C::kSlabBytes8;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int row = r * 8 + (lane >> 2);
-        const int col = lane & 3;
+        const int idx = r * 32 + lane;
+        const int row = idx / kCols, col = idx % kCols;
         const int j = slab0 + row;
         const bool ok = j < t1;
         const size_t off =
-            ok ? kv_row<kPaged>(p, b, kv_base, j, g, s_pages, pg0, staged) + col * 16 : 0;
-        cp_async_16(kdst + swz8(row, col), p.k8 + off, ok ? 16u : 0u);
-        cp_async_16(vdst + swz8(row, col), p.v8 + off, ok ? 16u : 0u);
+            ok ? kv_row<D, kPaged>(p, b, kv_base, j, g, s_pages, pg0, staged) + col * 16 : 0;
+        cp_async_16(kdst + swz8<D>(row, col), p.k8 + off, ok ? 16u : 0u);
+        cp_async_16(vdst + swz8<D>(row, col), p.v8 + off, ok ? 16u : 0u);
       }
       return;
     }
-    const uint32_t kdst = wbase + (i % kStages) * kStageBytes;
-    const uint32_t vdst = kdst + kSlabBytes;
+    // kSlab rows of D/8 chunks: 256 chunks, eight per lane
+    constexpr int kCols = D / 8;
+    const uint32_t kdst = wbase + (i % kStages) * C::kStageBytes;
+    const uint32_t vdst = kdst + C::kSlabBytes;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      const int row = r * 4 + (lane >> 3);
-      const int col = lane & 7;
+      const int idx = r * 32 + lane;
+      const int row = idx / kCols, col = idx % kCols;
       const int j = slab0 + row;
       const bool ok = j < t1;
-      const size_t off = ok ? kv_row<kPaged>(p, b, kv_base, j, g, s_pages, pg0, staged) + col * 8 : 0;
-      cp_async_16(kdst + swz(row, col), p.k + off, ok ? 16u : 0u);
-      cp_async_16(vdst + swz(row, col), p.v + off, ok ? 16u : 0u);
+      const size_t off =
+          ok ? kv_row<D, kPaged>(p, b, kv_base, j, g, s_pages, pg0, staged) + col * 8 : 0;
+      cp_async_16(kdst + swz<D>(row, col), p.k + off, ok ? 16u : 0u);
+      cp_async_16(vdst + swz<D>(row, col), p.v + off, ok ? 16u : 0u);
     }
   };
 
-  constexpr int kRing = kFp8 ? kStages8 : kStages;
 #pragma unroll
-  for (int i = 0; i < kRing - 1; ++i) {
+  for (int i = 0; i < kStages - 1; ++i) {
     if (i < my_slabs) load_slab(i);
     cp_async_commit();
   }
 
   for (int it = 0; it < my_slabs; ++it) {
-    cp_async_wait<kRing - 2>();
+    cp_async_wait<kStages - 2>();
     __syncwarp();
-    if (it + kRing - 1 < my_slabs) load_slab(it + kRing - 1);
+    if (it + kStages - 1 < my_slabs) load_slab(it + kStages - 1);
     cp_async_commit();
 
     const int slab0 = t0 + (warp + it * kWarps) * kSlab;
-    const uint32_t kb = wbase + (it % kRing) * (kFp8 ? kStageBytes8 : kStageBytes);
-    const uint32_t vb = kb + (kFp8 ? kSlabBytes8 : kSlabBytes);
+    const uint32_t kb = wbase + (it % kStages) * (kFp8 ? C::kStageBytes8 : C::kStageBytes);
+    const uint32_t vb = kb + (kFp8 ? C::kSlabBytes8 : C::kSlabBytes);
     // generic pointers to the same fp8 slabs, for the fragment loads
     const uint8_t *k8 = smem + (kb - smem_u32(smem));
-    const uint8_t *v8 = k8 + kSlabBytes8;
+    const uint8_t *v8 = k8 + C::kSlabBytes8;
     const int mi = lane >> 3, mr = lane & 7;
 
-    // scores: two 16-token m-tiles
-    float s[2][4];
+    // scores: kMT 16-token m-tiles
+    float s[kMT][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[mt][e] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
+      for (int ks = 0; ks < kKS; ++ks) {
         uint32_t a[4];
         if (kFp8) {
           // rows lr and lr + 8: dims 4lc..4lc+3 of the k-step, one word each
           const int r0 = mt * 16 + lr, r1 = r0 + 8;
-          const uint32_t x0 = *reinterpret_cast<const uint32_t *>(k8 + swz8(r0, ks) + 4 * lc);
-          const uint32_t x1 = *reinterpret_cast<const uint32_t *>(k8 + swz8(r1, ks) + 4 * lc);
+          const uint32_t x0 = *reinterpret_cast<const uint32_t *>(k8 + swz8<D>(r0, ks) + 4 * lc);
+          const uint32_t x1 = *reinterpret_cast<const uint32_t *>(k8 + swz8<D>(r1, ks) + 4 * lc);
           e4m3x4_to_f16x4(x0, a[0], a[2]);
           e4m3x4_to_f16x4(x1, a[1], a[3]);
           mma_f16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
         } else {
           const int row = mt * 16 + (mi & 1) * 8 + mr;
-          ldmatrix_x4(kb + swz(row, ks * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
+          ldmatrix_x4(kb + swz<D>(row, ks * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
           mma_bf16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
         }
       }
@@ -290,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     // scale to log2 units, mask the ragged end of the chunk, tile maximum
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = slab0 + mt * 16 + lr + ((e & 2) ? 8 : 0);
@@ -317,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     // carry 16 significant bits: a single bf16 P (8 bits) alone would add
     // about 1.6e-3 rms relative error to the output. With the fp16 MMAs of
     // the fp8 cache P is one fp16 term (11 bits).
-    uint32_t pb[2][2], pl[2][2];
+    uint32_t pb[kMT][2], pl[kMT][2];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int mt = 0; mt < kMT; ++mt) {
       const float p0 = fast_exp2(s[mt][0] - base0), p1 = fast_exp2(s[mt][1] - base1);
       const float p2 = fast_exp2(s[mt][2] - base0), p3 = fast_exp2(s[mt][3] - base1);
       sum0 += p0 + p2;
@@ -341,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     d0 = d0 * al0 + sum0;
     d1 = d1 * al1 + sum1;
 #pragma unroll
-    for (int dt = 0; dt < 4; ++dt) {
+    for (int dt = 0; dt < kKS; ++dt) {
       o[dt][0] *= al0;
       o[dt][1] *= al1;
       o[dt][2] *= al0;
@@ -349,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
     }
     // O^T += V^T P^T
 #pragma unroll
-    for (int dt = 0; dt < 4; ++dt)
+    for (int dt = 0; dt < kKS; ++dt)
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < kMT; ++mt) {
         uint32_t a[4];
         if (kFp8) {
           // MMA rows lr / lr + 8 are dims 2lr / 2lr + 1 of the 16-dim tile:
@@ -359,16 +378,16 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
           // across tokens with a byte permute
           const int t = mt * 16 + 2 * lc;
           const int off = 2 * lr;
-          const uint32_t w0 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t, dt) + off);
-          const uint32_t w1 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t + 1, dt) + off);
-          const uint32_t w2 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t + 8, dt) + off);
-          const uint32_t w3 = *reinterpret_cast<const uint16_t *>(v8 + swz8(t + 9, dt) + off);
+          const uint32_t w0 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t, dt) + off);
+          const uint32_t w1 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t + 1, dt) + off);
+          const uint32_t w2 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t + 8, dt) + off);
+          const uint32_t w3 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t + 9, dt) + off);
           e4m3x4_to_f16x4(__byte_perm(w0, w1, 0x5140), a[0], a[1]);
           e4m3x4_to_f16x4(__byte_perm(w2, w3, 0x5140), a[2], a[3]);
           mma_f16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
         } else {
           const int row = mt * 16 + (mi >> 1) * 8 + mr;
-          ldmatrix_x4_trans(vb + swz(row, dt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
+          ldmatrix_x4_trans(vb + swz<D>(row, dt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
           mma_bf16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
           mma_bf16_16816(o[dt], a, pl[mt][0], pl[mt][1]);
         }
@@ -386,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
   __syncthreads();  // every warp is done with its ring
   float *sm_m = reinterpret_cast<float *>(smem);          // [4][8]
   float *sm_d = sm_m + kWarps * kMaxGroup;                 // [4][8]
-  float *sm_o = sm_d + kWarps * kMaxGroup;                 // [4][8][64]
+  float *sm_o = sm_d + kWarps * kMaxGroup;                 // [4][8][D]
   if (lr == 0) {
     sm_m[warp * 8 + 2 * lc] = m0;
     sm_m[warp * 8 + 2 * lc + 1] = m1;
@@ -397,32 +416,39 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
   // dt*16 + 2lr / + 1 (fp8)
   const int dr0 = kFp8 ? 2 * lr : lr, dr1 = kFp8 ? 2 * lr + 1 : lr + 8;
 #pragma unroll
-  for (int dt = 0; dt < 4; ++dt) {
-    float *ow = sm_o + warp * 512;
-    ow[(2 * lc) * 64 + dt * 16 + dr0] = o[dt][0];
-    ow[(2 * lc + 1) * 64 + dt * 16 + dr0] = o[dt][1];
-    ow[(2 * lc) * 64 + dt * 16 + dr1] = o[dt][2];
-    ow[(2 * lc + 1) * 64 + dt * 16 + dr1] = o[dt][3];
+  for (int dt = 0; dt < kKS; ++dt) {
+    float *ow = sm_o + warp * kMaxGroup * D;
+    ow[(2 * lc) * D + dt * 16 + dr0] = o[dt][0];
+    ow[(2 * lc + 1) * D + dt * 16 + dr0] = o[dt][1];
+    ow[(2 * lc) * D + dt * 16 + dr1] = o[dt][2];
+    ow[(2 * lc + 1) * D + dt * 16 + dr1] = o[dt][3];
   }
   __syncthreads();
 
   const int tid = threadIdx.x;
-  const int hh = tid >> 4;          // head within the group
-  const int c0 = (tid & 15) * 4;    // 4 output dims
+  const int hh = tid >> 4;                        // head within the group
+  constexpr int kOut = C::kOutPer;                // output dims per thread
+  const int c0 = (tid & 15) * kOut;
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 + hh]);
   const float baseM = M == -INFINITY ? 0.f : M;
-  float Dn = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float Dn = 0.f, acc[kOut];
+#pragma unroll
+  for (int e = 0; e < kOut; ++e) acc[e] = 0.f;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
     const float f = fast_exp2(sm_m[w * 8 + hh] - baseM);
     Dn += f * sm_d[w * 8 + hh];
-    const float4 ov = *reinterpret_cast<const float4 *>(sm_o + w * 512 + hh * 64 + c0);
-    acc[0] += f * ov.x;
-    acc[1] += f * ov.y;
-    acc[2] += f * ov.z;
-    acc[3] += f * ov.w;
+#pragma unroll
+    for (int q4 = 0; q4 < kOut / 4; ++q4) {
+      const float4 ov =
+          *reinterpret_cast<const float4 *>(sm_o + (w * kMaxGroup + hh) * D + c0 + 4 * q4);
+      acc[4 * q4] += f * ov.x;
+      acc[4 * q4 + 1] += f * ov.y;
+      acc[4 * q4 + 2] += f * ov.z;
+      acc[4 * q4 + 3] += f * ov.w;
+    }
   }
   const float inv = Dn > 0.f ? out_scale / Dn : 0.f;
   // block lse in natural log (-inf when nothing is visible and no sink)
@@ -430,13 +456,20 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
   const bool head_ok = hh < p.group;
   const int qh = g * p.group + hh;
   const size_t row_h = static_cast<size_t>(b) * p.hq + qh;
+  // kOut values times `mul` -> bf16 at out[row_h][c0...]
+  auto store_out = [&](const float *x, float mul) {
+#pragma unroll
+    for (int q4 = 0; q4 < kOut / 4; ++q4) {
+      uint2 pk;
+      pk.x = pack_bf16x2(x[4 * q4] * mul, x[4 * q4 + 1] * mul);
+      pk.y = pack_bf16x2(x[4 * q4 + 2] * mul, x[4 * q4 + 3] * mul);
+      *reinterpret_cast<uint2 *>(p.out + row_h * D + c0 + 4 * q4) = pk;
+    }
+  };
 
   if (nsplit == 1) {
     if (head_ok) {
-      uint2 pk;
-      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<uint2 *>(p.out + row_h * kHeadDim + c0) = pk;
+      store_out(acc, inv);
       if (p.lse != nullptr && (tid & 15) == 0) p.lse[row_h] = blse;
     }
     return;
@@ -444,8 +477,11 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
 
   const size_t rows_hq = static_cast<size_t>(p.batch) * p.hq;
   if (head_ok) {
-    float4 pv = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<float4 *>(p.part_o + (split * rows_hq + row_h) * kHeadDim + c0) = pv;
+#pragma unroll
+    for (int q4 = 0; q4 < kOut / 4; ++q4)
+      *reinterpret_cast<float4 *>(p.part_o + (split * rows_hq + row_h) * D + c0 + 4 * q4) =
+          make_float4(acc[4 * q4] * inv, acc[4 * q4 + 1] * inv, acc[4 * q4 + 2] * inv,
+                      acc[4 * q4 + 3] * inv);
     if ((tid & 15) == 0) p.part_lse[split * rows_hq + row_h] = blse;
   }
   __threadfence();
@@ -463,26 +499,27 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
   if (head_ok) {
     float Mx = -INFINITY;
     for (int k = 0; k < nsplit; ++k) Mx = fmaxf(Mx, __ldcg(p.part_lse + k * rows_hq + row_h));
-    float W = 0.f, r[4] = {0.f, 0.f, 0.f, 0.f};
+    float W = 0.f, r[kOut];
+#pragma unroll
+    for (int e = 0; e < kOut; ++e) r[e] = 0.f;
     if (Mx != -INFINITY) {
       for (int k = 0; k < nsplit; ++k) {
         const float l = __ldcg(p.part_lse + k * rows_hq + row_h);
         const float w = fast_exp2((l - Mx) * kLog2e);
         if (w == 0.f) continue;
-        const float4 ov =
-            __ldcg(reinterpret_cast<const float4 *>(p.part_o + (k * rows_hq + row_h) * kHeadDim + c0));
         W += w;
-        r[0] += w * ov.x;
-        r[1] += w * ov.y;
-        r[2] += w * ov.z;
-        r[3] += w * ov.w;
+#pragma unroll
+        for (int q4 = 0; q4 < kOut / 4; ++q4) {
+          const float4 ov = __ldcg(reinterpret_cast<const float4 *>(
+              p.part_o + (k * rows_hq + row_h) * D + c0 + 4 * q4));
+          r[4 * q4] += w * ov.x;
+          r[4 * q4 + 1] += w * ov.y;
+          r[4 * q4 + 2] += w * ov.z;
+          r[4 * q4 + 3] += w * ov.w;
+        }
       }
     }
-    const float iw = W > 0.f ? 1.f / W : 0.f;
-    uint2 pk;
-    pk.x = pack_bf16x2(r[0] * iw, r[1] * iw);
-    pk.y = pack_bf16x2(r[2] * iw, r[3] * iw);
-    *reinterpret_cast<uint2 *>(p.out + row_h * kHeadDim + c0) = pk;
+    store_out(r, W > 0.f ? 1.f / W : 0.f);
     if (p.lse != nullptr && (tid & 15) == 0)
       p.lse[row_h] = W > 0.f ? Mx + fast_log2(W) * kLn2 : -INFINITY;
   }
@@ -511,7 +548,7 @@ DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num
     const long cap = (span + 63) / 64;  // at most 64 splits
     if (chunk < cap) chunk = cap;
   }
-  const long unit = kWarps * kSlab;
+  const long unit = kWarps * 32;  // whole warp steps at either head_dim (32 or 16 tokens)
   chunk = (chunk + unit - 1) / unit * unit;
   DecodePlan plan;
   plan.chunk = static_cast<int>(chunk);
@@ -520,11 +557,12 @@ DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num
   return plan;
 }
 
-DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const DecodePlan &plan) {
+DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const DecodePlan &plan,
+                                        int head_dim) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   DecodeWorkspace w;
   const size_t rows = static_cast<size_t>(plan.max_splits) * batch * hq;
-  w.off_lse = up(rows * kHeadDim * sizeof(float));
+  w.off_lse = up(rows * head_dim * sizeof(float));
   w.off_counters = w.off_lse + up(rows * sizeof(float));
   w.bytes = w.off_counters + up(static_cast<size_t>(batch) * hkv * sizeof(unsigned));
   return w;
@@ -559,7 +597,7 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   p.scale_log2 = a.scale * kLog2e;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.lse = a.lse;
-  const DecodeWorkspace w = decode_workspace_layout(a.batch, a.hq, a.hkv, a.plan);
+  const DecodeWorkspace w = decode_workspace_layout(a.batch, a.hq, a.hkv, a.plan, a.head_dim);
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
   p.part_o = reinterpret_cast<float *>(ws);
   p.part_lse = reinterpret_cast<float *>(ws + w.off_lse);
@@ -575,17 +613,25 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
     kernel<<<grid, kThreads, smem, stream>>>(p);
   };
   const bool paged = a.block_table != nullptr;
-  if (a.fp8) {
-    if (paged)
-      go(decode_kernel<true, true>, kSmemBytes8);
-    else
-      go(decode_kernel<false, true>, kSmemBytes8);
-  } else {
-    if (paged)
-      go(decode_kernel<true, false>, kSmemBytes);
-    else
-      go(decode_kernel<false, false>, kSmemBytes);
-  }
+  auto pick = [&](auto dim) {
+    constexpr int D = decltype(dim)::value;
+    using C = DCfg<D>;
+    if (a.fp8) {
+      if (paged)
+        go(decode_kernel<D, true, true>, C::kSmemBytes8);
+      else
+        go(decode_kernel<D, false, true>, C::kSmemBytes8);
+    } else {
+      if (paged)
+        go(decode_kernel<D, true, false>, C::kSmemBytes);
+      else
+        go(decode_kernel<D, false, false>, C::kSmemBytes);
+    }
+  };
+  if (a.head_dim == 128)
+    pick(std::integral_constant<int, 128>());
+  else
+    pick(std::integral_constant<int, 64>());
   return cudaGetLastError();
 }
 
@@ -660,7 +706,8 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
   const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
   // the plan's scratch must fit the fixed array
   if (plan.max_splits > 1 &&
-      decode_workspace_layout(batch, hq, hkv, plan).bytes > SINKATTN_NOALLOC_SCRATCH_BYTES)
+      decode_workspace_layout(batch, hq, hkv, plan, kHeadDim).bytes >
+          SINKATTN_NOALLOC_SCRATCH_BYTES)
     return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return SINKATTN_ERR_CUDA;

@@ -21,12 +21,16 @@ DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num
 struct DecodeWorkspace {
   size_t off_lse, off_counters, bytes;
 };
-DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const DecodePlan &plan);
+DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const DecodePlan &plan,
+                                        int head_dim);
+// head dims the decode kernels are built for
+inline bool decode_head_dim_ok(int d) { return d == 64 || d == 128; }
 
 struct DecodeLaunch {
   const void *q, *k, *v;  // k, v: bf16, or fp8 e4m3 bytes when fp8
   bool fp8 = false;
   const float *k_scale = nullptr, *v_scale = nullptr;  // fp8: per KV head (null = 1)
+  int head_dim = kHeadDim;  // 64 or 128
   const int32_t *kv_indptr, *block_table, *seqlens_k;
   int max_pages, page_size;
   int batch, max_seqlen_k, hq, hkv, window;

@@ -18,6 +18,7 @@ are not available here, so seeded normal values stand in for them):
                    131072-token causal context
   long_context_prefill   256 new query tokens at the end of a 131072-token
                    causal context (few query tiles: the split-KV case)
+  decode_contig_d128 decode_contig's lengths and heads with head_dim 128
   decode_contig_fp8  decode_contig's lengths and geometry over an fp8 e4m3 KV
                    cache with per-KV-head scales 2^-4 * U(0.5, 2)
   paged_chunked_prefill  the same as chunked_prefill, with K/V in 16-token pages and a randomly
@@ -302,6 +303,11 @@ def varlen_prefill(window=0, device="cpu", nseq=16) -> PrefillCase:
                         device=device)
 
 
+def decode_contig_d128(device="cpu", batch=64) -> DecodeCase:
+    lens = uniform_lengths(batch, 1024, 8192, seed=2000)
+    return make_decode("decode_contig_d128", lens, 64, 8, seed=10, device=device, head_dim=128)
+
+
 def decode_contig_fp8(device="cpu", batch=64) -> DecodeCase:
     lens = uniform_lengths(batch, 1024, 8192, seed=2000)
     return make_decode("decode_contig_fp8", lens, 64, 8, seed=9, device=device, kv_dtype="fp8")
@@ -343,6 +349,7 @@ WORKLOADS = {
     "varlen_prefill": varlen_prefill,
     "paged_decode": paged_decode,
     "decode_contig_fp8": decode_contig_fp8,
+    "decode_contig_d128": decode_contig_d128,
     "chunked_prefill": chunked_prefill,
     "long_context_prefill": long_context_prefill,
     "paged_chunked_prefill": paged_chunked_prefill,

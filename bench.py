@@ -74,8 +74,9 @@ def decode_bytes(case):
     (2 bytes per element, 1 for an fp8 cache), plus q, out (bf16), lse and
     sinks (fp32)."""
     elem = 1 if getattr(case, "kv_dtype", "bf16") == "fp8" else 2
-    kv = sum(decode_visible(case.seqlens_k, case.window)) * case.hkv * 64 * elem * 2
-    return kv + case.batch * case.hq * (64 * 2 * 2 + 4) + case.hq * 4
+    d = case.head_dim
+    kv = sum(decode_visible(case.seqlens_k, case.window)) * case.hkv * d * elem * 2
+    return kv + case.batch * case.hq * (d * 2 * 2 + 4) + case.hq * 4
 
 
 def prefill_pairs(case):
@@ -547,35 +548,37 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         del c, out, lse, dout, dq, dk, dv, ws
         torch.cuda.empty_cache()
 
-    # fp8 e4m3 cache with per-KV-head scales: contiguous (decode_contig's
-    # lengths) and paged (paged_decode's lengths, 16-token pages)
-    for name, mk in (("decode_contig_fp8", lambda: S.decode_contig_fp8(device="cuda")),
+    # head_dim 128 (bf16 cache), and an fp8 e4m3 cache with per-KV-head scales:
+    # contiguous (decode_contig's lengths) and paged (paged_decode's lengths,
+    # 16-token pages)
+    for name, mk in (("decode_contig_d128", lambda: S.decode_contig_d128(device="cuda")),
+                     ("decode_contig_fp8", lambda: S.decode_contig_fp8(device="cuda")),
                      ("paged_decode_fp8", lambda: S.make_decode(
                          "paged_decode_fp8", S.uniform_lengths(256, 1024, 32768, seed=4000), 64,
                          8, seed=4, sink_std=2.0, paged=True, device="cuda", kv_dtype="fp8"))):
         if only is not None and name != only:
             continue
         c = mk()
-        sk, ks, vs = c.sinks.to(dev), c.k_scale.to(dev), c.v_scale.to(dev)
+        sk = c.sinks.to(dev)
+        fp8 = c.kv_dtype == "fp8"
         out = torch.empty_like(c.q)
         lse = torch.empty((c.batch, c.hq), dtype=torch.float32, device=dev)
         ws = torch.empty(max(1, sa.sinkattn_decode_workspace_size(c.batch, c.max_seqlen_k, c.hq,
-                                                                   c.hkv)),
+                                                                   c.hkv, c.head_dim)),
                          dtype=torch.uint8, device=dev)
+        fn = sa.sinkattn_decode_fp8 if fp8 else sa.sinkattn_decode
+        kw = dict(max_seqlen_k=c.max_seqlen_k, sinks=sk, out=out, lse=lse, workspace=ws)
+        if fp8:
+            kw.update(k_scale=c.k_scale.to(dev), v_scale=c.v_scale.to(dev))
         if c.paged:
-            bt, sl = c.block_table.to(dev), c.seqlens_k_t.to(dev)
-
-            def call():
-                sa.sinkattn_decode_fp8(c.q, c.k_cache, c.v_cache, k_scale=ks, v_scale=vs,
-                                       block_table=bt, seqlens_k=sl, max_seqlen_k=c.max_seqlen_k,
-                                       sinks=sk, out=out, lse=lse, workspace=ws)
+            kw.update(block_table=c.block_table.to(dev), seqlens_k=c.seqlens_k_t.to(dev))
+            kc, vc = c.k_cache, c.v_cache
         else:
-            ind = c.kv_indptr.to(dev)
+            kw.update(kv_indptr=c.kv_indptr.to(dev))
+            kc, vc = c.k, c.v
 
-            def call():
-                sa.sinkattn_decode_fp8(c.q, c.k, c.v, k_scale=ks, v_scale=vs, kv_indptr=ind,
-                                       max_seqlen_k=c.max_seqlen_k, sinks=sk, out=out, lse=lse,
-                                       workspace=ws)
+        def call():
+            fn(c.q, kc, vc, **kw)
         for _ in range(3):
             call()
         t = time_calls(call, 10, stream, flush)

@@ -35,8 +35,8 @@
  *    captured in a CUDA graph.
  *  - Host-side argument errors return before anything is enqueued. A failed
  *    launch returns SINKATTN_ERR_CUDA. No C++ exception crosses the ABI.
- *  - head_dim must be 64 (SINKATTN_ERR_UNSUPPORTED otherwise) and hq must be a
- *    multiple of hkv.
+ *  - head_dim must be 64 (SINKATTN_ERR_UNSUPPORTED otherwise; the decode
+ *    calls also take 128) and hq must be a multiple of hkv.
  *  - Outputs: `out` is bf16 (round to nearest even) with the query layout;
  *    `lse` is float32, natural log, sink included; `lse` may be NULL.
  *  - Inputs must be finite. Rows of K/V outside a sequence may be read but get
@@ -187,6 +187,8 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
  *   num_splits     0 = automatic; n > 0 = split the longest sequence into
  *            about n blocks (shorter ones get proportionally fewer).
  *   hq / hkv must be at most 8 (one KV head and all its query heads per block).
+ *   head_dim 64 or 128 (decode only; the other calls take 64). q, out and
+ *            every K/V row then have head_dim elements.
  *   out      bf16 [batch, hq, 64];  lse float32 [batch, hq] or NULL.
  *   workspace      device scratch of at least sinkattn_decode_workspace_size()
  *            bytes for the same (batch, max_seqlen_k, hq, hkv, head_dim,

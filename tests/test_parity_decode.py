@@ -28,10 +28,12 @@ def oracle_decode(oracle, c, window=None):
     cu_q = torch.arange(0, c.batch + 1, dtype=torch.int32)
     if c.paged:
         return oracle.attention(c.q, c.k_cache, c.v_cache, cu_q, block_table=c.block_table,
-                                seqlens_k=c.seqlens_k_t, hq=c.hq, hkv=c.hkv, head_dim=64,
-                                sinks=c.sinks, causal=True, window=w, scale=c.scale)
-    return oracle.attention(c.q, c.k, c.v, cu_q, c.kv_indptr, hq=c.hq, hkv=c.hkv, head_dim=64,
-                            sinks=c.sinks, causal=True, window=w, scale=c.scale)
+                                seqlens_k=c.seqlens_k_t, hq=c.hq, hkv=c.hkv,
+                                head_dim=c.head_dim, sinks=c.sinks, causal=True, window=w,
+                                scale=c.scale)
+    return oracle.attention(c.q, c.k, c.v, cu_q, c.kv_indptr, hq=c.hq, hkv=c.hkv,
+                            head_dim=c.head_dim, sinks=c.sinks, causal=True, window=w,
+                            scale=c.scale)
 
 
 # lengths chosen to span several 32-token slabs, several 512-token blocks and
@@ -83,6 +85,26 @@ def test_decode_paged_small(oracle_lib, window, page_size):
     out, lse = run_decode(c)
     ro, rl = oracle_decode(oracle_lib, c)
     check_close(out, lse, ro, rl, "paged w=%d ps=%d" % (window, page_size))
+
+
+# head_dim 128: 16-token warp steps, 256-byte rows, 8 output dims per thread
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("window", [0, 1, 100])
+@pytest.mark.parametrize("hq,hkv", [(64, 8), (24, 3)])
+def test_decode_head_dim_128(oracle_lib, paged, window, hq, hkv):
+    c = S.make_decode("d128", LENS, hq, hkv, seed=161 + window + hq, window=window, paged=paged,
+                      page_size=16, sink_std=1.5, head_dim=128)
+    out, lse = run_decode(c)
+    ro, rl = oracle_decode(oracle_lib, c)
+    check_close(out, lse, ro, rl, "decode d=128 paged=%s w=%d hq=%d" % (paged, window, hq))
+
+
+@pytest.mark.parametrize("num_splits", [1, 5, 33])
+def test_decode_head_dim_128_splits(oracle_lib, num_splits):
+    c = S.make_decode("d128s", [5000, 4097, 1, 300, 6144], 64, 8, seed=163, head_dim=128)
+    out, lse = run_decode(c, num_splits=num_splits)
+    ro, rl = oracle_decode(oracle_lib, c)
+    check_close(out, lse, ro, rl, "d=128 splits=%d" % num_splits)
 
 
 def _sample_seqs(batch, k, seed):

@@ -46,8 +46,8 @@ def reference(c, seqs=None, scales=True):
         else:
             k0 = int(c.kv_indptr[b])
             kc, vc = c.k.numpy()[k0:k0 + L], c.v.numpy()[k0:k0 + L]
-        kd.append(F.dequantize(kc.reshape(L, c.hkv, 64), ks, 1))
-        vd.append(F.dequantize(vc.reshape(L, c.hkv, 64), vs, 1))
+        kd.append(F.dequantize(kc.reshape(L, c.hkv, c.head_dim), ks, 1))
+        vd.append(F.dequantize(vc.reshape(L, c.hkv, c.head_dim), vs, 1))
     lens = [c.seqlens_k[b] for b in seqs]
     cu_k = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     cu_q = np.arange(len(seqs) + 1)
@@ -85,6 +85,17 @@ def test_decode_fp8_splits_and_unit_scales(num_splits):
         out, lse = run(c, num_splits=num_splits, scales=scales)
         ro, rl = reference(c, scales=scales)
         check_close(out, lse, ro, rl, "fp8 splits=%d scales=%s" % (num_splits, scales))
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("window", [0, 100])
+def test_decode_fp8_head_dim_128(paged, window):
+    c = S.make_decode("fp8d128", LENS, 64, 8, seed=151 + window, window=window, paged=paged,
+                      page_size=16, sink_std=1.5, kv_dtype="fp8", head_dim=128)
+    for ns in (0, 7):
+        out, lse = run(c, num_splits=ns)
+        ro, rl = reference(c)
+        check_close(out, lse, ro, rl, "fp8 d=128 paged=%s w=%d ns=%d" % (paged, window, ns))
 
 
 def test_decode_fp8_without_sinks_and_empty():
