@@ -71,7 +71,7 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
       !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (sinks && !aligned(sinks, 4)) ||
       (lse && !aligned(lse, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (batch > 65535 || total_q > INT32_MAX || total_k > INT32_MAX ||
+  if (batch > 65535 || hq > 65535 || total_q > INT32_MAX || total_k > INT32_MAX ||
       (max_seqlen_q + 127) / 128 > 65535)
     return SINKATTN_ERR_UNSUPPORTED;
   const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
@@ -143,7 +143,7 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
       !aligned(cu_seqlens_q, 4) || !aligned(block_table, 4) || !aligned(seqlens_k, 4) ||
       (sinks && !aligned(sinks, 4)) || (lse && !aligned(lse, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (batch > 65535 || total_q > INT32_MAX || (max_seqlen_q + 127) / 128 > 65535 ||
+  if (batch > 65535 || hq > 65535 || total_q > INT32_MAX || (max_seqlen_q + 127) / 128 > 65535 ||
       static_cast<int64_t>(batch) * max_seqlen_k + 128 > INT32_MAX)
     return SINKATTN_ERR_UNSUPPORTED;
   const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,

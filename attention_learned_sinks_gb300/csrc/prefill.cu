@@ -76,7 +76,8 @@ struct Cfg {
   static constexpr int kOffK = kOffQ + 2 * NT * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + control block + alignment slack
+  static constexpr int kOffPend = kOffBar + 1024;  // 16 B per softmax thread: deferred epilogue
+  static constexpr int kSmemBytes = kOffPend + NT * 128 * 16 + 1024;  // + alignment slack
 };
 
 static_assert(Cfg<2>::kRegsOther * 128 + Cfg<2>::kRegsSoftmax * 256 <=
@@ -110,6 +111,7 @@ struct Params {
 struct Tile {
   int valid;  // 0: no more work
   int h0, b, qt, q0, lq, k0, lk, rows, kvh, p_min, p_max, kt_lo, n, split;
+  float sink_log2[2];  // initial running maximum of head h0 + t (log2 units; -inf: none)
 };
 
 struct Barriers {
@@ -191,6 +193,10 @@ __device__ __forceinline__ void decode_work(const Params &p, int NT, int npairs,
   if (p.window > 0) key_lo = max(0, t.p_min - p.window + 1);
   t.kt_lo = key_lo / kBN;
   t.n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - t.kt_lo : 0;
+  // the sink enters split 0 only; read here, off the softmax warps' path
+  for (int i = 0; i < 2; ++i)
+    t.sink_log2[i] = p.sinks != nullptr && split == 0 && i < NT ? p.sinks[t.h0 + i] * kLog2e
+                                                                : -INFINITY;
   if (p.num_splits > 1) {  // this split's share of the key tiles
     const int lo = static_cast<int>(static_cast<int64_t>(t.n) * split / p.num_splits);
     const int hi = static_cast<int>(static_cast<int64_t>(t.n) * (split + 1) / p.num_splits);
@@ -521,7 +527,82 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const float2 c2 = make_float2(c, c);
     int K = 0;        // items of earlier tiles
     int o_waits = 0;  // o_done[t] phases consumed
-    for (int nt = 0;; ++nt) {
+    // The epilogue of a tile runs after the first P of the next tile has been
+    // handed to the tensor core: the last P V of the tile then completes while
+    // this warpgroup already works on the next tile (it only needs O once
+    // that P V is done, and the next P V into O waits for o_free).
+    // The pending tile's state lives in shared memory (16 bytes per thread:
+    // m, d, query row, rows | split | keys | head), not in registers that the
+    // softmax loop would have to carry.
+    float4 *pend_slot = reinterpret_cast<float4 *>(smem + C::kOffPend) + threadIdx.x;
+    bool pend_on = false;
+    bool ok = true;
+    auto finish = [&]() {  // epilogue of the pending tile
+      const float4 st = *pend_slot;
+      const float pm = st.x, pd = st.y;
+      const int qrow = __float_as_int(st.z);
+      const unsigned bits = __float_as_uint(st.w);
+      const int prows = static_cast<int>(bits & 0xffu);
+      const int psplit = static_cast<int>((bits >> 8) & 0x7fu);
+      const bool pkeys = (bits >> 15) & 1u;
+      const int ph = static_cast<int>(bits >> 16);
+      const size_t prow_h = static_cast<size_t>(qrow) * p.hq + ph;
+      bool have_o = false;
+      if (pkeys) {
+        have_o = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], o_waits & 1, abort,
+                                                   &g_prefill_error));
+        ++o_waits;
+        if (!have_o) {
+          ok = false;
+          return;
+        }
+      }
+      const float inv = pd > 0.f ? 1.f / pd : 0.f;
+      uint32_t ov[2][32];
+      if (have_o) {
+        tc_fence_after();
+        tmem_ld32(o_addr, ov[0]);
+        tmem_ld32(o_addr + 32, ov[1]);
+        tmem_wait_ld();
+        // O_t may now be overwritten by the next tile's first P V (only tiles
+        // with keys wrote O_t, and only they signal)
+        tc_fence_before();
+        mbar_arrive(&bars->o_free[t]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[0][i] = ov[1][i] = 0u;
+      }
+      const float lse = pd > 0.f ? (pm + fast_log2(pd)) * kLn2 : -INFINITY;
+      if (r < prows && p.num_splits > 1) {
+        const size_t at = static_cast<size_t>(psplit) * p.total_q * p.hq + prow_h;
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + at * kHeadDim);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float *o = reinterpret_cast<const float *>(&ov[q][4 * i]);
+            dst[q * 8 + i] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+          }
+        p.part_lse[at] = lse;
+      } else if (r < prows) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + prow_h * kHeadDim);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float *o = reinterpret_cast<const float *>(&ov[q][8 * i]);
+            uint4 v;
+            v.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+            v.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+            v.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+            v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+            dst[q * 4 + i] = v;
+          }
+        if (p.lse != nullptr) p.lse[prow_h] = lse;
+      }
+      pend_on = false;
+    };
+    for (int nt = 0; ok; ++nt) {
       const int slot = nt & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->tile_full[slot], (nt >> 1) & 1, abort,
                                              &g_prefill_error)))
@@ -529,12 +610,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       const Tile ti = bars->tiles[slot];
       if (!ti.valid) break;
       const int h = ti.h0 + t;
-      const bool has_sink = p.sinks != nullptr && ti.split == 0;
-      float m_run = has_sink ? p.sinks[h] * kLog2e : -INFINITY;
-      float d_run = has_sink ? 1.f : 0.f;
+      float m_run = t == 0 ? ti.sink_log2[0] : ti.sink_log2[1];
+      float d_run = m_run != -INFINITY ? 1.f : 0.f;
       const int pos = ti.p_min + r;
       const int n = ti.n;
-      bool ok = true;
       for (int j = 0; j < n; ++j) {
         const int k = K + j * NT + t;  // work item: S buffer k % 3, its (k / 3)-th use
         const uint32_t s_addr = lane_addr + (k % kSBufs) * kBN;
@@ -622,66 +701,25 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&bars->p_full[k % kSBufs]);
+        if (j == 0 && pend_on) {  // the previous tile's epilogue, behind this P
+          finish();
+          if (!ok) break;
+        }
       }
       if (!ok) break;
-
-      // ----------------------------------------------------------- epilogue
-      bool have_o = false;
-      if (n > 0) {
-        have_o = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], o_waits & 1, abort,
-                                                   &g_prefill_error));
-        ++o_waits;
-        if (!have_o) break;
+      if (pend_on) {  // a tile without keys: nothing to hide the epilogue behind
+        finish();
+        if (!ok) break;
       }
-      const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
-      const size_t row_h = static_cast<size_t>(ti.q0 + ti.qt * kBM + r) * p.hq + h;
-      uint32_t ov[2][32];
-      if (have_o) {
-        tc_fence_after();
-        tmem_ld32(o_addr, ov[0]);
-        tmem_ld32(o_addr + 32, ov[1]);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ov[0][i] = ov[1][i] = 0u;
-      }
-      // O_t may now be overwritten by the next tile's first P V (only tiles
-      // with keys wrote O_t, and only they signal)
-      if (have_o) {
-        tc_fence_before();
-        mbar_arrive(&bars->o_free[t]);
-      }
-      const float lse = d_run > 0.f ? (m_run + fast_log2(d_run)) * kLn2 : -INFINITY;
-      if (r < ti.rows && p.num_splits > 1) {
-        const size_t at = static_cast<size_t>(ti.split) * p.total_q * p.hq + row_h;
-        float4 *dst = reinterpret_cast<float4 *>(p.part_o + at * kHeadDim);
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float *o = reinterpret_cast<const float *>(&ov[q][4 * i]);
-            dst[q * 8 + i] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-          }
-        p.part_lse[at] = lse;
-      } else if (r < ti.rows) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + row_h * kHeadDim);
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float *o = reinterpret_cast<const float *>(&ov[q][8 * i]);
-            uint4 v;
-            v.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-            v.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-            v.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-            v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-            dst[q * 4 + i] = v;
-          }
-        if (p.lse != nullptr) p.lse[row_h] = lse;
-      }
+      pend_on = true;
+      *pend_slot = make_float4(
+          m_run, d_run, __int_as_float(ti.q0 + ti.qt * kBM + r),
+          __uint_as_float(static_cast<unsigned>(ti.rows) | (static_cast<unsigned>(ti.split) << 8) |
+                          (n > 0 ? 1u << 15 : 0u) | (static_cast<unsigned>(h) << 16)));
       mbar_arrive(&bars->tile_empty[slot]);
       K += NT * n;
     }
+    if (ok && pend_on) finish();
   }
 
   tc_fence_before();
