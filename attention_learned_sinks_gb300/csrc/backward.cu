@@ -66,6 +66,7 @@ struct BwdParams {
   float *dt;           // [hq][total_q]: D, from the forward output, then exact (dQ kernel)
   const unsigned *q_pairs, *k_pairs;
   const int *num_q_pairs, *num_k_pairs;
+  unsigned *q_counter, *k_counter;  // work counters of the persistent kernels (zeroed by the lists)
   __nv_bfloat16 *dq, *dk, *dv;
 };
 
@@ -207,13 +208,21 @@ __device__ __forceinline__ void zero_row64(__nv_bfloat16 *dst) {
 }
 
 // ---------------------------------------------------------------- dQ -------
-// Warps 0-3: one query row per thread (TMEM lane); warp 4: TMA; warp 5: MMA
-// issue and TMEM owner. TMEM columns: S [0,128), dP [128,256), dS fp16
-// [256,320), P fp16 [320,384), dQ [384,448), Y [448,512). S and dP of the next
-// key tile are written only by MMAs issued after the previous tile's dQ / Y
-// MMAs, and dS / P only by the softmax warps after the commit that follows
-// them, so no MMA reads TMEM that a later write may clobber before it
-// completes.
+// Persistent: one CTA per SM takes (query tile, head) items from the query
+// tile list (longest first) through a global counter. Each 128-key tile is
+// handled as two 64-key halves ("sub-steps"); softmax-side warpgroup w (warps
+// 4w..4w+3, one query row per thread) takes the sub-steps of parity w, in its
+// own TMEM buffer, so the tensor core computes the scores of one half while
+// the other warpgroup turns the previous half into P and dS. Warp 8: TMA
+// (Q and dO double-buffered per item, K/V in a 3-stage ring); warp 9: MMA
+// issue and TMEM owner.
+//
+// TMEM columns: S_w [64w, 64w+64), dP_w [128+64w, ...), dS_w fp16
+// [256+32w, ...), P_w fp16 [320+32w, ...), dQ [384,448), Y [448,512). S_w and
+// dP_w of a sub-step are written only after the softmax warps finished the
+// sub-step two back (the MMA warp waits for them before issuing dQ there),
+// and dS_w / P_w only after the commit that follows those dQ / Y MMAs; dQ and
+// Y of an item start only after the previous item's epilogue has read them.
 //
 // D from the bf16 forward output (D_a) carries the output's rounding, and
 // dP - D cancels when one key dominates a row. This kernel therefore also
@@ -222,67 +231,90 @@ __device__ __forceinline__ void zero_row64(__nv_bfloat16 *dst) {
 // - (D_e - D_a) Y). The correction is small, so its own fp16 rounding does
 // not matter. D_e replaces D_a in the workspace for the dK/dV kernel and the
 // sink gradient, which run after this one.
-struct DqBars {
-  uint64_t qd_full;
-  uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full, ds_full, dq_done, drain;
-  uint32_t tmem_base;
-  int abort;
+constexpr int kHalf = 64;                           // keys per sub-step
+constexpr uint32_t kIdescSS64 = idesc_f32acc(128, kHalf, /*bf16=*/false, false, false);
+constexpr int kDqThreads = 320;
+constexpr int kDqStages = 3;
+
+struct DqTile {
+  int valid, b, qt, h, g, q0, lq, k0, lk, rows, p_min, kt_lo, n;
 };
 
-constexpr int kDqOffQ = 0, kDqOffDo = kTileBytes, kDqOffK = 2 * kTileBytes,
-              kDqOffV = kDqOffK + kStages * kTileBytes, kDqOffBar = kDqOffV + kStages * kTileBytes;
-static_assert(kDqOffBar + 1024 + 1024 <= kSmemRequest, "dQ shared memory");
+struct DqBars {
+  uint64_t tile_full[2], tile_empty[2];
+  uint64_t qd_full[2], qd_empty[2];
+  uint64_t kv_full[kDqStages], kv_empty[kDqStages];
+  uint64_t s_full[2], ds_full[2];
+  uint64_t dq_done, dq_free, drain;
+  uint64_t dsum_full[2];  // both warpgroups' partial sums of an item are in dsum
+  uint32_t tmem_base;
+  int abort;
+  DqTile tiles[2];
+  float dsum[2][2][128];  // [item parity][warpgroup][row]: partial exact D
+};
 
-__global__ void __launch_bounds__(192, 1)
+constexpr int kDqOffQ = 0;                                // 2 buffers of Q and dO
+constexpr int kDqOffK = 4 * kTileBytes;
+constexpr int kDqOffV = kDqOffK + kDqStages * kTileBytes;
+constexpr int kDqOffBar = kDqOffV + kDqStages * kTileBytes;
+static_assert(sizeof(DqBars) <= 4096, "dQ control block");
+constexpr int kDqSmem = kDqOffBar + 4096 + 1024;
+
+// (sequence, query tile) list entry w / hq, head w % hq -> item
+__device__ __forceinline__ void dq_decode(const BwdParams &p, int w, DqTile &t) {
+  const unsigned e = p.q_pairs[w / p.hq];
+  t.valid = 1;
+  t.h = w % p.hq;
+  t.g = t.h / p.group;
+  t.b = static_cast<int>(e >> 16);
+  t.qt = static_cast<int>(e & 0xffffu);
+  t.q0 = p.cu_q[t.b];
+  t.lq = p.cu_q[t.b + 1] - t.q0;
+  t.k0 = p.cu_k[t.b];
+  t.lk = p.cu_k[t.b + 1] - t.k0;
+  t.rows = min(kBM, t.lq - t.qt * kBM);
+  t.p_min = t.lk - t.lq + t.qt * kBM;
+  const int p_max = t.p_min + t.rows - 1;
+  int key_hi = t.lk, key_lo = 0;
+  if (p.causal) key_hi = min(key_hi, p_max + 1);
+  if (p.window > 0) key_lo = max(0, t.p_min - p.window + 1);
+  t.kt_lo = key_lo / kBN;
+  t.n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - t.kt_lo : 0;
+}
+
+__global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const BwdParams p) {
-  const int w = blockIdx.x;
-  if (w >= *p.num_q_pairs * p.hq) return;
-  const unsigned e = p.q_pairs[w / p.hq];
-  const int h = w % p.hq, g = h / p.group;
-  const int b = static_cast<int>(e >> 16), qt = static_cast<int>(e & 0xffffu);
-  const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
-  const int k0 = p.cu_k[b], lk = p.cu_k[b + 1] - k0;
-  const int rows = min(kBM, lq - qt * kBM);
-  const int p_min = lk - lq + qt * kBM, p_max = p_min + rows - 1;
-  int key_hi = lk, key_lo = 0;
-  if (p.causal) key_hi = min(key_hi, p_max + 1);
-  if (p.window > 0) key_lo = max(0, p_min - p.window + 1);
-  const int kt_lo = key_lo / kBN;
-  const int n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - kt_lo : 0;
-  const int r = threadIdx.x & 127;
-  const int warp = threadIdx.x >> 5;
-  __nv_bfloat16 *dq_row = p.dq + (static_cast<size_t>(q0 + qt * kBM + r) * p.hq + h) * kHeadDim;
-  const size_t lidx = static_cast<size_t>(h) * p.total_q + q0 + qt * kBM + r;
-  if (n == 0) {  // no row of this tile sees a key: dq = 0, D = 0
-    if (warp < 4 && r < rows) {
-      zero_row64(dq_row);
-      p.dt[lidx] = 0.f;
-    }
-    return;
-  }
-
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   DqBars *bars = reinterpret_cast<DqBars *>(smem_raw + (sbase - raw) + kDqOffBar);
   volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int *err = &g_backward_error;
   if (threadIdx.x == 0) {
-    mbar_init(&bars->qd_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->tile_full[i], 1);
+      mbar_init(&bars->tile_empty[i], 256 + 1);
+      mbar_init(&bars->qd_full[i], 1);
+      mbar_init(&bars->qd_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->ds_full[i], 128);
+    }
+    for (int s = 0; s < kDqStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->ds_full, 128);
     mbar_init(&bars->dq_done, 1);
+    mbar_init(&bars->dq_free, 256);
+    mbar_init(&bars->dsum_full[0], 256);
+    mbar_init(&bars->dsum_full[1], 256);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -290,159 +322,243 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  int *err = &g_backward_error;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    mbar_arrive_expect_tx_elect(&bars->qd_full, 2 * kTileBytes);
-    tma_load_3d_elect(sbase + kDqOffQ, &tm_q, &bars->qd_full, 0, h, q0 + qt * kBM);
-    tma_load_3d_elect(sbase + kDqOffDo, &tm_do, &bars->qd_full, 0, h, q0 + qt * kBM);
-    int j = 0;
-    for (; j < n; ++j) {
-      const int st = j % kStages;
-      if (j >= kStages &&
-          !mbar_wait_warp(&bars->kv_empty[st], ((j / kStages) - 1) & 1, abort, err))
+    const int num_work = *p.num_q_pairs * p.hq;
+    int J = 0, nq = 0;
+    bool ok = true;
+    for (int nt = 0; ok; ++nt) {
+      const int slot = nt & 1;
+      if (nt >= 2 && !mbar_wait_warp(&bars->tile_empty[slot], ((nt >> 1) - 1) & 1, abort, err))
         break;
-      const int row = k0 + (kt_lo + j) * kBN;
-      mbar_arrive_expect_tx_elect(&bars->kv_full[st], 2 * kTileBytes);
-      tma_load_3d_elect(sbase + kDqOffK + st * kTileBytes, &tm_k, &bars->kv_full[st], 0, g, row);
-      tma_load_3d_elect(sbase + kDqOffV + st * kTileBytes, &tm_v, &bars->kv_full[st], 0, g, row);
+      if (lane == 0) {
+        DqTile t;
+        t.valid = 0;
+        const int w = static_cast<int>(atomicAdd(p.q_counter, 1u));
+        if (w < num_work) dq_decode(p, w, t);
+        bars->tiles[slot] = t;
+        mbar_arrive(&bars->tile_full[slot]);
+      }
+      __syncwarp();
+      const DqTile t = bars->tiles[slot];
+      if (!t.valid) break;
+      if (t.n == 0) continue;  // nothing to load (and no MMAs) for this item
+      const int qb = nq & 1;
+      if (nq >= 2 && !mbar_wait_warp(&bars->qd_empty[qb], ((nq >> 1) - 1) & 1, abort, err)) break;
+      mbar_arrive_expect_tx_elect(&bars->qd_full[qb], 2 * kTileBytes);
+      tma_load_3d_elect(sbase + kDqOffQ + qb * 2 * kTileBytes, &tm_q, &bars->qd_full[qb], 0, t.h,
+                        t.q0 + t.qt * kBM);
+      tma_load_3d_elect(sbase + kDqOffQ + (qb * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[qb], 0,
+                        t.h, t.q0 + t.qt * kBM);
+      ++nq;
+      for (int j = 0; j < t.n; ++j, ++J) {
+        const int st = J % kDqStages;
+        if (J >= kDqStages &&
+            !mbar_wait_warp(&bars->kv_empty[st], ((J / kDqStages) - 1) & 1, abort, err)) {
+          ok = false;
+          break;
+        }
+        const int row = t.k0 + (t.kt_lo + j) * kBN;
+        mbar_arrive_expect_tx_elect(&bars->kv_full[st], 2 * kTileBytes);
+        tma_load_3d_elect(sbase + kDqOffK + st * kTileBytes, &tm_k, &bars->kv_full[st], 0, t.g, row);
+        tma_load_3d_elect(sbase + kDqOffV + st * kTileBytes, &tm_v, &bars->kv_full[st], 0, t.g, row);
+      }
     }
     if (*abort) {  // copies already issued still land here: wait for them (bounded)
-      mbar_wait_warp(&bars->qd_full, 0, abort, err, true);
-      for (int i = max(0, j - kStages); i < j; ++i)
-        mbar_wait_warp(&bars->kv_full[i % kStages], (i / kStages) & 1, abort, err, true);
+      for (int i = max(0, nq - 2); i < nq; ++i)
+        mbar_wait_warp(&bars->qd_full[i & 1], (i >> 1) & 1, abort, err, true);
+      for (int i = max(0, J - kDqStages); i < J; ++i)
+        mbar_wait_warp(&bars->kv_full[i % kDqStages], (i / kDqStages) & 1, abort, err, true);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA
-    const uint64_t qdesc = sdesc_sw128(sbase + kDqOffQ);
-    const uint64_t dodesc = sdesc_sw128(sbase + kDqOffDo);
+    const uint64_t qdesc0 = sdesc_sw128(sbase + kDqOffQ);
     const uint64_t kdesc0 = sdesc_sw128(sbase + kDqOffK);
     const uint64_t vdesc0 = sdesc_sw128(sbase + kDqOffV);
-    const uint32_t t_s = tmem, t_dp = tmem + 128, t_ds = tmem + 256, t_p = tmem + 320;
+    constexpr uint64_t kHalfDesc = (kHalf * 128) >> 4;  // 64 rows of 128 B
     const uint32_t t_dq = tmem + 384, t_y = tmem + 448;
-    bool ok = mbar_wait_warp(&bars->qd_full, 0, abort, err) &&
-              mbar_wait_warp(&bars->kv_full[0], 0, abort, err);
-    if (ok) {
-      tc_fence_after();
+    int J = 0, nq = 0, G = 0;  // K/V tiles, items with keys, global sub-steps
+    int dq_items = 0;          // items whose dQ/Y the epilogue has to release
+    bool ok = true;
+    // S_b, dP_b of global sub-step g (item-local ss) from Q/dO buffer qb
+    auto issue_s = [&](int g, int ss, int qb, int j0) {
+      const int b = g & 1, u = ss & 1, st = (j0 + (ss >> 1)) % kDqStages;
+      const uint64_t qd = qdesc0 + qb * 2 * kTileDesc, dod = qd + kTileDesc;
+      const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
+      const uint64_t vd = vdesc0 + st * kTileDesc + u * kHalfDesc;
 #pragma unroll
       for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(t_s, qdesc + 2 * ks, kdesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
+        umma_ss_elect(tmem + 64 * b, qd + 2 * ks, kd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(t_dp, dodesc + 2 * ks, vdesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
-      umma_commit_elect(&bars->s_full);
-    }
-    for (int j = 0; ok && j < n; ++j) {
-      if (!mbar_wait_warp(&bars->ds_full, j & 1, abort, err)) {
-        ok = false;
-        break;
+        umma_ss_elect(tmem + 128 + 64 * b, dod + 2 * ks, vd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
+      umma_commit_elect(&bars->s_full[b]);
+    };
+    for (int nt = 0; ok; ++nt) {
+      const int slot = nt & 1;
+      if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
+      const DqTile t = bars->tiles[slot];
+      if (!t.valid) break;
+      if (t.n > 0) {
+        const int qb = nq & 1, steps = 2 * t.n;
+        ok = mbar_wait_warp(&bars->qd_full[qb], (nq >> 1) & 1, abort, err);
+        // first two sub-steps: K/V tile J, both halves
+        if (ok) ok = mbar_wait_warp(&bars->kv_full[J % kDqStages], (J / kDqStages) & 1, abort, err);
+        if (ok) {
+          tc_fence_after();
+          issue_s(G, 0, qb, J);
+          issue_s(G + 1, 1, qb, J);
+        }
+        // dQ/Y of the previous item must have been read by its epilogue
+        if (ok && dq_items > 0)
+          ok = mbar_wait_warp(&bars->dq_free, (dq_items - 1) & 1, abort, err);
+        for (int ss = 0; ok && ss < steps; ++ss) {
+          const int g = G + ss, b = g & 1, j = ss >> 1, u = ss & 1;
+          const int st = (J + j) % kDqStages;
+          if (!mbar_wait_warp(&bars->ds_full[b], (g >> 1) & 1, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
+#pragma unroll
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            umma_ts_elect(t_dq, tmem + 256 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                          (ss > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            umma_ts_elect(t_y, tmem + 320 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                          (ss > 0 || kk > 0) ? 1u : 0u);
+          if (u == 1) umma_commit_elect(&bars->kv_empty[st]);  // both halves done with K/V
+          if (ss + 2 < steps) {
+            if (u == 0 && !mbar_wait_warp(&bars->kv_full[(J + j + 1) % kDqStages],
+                                          ((J + j + 1) / kDqStages) & 1, abort, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(g + 2, ss + 2, qb, J);
+          }
+        }
+        if (!ok) break;
+        umma_commit_elect(&bars->qd_empty[qb]);
+        umma_commit_elect(&bars->dq_done);
+        ++dq_items;
+        ++nq;
+        J += t.n;
+        G += steps;
       }
-      tc_fence_after();
-      const int st = j % kStages;
-      const uint64_t kd = kdesc0 + st * kTileDesc;
+      if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
+    }
+    umma_commit_elect(&bars->drain);
+    mbar_wait_warp(&bars->drain, 0, abort, err, true);
+  } else {
+    // ---------------------------------------- P, dS (one query row / thread)
+    const int wg = warp >> 2;             // warpgroup: sub-steps of this parity
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + 64 * wg, t_dp = t_s + 128;
+    const uint32_t t_ds = tmem + lane_off + 256 + 32 * wg, t_p = t_ds + 64;
+    const uint32_t t_dq = tmem + lane_off + 384 + 32 * wg, t_y = t_dq + 64;
+    int G = 0, dq_items = 0;
+    bool ok = true;
+    for (int nt = 0; ok; ++nt) {
+      const int slot = nt & 1;
+      if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
+      const DqTile t = bars->tiles[slot];
+      if (!t.valid) break;
+      const size_t qrow = static_cast<size_t>(t.q0 + t.qt * kBM + r);
+      const size_t lidx = static_cast<size_t>(t.h) * p.total_q + qrow;
+      __nv_bfloat16 *dq_row = p.dq + (qrow * p.hq + t.h) * kHeadDim + 32 * wg;
+      if (t.n == 0) {  // no row of this tile sees a key: dq = 0, D = 0
+        if (r < t.rows) {
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        umma_ts_elect(t_dq, t_ds + kk * 8, kd + kk * kRows16Desc, kIdescTS,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        umma_ts_elect(t_y, t_p + kk * 8, kd + kk * kRows16Desc, kIdescTS,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_elect(&bars->kv_empty[st]);
-      if (j + 1 < n) {
-        const int s1 = (j + 1) % kStages;
-        if (!mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kStages) & 1, abort, err)) {
+          for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dq_row)[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (wg == 0) p.dt[lidx] = 0.f;
+        }
+        mbar_arrive(&bars->tile_empty[slot]);
+        continue;
+      }
+      const float l2 = r < t.rows ? p.lse2t[lidx] : INFINITY;
+      const float d = r < t.rows ? p.dt[lidx] : 0.f;
+      const int pos = t.p_min + r;
+      int hi = t.lk, lo = 0;
+      if (p.causal) hi = min(hi, pos + 1);
+      if (p.window > 0) lo = max(lo, pos - p.window + 1);
+      if (r >= t.rows) hi = lo = 0;
+      float2 dsum = make_float2(0.f, 0.f);
+      const int steps = 2 * t.n;
+      // this warpgroup's sub-steps: global index G + ss with ss = wg, wg + 2, ...
+      for (int ss = wg; ss < steps; ss += 2) {
+        const int g = G + ss;
+        if (!mbar_wait_warp(&bars->s_full[wg], (g >> 1) & 1, abort, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const int key0 = (t.kt_lo + (ss >> 1)) * kBN + (ss & 1) * kHalf;
+        const int c_lo = min(max(lo - key0, 0), kHalf);
+        const int len = max(min(hi - key0, kHalf) - c_lo, 0);
 #pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_ss_elect(t_s, qdesc + 2 * ks, kdesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
-                        ks > 0 ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_ss_elect(t_dp, dodesc + 2 * ks, vdesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
-                        ks > 0 ? 1u : 0u);
-        umma_commit_elect(&bars->s_full);
-      }
-    }
-    if (ok) umma_commit_elect(&bars->dq_done);
-    // every MMA issued here has finished before TMEM is released
-    umma_commit_elect(&bars->drain);
-    mbar_wait_warp(&bars->drain, 0, abort, err, true);
-  } else {
-    // -------------------------------------------------- dS (one row / thread)
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = t_s + 128, t_ds = t_s + 256, t_p = t_s + 320;
-    const uint32_t t_dq = t_s + 384, t_y = t_s + 448;
-    const float l2 = r < rows ? p.lse2t[lidx] : INFINITY;
-    const float d = r < rows ? p.dt[lidx] : 0.f;
-    const int pos = p_min + r;
-    int hi = lk, lo = 0;
-    if (p.causal) hi = min(hi, pos + 1);
-    if (p.window > 0) lo = max(lo, pos - p.window + 1);
-    if (r >= rows) hi = lo = 0;
-    bool ok = true;
-    float2 dsum = make_float2(0.f, 0.f);  // sum_j P_j dP_j
-    for (int j = 0; j < n; ++j) {
-      if (!mbar_wait_warp(&bars->s_full, j & 1, abort, err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int key0 = (kt_lo + j) * kBN;
-      const int c_lo = min(max(lo - key0, 0), kBN);
-      const int len = max(min(hi - key0, kBN) - c_lo, 0);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float s[32], dp[32];
-        tmem_ld32f(t_s + 32 * c, s);
-        tmem_ld32f(t_dp + 32 * c, dp);
-        tmem_wait_ld();
-        mask32(s, 32 * c, c_lo, len);
-        uint32_t p16[16], ds16[16];
-        p_ds_row(s, dp, p.scale_log2, l2, d, p16, ds16, dsum);
-        tmem_st16(t_ds + 16 * c, ds16);
-        tmem_st16(t_p + 16 * c, p16);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_full);
-    }
-    if (ok && mbar_wait_warp(&bars->dq_done, 0, abort, err)) {
-      tc_fence_after();
-      const float d_e = dsum.x + dsum.y;
-      const float corr = d_e - d;
-      for (int half = 0; half < 2; ++half) {
-        float a[32], y[32];
-        tmem_ld32f(t_dq + 32 * half, a);
-        tmem_ld32f(t_y + 32 * half, y);
-        tmem_wait_ld();
-        if (r < rows) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dq_row) + 4 * half;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float o[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) o[t] = p.scale * fmaf(-corr, y[8 * i + t], a[8 * i + t]);
-            d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                               pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-          }
+        for (int c = 0; c < 2; ++c) {
+          float sv[32], dp[32];
+          tmem_ld32f(t_s + 32 * c, sv);
+          tmem_ld32f(t_dp + 32 * c, dp);
+          tmem_wait_ld();
+          mask32(sv, 32 * c, c_lo, len);
+          uint32_t p16[16], ds16[16];
+          p_ds_row(sv, dp, p.scale_log2, l2, d, p16, ds16, dsum);
+          tmem_st16(t_ds + 16 * c, ds16);
+          tmem_st16(t_p + 16 * c, p16);
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_full[wg]);
       }
-      if (r < rows) p.dt[lidx] = d_e;
+      if (!ok) break;
+      G += steps;
+      // exact D = both warpgroups' partial sums of P dP (exchanged through
+      // shared memory; a bounded mbarrier wait, so an aborting CTA cannot
+      // leave the other warpgroup waiting)
+      float *xs = bars->dsum[dq_items & 1][0];
+      xs[wg * 128 + r] = dsum.x + dsum.y;
+      mbar_arrive(&bars->dsum_full[dq_items & 1]);
+      if (!mbar_wait_warp(&bars->dsum_full[dq_items & 1], (dq_items >> 1) & 1, abort, err)) break;
+      const float d_e = xs[r] + xs[128 + r];
+      const float corr = d_e - d;
+      if (!mbar_wait_warp(&bars->dq_done, dq_items & 1, abort, err)) break;
+      ++dq_items;
+      tc_fence_after();
+      float a[32], y[32];
+      tmem_ld32f(t_dq, a);
+      tmem_ld32f(t_y, y);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);  // the next item's dQ / Y may start
+      if (r < t.rows) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dq_row);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = p.scale * fmaf(-corr, y[8 * i + e], a[8 * i + e]);
+          d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                             pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+        }
+        if (wg == 0) p.dt[lidx] = d_e;
+      }
+      mbar_arrive(&bars->tile_empty[slot]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -750,6 +866,8 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
   p.dt = dt;
   p.q_pairs = reinterpret_cast<const unsigned *>(qlist + 256);
   p.num_q_pairs = reinterpret_cast<const int *>(qlist + 4);
+  p.q_counter = reinterpret_cast<unsigned *>(qlist);
+  p.k_counter = reinterpret_cast<unsigned *>(klist);
   p.k_pairs = reinterpret_cast<const unsigned *>(klist + 256);
   p.num_k_pairs = reinterpret_cast<const int *>(klist + 4);
   p.dq = static_cast<__nv_bfloat16 *>(a.dq);
@@ -778,13 +896,14 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
     return cudaErrorInvalidValue;
   }
   if ((e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemRequest)) != cudaSuccess ||
+                                kDqSmem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemRequest)) != cudaSuccess)
     return e;
   if (a.total_q > 0) {
     const int64_t items = (a.total_q / kBM + a.batch) * a.hq;
-    bwd_dq_kernel<<<static_cast<unsigned>(items), 192, kSmemRequest, stream>>>(tq, tdo, tk, tv, p);
+    const int64_t grid = items < sm_count() ? items : sm_count();
+    bwd_dq_kernel<<<static_cast<unsigned>(grid), kDqThreads, kDqSmem, stream>>>(tq, tdo, tk, tv, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.sinks != nullptr && a.dsinks != nullptr) {  // after dQ: D is exact by now
