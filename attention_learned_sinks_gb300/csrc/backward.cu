@@ -41,16 +41,10 @@ namespace {
 constexpr int kBM = 128;                        // query rows per tile
 constexpr int kBN = 128;                        // keys per tile
 constexpr int kTileBytes = 128 * kHeadDim * 2;  // 16 KB
-constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
-// Dynamic shared memory requested by the two MMA kernels: more than half of
-// the SM's, so one CTA per SM holds all 512 TMEM columns without contention.
-constexpr int kSmemRequest = 120 * 1024;
 
-// ss: both operands K-major in shared memory (S = Q K^T, dP = dO V^T, ...);
 // ts: A from TMEM, B MN-major in shared memory (dQ += dS K, ...). fp16 inputs.
-constexpr uint32_t kIdescSS = idesc_f32acc(128, 128, /*bf16=*/false, false, false);
 constexpr uint32_t kIdescTS = idesc_f32acc(128, kHeadDim, /*bf16=*/false, false, true);
 constexpr uint64_t kTileDesc = kTileBytes >> 4;        // one tile in descriptor units
 constexpr uint64_t kRows16Desc = (16 * 128) >> 4;      // 16 rows of 128 B
@@ -176,35 +170,6 @@ __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], 
     p16[i] = pack_f16x2(p.x, p.y);
     ds16[i] = pack_f16x2(ds.x, ds.y);
   }
-}
-
-// 64 fp32 TMEM columns (a row of dQ, dK or dV) times `mul` -> 64 bf16 in global.
-__device__ __forceinline__ void store_row64(uint32_t taddr, float mul, __nv_bfloat16 *dst,
-                                            bool write) {
-  uint32_t a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-  tmem_wait_ld();
-  if (!write) return;
-  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float *x = reinterpret_cast<const float *>(&a[8 * i]);
-    d4[i] = make_uint4(pack_bf16x2(x[0] * mul, x[1] * mul), pack_bf16x2(x[2] * mul, x[3] * mul),
-                       pack_bf16x2(x[4] * mul, x[5] * mul), pack_bf16x2(x[6] * mul, x[7] * mul));
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float *x = reinterpret_cast<const float *>(&b[8 * i]);
-    d4[4 + i] = make_uint4(pack_bf16x2(x[0] * mul, x[1] * mul), pack_bf16x2(x[2] * mul, x[3] * mul),
-                           pack_bf16x2(x[4] * mul, x[5] * mul), pack_bf16x2(x[6] * mul, x[7] * mul));
-  }
-}
-
-__device__ __forceinline__ void zero_row64(__nv_bfloat16 *dst) {
-  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) d4[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // ---------------------------------------------------------------- dQ -------
@@ -565,80 +530,97 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 // ------------------------------------------------------------- dK / dV -----
-// Warps 0-3: one key row per thread (TMEM lane); warp 4: TMA and the per-
-// query-tile lse / D vectors; warp 5: MMA issue and TMEM owner. TMEM columns:
-// S^T [0,128), dP^T [128,256), P^T fp16 [256,320), dS^T fp16 [320,384),
-// dV [384,448), dK [448,512). Steps run over (query head of the group, query
-// tile that sees the key tile); Q, dO, lse and D are double-buffered.
-struct DkvBars {
-  uint64_t kv_full;
-  uint64_t qd_full[kStages], qd_empty[kStages];
-  uint64_t st_full, ew_done, done, drain;
-  uint32_t tmem_base;
-  int abort;
+// Persistent: one CTA per SM takes (key tile, KV head) items from the key
+// tile list (walked backwards: under a causal mask the low key tiles are seen
+// by the most queries, so this is longest first). An item's steps run over
+// (query head of the group, query tile that sees the key tile); each step's
+// 128 queries are two 64-query halves, taken by softmax-side warpgroup w
+// (one key per thread) for halves of parity w, in its own TMEM buffers, so
+// the tensor core computes one half's S^T / dP^T while the other warpgroup
+// forms P^T and dS^T. Warp 8: TMA (K/V double-buffered per item; Q, dO and
+// the step's lse / D vectors in a 3-stage ring); warp 9: MMA issue, TMEM.
+//
+// TMEM columns: S^T_w [64w, ...), dP^T_w [128+64w, ...), P^T_w fp16
+// [256+32w, ...), dS^T_w fp16 [320+32w, ...), dV [384,448), dK [448,512).
+constexpr int kKvThreads = 320;
+constexpr int kKvQStages = 3;
+
+struct KvTile {
+  int valid, b, kt, g, q0, lq, k0, lk, krows, qt_lo, nqt, steps;
 };
 
-constexpr int kKvOffK = 0, kKvOffV = kTileBytes, kKvOffQ = 2 * kTileBytes,
-              kKvOffDo = kKvOffQ + kStages * kTileBytes,
-              kKvOffVec = kKvOffDo + kStages * kTileBytes,  // per stage: lse2[128], D[128]
-    kKvOffBar = kKvOffVec + kStages * 1024;
-static_assert(kKvOffBar + 1024 + 1024 <= kSmemRequest, "dK/dV shared memory");
+struct KvBars {
+  uint64_t tile_full[2], tile_empty[2];
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t qd_full[kKvQStages], qd_empty[kKvQStages];
+  uint64_t st_full[2], ew_done[2];
+  uint64_t dkv_done, dkv_free, drain;
+  uint32_t tmem_base;
+  int abort;
+  KvTile tiles[2];
+};
 
-__global__ void __launch_bounds__(192, 1)
+constexpr int kKvOffK = 0;                                   // 2 item buffers of K and V
+constexpr int kKvOffQ = 4 * kTileBytes;                      // per stage: Q, dO
+constexpr int kKvOffVec = kKvOffQ + kKvQStages * 2 * kTileBytes;  // per stage: lse2[128], D[128]
+constexpr int kKvOffBar = kKvOffVec + kKvQStages * 1024;
+static_assert(sizeof(KvBars) <= 1024, "dK/dV control block");
+constexpr int kKvSmem = kKvOffBar + 1024 + 1024;
+
+__device__ __forceinline__ void kv_decode(const BwdParams &p, int npairs, int w, KvTile &t) {
+  const unsigned e = p.k_pairs[npairs - 1 - w / p.hkv];
+  t.valid = 1;
+  t.g = w % p.hkv;
+  t.b = static_cast<int>(e >> 16);
+  t.kt = static_cast<int>(e & 0xffffu);
+  t.q0 = p.cu_q[t.b];
+  t.lq = p.cu_q[t.b + 1] - t.q0;
+  t.k0 = p.cu_k[t.b];
+  t.lk = p.cu_k[t.b + 1] - t.k0;
+  t.krows = min(kBN, t.lk - t.kt * kBN);
+  const int base = t.lk - t.lq;  // position of query 0
+  const int jmin = t.kt * kBN, jmax = jmin + t.krows - 1;
+  int iq_lo = 0, iq_hi = t.lq;   // queries that see at least one key of the tile
+  if (p.causal) iq_lo = max(0, jmin - base);
+  if (p.window > 0) iq_hi = min(iq_hi, jmax + p.window - base);
+  t.qt_lo = iq_lo / kBM;
+  t.nqt = iq_hi > iq_lo ? (iq_hi + kBM - 1) / kBM - t.qt_lo : 0;
+  t.steps = t.nqt * p.group;
+}
+
+__global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
-  const int w = blockIdx.x;
-  const int npairs = *p.num_k_pairs;
-  if (w >= npairs * p.hkv) return;
-  // the list holds key tiles of higher index first; under a causal mask the
-  // low tiles have the most queries, so walk it backwards (longest first)
-  const unsigned e = p.k_pairs[npairs - 1 - w / p.hkv];
-  const int g = w % p.hkv;
-  const int b = static_cast<int>(e >> 16), kt = static_cast<int>(e & 0xffffu);
-  const int q0 = p.cu_q[b], lq = p.cu_q[b + 1] - q0;
-  const int k0 = p.cu_k[b], lk = p.cu_k[b + 1] - k0;
-  const int krows = min(kBN, lk - kt * kBN);
-  const int base = lk - lq;  // position of query 0
-  const int jmin = kt * kBN, jmax = jmin + krows - 1;
-  int iq_lo = 0, iq_hi = lq;  // queries that see at least one key of the tile
-  if (p.causal) iq_lo = max(0, jmin - base);
-  if (p.window > 0) iq_hi = min(iq_hi, jmax + p.window - base);
-  const int qt_lo = iq_lo / kBM;
-  const int nqt = iq_hi > iq_lo ? (iq_hi + kBM - 1) / kBM - qt_lo : 0;
-  const int steps = nqt * p.group;
-  const int r = threadIdx.x & 127;
-  const int warp = threadIdx.x >> 5;
-  const size_t krow = (static_cast<size_t>(k0 + kt * kBN + r) * p.hkv + g) * kHeadDim;
-  if (steps == 0) {  // no query sees this key tile
-    if (warp < 4 && r < krows) {
-      zero_row64(p.dk + krow);
-      zero_row64(p.dv + krow);
-    }
-    return;
-  }
-
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (sbase - raw);
-  DkvBars *bars = reinterpret_cast<DkvBars *>(smem + kKvOffBar);
+  KvBars *bars = reinterpret_cast<KvBars *>(smem + kKvOffBar);
   volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int *err = &g_backward_error;
   if (threadIdx.x == 0) {
-    mbar_init(&bars->kv_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->tile_full[i], 1);
+      mbar_init(&bars->tile_empty[i], 256 + 1);
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->st_full[i], 1);
+      mbar_init(&bars->ew_done[i], 128);
+    }
+    for (int s = 0; s < kKvQStages; ++s) {
       mbar_init(&bars->qd_full[s], 1);
       mbar_init(&bars->qd_empty[s], 1);
     }
-    mbar_init(&bars->st_full, 1);
-    mbar_init(&bars->ew_done, 128);
-    mbar_init(&bars->done, 1);
+    mbar_init(&bars->dkv_done, 1);
+    mbar_init(&bars->dkv_free, 256);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -646,156 +628,253 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  int *err = &g_backward_error;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
-    const int lane = threadIdx.x & 31;
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    mbar_arrive_expect_tx_elect(&bars->kv_full, 2 * kTileBytes);
-    tma_load_3d_elect(sbase + kKvOffK, &tm_k, &bars->kv_full, 0, g, k0 + kt * kBN);
-    tma_load_3d_elect(sbase + kKvOffV, &tm_v, &bars->kv_full, 0, g, k0 + kt * kBN);
-    int s = 0;
-    for (; s < steps; ++s) {
-      const int st = s % kStages;
-      const int h = g * p.group + s / nqt, qt = qt_lo + s % nqt;
-      if (s >= kStages &&
-          !mbar_wait_warp(&bars->qd_empty[st], ((s / kStages) - 1) & 1, abort, err))
+    const int npairs = *p.num_k_pairs;
+    const int num_work = npairs * p.hkv;
+    int ni = 0, S = 0;  // items with work, steps so far
+    bool ok = true;
+    for (int nt = 0; ok; ++nt) {
+      const int slot = nt & 1;
+      if (nt >= 2 && !mbar_wait_warp(&bars->tile_empty[slot], ((nt >> 1) - 1) & 1, abort, err))
         break;
-      // lse2 / D of the tile's 128 query rows (rows past the sequence: empty)
-      float *vec = reinterpret_cast<float *>(smem + kKvOffVec + st * 1024);
-      const int valid = lq - qt * kBM;
-      const size_t at = static_cast<size_t>(h) * p.total_q + q0 + qt * kBM;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = lane + 32 * i;
-        vec[row] = row < valid ? p.lse2t[at + row] : INFINITY;
-        vec[128 + row] = row < valid ? p.dt[at + row] : 0.f;
+      if (lane == 0) {
+        KvTile t;
+        t.valid = 0;
+        const int w = static_cast<int>(atomicAdd(p.k_counter, 1u));
+        if (w < num_work) kv_decode(p, npairs, w, t);
+        bars->tiles[slot] = t;
+        mbar_arrive(&bars->tile_full[slot]);
       }
       __syncwarp();
-      mbar_arrive_expect_tx_elect(&bars->qd_full[st], 2 * kTileBytes);
-      tma_load_3d_elect(sbase + kKvOffQ + st * kTileBytes, &tm_q, &bars->qd_full[st], 0, h,
-                        q0 + qt * kBM);
-      tma_load_3d_elect(sbase + kKvOffDo + st * kTileBytes, &tm_do, &bars->qd_full[st], 0, h,
-                        q0 + qt * kBM);
+      const KvTile t = bars->tiles[slot];
+      if (!t.valid) break;
+      if (t.steps == 0) continue;
+      const int kb = ni & 1;
+      if (ni >= 2 && !mbar_wait_warp(&bars->kv_empty[kb], ((ni >> 1) - 1) & 1, abort, err)) break;
+      mbar_arrive_expect_tx_elect(&bars->kv_full[kb], 2 * kTileBytes);
+      tma_load_3d_elect(sbase + kKvOffK + kb * 2 * kTileBytes, &tm_k, &bars->kv_full[kb], 0, t.g,
+                        t.k0 + t.kt * kBN);
+      tma_load_3d_elect(sbase + kKvOffK + (kb * 2 + 1) * kTileBytes, &tm_v, &bars->kv_full[kb], 0,
+                        t.g, t.k0 + t.kt * kBN);
+      ++ni;
+      for (int s = 0; s < t.steps; ++s, ++S) {
+        const int st = S % kKvQStages;
+        const int h = t.g * p.group + s / t.nqt, qt = t.qt_lo + s % t.nqt;
+        if (S >= kKvQStages &&
+            !mbar_wait_warp(&bars->qd_empty[st], ((S / kKvQStages) - 1) & 1, abort, err)) {
+          ok = false;
+          break;
+        }
+        // lse2 / D of the tile's 128 query rows (rows past the sequence: empty)
+        float *vec = reinterpret_cast<float *>(smem + kKvOffVec + st * 1024);
+        const int valid = t.lq - qt * kBM;
+        const size_t at = static_cast<size_t>(h) * p.total_q + t.q0 + qt * kBM;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = lane + 32 * i;
+          vec[row] = row < valid ? p.lse2t[at + row] : INFINITY;
+          vec[128 + row] = row < valid ? p.dt[at + row] : 0.f;
+        }
+        __syncwarp();
+        mbar_arrive_expect_tx_elect(&bars->qd_full[st], 2 * kTileBytes);
+        tma_load_3d_elect(sbase + kKvOffQ + st * 2 * kTileBytes, &tm_q, &bars->qd_full[st], 0, h,
+                          t.q0 + qt * kBM);
+        tma_load_3d_elect(sbase + kKvOffQ + (st * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[st], 0,
+                          h, t.q0 + qt * kBM);
+      }
     }
     if (*abort) {
-      mbar_wait_warp(&bars->kv_full, 0, abort, err, true);
-      for (int i = max(0, s - kStages); i < s; ++i)
-        mbar_wait_warp(&bars->qd_full[i % kStages], (i / kStages) & 1, abort, err, true);
+      for (int i = max(0, ni - 2); i < ni; ++i)
+        mbar_wait_warp(&bars->kv_full[i & 1], (i >> 1) & 1, abort, err, true);
+      for (int i = max(0, S - kKvQStages); i < S; ++i)
+        mbar_wait_warp(&bars->qd_full[i % kKvQStages], (i / kKvQStages) & 1, abort, err, true);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA
-    const uint64_t kdesc = sdesc_sw128(sbase + kKvOffK);
-    const uint64_t vdesc = sdesc_sw128(sbase + kKvOffV);
+    const uint64_t kvdesc0 = sdesc_sw128(sbase + kKvOffK);
     const uint64_t qdesc0 = sdesc_sw128(sbase + kKvOffQ);
-    const uint64_t dodesc0 = sdesc_sw128(sbase + kKvOffDo);
-    const uint32_t t_st = tmem, t_dpt = tmem + 128, t_pt = tmem + 256, t_dst = tmem + 320;
+    constexpr uint64_t kHalfDesc = (kHalf * 128) >> 4;  // 64 rows of 128 B
     const uint32_t t_dv = tmem + 384, t_dk = tmem + 448;
-    bool ok = mbar_wait_warp(&bars->kv_full, 0, abort, err) &&
-              mbar_wait_warp(&bars->qd_full[0], 0, abort, err);
-    if (ok) {
-      tc_fence_after();
+    int ni = 0, S = 0, G = 0, done_items = 0;
+    bool ok = true;
+    // S^T_b, dP^T_b of global sub-step g (item-local ss; step stage st)
+    auto issue_s = [&](int g, int ss, int st, int kb) {
+      const int b = g & 1, u = ss & 1;
+      const uint64_t kd = kvdesc0 + kb * 2 * kTileDesc, vd = kd + kTileDesc;
+      const uint64_t qd = qdesc0 + st * 2 * kTileDesc + u * kHalfDesc;
+      const uint64_t dod = qdesc0 + (st * 2 + 1) * kTileDesc + u * kHalfDesc;
 #pragma unroll
       for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(t_st, kdesc + 2 * ks, qdesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
+        umma_ss_elect(tmem + 64 * b, kd + 2 * ks, qd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(t_dpt, vdesc + 2 * ks, dodesc0 + 2 * ks, kIdescSS, ks > 0 ? 1u : 0u);
-      umma_commit_elect(&bars->st_full);
-    }
-    for (int s = 0; ok && s < steps; ++s) {
-      if (!mbar_wait_warp(&bars->ew_done, s & 1, abort, err)) {
-        ok = false;
-        break;
+        umma_ss_elect(tmem + 128 + 64 * b, vd + 2 * ks, dod + 2 * ks, kIdescSS64,
+                      ks > 0 ? 1u : 0u);
+      umma_commit_elect(&bars->st_full[b]);
+    };
+    for (int nt = 0; ok; ++nt) {
+      const int slot = nt & 1;
+      if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
+      const KvTile t = bars->tiles[slot];
+      if (!t.valid) break;
+      if (t.steps > 0) {
+        const int kb = ni & 1, subs = 2 * t.steps;
+        ok = mbar_wait_warp(&bars->kv_full[kb], (ni >> 1) & 1, abort, err) &&
+             mbar_wait_warp(&bars->qd_full[S % kKvQStages], (S / kKvQStages) & 1, abort, err);
+        if (ok) {
+          tc_fence_after();
+          issue_s(G, 0, S % kKvQStages, kb);
+          issue_s(G + 1, 1, S % kKvQStages, kb);
+        }
+        // dV/dK of the previous item must have been read by its epilogue
+        if (ok && done_items > 0)
+          ok = mbar_wait_warp(&bars->dkv_free, (done_items - 1) & 1, abort, err);
+        for (int ss = 0; ok && ss < subs; ++ss) {
+          const int g = G + ss, b = g & 1, s = ss >> 1, u = ss & 1;
+          const int st = (S + s) % kKvQStages;
+          if (!mbar_wait_warp(&bars->ew_done[b], (g >> 1) & 1, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qd = qdesc0 + st * 2 * kTileDesc + u * kHalfDesc;
+          const uint64_t dod = qdesc0 + (st * 2 + 1) * kTileDesc + u * kHalfDesc;
+#pragma unroll
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            umma_ts_elect(t_dv, tmem + 256 + 32 * b + kk * 8, dod + kk * kRows16Desc, kIdescTS,
+                          (ss > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            umma_ts_elect(t_dk, tmem + 320 + 32 * b + kk * 8, qd + kk * kRows16Desc, kIdescTS,
+                          (ss > 0 || kk > 0) ? 1u : 0u);
+          if (u == 1) umma_commit_elect(&bars->qd_empty[st]);  // both halves done with the step
+          if (ss + 2 < subs) {
+            const int st2 = (S + s + 1) % kKvQStages;
+            if (u == 0 && !mbar_wait_warp(&bars->qd_full[st2], ((S + s + 1) / kKvQStages) & 1,
+                                          abort, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(g + 2, ss + 2, st2, kb);
+          }
+        }
+        if (!ok) break;
+        umma_commit_elect(&bars->kv_empty[kb]);
+        umma_commit_elect(&bars->dkv_done);
+        ++done_items;
+        ++ni;
+        S += t.steps;
+        G += subs;
       }
-      tc_fence_after();
-      const int st = s % kStages;
-      const uint64_t qd = qdesc0 + st * kTileDesc, dod = dodesc0 + st * kTileDesc;
+      if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
+    }
+    umma_commit_elect(&bars->drain);
+    mbar_wait_warp(&bars->drain, 0, abort, err, true);
+  } else {
+    // ---------------------------------------- P^T, dS^T (one key / thread)
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_st = tmem + lane_off + 64 * wg, t_dpt = t_st + 128;
+    const uint32_t t_pt = tmem + lane_off + 256 + 32 * wg, t_dst = t_pt + 64;
+    const uint32_t t_dv = tmem + lane_off + 384 + 32 * wg, t_dk = t_dv + 64;
+    int S = 0, G = 0, done_items = 0;
+    bool ok = true;
+    for (int nt = 0; ok; ++nt) {
+      const int slot = nt & 1;
+      if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
+      const KvTile t = bars->tiles[slot];
+      if (!t.valid) break;
+      const size_t krow = (static_cast<size_t>(t.k0 + t.kt * kBN + r) * p.hkv + t.g) * kHeadDim +
+                          32 * wg;
+      if (t.steps == 0) {  // no query sees this key tile
+        if (r < t.krows) {
 #pragma unroll
-      for (int kk = 0; kk < kBM / 16; ++kk)
-        umma_ts_elect(t_dv, t_pt + kk * 8, dod + kk * kRows16Desc, kIdescTS,
-                      (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < kBM / 16; ++kk)
-        umma_ts_elect(t_dk, t_dst + kk * 8, qd + kk * kRows16Desc, kIdescTS,
-                      (s > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_elect(&bars->qd_empty[st]);
-      if (s + 1 < steps) {
-        const int s1 = (s + 1) % kStages;
-        if (!mbar_wait_warp(&bars->qd_full[s1], ((s + 1) / kStages) & 1, abort, err)) {
+          for (int i = 0; i < 4; ++i) {
+            reinterpret_cast<uint4 *>(p.dk + krow)[i] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4 *>(p.dv + krow)[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        mbar_arrive(&bars->tile_empty[slot]);
+        continue;
+      }
+      const int jk = t.kt * kBN + r;  // this thread's key
+      const int subs = 2 * t.steps;
+      for (int ss = wg; ss < subs; ss += 2) {
+        const int g = G + ss, s = ss >> 1, u = ss & 1;
+        const int st = (S + s) % kKvQStages;
+        // the lse / D vectors are plain shared-memory stores: wait on their
+        // barrier directly, then on the MMAs
+        if (!mbar_wait_warp(&bars->qd_full[st], ((S + s) / kKvQStages) & 1, abort, err) ||
+            !mbar_wait_warp(&bars->st_full[wg], (g >> 1) & 1, abort, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const int qt = t.qt_lo + s % t.nqt;
+        // visible query columns of this key in the half: [c_lo, c_hi)
+        const int qb = t.lk - t.lq + qt * kBM + u * kHalf;  // position of the half's query 0
+        int c_lo = 0, c_hi = min(kHalf, t.lq - qt * kBM - u * kHalf);
+        if (p.causal) c_lo = min(max(jk - qb, 0), kHalf);
+        if (p.window > 0) c_hi = min(c_hi, max(jk - qb + p.window, 0));
+        const int len = r < t.krows ? max(c_hi - c_lo, 0) : 0;
+        const float *vec = reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024) + u * kHalf;
 #pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_ss_elect(t_st, kdesc + 2 * ks, qdesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
-                        ks > 0 ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          umma_ss_elect(t_dpt, vdesc + 2 * ks, dodesc0 + s1 * kTileDesc + 2 * ks, kIdescSS,
-                        ks > 0 ? 1u : 0u);
-        umma_commit_elect(&bars->st_full);
+        for (int c = 0; c < 2; ++c) {
+          float sv[32], dp[32];
+          tmem_ld32f(t_st + 32 * c, sv);
+          tmem_ld32f(t_dpt + 32 * c, dp);
+          tmem_wait_ld();
+          mask32(sv, 32 * c, c_lo, len);
+          uint32_t p16[16], ds16[16];
+          p_ds_col(sv, dp, p.scale_log2, vec + 32 * c, vec + 128 + 32 * c, p16, ds16);
+          tmem_st16(t_pt + 16 * c, p16);
+          tmem_st16(t_dst + 16 * c, ds16);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->ew_done[wg]);
       }
-    }
-    if (ok) umma_commit_elect(&bars->done);
-    umma_commit_elect(&bars->drain);
-    mbar_wait_warp(&bars->drain, 0, abort, err, true);
-  } else {
-    // ------------------------------------------- P^T, dS^T (one key / thread)
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_st = tmem + lane_off, t_dpt = t_st + 128, t_pt = t_st + 256,
-                   t_dst = t_st + 320, t_dv = t_st + 384, t_dk = t_st + 448;
-    const int jk = kt * kBN + r;  // this thread's key
-    bool ok = true;
-    for (int s = 0; s < steps; ++s) {
-      const int st = s % kStages;
-      const int qt = qt_lo + s % nqt;
-      // the lse / D vectors are plain shared-memory stores: wait on their
-      // barrier directly, then on the MMAs
-      if (!mbar_wait_warp(&bars->qd_full[st], (s / kStages) & 1, abort, err) ||
-          !mbar_wait_warp(&bars->st_full, s & 1, abort, err)) {
-        ok = false;
-        break;
-      }
+      if (!ok) break;
+      S += t.steps;
+      G += subs;
+      if (!mbar_wait_warp(&bars->dkv_done, done_items & 1, abort, err)) break;
+      ++done_items;
       tc_fence_after();
-      // visible query columns of this key: [c_lo, c_hi)
-      const int qb = base + qt * kBM;  // position of the tile's query 0
-      int c_lo = 0, c_hi = min(kBM, lq - qt * kBM);
-      if (p.causal) c_lo = min(max(jk - qb, 0), kBM);
-      if (p.window > 0) c_hi = min(c_hi, max(jk - qb + p.window, 0));
-      const int len = r < krows ? max(c_hi - c_lo, 0) : 0;
-      const float *vec = reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float sv[32], dp[32];
-        tmem_ld32f(t_st + 32 * c, sv);
-        tmem_ld32f(t_dpt + 32 * c, dp);
-        tmem_wait_ld();
-        mask32(sv, 32 * c, c_lo, len);
-        uint32_t p16[16], ds16[16];
-        p_ds_col(sv, dp, p.scale_log2, vec + 32 * c, vec + 128 + 32 * c, p16, ds16);
-        tmem_st16(t_pt + 16 * c, p16);
-        tmem_st16(t_dst + 16 * c, ds16);
-      }
-      tmem_wait_st();
+      uint32_t dvv[32], dkv[32];
+      tmem_ld32(t_dv, dvv);
+      tmem_ld32(t_dk, dkv);
+      tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bars->ew_done);
-    }
-    if (ok && mbar_wait_warp(&bars->done, 0, abort, err)) {
-      tc_fence_after();
-      store_row64(t_dv, 1.f, p.dv + krow, r < krows);
-      store_row64(t_dk, p.scale, p.dk + krow, r < krows);
+      mbar_arrive(&bars->dkv_free);
+      if (r < t.krows) {
+        uint4 *v4 = reinterpret_cast<uint4 *>(p.dv + krow);
+        uint4 *k4 = reinterpret_cast<uint4 *>(p.dk + krow);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float *x = reinterpret_cast<const float *>(&dvv[8 * i]);
+          const float *y = reinterpret_cast<const float *>(&dkv[8 * i]);
+          v4[i] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                             pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+          const float sc = p.scale;
+          k4[i] = make_uint4(pack_bf16x2(y[0] * sc, y[1] * sc), pack_bf16x2(y[2] * sc, y[3] * sc),
+                             pack_bf16x2(y[4] * sc, y[5] * sc), pack_bf16x2(y[6] * sc, y[7] * sc));
+        }
+      }
+      mbar_arrive(&bars->tile_empty[slot]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -898,7 +977,7 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
   if ((e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kDqSmem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemRequest)) != cudaSuccess)
+                                kKvSmem)) != cudaSuccess)
     return e;
   if (a.total_q > 0) {
     const int64_t items = (a.total_q / kBM + a.batch) * a.hq;
@@ -912,8 +991,9 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
   }
   if (a.total_k > 0) {
     const int64_t items = (a.total_k / kBN + a.batch) * a.hkv;
-    bwd_dkdv_kernel<<<static_cast<unsigned>(items), 192, kSmemRequest, stream>>>(tq, tdo, tk, tv,
-                                                                                p);
+    const int64_t grid = items < sm_count() ? items : sm_count();
+    bwd_dkdv_kernel<<<static_cast<unsigned>(grid), kKvThreads, kKvSmem, stream>>>(tq, tdo, tk, tv,
+                                                                                 p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
