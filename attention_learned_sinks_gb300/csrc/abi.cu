@@ -18,13 +18,22 @@ bool mask_ok(const sinkattn_mask_t &m) {
   return m.window >= 0 && isfinite(m.scale) && m.scale > 0.f;
 }
 
+// The CUDA error behind the calling thread's last SINKATTN_ERR_CUDA.
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 sinkattn_status_t from_cuda(cudaError_t e) {
-  return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+  if (e == cudaSuccess) return SINKATTN_OK;
+  t_last_cuda_error = e;
+  return SINKATTN_ERR_CUDA;
 }
 
 }  // namespace
 
 extern "C" {
+
+const char *sinkattn_last_cuda_error(void) {
+  return t_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorName(t_last_cuda_error);
+}
 
 const char *sinkattn_status_string(sinkattn_status_t s) {
   switch (s) {

@@ -22,6 +22,7 @@ SINKATTN_ERR_CUDA = 4
 
 EXPORTED = (
     "sinkattn_status_string",
+    "sinkattn_last_cuda_error",
     "sinkattn_prefill_workspace_size",
     "sinkattn_prefill",
     "sinkattn_prefill_paged_workspace_size",
@@ -40,7 +41,13 @@ EXPORTED = (
 class SinkAttnError(RuntimeError):
     def __init__(self, status, what):
         self.status = status
-        super().__init__("%s: %s (status %d)" % (what, _status_string(status), status))
+        msg = "%s: %s (status %d)" % (what, _status_string(status), status)
+        if status == SINKATTN_ERR_CUDA:
+            try:
+                msg += ": " + load().sinkattn_last_cuda_error().decode()
+            except Exception:  # library missing: the status alone
+                pass
+        super().__init__(msg)
 
 
 class Mask(ctypes.Structure):
@@ -62,6 +69,8 @@ def load(path: str = LIB_PATH):
     P, I, L, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.sinkattn_status_string.argtypes = [I]
     lib.sinkattn_status_string.restype = ctypes.c_char_p
+    lib.sinkattn_last_cuda_error.argtypes = []
+    lib.sinkattn_last_cuda_error.restype = ctypes.c_char_p
     lib.sinkattn_prefill_workspace_size.argtypes = [I, L, L, I, I, I, I, I, I, I]
     lib.sinkattn_prefill_workspace_size.restype = S
     lib.sinkattn_prefill.argtypes = [P, P, P, P, P, I, L, L, I, I, I, I, I, P, Mask, I,

@@ -71,6 +71,11 @@ typedef struct {
 /* Human-readable name of a status code (static storage). */
 const char *sinkattn_status_string(sinkattn_status_t status);
 
+/* Name of the CUDA error behind the calling thread's most recent
+ * SINKATTN_ERR_CUDA (e.g. "cudaErrorLaunchOutOfResources"), or "no CUDA
+ * error"; static storage. */
+const char *sinkattn_last_cuda_error(void);
+
 /*
  * Prefill over packed variable-length sequences (page "Fast embeddings on
  * GPUs", section "ROSE": attention over ragged inputs without padding).
