@@ -55,12 +55,12 @@ size_t sinkattn_prefill_workspace_size(int batch, int64_t total_q, int64_t total
                                        int max_seqlen_q, int max_seqlen_k, int hq, int hkv,
                                        int head_dim, int window, int num_splits) {
   if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
-      hq <= 0 || hkv <= 0 || hq % hkv != 0 || head_dim != kHeadDim || window < 0 ||
+      hq <= 0 || hkv <= 0 || hq % hkv != 0 || !prefill_head_dim_ok(head_dim) || window < 0 ||
       num_splits < 0)
     return 0;
   const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
-                                         hq, hkv, window);
-  return prefill_workspace_bytes(batch, total_q, total_k, hq, hkv, splits);
+                                         hq, hkv, window, head_dim);
+  return prefill_workspace_bytes(batch, total_q, total_k, hq, hkv, splits, head_dim);
 }
 
 sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
@@ -73,7 +73,7 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
   if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 ||
       hkv <= 0 || hq % hkv != 0 || num_splits < 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (!prefill_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return SINKATTN_OK;
   if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return SINKATTN_ERR_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
@@ -84,10 +84,10 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
       (max_seqlen_q + 127) / 128 > 65535)
     return SINKATTN_ERR_UNSUPPORTED;
   const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
-                                         hq, hkv, mask.window);
+                                         hq, hkv, mask.window, head_dim);
   if (splits > 1 && static_cast<int64_t>(splits) * total_q * hq > INT32_MAX)
     return SINKATTN_ERR_UNSUPPORTED;
-  const size_t need = prefill_workspace_bytes(batch, total_q, total_k, hq, hkv, splits);
+  const size_t need = prefill_workspace_bytes(batch, total_q, total_k, hq, hkv, splits, head_dim);
   if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
   PrefillLaunch a;
@@ -110,6 +110,7 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
   a.out = out;
   a.lse = lse;
   a.num_splits = splits;
+  a.head_dim = head_dim;
   a.v_f16 = workspace;
   bool encode_failed = false;
   cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream), &encode_failed);
@@ -121,11 +122,11 @@ size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max
                                              int max_seqlen_k, int hq, int hkv, int head_dim,
                                              int window, int num_splits) {
   if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 ||
-      hq % hkv != 0 || head_dim != kHeadDim || window < 0 || num_splits < 0)
+      hq % hkv != 0 || !prefill_head_dim_ok(head_dim) || window < 0 || num_splits < 0)
     return 0;
   const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
-                                         hq, hkv, window);
-  return prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hq, hkv, splits);
+                                         hq, hkv, window, head_dim);
+  return prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hq, hkv, splits, head_dim);
 }
 
 sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q,
@@ -141,7 +142,7 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
       hq % hkv != 0 || num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0 ||
       num_splits < 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (!prefill_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_seqlen_k) > static_cast<int64_t>(max_pages_per_seq) * page_size)
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return SINKATTN_OK;
@@ -156,10 +157,11 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
       static_cast<int64_t>(batch) * max_seqlen_k + 128 > INT32_MAX)
     return SINKATTN_ERR_UNSUPPORTED;
   const int splits = prefill_plan_splits(num_splits, batch, total_q, max_seqlen_q, max_seqlen_k,
-                                         hq, hkv, mask.window);
+                                         hq, hkv, mask.window, head_dim);
   if (splits > 1 && static_cast<int64_t>(splits) * total_q * hq > INT32_MAX)
     return SINKATTN_ERR_UNSUPPORTED;
-  const size_t need = prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hq, hkv, splits);
+  const size_t need =
+      prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hq, hkv, splits, head_dim);
   if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
   PrefillPagedLaunch a;
@@ -182,6 +184,7 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
   a.base.out = out;
   a.base.lse = lse;
   a.base.num_splits = splits;
+  a.base.head_dim = head_dim;
   a.base.v_f16 = nullptr;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
@@ -306,14 +309,14 @@ sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_ls
                                  int64_t rows, int hq, int head_dim, const float *sinks, void *out,
                                  float *lse, void *stream) {
   if (num_splits < 0 || rows < 0 || hq <= 0) return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (!prefill_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   if (rows == 0) return SINKATTN_OK;
   if (!out || (num_splits > 0 && (!partial_o || !partial_lse))) return SINKATTN_ERR_INVALID_ARGUMENT;
   if ((partial_o && !aligned(partial_o, 16)) || (partial_lse && !aligned(partial_lse, 4)) ||
       !aligned(out, 16) || (sinks && !aligned(sinks, 4)) || (lse && !aligned(lse, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if ((rows * hq + 7) / 8 > INT32_MAX) return SINKATTN_ERR_UNSUPPORTED;
-  return from_cuda(launch_merge(partial_o, partial_lse, num_splits, rows, hq, sinks, out, lse,
+  return from_cuda(launch_merge(partial_o, partial_lse, num_splits, rows, hq, head_dim, sinks, out, lse,
                                 static_cast<cudaStream_t>(stream)));
 }
 

@@ -17,14 +17,15 @@
 //     head are contiguous);
 //  2. bwd_prep_kv_kernel: fp16 copies of k and v;
 //  3. two tile lists (query tiles, key tiles);
-//  4. bwd_dq_kernel: one CTA per (query tile, head); per key tile S = Q K^T
-//     and dP = dO V^T on tcgen05 into TMEM, P and dS in registers, dQ += dS K
-//     (dS as the TMEM A operand) and Y += P K; it also forms the exact
-//     D = sum_j P_j dP_j and corrects dQ with it;
+//  4. bwd_dq_kernel: persistent; per (query tile, head) item and key tile,
+//     S = Q K^T and dP = dO V^T on tcgen05 into TMEM, P and dS in registers,
+//     dQ += dS K (dS as the TMEM A operand) and Y += P K; it also forms the
+//     exact D = sum_j P_j dP_j and corrects dQ with it;
 //  5. bwd_dsink_kernel: dc_h, one block per head, fixed summation order;
-//  6. bwd_dkdv_kernel: one CTA per (key tile, KV head); per (query head,
-//     query tile) S^T = K Q^T and dP^T = V dO^T, P^T and dS^T in registers,
-//     dV += P^T dO and dK += dS^T Q with P^T / dS^T as TMEM A operands.
+//  6. bwd_dkdv_kernel: persistent; per (key tile, KV head) item and (query
+//     head, query tile) step, S^T = K Q^T and dP^T = V dO^T, P^T and dS^T in
+//     registers, dV += P^T dO and dK += dS^T Q with P^T / dS^T as TMEM A
+//     operands.
 // Every gradient element is written by exactly one CTA (no atomics), so the
 // results are deterministic. All MMA operands are fp16 (bf16 inputs convert
 // exactly except below 2^-14, and P, dS in fp16 keep 11 significant bits);
@@ -532,7 +533,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // ------------------------------------------------------------- dK / dV -----
 // Persistent: one CTA per SM takes (key tile, KV head) items from the key
 // tile list (walked backwards: under a causal mask the low key tiles are seen
-// by the most queries, so this is longest first within each KV head). An item's steps run over
+// by the most queries, so this is longest first within each KV head). An
+// item's steps run over
 // (query head of the group, query tile that sees the key tile); each step's
 // 128 queries are two 64-query halves, taken by softmax-side warpgroup w
 // (one key per thread) for halves of parity w, in its own TMEM buffers, so

@@ -689,7 +689,7 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
   if (batch < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || num_splits < 0 ||
       kv_rows < 0 || mask.window < 0 || !isfinite(mask.scale) || !(mask.scale > 0.f))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (head_dim != kHeadDim || hq / hkv > 8) return SINKATTN_ERR_UNSUPPORTED;
+  if (!decode_head_dim_ok(head_dim) || hq / hkv > 8) return SINKATTN_ERR_UNSUPPORTED;
   const bool paged = block_table != nullptr;
   if (paged == (kv_indptr != nullptr)) return SINKATTN_ERR_INVALID_ARGUMENT;
   if (paged && (seqlens_k == nullptr || page_size <= 0 || max_pages_per_seq <= 0))
@@ -706,7 +706,7 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
   const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
   // the plan's scratch must fit the fixed array
   if (plan.max_splits > 1 &&
-      decode_workspace_layout(batch, hq, hkv, plan, kHeadDim).bytes >
+      decode_workspace_layout(batch, hq, hkv, plan, head_dim).bytes >
           SINKATTN_NOALLOC_SCRATCH_BYTES)
     return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
   int device = 0;
@@ -733,6 +733,7 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
   a.lse = lse;
   a.workspace = scratch;
   a.plan = plan;
+  a.head_dim = head_dim;
   return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
                                                                              : SINKATTN_ERR_CUDA;
 }

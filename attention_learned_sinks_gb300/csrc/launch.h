@@ -45,8 +45,8 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream);
 
 // ---- merge -----------------------------------------------------------------
 cudaError_t launch_merge(const float *partial_o, const float *partial_lse, int num_splits,
-                         int64_t rows, int hq, const float *sinks, void *out, float *lse,
-                         cudaStream_t stream);
+                         int64_t rows, int hq, int head_dim, const float *sinks, void *out,
+                         float *lse, cudaStream_t stream);
 
 // ---- tile lists ------------------------------------------------------------
 // One block on `stream`: the non-empty (sequence b, 128-row tile t) pairs of
@@ -69,6 +69,7 @@ struct PrefillLaunch {
   void *out;
   float *lse;
   int num_splits;  // key-range splits per work item (>= 1), from prefill_plan_splits
+  int head_dim = kHeadDim;  // 64 or 128
   // workspace (prefill_workspace_bytes): fp16 copy of v, tile counter, work
   // list, split partials
   void *v_f16;
@@ -78,9 +79,11 @@ struct PrefillLaunch {
 // few (query tile, head) items over long contexts fill the GPU.
 constexpr int kMaxPrefillSplits = 64;
 int prefill_plan_splits(int requested, int batch, int64_t total_q, int max_seqlen_q,
-                        int max_seqlen_k, int hq, int hkv, int window);
+                        int max_seqlen_k, int hq, int hkv, int window, int head_dim);
 size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv,
-                               int splits);
+                               int splits, int head_dim);
+// head dims the prefill kernels are built for
+inline bool prefill_head_dim_ok(int d) { return d == 64 || d == 128; }
 // Returns cudaSuccess, or the failing CUDA error; *encode_failed is set when
 // the tensor-map encoding (driver entry point) failed.
 cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *encode_failed);
@@ -95,7 +98,7 @@ struct PrefillPagedLaunch {
   void *workspace;
 };
 size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hq,
-                                     int hkv, int splits);
+                                     int hkv, int splits, int head_dim);
 cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,
                                  bool *encode_failed);
 // ---- backward --------------------------------------------------------------

@@ -5,8 +5,8 @@
 // and the sink must be counted once. Here each block k brings a normalised
 // output o_k and its natural-log lse_k; the optional sink is one more block
 // with lse = sink_h and a zero output. One warp per (row, head); each lane
-// owns two of the 64 output dims. HBM-bound: reads num_splits * 260 B and
-// writes 132 B per (row, head).
+// owns D/32 of the D output dims (D = 64 or 128). HBM-bound: reads
+// num_splits * (4 D + 4) B and writes 2 D + 4 B per (row, head).
 #include <math.h>
 
 #include "launch.h"
@@ -19,6 +19,7 @@ constexpr int kWarpsPerBlock = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+template <int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(
     const float *__restrict__ po, const float *__restrict__ pl, int nsplit, int64_t rows, int hq,
     const float *__restrict__ sinks, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
@@ -31,34 +32,50 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(
 
   float M = sink;
   for (int k = 0; k < nsplit; ++k) M = fmaxf(M, pl[k * n + idx]);
-  float W = 0.f, a0 = 0.f, a1 = 0.f;
+  constexpr int kPer = D / 32;  // dims per lane: 2 or 4
+  float W = 0.f, acc[kPer] = {};
   if (M != -INFINITY) {
     W = sinks != nullptr ? fast_exp2((sink - M) * kLog2e) : 0.f;
     for (int k = 0; k < nsplit; ++k) {
       const float l = pl[k * n + idx];
       if (l == -INFINITY) continue;
       const float w = fast_exp2((l - M) * kLog2e);
-      const float2 o = *reinterpret_cast<const float2 *>(po + (k * n + idx) * kHeadDim + 2 * lane);
+      const float *o = po + (k * n + idx) * D + kPer * lane;
+      float ov[kPer];
+      if constexpr (kPer == 2) {
+        const float2 t = *reinterpret_cast<const float2 *>(o);
+        ov[0] = t.x, ov[1] = t.y;
+      } else {
+        const float4 t = *reinterpret_cast<const float4 *>(o);
+        ov[0] = t.x, ov[1] = t.y, ov[2] = t.z, ov[3] = t.w;
+      }
       W += w;
-      a0 += w * o.x;
-      a1 += w * o.y;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) acc[i] += w * ov[i];
     }
   }
   const float iw = W > 0.f ? 1.f / W : 0.f;
-  reinterpret_cast<uint32_t *>(out + idx * kHeadDim)[lane] = pack_bf16x2(a0 * iw, a1 * iw);
+  uint32_t *dst = reinterpret_cast<uint32_t *>(out + idx * D) + (kPer / 2) * lane;
+#pragma unroll
+  for (int i = 0; i < kPer / 2; ++i) dst[i] = pack_bf16x2(acc[2 * i] * iw, acc[2 * i + 1] * iw);
   if (lse != nullptr && lane == 0) lse[idx] = W > 0.f ? M + fast_log2(W) * kLn2 : -INFINITY;
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const float *partial_o, const float *partial_lse, int num_splits,
-                         int64_t rows, int hq, const float *sinks, void *out, float *lse,
-                         cudaStream_t stream) {
+                         int64_t rows, int hq, int head_dim, const float *sinks, void *out,
+                         float *lse, cudaStream_t stream) {
   const int64_t n = rows * hq;
   if (n == 0) return cudaSuccess;
   const int64_t blocks = (n + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  merge_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
-      partial_o, partial_lse, num_splits, rows, hq, sinks, static_cast<__nv_bfloat16 *>(out), lse);
+  auto *o = static_cast<__nv_bfloat16 *>(out);
+  if (head_dim == 128)
+    merge_kernel<128><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
+        partial_o, partial_lse, num_splits, rows, hq, sinks, o, lse);
+  else
+    merge_kernel<64><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
+        partial_o, partial_lse, num_splits, rows, hq, sinks, o, lse);
   return cudaGetLastError();
 }
 

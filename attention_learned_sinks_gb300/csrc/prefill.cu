@@ -52,16 +52,22 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per KV tile
-constexpr int kStages = 3;
-constexpr int kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
+constexpr int kMaxStages = 3;                    // K/V ring depth at head_dim 64 (2 at 128)
+constexpr int kBlockBytes = kBM * 64 * 2;        // 16 KB: 128 rows x 64 elements (one swizzle block)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;                        // S buffers shared round-robin by the tiles
-constexpr uint32_t kTmemO = kSBufs * 128;        // O_t at 384 + 64 t
+constexpr uint32_t kTmemO = kSBufs * 128;        // O_t at 384 + D t
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int NT>
+// NT query heads per item (2 when the group size is even), head dimension D:
+// 64 (NT 1 or 2) or 128 (NT 1). A 128-row tile of one head is D / 64
+// blocks of 128 rows x 128 bytes, each loaded by one TMA box with 128-byte
+// swizzle; at D = 128 the K/V ring has two stages so that two Q buffers and
+// the ring fit in shared memory, and O (128 columns) fills TMEM beside the
+// three S buffers.
+template <int NT, int D>
 struct Cfg {
   // NT = 2: three full warpgroups, so setmaxnreg can move registers from the
   // producer/MMA warpgroup to the two softmax warpgroups.
@@ -72,20 +78,22 @@ struct Cfg {
   static constexpr int kProducerWarp = NT * 4;
   static constexpr int kMmaWarp = NT * 4 + 1;    // P V issuer, TMEM owner
   static constexpr int kQkWarp = NT * 4 + 2;     // Q K^T issuer
+  static constexpr int kTile = kBM * D * 2;                        // one 128-row tile of one head
+  static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kOffQ = 0;                                  // 2 buffers x NT tiles
-  static constexpr int kOffK = kOffQ + 2 * NT * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffK = kOffQ + 2 * NT * kTile;
+  static constexpr int kOffV = kOffK + kStages * kTile;
+  static constexpr int kOffBar = kOffV + kStages * kTile;
   static constexpr int kOffPend = kOffBar + 1024;  // 16 B per softmax thread: deferred epilogue
   static constexpr int kSmemBytes = kOffPend + NT * 128 * 16 + 1024;  // + alignment slack
 };
 
-static_assert(Cfg<2>::kRegsOther * 128 + Cfg<2>::kRegsSoftmax * 256 <=
-                  Cfg<2>::kLaunchRegs * Cfg<2>::kThreads,
+static_assert(Cfg<2, 64>::kRegsOther * 128 + Cfg<2, 64>::kRegsSoftmax * 256 <=
+                  Cfg<2, 64>::kLaunchRegs * Cfg<2, 64>::kThreads,
               "register split must fit the registers the block is launched with");
 
 constexpr uint32_t kIdescQK = idesc_f32acc(kBM, kBN, /*bf16=*/true, false, false);
-constexpr uint32_t kIdescPV = idesc_f32acc(kBM, kHeadDim, /*bf16=*/false, false, true);
+constexpr uint32_t kIdescPV = idesc_f32acc(kBM, 64, /*bf16=*/false, false, true);  // per 64 dims
 
 __device__ int g_prefill_error;
 
@@ -101,7 +109,7 @@ struct Params {
   const int *num_pairs;        // its length
   // Split-KV: with num_splits > 1 every (tile, heads) item is cut into that
   // many key ranges; split s writes its normalised partial output and lse to
-  // part_o [s][total_q][hq][64] / part_lse [s][total_q][hq] (fp32) instead of
+  // part_o [s][total_q][hq][D] / part_lse [s][total_q][hq] (fp32) instead of
   // out/lse, and only split 0 starts from the sink.
   int num_splits, total_q;
   float *part_o, *part_lse;
@@ -116,9 +124,9 @@ struct Tile {
 
 struct Barriers {
   uint64_t q_full[2], q_empty[2];       // double-buffered Q tiles
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_full[kMaxStages];
+  uint64_t v_full[kMaxStages];
+  uint64_t kv_empty[kMaxStages];
   uint64_t s_full[kSBufs];
   uint64_t p_full[kSBufs];
   uint64_t pv_done[kSBufs];             // P V of the item in this S buffer has completed
@@ -303,11 +311,13 @@ __global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_
 // is exhausted. Every role keeps running counters (S buffer items, K/V stages,
 // Q buffers, tiles) across tiles, so the next tile's loads and Q K^T overlap
 // the current tile's softmax and epilogue.
-template <int NT>
-__global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
+template <int NT, int D>
+__global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<NT>;
+  using C = Cfg<NT, D>;
+  constexpr int kStages = C::kStages;
+  constexpr int kTileBytes = C::kTile;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       mbar_init(&bars->tile_empty[i], NT * kBM + 2);
       mbar_init(&bars->drain[i], 1);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= C::kProducerWarp) {
-    if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsOther));
+    if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<2, 64>::kRegsOther));
     if (warp == C::kProducerWarp) {
       // ---------------------------------------------------------- producer
       // Fetches tiles, publishes them in the 2-slot ring, and streams each
@@ -359,6 +369,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      // one tile = D / 64 boxes of 64 elements, into consecutive 16 KB blocks
+      auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint64_t *bar, int head, int row) {
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_3d_elect(dst + blk * kBlockBytes, map, bar, blk * 64, head, row);
+      };
       int J = 0;  // K/V stage uses so far
       int q_loads = 0;
       const int npairs = *p.num_pairs;
@@ -386,8 +402,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         mbar_arrive_expect_tx_elect(&bars->q_full[qb], NT * kTileBytes);
         ++q_loads;
         for (int i = 0; i < NT; ++i)
-          tma_load_3d_elect(sbase + C::kOffQ + (qb * NT + i) * kTileBytes, &tm_q, &bars->q_full[qb],
-                            0, t.h0 + i, t.q0 + t.qt * kBM);
+          load_tile(sbase + C::kOffQ + (qb * NT + i) * kTileBytes, &tm_q, &bars->q_full[qb],
+                    t.h0 + i, t.q0 + t.qt * kBM);
         bool ok = true;
         for (int j = 0; j < t.n; ++j, ++J) {
           const int st = J % kStages;
@@ -398,11 +414,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           }
           const int row = t.k0 + (t.kt_lo + j) * kBN;
           mbar_arrive_expect_tx_elect(&bars->k_full[st], kTileBytes);
-          tma_load_3d_elect(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, t.kvh,
-                            row);
+          load_tile(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], t.kvh, row);
           mbar_arrive_expect_tx_elect(&bars->v_full[st], kTileBytes);
-          tma_load_3d_elect(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, t.kvh,
-                            row);
+          load_tile(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], t.kvh, row);
         }
         if (!ok) break;
       }
@@ -427,7 +441,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       // P. With three buffers Q K^T runs up to two items ahead of the softmax,
       // also across tile boundaries. Each warp runs its loop whole (uniform
       // operands); one elected lane issues each MMA and commit.
-      constexpr uint64_t kTileDesc = kTileBytes >> 4;  // one tile, in descriptor address units
+      constexpr uint64_t kTileDesc = kTileBytes >> 4;   // one tile, in descriptor address units
+      constexpr uint64_t kBlockDesc = kBlockBytes >> 4;  // one 64-element block of a tile
       const int role = warp == C::kMmaWarp ? 0 : 1;
       const uint64_t qdesc0 = sdesc_sw128(sbase + C::kOffQ);
       const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
@@ -464,8 +479,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const uint64_t kd = kdesc0 + (Jc % kStages) * kTileDesc;
             const uint32_t sbuf = tmem + b * kBN;
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              umma_ss_elect(sbuf, qd + 2 * ks, kd + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks) {  // k-step ks: block ks / 4, 32-byte step ks % 4
+              const uint64_t off = (ks >> 2) * kBlockDesc + 2 * (ks & 3);
+              umma_ss_elect(sbuf, qd + off, kd + off, kIdescQK, ks > 0 ? 1u : 0u);
+            }
             umma_commit_elect(&bars->s_full[b]);
           }
           if (ok) umma_commit_elect(&bars->q_empty[qb]);  // Q buffer free once these QK finish
@@ -493,11 +510,14 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             tc_fence_after();
             const uint64_t vd = vdesc0 + (Jc % kStages) * kTileDesc;
             const uint32_t pbuf = tmem + b * kBN;
-            const uint32_t obuf = tmem + kTmemO + tt * kHeadDim;
+            const uint32_t obuf = tmem + kTmemO + tt * D;
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              umma_ts_elect(obuf, pbuf + kk * 8, vd + kk * (16 * 128 / 16), kIdescPV,
-                            (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int hb = 0; hb < D / 64; ++hb)  // O columns of dims 64 hb.. from V block hb
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                umma_ts_elect(obuf + hb * 64, pbuf + kk * 8,
+                              vd + hb * kBlockDesc + kk * (16 * 128 / 16), kIdescPV,
+                              (jj > 0 || kk > 0) ? 1u : 0u);
             umma_commit_elect(&bars->o_done[tt]);
             umma_commit_elect(&bars->pv_done[b]);
             // PV(K) completing implies QK of every item of this KV tile
@@ -517,12 +537,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
       mbar_wait_warp(&bars->drain[role], 0, abort, &g_prefill_error, true);
     }
   } else {
-    if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<2>::kRegsSoftmax));
+    if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<2, 64>::kRegsSoftmax));
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;          // which query tile (head h0 + t)
     const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t o_addr = lane_addr + kTmemO + t * kHeadDim;
+    const uint32_t o_addr = lane_addr + kTmemO + t * D;
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     int K = 0;        // items of earlier tiles
@@ -558,11 +578,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         }
       }
       const float inv = pd > 0.f ? 1.f / pd : 0.f;
-      uint32_t ov[2][32];
+      constexpr int kQ = D / 32;  // 32-column TMEM loads of O
+      uint32_t ov[kQ][32];
       if (have_o) {
         tc_fence_after();
-        tmem_ld32(o_addr, ov[0]);
-        tmem_ld32(o_addr + 32, ov[1]);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) tmem_ld32(o_addr + 32 * q, ov[q]);
         tmem_wait_ld();
         // O_t may now be overwritten by the next tile's first P V (only tiles
         // with keys wrote O_t, and only they signal)
@@ -570,14 +591,16 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         mbar_arrive(&bars->o_free[t]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[0][i] = ov[1][i] = 0u;
+        for (int q = 0; q < kQ; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[q][i] = 0u;
       }
       const float lse = pd > 0.f ? (pm + fast_log2(pd)) * kLn2 : -INFINITY;
       if (r < prows && p.num_splits > 1) {
         const size_t at = static_cast<size_t>(psplit) * p.total_q * p.hq + prow_h;
-        float4 *dst = reinterpret_cast<float4 *>(p.part_o + at * kHeadDim);
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + at * D);
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < kQ; ++q)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float *o = reinterpret_cast<const float *>(&ov[q][4 * i]);
@@ -585,9 +608,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           }
         p.part_lse[at] = lse;
       } else if (r < prows) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + prow_h * kHeadDim);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + prow_h * D);
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < kQ; ++q)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float *o = reinterpret_cast<const float *>(&ov[q][8 * i]);
@@ -688,7 +711,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
           if (__any_sync(0xffffffffu, rescale)) {
             tc_fence_after();
 #pragma unroll
-            for (int q = 0; q < kHeadDim / 32; ++q) {
+            for (int q = 0; q < D / 32; ++q) {
               uint32_t ov[32];
               tmem_ld32(o_addr + q * 32, ov);
               tmem_wait_ld();
@@ -752,18 +775,18 @@ namespace {
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace pieces. Every piece starts on a 256-byte boundary.
-size_t vcopy_bytes(int64_t total_k, int hkv) {  // fp16 copy of V
-  return round256(static_cast<size_t>(total_k) * hkv * kHeadDim * 2);
+// Workspace pieces (head dimension d). Every piece starts on a 256-byte boundary.
+size_t vcopy_bytes(int64_t total_k, int hkv, int d) {  // fp16 copy of V
+  return round256(static_cast<size_t>(total_k) * hkv * d * 2);
 }
 size_t schedule_bytes(int batch, int64_t total_q) {  // tile counter + work list
   return 256 + round256(static_cast<size_t>(total_q / kBM + batch) * 4);
 }
-size_t partial_o_bytes(int64_t total_q, int hq, int splits) {
-  return splits > 1 ? round256(static_cast<size_t>(splits) * total_q * hq * kHeadDim * 4) : 0;
+size_t partial_o_bytes(int64_t total_q, int hq, int splits, int d) {
+  return splits > 1 ? round256(static_cast<size_t>(splits) * total_q * hq * d * 4) : 0;
 }
-size_t partials_bytes(int64_t total_q, int hq, int splits) {  // o, then lse
-  return splits > 1 ? partial_o_bytes(total_q, hq, splits) +
+size_t partials_bytes(int64_t total_q, int hq, int splits, int d) {  // o, then lse
+  return splits > 1 ? partial_o_bytes(total_q, hq, splits, d) +
                           round256(static_cast<size_t>(splits) * total_q * hq * 4)
                     : 0;
 }
@@ -772,16 +795,16 @@ size_t partials_bytes(int64_t total_q, int hq, int splits) {  // o, then lse
 int64_t paged_stage_rows(int batch, int max_seqlen_k) {
   return static_cast<int64_t>(batch) * max_seqlen_k + kBM;
 }
-size_t paged_stage_bytes(int batch, int max_seqlen_k, int hkv) {
-  return round256(static_cast<size_t>(paged_stage_rows(batch, max_seqlen_k)) * hkv * kHeadDim * 2);
+size_t paged_stage_bytes(int batch, int max_seqlen_k, int hkv, int d) {
+  return round256(static_cast<size_t>(paged_stage_rows(batch, max_seqlen_k)) * hkv * d * 2);
 }
 
 }  // namespace
 
 int prefill_plan_splits(int requested, int batch, int64_t total_q, int max_seqlen_q,
-                        int max_seqlen_k, int hq, int hkv, int window) {
+                        int max_seqlen_k, int hq, int hkv, int window, int head_dim) {
   if (requested > 0) return requested < kMaxPrefillSplits ? requested : kMaxPrefillSplits;
-  const int nt = (hq / hkv) % 2 == 0 ? 2 : 1;
+  const int nt = head_dim == 64 && (hq / hkv) % 2 == 0 ? 2 : 1;
   const int64_t qtiles = (max_seqlen_q + kBM - 1) / kBM;
   const int64_t pairs = std::min<int64_t>(total_q / kBM + batch, batch * qtiles);
   const int64_t items = pairs * (hq / nt);
@@ -809,18 +832,18 @@ int prefill_plan_splits(int requested, int batch, int64_t total_q, int max_seqle
 }
 
 size_t prefill_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv,
-                               int splits) {
-  return vcopy_bytes(total_k, hkv) + schedule_bytes(batch, total_q) +
-         partials_bytes(total_q, hq, splits);
+                               int splits, int head_dim) {
+  return vcopy_bytes(total_k, hkv, head_dim) + schedule_bytes(batch, total_q) +
+         partials_bytes(total_q, hq, splits, head_dim);
 }
 
 // Paged prefill workspace: K staging, V staging, the sequence offsets, the
 // schedule, the split partials.
 size_t prefill_paged_workspace_bytes(int batch, int64_t total_q, int max_seqlen_k, int hq,
-                                     int hkv, int splits) {
-  return 2 * paged_stage_bytes(batch, max_seqlen_k, hkv) +
+                                     int hkv, int splits, int head_dim) {
+  return 2 * paged_stage_bytes(batch, max_seqlen_k, hkv, head_dim) +
          round256(static_cast<size_t>(batch + 1) * 4) + schedule_bytes(batch, total_q) +
-         partials_bytes(total_q, hq, splits);
+         partials_bytes(total_q, hq, splits, head_dim);
 }
 
 namespace {
@@ -855,17 +878,17 @@ __global__ void __launch_bounds__(1024) seqlen_offsets_kernel(const int32_t *seq
 __global__ void __launch_bounds__(256) gather_paged_kernel(
     const __nv_bfloat16 *__restrict__ kc, const __nv_bfloat16 *__restrict__ vc,
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ cu_k, int batch,
-    int max_pages, int page_size, int num_pages, int hkv, int64_t cap_rows,
+    int max_pages, int page_size, int num_pages, int hkv, int d, int64_t cap_rows,
     __nv_bfloat16 *__restrict__ k_out,
     __half *__restrict__ v_out) {
   const int lane = threadIdx.x & 31;
   const int64_t total = cu_k[batch];
   const int64_t end = total + kBM < cap_rows ? total + kBM : cap_rows;
-  const int chunks = hkv * (kHeadDim / 8);  // 16-byte chunks per token row of all heads
+  const int chunks = hkv * (d / 8);  // 16-byte chunks per token row of all heads
   for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; r < end;
        r += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
-    uint4 *kd = reinterpret_cast<uint4 *>(k_out + r * hkv * kHeadDim);
-    uint4 *vd = reinterpret_cast<uint4 *>(v_out + r * hkv * kHeadDim);
+    uint4 *kd = reinterpret_cast<uint4 *>(k_out + r * hkv * d);
+    uint4 *vd = reinterpret_cast<uint4 *>(v_out + r * hkv * d);
     int page = -1, slot = 0;
     if (r < total) {
       int lo = 0, hi = batch;  // sequence b with cu_k[b] <= r < cu_k[b + 1]
@@ -889,8 +912,8 @@ __global__ void __launch_bounds__(256) gather_paged_kernel(
       continue;
     }
     for (int c = lane; c < chunks; c += 32) {
-      const int h = c / (kHeadDim / 8), e = c % (kHeadDim / 8);
-      const size_t src = ((static_cast<size_t>(page) * hkv + h) * page_size + slot) * kHeadDim;
+      const int h = c / (d / 8), e = c % (d / 8);
+      const size_t src = ((static_cast<size_t>(page) * hkv + h) * page_size + slot) * d;
       kd[c] = reinterpret_cast<const uint4 *>(kc + src)[e];
       vd[c] = bf16x8_to_f16x8(reinterpret_cast<const uint4 *>(vc + src)[e]);
     }
@@ -911,9 +934,10 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   // With no keys at all nothing reads K or V; the maps then point at q.
   const void *kbase = k_rows > 0 ? k : a.q;
   const void *vbase = k_rows > 0 ? v16 : a.q;
-  if (fn == nullptr || !encode_rows_heads(fn, &tq, a.q, a.total_q, a.hq, bf16) ||
-      !encode_rows_heads(fn, &tk, kbase, k_rows, a.hkv, bf16) ||
-      !encode_rows_heads(fn, &tv, vbase, k_rows, a.hkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) {
+  const int d = a.head_dim;
+  if (fn == nullptr || !encode_rows_heads(fn, &tq, a.q, a.total_q, a.hq, bf16, d) ||
+      !encode_rows_heads(fn, &tk, kbase, k_rows, a.hkv, bf16, d) ||
+      !encode_rows_heads(fn, &tv, vbase, k_rows, a.hkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d)) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
@@ -940,9 +964,11 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   p.total_q = static_cast<int>(a.total_q);
   uint8_t *part = sched + schedule_bytes(a.batch, a.total_q);
   p.part_o = splits > 1 ? reinterpret_cast<float *>(part) : nullptr;
-  p.part_lse = splits > 1 ? reinterpret_cast<float *>(part + partial_o_bytes(a.total_q, a.hq, splits))
+  p.part_lse = splits > 1 ? reinterpret_cast<float *>(
+                                part + partial_o_bytes(a.total_q, a.hq, splits, d))
                           : nullptr;
-  const int nt = p.group % 2 == 0 ? 2 : 1;
+  // head_dim 64: two heads per item when the group size is even; 128: one
+  const int nt = d == 64 && p.group % 2 == 0 ? 2 : 1;
   build_worklist_kernel<<<1, 1024, 0, stream>>>(a.cu_q, a.batch, max_qtiles, pairs, num_pairs,
                                                 p.work_counter);
   cudaError_t e = cudaGetLastError();
@@ -953,31 +979,39 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   const int num_sms = sm_count();
   const unsigned grid = static_cast<unsigned>(max_work < num_sms ? max_work : num_sms);
   if (nt == 2) {
-    e = cudaFuncSetAttribute(prefill_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<2>::kSmemBytes);
+    using C2 = Cfg<2, 64>;
+    e = cudaFuncSetAttribute(prefill_kernel<2, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C2::kSmemBytes);
     if (e != cudaSuccess) return e;
     // setmaxnreg.inc waits until the registers exist: the block must be launched
     // with at least the split's total, or the softmax warps would never start.
     static int launch_regs = -1;
     if (launch_regs < 0) {
       cudaFuncAttributes attr;
-      e = cudaFuncGetAttributes(&attr, prefill_kernel<2>);
+      e = cudaFuncGetAttributes(&attr, prefill_kernel<2, 64>);
       if (e != cudaSuccess) return e;
       launch_regs = attr.numRegs;
     }
-    if (launch_regs * Cfg<2>::kThreads < Cfg<2>::kRegsOther * 128 + Cfg<2>::kRegsSoftmax * 256)
+    if (launch_regs * C2::kThreads < C2::kRegsOther * 128 + C2::kRegsSoftmax * 256)
       return cudaErrorNotSupported;
-    prefill_kernel<2><<<grid, Cfg<2>::kThreads, Cfg<2>::kSmemBytes, stream>>>(tq, tk, tv, p);
-  } else {
-    e = cudaFuncSetAttribute(prefill_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<1>::kSmemBytes);
+    prefill_kernel<2, 64><<<grid, C2::kThreads, C2::kSmemBytes, stream>>>(tq, tk, tv, p);
+  } else if (d == 64) {
+    using C1 = Cfg<1, 64>;
+    e = cudaFuncSetAttribute(prefill_kernel<1, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C1::kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_kernel<1><<<grid, Cfg<1>::kThreads, Cfg<1>::kSmemBytes, stream>>>(tq, tk, tv, p);
+    prefill_kernel<1, 64><<<grid, C1::kThreads, C1::kSmemBytes, stream>>>(tq, tk, tv, p);
+  } else {
+    using C1 = Cfg<1, 128>;
+    e = cudaFuncSetAttribute(prefill_kernel<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C1::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    prefill_kernel<1, 128><<<grid, C1::kThreads, C1::kSmemBytes, stream>>>(tq, tk, tv, p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
   // split 0 carried the sink: the merge adds no sink of its own
-  return launch_merge(p.part_o, p.part_lse, splits, a.total_q, a.hq, nullptr, a.out, a.lse,
+  return launch_merge(p.part_o, p.part_lse, splits, a.total_q, a.hq, d, nullptr, a.out, a.lse,
                       stream);
 }
 
@@ -987,15 +1021,15 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
   *encode_failed = false;
   const int max_qtiles = (a.max_seqlen_q + kBM - 1) / kBM;
   if (a.batch == 0 || a.total_q == 0 || max_qtiles == 0) return cudaSuccess;
-  const int64_t n8 = a.total_k * a.hkv * kHeadDim / 8;
+  const int64_t n8 = a.total_k * a.hkv * a.head_dim / 8;
   if (n8 > 0) {
     const int64_t blocks = (n8 + 255) / 256;
     convert_v_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
         static_cast<const uint4 *>(a.v), static_cast<uint4 *>(a.v_f16), n8);
   }
   uint8_t *ws = static_cast<uint8_t *>(a.v_f16);
-  return launch_core(a, a.k, a.v_f16, a.total_k, a.cu_k, ws + vcopy_bytes(a.total_k, a.hkv),
-                     stream, encode_failed);
+  return launch_core(a, a.k, a.v_f16, a.total_k, a.cu_k,
+                     ws + vcopy_bytes(a.total_k, a.hkv, a.head_dim), stream, encode_failed);
 }
 
 cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,
@@ -1005,7 +1039,7 @@ cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t strea
   const int max_qtiles = (c.max_seqlen_q + kBM - 1) / kBM;
   if (c.batch == 0 || c.total_q == 0 || max_qtiles == 0) return cudaSuccess;
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-  const size_t stage = paged_stage_bytes(c.batch, c.max_seqlen_k, c.hkv);
+  const size_t stage = paged_stage_bytes(c.batch, c.max_seqlen_k, c.hkv, c.head_dim);
   __nv_bfloat16 *k_st = reinterpret_cast<__nv_bfloat16 *>(ws);
   __half *v_st = reinterpret_cast<__half *>(ws + stage);
   int32_t *cu_k = reinterpret_cast<int32_t *>(ws + 2 * stage);
@@ -1015,8 +1049,8 @@ cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t strea
   const int64_t warps = cap < sm_count() * 64 ? cap : sm_count() * 64;
   gather_paged_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(a.k_cache), static_cast<const __nv_bfloat16 *>(a.v_cache),
-      a.block_table, cu_k, c.batch, a.max_pages, a.page_size, a.num_pages, c.hkv, cap, k_st,
-      v_st);
+      a.block_table, cu_k, c.batch, a.max_pages, a.page_size, a.num_pages, c.hkv, c.head_dim, cap,
+      k_st, v_st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_core(c, k_st, v_st, cap, cu_k, sched, stream, encode_failed);

@@ -33,15 +33,15 @@ inline EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [rows, heads, 64] 16-bit tensor; a box is 128 rows of one head, 128-byte
-// swizzle. Rows past the end read as zeros.
+// [rows, heads, d] 16-bit tensor (d a multiple of 64); a box is 64 elements
+// of 128 rows of one head, 128-byte swizzle. Rows past the end read as zeros.
 inline bool encode_rows_heads(EncodeTiledFn fn, CUtensorMap *map, const void *base, int64_t rows,
-                              int heads, CUtensorMapDataType dtype) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(heads),
+                              int heads, CUtensorMapDataType dtype, int d = kHeadDim) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
-                                 static_cast<cuuint64_t>(heads) * kHeadDim * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1, 128};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
+                                 static_cast<cuuint64_t>(heads) * d * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

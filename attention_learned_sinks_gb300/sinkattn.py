@@ -194,7 +194,7 @@ def sinkattn_prefill_paged(q, cu_seqlens_q, k_cache, v_cache, block_table, seqle
                            scale=None, num_splits=0, out=None, lse=None, return_lse=True,
                            workspace=None, stream=None):
     """Sink-attention prefill of packed queries against a paged KV cache
-    [num_pages, hkv, page_size, 64] addressed by block_table / seqlens_k.
+    [num_pages, hkv, page_size, head_dim] addressed by block_table / seqlens_k.
     Returns (out, lse)."""
     lib = load()
     _req(q, torch.bfloat16, "q")
@@ -373,7 +373,7 @@ def sinkattn_decode_noalloc(q, k_cache, v_cache, *, kv_indptr=None, block_table=
 
 def sinkattn_merge(partial_o, partial_lse, *, sinks=None, out=None, lse=None, return_lse=True,
                    stream=None):
-    """Merge split-KV partials [S, rows, hq, 64] / [S, rows, hq] by log-sum-exp."""
+    """Merge split-KV partials [S, rows, hq, D] / [S, rows, hq] by log-sum-exp (D 64 or 128)."""
     lib = load()
     _req(partial_o, torch.float32, "partial_o")
     _req(partial_lse, torch.float32, "partial_lse")

@@ -92,7 +92,7 @@ def prefill_pairs(case):
 
 
 def prefill_flops(case):
-    return 4 * 64 * prefill_pairs(case) * case.hq
+    return 4 * case.head_dim * prefill_pairs(case) * case.hq
 
 
 # ---------------------------------------------------------------- clocks ---
@@ -452,6 +452,7 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
     for name, mk, ns in (
             ("varlen_prefill", lambda: S.varlen_prefill(device="cuda"), 0),
             ("varlen_prefill_w128", lambda: S.varlen_prefill(window=128, device="cuda"), 0),
+            ("varlen_prefill_d128", lambda: S.varlen_prefill_d128(device="cuda"), 0),
             ("chunked_prefill", lambda: S.chunked_prefill(device="cuda"), 0),
             ("long_context_prefill", lambda: S.long_context_prefill(device="cuda"), 0),
             ("long_context_prefill_unsplit", lambda: S.long_context_prefill(device="cuda"), 1)):
@@ -464,8 +465,8 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         lse = torch.empty((c.q.shape[0], c.hq), dtype=torch.float32, device=dev)
         ws = torch.empty(sa.sinkattn_prefill_workspace_size(c.batch, c.q.shape[0], c.k.shape[0],
                                                             c.max_seqlen_q, c.max_seqlen_k, c.hq,
-                                                            c.hkv, window=c.window,
-                                                            num_splits=ns),
+                                                            c.hkv, head_dim=c.head_dim,
+                                                            window=c.window, num_splits=ns),
                          dtype=torch.uint8, device=dev)
 
         def call():
@@ -497,7 +498,8 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         lse = torch.empty((c.q.shape[0], c.hq), dtype=torch.float32, device=dev)
         ws = torch.empty(sa.sinkattn_prefill_paged_workspace_size(c.batch, c.q.shape[0],
                                                                   c.max_seqlen_q, c.max_seqlen_k,
-                                                                  c.hq, c.hkv, window=c.window),
+                                                                  c.hq, c.hkv, head_dim=c.head_dim,
+                                                                  window=c.window),
                          dtype=torch.uint8, device=dev)
 
         def call():
@@ -508,7 +510,7 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
             call()
         t = time_calls(call, 10, stream, flush)
         fl = prefill_flops(c)
-        kv = sum(c.seqlens_k) * c.hkv * 64 * 2 * 2
+        kv = sum(c.seqlens_k) * c.hkv * c.head_dim * 2 * 2
         res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3,
                      "tokens_per_s": sum(c.seqlens_q) / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,

@@ -35,8 +35,9 @@
  *    captured in a CUDA graph.
  *  - Host-side argument errors return before anything is enqueued. A failed
  *    launch returns SINKATTN_ERR_CUDA. No C++ exception crosses the ABI.
- *  - head_dim must be 64 (SINKATTN_ERR_UNSUPPORTED otherwise; the decode
- *    calls also take 128) and hq must be a multiple of hkv.
+ *  - head_dim must be 64 or 128 (SINKATTN_ERR_UNSUPPORTED otherwise; the
+ *    backward takes 64 only) and hq must be a multiple of hkv. Below, D
+ *    stands for head_dim.
  *  - Outputs: `out` is bf16 (round to nearest even) with the query layout;
  *    `lse` is float32, natural log, sink included; `lse` may be NULL.
  *  - Inputs must be finite. Rows of K/V outside a sequence may be read but get
@@ -80,8 +81,8 @@ const char *sinkattn_last_cuda_error(void);
  * Prefill over packed variable-length sequences (page "Fast embeddings on
  * GPUs", section "ROSE": attention over ragged inputs without padding).
  *
- *   q        bf16 [total_q, hq, 64]   sequence b owns rows cu_seqlens_q[b]..[b+1]
- *   k, v     bf16 [total_k, hkv, 64]  sequence b owns rows cu_seqlens_k[b]..[b+1]
+ *   q        bf16 [total_q, hq, D]    sequence b owns rows cu_seqlens_q[b]..[b+1]
+ *   k, v     bf16 [total_k, hkv, D]   sequence b owns rows cu_seqlens_k[b]..[b+1]
  *   cu_seqlens_q, cu_seqlens_k  int32 [batch+1], device, non-decreasing,
  *            starting at 0; the last entries equal total_q and total_k.
  *   total_q, total_k            host copies of those last entries (bounds for
@@ -99,14 +100,14 @@ const char *sinkattn_last_cuda_error(void);
  *            the GPU's SMs and long key ranges (e.g. a few hundred new tokens
  *            over a long context); the choice depends on the current device's
  *            SM count.
- *   out      bf16 [total_q, hq, 64];   lse  float32 [total_q, hq] or NULL.
+ *   out      bf16 [total_q, hq, D];    lse  float32 [total_q, hq] or NULL.
  *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
  *            sinkattn_prefill_workspace_size() bytes for the same arguments;
  *            contents need not be initialised. It receives an fp16 copy of v
  *            for the P.V product (values of magnitude above 65504 are clamped
  *            to +-65504 there), the list of query tiles that the persistent
  *            kernel works through, longest first, and with splits the fp32
- *            partials (splits * total_q * hq * 260 bytes).
+ *            partials (splits * total_q * hq * (4 D + 4) bytes).
  * A sequence with Lq_b > Lk_b is allowed: its first Lq_b - Lk_b queries see no
  * key under a causal mask.
  */
@@ -129,10 +130,10 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
  * padding). Same operation, mask and outputs as sinkattn_prefill; only the
  * key/value addressing differs.
  *
- *   q        bf16 [total_q, hq, 64]   sequence b owns rows cu_seqlens_q[b]..[b+1]
+ *   q        bf16 [total_q, hq, D]    sequence b owns rows cu_seqlens_q[b]..[b+1]
  *   cu_seqlens_q  int32 [batch+1], device, non-decreasing, starting at 0,
  *            last entry total_q.
- *   k_cache, v_cache  bf16 [num_pages, hkv, page_size, 64]. Key j of sequence
+ *   k_cache, v_cache  bf16 [num_pages, hkv, page_size, D]. Key j of sequence
  *            b is slot j % page_size of page block_table[b][j / page_size].
  *   block_table   int32 [batch, max_pages_per_seq], device.
  *   seqlens_k     int32 [batch], device: Lk_b, which counts the cached keys and
@@ -144,7 +145,7 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
  *   num_splits    as for sinkattn_prefill.
  *   workspace/workspace_bytes   device scratch, 256-byte aligned, at least
  *            sinkattn_prefill_paged_workspace_size() bytes for the same
- *            arguments (about batch * max_seqlen_k * hkv * 256 bytes, plus
+ *            arguments (about batch * max_seqlen_k * hkv * 4 D bytes, plus
  *            the split partials); contents need not be initialised. The call
  *            first gathers every sequence's pages into contiguous rows there
  *            (K as bf16, V as fp16 for the P.V product, clamped to +-65504),
@@ -192,8 +193,7 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
  *   num_splits     0 = automatic; n > 0 = split the longest sequence into
  *            about n blocks (shorter ones get proportionally fewer).
  *   hq / hkv must be at most 8 (one KV head and all its query heads per block).
- *   head_dim 64 or 128 (decode only; the other calls take 64). q, out and
- *            every K/V row then have head_dim elements.
+ *   head_dim 64 or 128. q, out and every K/V row have head_dim elements.
  *   out      bf16 [batch, hq, 64];  lse float32 [batch, hq] or NULL.
  *   workspace      device scratch of at least sinkattn_decode_workspace_size()
  *            bytes for the same (batch, max_seqlen_k, hq, hkv, head_dim,
@@ -275,12 +275,12 @@ sinkattn_status_t sinkattn_decode_noalloc(const void *q, const void *k_cache,
  * Sink Attention": when the KV sequence is split into blocks, the sink belongs
  * to one block only; here it may enter as its own block, exactly once).
  *
- *   partial_o    float32 [num_splits, rows, hq, 64]: each block's normalised output
+ *   partial_o    float32 [num_splits, rows, hq, D]: each block's normalised output
  *   partial_lse  float32 [num_splits, rows, hq]: each block's natural-log lse;
  *                -inf marks an empty block (its partial_o is ignored).
  *   sinks        float32 [hq] or NULL; when given, the sink is one more block
  *                with lse = sinks[h] and a zero output.
- *   out          bf16 [rows, hq, 64];  lse float32 [rows, hq] or NULL.
+ *   out          bf16 [rows, hq, D];   lse float32 [rows, hq] or NULL.
  * With M = max_k lse_k: out = sum_k e^{lse_k - M} o_k / sum_k e^{lse_k - M},
  * lse = M + ln sum_k e^{lse_k - M}. All blocks empty: out = 0, lse = -inf.
  */

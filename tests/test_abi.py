@@ -65,7 +65,8 @@ def decode(lib, **kw):
 
 
 def test_prefill_rejects_bad_arguments(lib):
-    assert prefill(lib, d=128) == B.SINKATTN_ERR_UNSUPPORTED
+    assert prefill(lib, d=96) == B.SINKATTN_ERR_UNSUPPORTED
+    assert prefill(lib, d=256) == B.SINKATTN_ERR_UNSUPPORTED
     assert prefill(lib, hq=6, hkv=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill(lib, hkv=0) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill(lib, mask=B.Mask(1, 0, 0.0)) == B.SINKATTN_ERR_INVALID_ARGUMENT
@@ -84,6 +85,11 @@ def test_prefill_rejects_bad_arguments(lib):
     # nothing to do: returns before any launch
     assert prefill(lib, batch=0) == B.SINKATTN_OK
     assert prefill(lib, tq=0) == B.SINKATTN_OK
+    # head_dim 128 is accepted and needs twice the V copy
+    need128 = lib.sinkattn_prefill_workspace_size(2, 10, 10, 5, 5, 8, 2, 128, 0, 0)
+    assert need128 >= 10 * 2 * 128 * 2 and need128 > need
+    assert prefill(lib, d=128, ws=FAKE, wsb=need) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert prefill(lib, d=128, batch=0) == B.SINKATTN_OK
 
 
 def prefill_paged(lib, **kw):
@@ -99,7 +105,7 @@ def prefill_paged(lib, **kw):
 
 
 def test_prefill_paged_rejects_bad_arguments(lib):
-    assert prefill_paged(lib, d=128) == B.SINKATTN_ERR_UNSUPPORTED
+    assert prefill_paged(lib, d=80) == B.SINKATTN_ERR_UNSUPPORTED
     assert prefill_paged(lib, hq=6, hkv=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert prefill_paged(lib, page=0) == B.SINKATTN_ERR_INVALID_ARGUMENT
     # the block table must be able to address max_seqlen_k keys
@@ -121,6 +127,9 @@ def test_prefill_paged_rejects_bad_arguments(lib):
     assert prefill_paged(lib, tq=0) == B.SINKATTN_OK
     assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 5, 64, 8, 2, 96, 0, 0) == 0
     assert lib.sinkattn_prefill_paged_workspace_size(2, 10, 5, 128, 8, 2, 64, 0, 0) > need
+    need128 = lib.sinkattn_prefill_paged_workspace_size(2, 10, 5, 64, 8, 2, 128, 0, 0)
+    assert need128 >= 2 * (2 * 64 + 128) * 2 * 128 * 2
+    assert prefill_paged(lib, d=128, ws=FAKE, wsb=need) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
 
 
 def backward(lib, **kw):
@@ -176,6 +185,7 @@ def test_decode_rejects_bad_arguments(lib):
 def test_merge_rejects_bad_arguments(lib):
     f = lib.sinkattn_merge
     assert f(FAKE, FAKE, 2, 4, 8, 32, None, FAKE, None, None) == B.SINKATTN_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, 2, 0, 8, 128, None, FAKE, None, None) == B.SINKATTN_OK
     assert f(None, FAKE, 2, 4, 8, 64, None, FAKE, None, None) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert f(FAKE, FAKE, -1, 4, 8, 64, None, FAKE, None, None) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert f(FAKE, FAKE, 2, 0, 8, 64, None, FAKE, None, None) == B.SINKATTN_OK
@@ -190,7 +200,8 @@ def test_workspace_sizes_follow_the_split_plan(lib):
     assert lib.sinkattn_decode_workspace_size(0, 10, 8, 2, 64, 0, 0) == 0
     pws = lambda *a: lib.sinkattn_prefill_workspace_size(*a)
     assert pws(3, 1000, 1000, 500, 500, 64, 8, 64, 0, 1) >= 1000 * 8 * 64 * 2 + 256
-    assert pws(3, 1000, 1000, 500, 500, 64, 8, 128, 0, 1) == 0
+    assert pws(3, 1000, 1000, 500, 500, 64, 8, 96, 0, 1) == 0
+    assert pws(3, 1000, 1000, 500, 500, 64, 8, 128, 0, 1) >= 1000 * 8 * 128 * 2 + 256
     assert pws(3, 1000, 1000, 500, 500, 64, 8, 64, -1, 0) == 0
     # explicit splits add fp32 partials: splits * total_q * hq * (64 + 1) * 4 bytes
     one = pws(3, 1000, 1000, 500, 500, 64, 8, 64, 0, 1)

@@ -13,10 +13,11 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("nsplit", [1, 2, 5, 16])
 @pytest.mark.parametrize("with_sinks", [True, False])
-def test_merge_random_partials(oracle_lib, nsplit, with_sinks):
-    g = torch.Generator().manual_seed(80 + nsplit)
+@pytest.mark.parametrize("d", [64, 128])
+def test_merge_random_partials(oracle_lib, nsplit, with_sinks, d):
+    g = torch.Generator().manual_seed(80 + nsplit + d)
     rows, hq = 37, 12
-    po = torch.randn((nsplit, rows, hq, 64), generator=g)
+    po = torch.randn((nsplit, rows, hq, d), generator=g)
     pl = torch.randn((nsplit, rows, hq), generator=g) * 3
     # some empty blocks, and one row empty everywhere
     pl[torch.rand((nsplit, rows, hq), generator=g) < 0.2] = -float("inf")
@@ -24,7 +25,7 @@ def test_merge_random_partials(oracle_lib, nsplit, with_sinks):
     sinks = torch.randn(hq, generator=g) if with_sinks else None
     out, lse = sa.sinkattn_merge(po.cuda(), pl.cuda(), sinks=None if sinks is None else sinks.cuda())
     ro, rl = oracle_lib.merge(po.double().numpy(), pl.double().numpy(), sinks=sinks)
-    check_close(out, lse, ro, rl, "merge n=%d" % nsplit)
+    check_close(out, lse, ro, rl, "merge n=%d d=%d" % (nsplit, d))
 
 
 def test_merge_of_oracle_split_blocks_equals_whole(oracle_lib):

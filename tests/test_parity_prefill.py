@@ -20,7 +20,7 @@ def run_prefill(c, device_tensors=False, num_splits=0):
 
 def oracle_prefill(oracle, c):
     return oracle.attention(c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k, hq=c.hq, hkv=c.hkv,
-                            head_dim=64, sinks=c.sinks, causal=c.causal, window=c.window,
+                            head_dim=c.head_dim, sinks=c.sinks, causal=c.causal, window=c.window,
                             scale=c.scale)
 
 
@@ -148,7 +148,7 @@ def _sample_rows(c, per_seq, seed):
 
 def _check_rows(oracle, c, out, lse, rows, what):
     ro, rl = oracle.attention_rows(rows, c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k, hq=c.hq,
-                                   hkv=c.hkv, head_dim=64, sinks=c.sinks, causal=c.causal,
+                                   hkv=c.hkv, head_dim=c.head_dim, sinks=c.sinks, causal=c.causal,
                                    window=c.window, scale=c.scale)
     cu = c.cu_seqlens_q.tolist()
     pr = torch.tensor([cu[b] + i for b, _, i in rows], device=out.device)
@@ -195,3 +195,59 @@ def test_prefill_chunked_full_config(oracle_lib):
     out, lse = run_prefill(c)
     torch.cuda.synchronize()
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 40, 73), "chunked_prefill")
+
+
+# head_dim 128: one head per item, two 64-dim blocks per tile, a two-stage
+# K/V ring, O in 128 TMEM columns
+D128_MASKS = [(True, 0), (False, 0), (True, 1), (True, 128), (False, 50)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
+@pytest.mark.parametrize("causal,window", D128_MASKS)
+def test_prefill_head_dim_128_shapes(oracle_lib, shape, causal, window):
+    lq, lk = shape
+    c = S.make_prefill("d128", lq, lk, 8, 2, seed=131 + sum(lq), causal=causal, window=window,
+                       sink_std=1.5, head_dim=128)
+    out, lse = run_prefill(c)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "d128 %s causal=%s w=%d" % (shape, causal, window))
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (12, 3), (64, 8)])
+def test_prefill_head_dim_128_groups_and_no_sink(oracle_lib, hq, hkv):
+    for with_sinks in (True, False):
+        c = S.make_prefill("d128grp", [190, 260], [300, 260], hq, hkv, seed=133 + hq,
+                           with_sinks=with_sinks, head_dim=128)
+        out, lse = run_prefill(c)
+        ro, rl = oracle_prefill(oracle_lib, c)
+        check_close(out, lse, ro, rl, "d128 hq=%d hkv=%d sinks=%s" % (hq, hkv, with_sinks))
+
+
+def test_prefill_head_dim_128_keyless_and_large_sink(oracle_lib):
+    c = S.make_prefill("d128kl", [400] * 6 + [700] * 6, [100] * 6 + [900] * 6, 4, 1, seed=135,
+                       head_dim=128)
+    c.sinks = torch.tensor([30.0, -30.0, 0.0, 9.0])
+    out, lse = run_prefill(c)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "d128 keyless tiles, large sinks")
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=[str(i) for i in range(len(SPLIT_SHAPES))])
+@pytest.mark.parametrize("num_splits", [2, 7])
+def test_prefill_head_dim_128_splits(oracle_lib, shape, num_splits):
+    lq, lk = shape
+    c = S.make_prefill("d128split", lq, lk, 8, 2, seed=137 + sum(lk) + num_splits,
+                       sink_std=1.5, head_dim=128)
+    out, lse = run_prefill(c, num_splits=num_splits)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "d128 %s splits=%d" % (shape, num_splits))
+
+
+def test_prefill_head_dim_128_varlen_full_config(oracle_lib):
+    """varlen_prefill's lengths and heads at head_dim 128. Sampled rows against
+    the oracle."""
+    c = S.varlen_prefill_d128()
+    out, lse = run_prefill(c)
+    torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 16, 139), "varlen_prefill_d128")
+    assert sa.sinkattn_get_device_error() == 0

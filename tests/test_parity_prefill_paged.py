@@ -23,7 +23,7 @@ def run_paged(c, max_seqlen_k=None, block_table=None, seqlens_k=None):
 def oracle_paged(oracle, c):
     return oracle.attention(c.q, c.k_cache, c.v_cache, c.cu_seqlens_q,
                             block_table=c.block_table, seqlens_k=c.seqlens_k_t, hq=c.hq,
-                            hkv=c.hkv, head_dim=64, sinks=c.sinks, causal=c.causal,
+                            hkv=c.hkv, head_dim=c.head_dim, sinks=c.sinks, causal=c.causal,
                             window=c.window, scale=c.scale)
 
 
@@ -154,7 +154,7 @@ def _sample_rows(c, per_seq, seed):
 def _check_rows(oracle, c, out, lse, rows, what):
     ro, rl = oracle.attention_rows(rows, c.q, c.k_cache, c.v_cache, c.cu_seqlens_q,
                                    block_table=c.block_table, seqlens_k=c.seqlens_k_t, hq=c.hq,
-                                   hkv=c.hkv, head_dim=64, sinks=c.sinks, causal=c.causal,
+                                   hkv=c.hkv, head_dim=c.head_dim, sinks=c.sinks, causal=c.causal,
                                    window=c.window, scale=c.scale)
     cu = c.cu_seqlens_q.tolist()
     pr = torch.tensor([cu[b] + i for b, _, i in rows], device=out.device)
@@ -178,3 +178,26 @@ def test_paged_prefill_batch_full_config(oracle_lib):
     torch.cuda.synchronize()
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 12, 95), "paged_prefill_batch")
     assert sa.sinkattn_get_device_error() == 0
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
+@pytest.mark.parametrize("page_size", [16, 7])
+def test_prefill_paged_head_dim_128(oracle_lib, shape, page_size):
+    lq, lk = shape
+    c = S.make_prefill_paged("pd128", lq, lk, 8, 2, seed=141 + sum(lk) + page_size,
+                             page_size=page_size, spare_pages=3, sink_std=1.5, head_dim=128)
+    poison_unreferenced(c)
+    out, lse = run_paged(c)
+    ro, rl = oracle_paged(oracle_lib, c)
+    check_close(out, lse, ro, rl, "paged d128 %s page=%d" % (shape, page_size))
+
+
+def test_paged_equals_contiguous_bitwise_head_dim_128():
+    c = S.make_prefill_paged("peq128", [700, 1, 333], [3000, 1, 500], 16, 4, seed=143,
+                             page_size=16, spare_pages=5, head_dim=128)
+    k, v, cu_k = _contiguous_copy(c)
+    a = run_paged(c)
+    b = sa.sinkattn_prefill(c.q.cuda(), k.cuda(), v.cuda(), c.cu_seqlens_q.cuda(), cu_k.cuda(),
+                            c.max_seqlen_q, c.max_seqlen_k, sinks=c.sinks.cuda(), causal=True,
+                            scale=c.scale)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
