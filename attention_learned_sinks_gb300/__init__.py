@@ -18,6 +18,7 @@ from .sinkattn import (  # noqa: F401
     sinkattn_prefill_backward,
     sinkattn_prefill_backward_workspace_size,
     sinkattn_prefill_paged,
+    sinkattn_prefill_paged_fp8,
     sinkattn_prefill_paged_workspace_size,
     sinkattn_prefill_workspace_size,
 )

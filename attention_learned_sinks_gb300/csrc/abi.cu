@@ -129,15 +129,20 @@ size_t sinkattn_prefill_paged_workspace_size(int batch, int64_t total_q, int max
   return prefill_paged_workspace_bytes(batch, total_q, max_seqlen_k, hq, hkv, splits, head_dim);
 }
 
-sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q,
-                                         const void *k_cache, const void *v_cache,
-                                         const int32_t *block_table, const int32_t *seqlens_k,
-                                         int num_pages, int max_pages_per_seq, int page_size,
-                                         int batch, int64_t total_q, int max_seqlen_q,
-                                         int max_seqlen_k, int hq, int hkv, int head_dim,
-                                         const float *sinks, sinkattn_mask_t mask,
-                                         int num_splits, void *out, float *lse, void *workspace,
-                                         size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+sinkattn_status_t prefill_paged_impl(const void *q, const int32_t *cu_seqlens_q,
+                                     const void *k_cache, const void *v_cache, bool fp8,
+                                     const float *k_scale, const float *v_scale,
+                                     const int32_t *block_table, const int32_t *seqlens_k,
+                                     int num_pages, int max_pages_per_seq, int page_size,
+                                     int batch, int64_t total_q, int max_seqlen_q,
+                                     int max_seqlen_k, int hq, int hkv, int head_dim,
+                                     const float *sinks, sinkattn_mask_t mask, int num_splits,
+                                     void *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
   if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 ||
       hq % hkv != 0 || num_pages < 0 || max_pages_per_seq < 0 || page_size <= 0 ||
       num_splits < 0 || !mask_ok(mask))
@@ -151,7 +156,8 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(cu_seqlens_q, 4) || !aligned(block_table, 4) || !aligned(seqlens_k, 4) ||
-      (sinks && !aligned(sinks, 4)) || (lse && !aligned(lse, 4)))
+      (sinks && !aligned(sinks, 4)) || (lse && !aligned(lse, 4)) ||
+      (k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (batch > 65535 || hq > 65535 || total_q > INT32_MAX || (max_seqlen_q + 127) / 128 > 65535 ||
       static_cast<int64_t>(batch) * max_seqlen_k + 128 > INT32_MAX)
@@ -185,7 +191,10 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
   a.base.lse = lse;
   a.base.num_splits = splits;
   a.base.head_dim = head_dim;
+  a.base.k_scale = k_scale;
+  a.base.v_scale = v_scale;
   a.base.v_f16 = nullptr;
+  a.fp8 = fp8;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.block_table = block_table;
@@ -198,6 +207,38 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
   cudaError_t e = launch_prefill_paged(a, static_cast<cudaStream_t>(stream), &encode_failed);
   if (encode_failed) return SINKATTN_ERR_CUDA;
   return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q,
+                                         const void *k_cache, const void *v_cache,
+                                         const int32_t *block_table, const int32_t *seqlens_k,
+                                         int num_pages, int max_pages_per_seq, int page_size,
+                                         int batch, int64_t total_q, int max_seqlen_q,
+                                         int max_seqlen_k, int hq, int hkv, int head_dim,
+                                         const float *sinks, sinkattn_mask_t mask,
+                                         int num_splits, void *out, float *lse, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+  return prefill_paged_impl(q, cu_seqlens_q, k_cache, v_cache, false, nullptr, nullptr,
+                            block_table, seqlens_k, num_pages, max_pages_per_seq, page_size,
+                            batch, total_q, max_seqlen_q, max_seqlen_k, hq, hkv, head_dim, sinks,
+                            mask, num_splits, out, lse, workspace, workspace_bytes, stream);
+}
+
+sinkattn_status_t sinkattn_prefill_paged_fp8(
+    const void *q, const int32_t *cu_seqlens_q, const void *k_cache, const void *v_cache,
+    const float *k_scale, const float *v_scale, const int32_t *block_table,
+    const int32_t *seqlens_k, int num_pages, int max_pages_per_seq, int page_size, int batch,
+    int64_t total_q, int max_seqlen_q, int max_seqlen_k, int hq, int hkv, int head_dim,
+    const float *sinks, sinkattn_mask_t mask, int num_splits, void *out, float *lse,
+    void *workspace, size_t workspace_bytes, void *stream) {
+  return prefill_paged_impl(q, cu_seqlens_q, k_cache, v_cache, true, k_scale, v_scale,
+                            block_table, seqlens_k, num_pages, max_pages_per_seq, page_size,
+                            batch, total_q, max_seqlen_q, max_seqlen_k, hq, hkv, head_dim, sinks,
+                            mask, num_splits, out, lse, workspace, workspace_bytes, stream);
 }
 
 size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int hkv, int head_dim,

@@ -70,6 +70,8 @@ struct PrefillLaunch {
   float *lse;
   int num_splits;  // key-range splits per work item (>= 1), from prefill_plan_splits
   int head_dim = kHeadDim;  // 64 or 128
+  // per-KV-head scales of fp8 K/V values (NULL: 1); set by the fp8 paged call
+  const float *k_scale = nullptr, *v_scale = nullptr;
   // workspace (prefill_workspace_bytes): fp16 copy of v, tile counter, work
   // list, split partials
   void *v_f16;
@@ -92,7 +94,8 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
 // runs. base.k/v/cu_k/total_k/v_f16 are unused.
 struct PrefillPagedLaunch {
   PrefillLaunch base;
-  const void *k_cache, *v_cache;  // [num_pages, hkv, page_size, 64] bf16
+  const void *k_cache, *v_cache;  // [num_pages, hkv, page_size, D] bf16, or e4m3 with fp8
+  bool fp8 = false;
   const int32_t *block_table, *seqlens_k;
   int max_pages, page_size, num_pages;
   void *workspace;

@@ -85,7 +85,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTile;
   static constexpr int kOffBar = kOffV + kStages * kTile;
   static constexpr int kOffPend = kOffBar + 1024;  // 16 B per softmax thread: deferred epilogue
-  static constexpr int kSmemBytes = kOffPend + NT * 128 * 16 + 1024;  // + alignment slack
+  static constexpr int kOffPendVs = kOffPend + NT * 128 * 16;  // + its value scale (4 B)
+  static constexpr int kSmemBytes = kOffPendVs + NT * 128 * 4 + 1024;  // + alignment slack
 };
 
 static_assert(Cfg<2, 64>::kRegsOther * 128 + Cfg<2, 64>::kRegsSoftmax * 256 <=
@@ -113,6 +114,10 @@ struct Params {
   // out/lse, and only split 0 starts from the sink.
   int num_splits, total_q;
   float *part_o, *part_lse;
+  // Per-KV-head value scales of an fp8 cache (NULL: 1). Key j of KV head g
+  // stands for k_scale[g] * K_j: k_scale multiplies the softmax scale, and
+  // v_scale the normalised output (it is linear in V).
+  const float *k_scale, *v_scale;
 };
 
 // One unit of work: 128 query rows of sequence b for the NT heads h0...
@@ -543,8 +548,6 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t o_addr = lane_addr + kTmemO + t * D;
-    const float c = p.scale_log2;
-    const float2 c2 = make_float2(c, c);
     int K = 0;        // items of earlier tiles
     int o_waits = 0;  // o_done[t] phases consumed
     // The epilogue of a tile runs after the first P of the next tile has been
@@ -555,6 +558,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     // m, d, query row, rows | split | keys | head), not in registers that the
     // softmax loop would have to carry.
     float4 *pend_slot = reinterpret_cast<float4 *>(smem + C::kOffPend) + threadIdx.x;
+    float *pend_vs = reinterpret_cast<float *>(smem + C::kOffPendVs) + threadIdx.x;
     bool pend_on = false;
     bool ok = true;
     auto finish = [&]() {  // epilogue of the pending tile
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           return;
         }
       }
-      const float inv = pd > 0.f ? 1.f / pd : 0.f;
+      const float inv = pd > 0.f ? *pend_vs / pd : 0.f;
       constexpr int kQ = D / 32;  // 32-column TMEM loads of O
       uint32_t ov[kQ][32];
       if (have_o) {
@@ -633,6 +637,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const Tile ti = bars->tiles[slot];
       if (!ti.valid) break;
       const int h = ti.h0 + t;
+      const float c =
+          p.k_scale != nullptr ? p.scale_log2 * __ldg(p.k_scale + ti.kvh) : p.scale_log2;
+      const float2 c2 = make_float2(c, c);
       float m_run = t == 0 ? ti.sink_log2[0] : ti.sink_log2[1];
       float d_run = m_run != -INFINITY ? 1.f : 0.f;
       const int pos = ti.p_min + r;
@@ -739,6 +746,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           m_run, d_run, __int_as_float(ti.q0 + ti.qt * kBM + r),
           __uint_as_float(static_cast<unsigned>(ti.rows) | (static_cast<unsigned>(ti.split) << 8) |
                           (n > 0 ? 1u << 15 : 0u) | (static_cast<unsigned>(h) << 16)));
+      *pend_vs = p.v_scale != nullptr ? __ldg(p.v_scale + ti.kvh) : 1.f;
       mbar_arrive(&bars->tile_empty[slot]);
       K += NT * n;
     }
@@ -871,12 +879,37 @@ __global__ void __launch_bounds__(1024) seqlen_offsets_kernel(const int32_t *seq
   if (threadIdx.x == 0) cu_k[batch] = carry;
 }
 
+// e4m3 -> bf16 for 8 elements (exact: 3 mantissa bits, exponents well
+// inside bf16's range)
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 x) {
+  uint32_t h[4];
+  e4m3x4_to_f16x4(x.x, h[0], h[1]);
+  e4m3x4_to_f16x4(x.y, h[2], h[3]);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[i]));
+    o[i] = pack_bf16x2(f.x, f.y);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// e4m3 -> fp16 for 8 elements (exact)
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 x) {
+  uint4 r;
+  e4m3x4_to_f16x4(x.x, r.x, r.y);
+  e4m3x4_to_f16x4(x.y, r.z, r.w);
+  return r;
+}
+
 // Paged K/V -> contiguous staging, one warp per token (all KV heads): K as
-// bf16, V converted to fp16 (clamped to +-65504) for the P V product. Rows
-// [total, total + 128) are zeroed so that a tile running past the last
-// sequence reads zeros.
+// bf16, V converted to fp16 (clamped to +-65504) for the P V product. With
+// kFp8 the cache holds e4m3 codes, staged as their exact values (the scales
+// are applied by the attention kernel). Rows [total, total + 128) are zeroed
+// so that a tile running past the last sequence reads zeros.
+template <bool kFp8>
 __global__ void __launch_bounds__(256) gather_paged_kernel(
-    const __nv_bfloat16 *__restrict__ kc, const __nv_bfloat16 *__restrict__ vc,
+    const void *__restrict__ kc, const void *__restrict__ vc,
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ cu_k, int batch,
     int max_pages, int page_size, int num_pages, int hkv, int d, int64_t cap_rows,
     __nv_bfloat16 *__restrict__ k_out,
@@ -914,8 +947,16 @@ __global__ void __launch_bounds__(256) gather_paged_kernel(
     for (int c = lane; c < chunks; c += 32) {
       const int h = c / (d / 8), e = c % (d / 8);
       const size_t src = ((static_cast<size_t>(page) * hkv + h) * page_size + slot) * d;
-      kd[c] = reinterpret_cast<const uint4 *>(kc + src)[e];
-      vd[c] = bf16x8_to_f16x8(reinterpret_cast<const uint4 *>(vc + src)[e]);
+      if constexpr (kFp8) {
+        kd[c] = e4m3x8_to_bf16x8(reinterpret_cast<const uint2 *>(
+            static_cast<const uint8_t *>(kc) + src)[e]);
+        vd[c] = e4m3x8_to_f16x8(reinterpret_cast<const uint2 *>(
+            static_cast<const uint8_t *>(vc) + src)[e]);
+      } else {
+        kd[c] = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(kc) + src)[e];
+        vd[c] = bf16x8_to_f16x8(
+            reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(vc) + src)[e]);
+      }
     }
   }
 }
@@ -962,6 +1003,8 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   const int splits = a.num_splits > 1 ? a.num_splits : 1;
   p.num_splits = splits;
   p.total_q = static_cast<int>(a.total_q);
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   uint8_t *part = sched + schedule_bytes(a.batch, a.total_q);
   p.part_o = splits > 1 ? reinterpret_cast<float *>(part) : nullptr;
   p.part_lse = splits > 1 ? reinterpret_cast<float *>(
@@ -1047,10 +1090,15 @@ cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t strea
   seqlen_offsets_kernel<<<1, 1024, 0, stream>>>(a.seqlens_k, c.batch, c.max_seqlen_k, cu_k);
   const int64_t cap = paged_stage_rows(c.batch, c.max_seqlen_k);
   const int64_t warps = cap < sm_count() * 64 ? cap : sm_count() * 64;
-  gather_paged_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(a.k_cache), static_cast<const __nv_bfloat16 *>(a.v_cache),
-      a.block_table, cu_k, c.batch, a.max_pages, a.page_size, a.num_pages, c.hkv, c.head_dim, cap,
-      k_st, v_st);
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+  if (a.fp8)
+    gather_paged_kernel<true><<<blocks, 256, 0, stream>>>(
+        a.k_cache, a.v_cache, a.block_table, cu_k, c.batch, a.max_pages, a.page_size, a.num_pages,
+        c.hkv, c.head_dim, cap, k_st, v_st);
+  else
+    gather_paged_kernel<false><<<blocks, 256, 0, stream>>>(
+        a.k_cache, a.v_cache, a.block_table, cu_k, c.batch, a.max_pages, a.page_size, a.num_pages,
+        c.hkv, c.head_dim, cap, k_st, v_st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_core(c, k_st, v_st, cap, cu_k, sched, stream, encode_failed);

@@ -33,6 +33,7 @@ EXPORTED = (
     "sinkattn_decode",
     "sinkattn_decode_fp8",
     "sinkattn_decode_noalloc",
+    "sinkattn_prefill_paged_fp8",
     "sinkattn_merge",
     "sinkattn_get_device_error",
 )
@@ -81,6 +82,9 @@ def load(path: str = LIB_PATH):
     lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, L, I, I, I, I, I, P,
                                            Mask, I, P, P, P, S, P]
     lib.sinkattn_prefill_paged.restype = I
+    lib.sinkattn_prefill_paged_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, L, I, I, I,
+                                               I, I, P, Mask, I, P, P, P, S, P]
+    lib.sinkattn_prefill_paged_fp8.restype = I
     lib.sinkattn_prefill_backward_workspace_size.argtypes = [I, L, L, I, I, I]
     lib.sinkattn_prefill_backward_workspace_size.restype = S
     lib.sinkattn_prefill_backward.argtypes = [P, P, P, P, P, P, P, P, I, L, L, I, I, I, I, I, P,
@@ -225,6 +229,48 @@ def sinkattn_prefill_paged(q, cu_seqlens_q, k_cache, v_cache, block_table, seqle
                                     _ptr(sinks), mask, int(num_splits), _ptr(out), _ptr(lse),
                                     _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "sinkattn_prefill_paged")
+    return out, lse
+
+
+def sinkattn_prefill_paged_fp8(q, cu_seqlens_q, k_cache, v_cache, block_table, seqlens_k,
+                               max_seqlen_q, max_seqlen_k, *, k_scale=None, v_scale=None,
+                               sinks=None, causal=True, window=0, scale=None, num_splits=0,
+                               out=None, lse=None, return_lse=True, workspace=None,
+                               stream=None):
+    """sinkattn_prefill_paged over an fp8 e4m3 cache: k_cache / v_cache hold
+    uint8 codes [num_pages, hkv, page_size, head_dim]; k_scale / v_scale are
+    float32 [hkv] (None = 1). Returns (out, lse)."""
+    lib = load()
+    _req(q, torch.bfloat16, "q")
+    _req(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _req(k_cache, torch.uint8, "k_cache")
+    _req(v_cache, torch.uint8, "v_cache")
+    _req(block_table, torch.int32, "block_table")
+    _req(seqlens_k, torch.int32, "seqlens_k")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale"), (sinks, "sinks")):
+        if t is not None:
+            _req(t, torch.float32, n)
+    tq, hq, d = q.shape
+    num_pages, hkv, page_size, _ = k_cache.shape
+    batch = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((tq, hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = lib.sinkattn_prefill_paged_workspace_size(batch, tq, int(max_seqlen_q),
+                                                         int(max_seqlen_k), hq, hkv, d,
+                                                         int(window), int(num_splits))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    mask = Mask(1 if causal else 0, int(window), float(d ** -0.5 if scale is None else scale))
+    st = lib.sinkattn_prefill_paged_fp8(_ptr(q), _ptr(cu_seqlens_q), _ptr(k_cache),
+                                        _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                        _ptr(block_table), _ptr(seqlens_k), num_pages,
+                                        block_table.shape[1], page_size, batch, tq,
+                                        int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
+                                        _ptr(sinks), mask, int(num_splits), _ptr(out), _ptr(lse),
+                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sinkattn_prefill_paged_fp8")
     return out, lse
 
 

@@ -26,6 +26,8 @@ are not available here, so seeded normal values stand in for them):
                    permuted block table
   paged_prefill_batch    16 sequences, new chunks uniform in [256, 2048] after
                    cached contexts uniform in [1024, 32768], 16-token pages
+  paged_chunked_prefill_fp8  paged_chunked_prefill over an fp8 e4m3 cache with
+                   decode_contig_fp8's scale recipe
 
 Conventions: "uniform in [a, b]" draws integers with both ends included; values
 are float32 normal samples rounded to bf16 (round to nearest even); sinks stay
@@ -109,6 +111,11 @@ class PrefillCase:
     block_table: Optional[torch.Tensor] = None  # int32 [batch, max_pages]
     seqlens_k_t: Optional[torch.Tensor] = None  # int32 [batch]
     page_size: int = PAGE_SIZE
+    # fp8 paged cache: k_cache/v_cache hold e4m3 codes as uint8; the value of
+    # a code c of KV head g is k_scale[g] * e4m3(c)
+    kv_dtype: str = "bf16"
+    k_scale: Optional[torch.Tensor] = None  # f32 [hkv]
+    v_scale: Optional[torch.Tensor] = None
 
     @property
     def batch(self):
@@ -205,26 +212,34 @@ def _page_table(seqlens_k, page_size, seed, spare_pages=0):
 def make_prefill_paged(name, seqlens_q, seqlens_k, hq, hkv, *, seed, causal=True,
                        window=0, sink_std=1.0, with_sinks=True, scale=None,
                        page_size=PAGE_SIZE, spare_pages=0, device="cpu",
-                       head_dim=HEAD_DIM) -> PrefillCase:
+                       head_dim=HEAD_DIM, kv_dtype="bf16") -> PrefillCase:
     """Packed queries against K/V in pages; the queries of sequence b are the
-    last Lq_b of its Lk_b positions."""
+    last Lq_b of its Lk_b positions. kv_dtype "fp8": e4m3 codes with
+    per-KV-head scales, as make_decode draws them."""
     tq = sum(seqlens_q)
     q = bf16_normal((tq, hq, head_dim), seed * 10 + 1, device=device)
     table, num_pages = _page_table(seqlens_k, page_size, seed * 10 + 5, spare_pages)
     sinks = normal_f32(hq, seed * 10 + 4, sink_std) if with_sinks else None
+    shape = (num_pages, hkv, page_size, head_dim)
+    k_scale = v_scale = None
+    if kv_dtype == "fp8":
+        k_scale = fp8_scales(hkv, seed * 10 + 6)
+        v_scale = fp8_scales(hkv, seed * 10 + 7)
+        k_cache = e4m3_codes(shape, seed * 10 + 2, k_scale, 1, device=device)
+        v_cache = e4m3_codes(shape, seed * 10 + 3, v_scale, 1, device=device)
+    else:
+        k_cache = bf16_normal(shape, seed * 10 + 2, device=device)
+        v_cache = bf16_normal(shape, seed * 10 + 3, device=device)
     return PrefillCase(name=name, q=q, k=None, v=None, cu_seqlens_q=offsets(seqlens_q),
                        cu_seqlens_k=None, seqlens_q=list(seqlens_q),
                        seqlens_k=list(seqlens_k), hq=hq, hkv=hkv, sinks=sinks,
                        causal=causal, window=window,
                        scale=scale if scale is not None else head_dim ** -0.5,
-                       head_dim=head_dim,
-                       k_cache=bf16_normal((num_pages, hkv, page_size, head_dim),
-                                           seed * 10 + 2, device=device),
-                       v_cache=bf16_normal((num_pages, hkv, page_size, head_dim),
-                                           seed * 10 + 3, device=device),
+                       head_dim=head_dim, k_cache=k_cache, v_cache=v_cache,
                        block_table=table,
                        seqlens_k_t=torch.tensor(seqlens_k, dtype=torch.int32),
-                       page_size=page_size)
+                       page_size=page_size, kv_dtype=kv_dtype, k_scale=k_scale,
+                       v_scale=v_scale)
 
 
 def fp8_scales(hkv: int, seed: int) -> torch.Tensor:
@@ -342,6 +357,11 @@ def paged_chunked_prefill(device="cpu", lq=4096, lk=131072) -> PrefillCase:
                               causal=True, device=device)
 
 
+def paged_chunked_prefill_fp8(device="cpu", lq=4096, lk=131072) -> PrefillCase:
+    return make_prefill_paged("paged_chunked_prefill_fp8", [lq], [lk], 64, 8, seed=12,
+                              causal=True, device=device, kv_dtype="fp8")
+
+
 def paged_prefill_batch(device="cpu", nseq=16) -> PrefillCase:
     new = uniform_lengths(nseq, 256, 2048, seed=6000)
     cached = uniform_lengths(nseq, 1024, 32768, seed=6001)
@@ -362,4 +382,5 @@ WORKLOADS = {
     "long_context_prefill": long_context_prefill,
     "paged_chunked_prefill": paged_chunked_prefill,
     "paged_prefill_batch": paged_prefill_batch,
+    "paged_chunked_prefill_fp8": paged_chunked_prefill_fp8,
 }

@@ -488,7 +488,9 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
     # prefill against the paged cache: gather of the pages into contiguous
     # staging, then the same kernel; timed as one call (4 launches)
     for name, mk in (("paged_chunked_prefill", lambda: S.paged_chunked_prefill(device="cuda")),
-                     ("paged_prefill_batch", lambda: S.paged_prefill_batch(device="cuda"))):
+                     ("paged_prefill_batch", lambda: S.paged_prefill_batch(device="cuda")),
+                     ("paged_chunked_prefill_fp8",
+                      lambda: S.paged_chunked_prefill_fp8(device="cuda"))):
         if only is not None and name != only:
             continue
         c = mk()
@@ -502,15 +504,20 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
                                                                   window=c.window),
                          dtype=torch.uint8, device=dev)
 
+        fp8 = c.kv_dtype == "fp8"
+        scales = {}
+        if fp8:
+            scales = {"k_scale": c.k_scale.to(dev), "v_scale": c.v_scale.to(dev)}
+
         def call():
-            sa.sinkattn_prefill_paged(c.q, cq, c.k_cache, c.v_cache, bt, sl, c.max_seqlen_q,
-                                      c.max_seqlen_k, sinks=sk, causal=c.causal,
-                                      window=c.window, out=out, lse=lse, workspace=ws)
+            f = sa.sinkattn_prefill_paged_fp8 if fp8 else sa.sinkattn_prefill_paged
+            f(c.q, cq, c.k_cache, c.v_cache, bt, sl, c.max_seqlen_q, c.max_seqlen_k, sinks=sk,
+              causal=c.causal, window=c.window, out=out, lse=lse, workspace=ws, **scales)
         for _ in range(3):
             call()
         t = time_calls(call, 10, stream, flush)
         fl = prefill_flops(c)
-        kv = sum(c.seqlens_k) * c.hkv * c.head_dim * 2 * 2
+        kv = sum(c.seqlens_k) * c.hkv * c.head_dim * 2 * (1 if fp8 else 2)
         res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3,
                      "tokens_per_s": sum(c.seqlens_q) / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,

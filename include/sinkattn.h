@@ -170,6 +170,29 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlen
                                          size_t workspace_bytes, void *stream);
 
 /*
+ * Prefill of packed queries against a paged fp8 KV cache (page "GPT-OSS on
+ * day 0": the model is served with FP8; a chunked prefill then reads the
+ * cache that decode reads). Same arguments, workspace
+ * (sinkattn_prefill_paged_workspace_size), error reporting and results as
+ * sinkattn_prefill_paged, except:
+ *   k_cache, v_cache  fp8 e4m3 codes (the encoding of sinkattn_decode_fp8),
+ *            one byte per element, [num_pages, hkv, page_size, D].
+ *   k_scale, v_scale  float32 [hkv] or NULL (= 1): key j of KV head g stands
+ *            for k_scale[g] * e4m3(k_cache[...]), likewise for v.
+ * The gather stages the codes' exact values (K as bf16, V as fp16); k_scale
+ * multiplies the softmax scale and v_scale the normalised output, so the
+ * products are those of the bf16 call on the dequantised values up to the
+ * rounding of scale * k_scale and of the final scaling.
+ */
+sinkattn_status_t sinkattn_prefill_paged_fp8(
+    const void *q, const int32_t *cu_seqlens_q, const void *k_cache, const void *v_cache,
+    const float *k_scale, const float *v_scale, const int32_t *block_table,
+    const int32_t *seqlens_k, int num_pages, int max_pages_per_seq, int page_size, int batch,
+    int64_t total_q, int max_seqlen_q, int max_seqlen_k, int hq, int hkv, int head_dim,
+    const float *sinks, sinkattn_mask_t mask, int num_splits, void *out, float *lse,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Decode: one query token per sequence over a KV cache, split along the KV
  * sequence (section "Kernels for GPT-OSS / Sink Attention": attention is
  * parallelised over heads and over the KV length; the sink enters one block

@@ -132,6 +132,26 @@ def test_prefill_paged_rejects_bad_arguments(lib):
     assert prefill_paged(lib, d=128, ws=FAKE, wsb=need) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_prefill_paged_fp8_rejects_bad_arguments(lib):
+    def f(**kw):
+        a = dict(q=FAKE, cuq=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, table=FAKE, seqlens=FAKE,
+                 npages=8, maxp=4, page=16, batch=2, tq=10, mq=5, mk=64, hq=8, hkv=2, d=64,
+                 sinks=None, mask=M, ns=0, out=FAKE, lse=None, ws=None, wsb=0)
+        a.update(kw)
+        return lib.sinkattn_prefill_paged_fp8(
+            a["q"], a["cuq"], a["k"], a["v"], a["ks"], a["vs"], a["table"], a["seqlens"],
+            a["npages"], a["maxp"], a["page"], a["batch"], a["tq"], a["mq"], a["mk"], a["hq"],
+            a["hkv"], a["d"], a["sinks"], a["mask"], a["ns"], a["out"], a["lse"], a["ws"],
+            a["wsb"], None)
+    assert f(d=96) == B.SINKATTN_ERR_UNSUPPORTED
+    assert f(hq=6, hkv=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert f(ks=ctypes.c_void_p((1 << 20) + 2)) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert f(mk=65) == B.SINKATTN_ERR_INVALID_ARGUMENT
+    assert f() == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert f(ks=FAKE, vs=FAKE) == B.SINKATTN_ERR_WORKSPACE_TOO_SMALL
+    assert f(batch=0) == B.SINKATTN_OK
+
+
 def backward(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, dout=FAKE, lse=FAKE, cuq=FAKE, cuk=FAKE, batch=2,
              tq=10, tk=10, mq=5, mk=5, hq=8, hkv=2, d=64, sinks=None, mask=M, dq=FAKE, dk=FAKE,
