@@ -155,21 +155,27 @@ __device__ __forceinline__ void p_ds_row(float (&s)[32], const float (&dp)[32], 
   }
 }
 
+// nl2 / nd: the columns' -l2 and -D (16-byte aligned shared memory)
 __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], float c,
-                                         const float *l2, const float *d, uint32_t (&p16)[16],
+                                         const float *nl2, const float *nd, uint32_t (&p16)[16],
                                          uint32_t (&ds16)[16]) {
   const float2 c2 = make_float2(c, c);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 l = *reinterpret_cast<const float2 *>(l2 + 2 * i);
-    const float2 dd = *reinterpret_cast<const float2 *>(d + 2 * i);
-    const float2 a = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2,
-                                make_float2(-l.x, -l.y));
-    const float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-    const float2 g = __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]), make_float2(-dd.x, -dd.y));
-    const float2 ds = __fmul2_rn(p, g);
-    p16[i] = pack_f16x2(p.x, p.y);
-    ds16[i] = pack_f16x2(ds.x, ds.y);
+  for (int i = 0; i < 8; ++i) {
+    const float4 l = *reinterpret_cast<const float4 *>(nl2 + 4 * i);
+    const float4 dd = *reinterpret_cast<const float4 *>(nd + 4 * i);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = 4 * i + 2 * h;
+      const float2 a = __ffma2_rn(make_float2(s[j], s[j + 1]), c2,
+                                  h == 0 ? make_float2(l.x, l.y) : make_float2(l.z, l.w));
+      const float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+      const float2 g = __fadd2_rn(make_float2(dp[j], dp[j + 1]),
+                                  h == 0 ? make_float2(dd.x, dd.y) : make_float2(dd.z, dd.w));
+      const float2 ds = __fmul2_rn(p, g);
+      p16[j / 2] = pack_f16x2(p.x, p.y);
+      ds16[j / 2] = pack_f16x2(ds.x, ds.y);
+    }
   }
 }
 
@@ -470,13 +476,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int key0 = (t.kt_lo + (ss >> 1)) * kBN + (ss & 1) * kHalf;
         const int c_lo = min(max(lo - key0, 0), kHalf);
         const int len = max(min(hi - key0, kHalf) - c_lo, 0);
+        // boundary halves only (warp-uniform, so the loads stay collective)
+        const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float sv[32], dp[32];
           tmem_ld32f(t_s + 32 * c, sv);
           tmem_ld32f(t_dp + 32 * c, dp);
           tmem_wait_ld();
-          mask32(sv, 32 * c, c_lo, len);
+          if (masked) mask32(sv, 32 * c, c_lo, len);
           uint32_t p16[16], ds16[16];
           p_ds_row(sv, dp, p.scale_log2, l2, d, p16, ds16, dsum);
           tmem_st16(t_ds + 16 * c, ds16);
@@ -564,7 +572,7 @@ struct KvBars {
 
 constexpr int kKvOffK = 0;                                   // 2 item buffers of K and V
 constexpr int kKvOffQ = 4 * kTileBytes;                      // per stage: Q, dO
-constexpr int kKvOffVec = kKvOffQ + kKvQStages * 2 * kTileBytes;  // per stage: lse2[128], D[128]
+constexpr int kKvOffVec = kKvOffQ + kKvQStages * 2 * kTileBytes;  // per stage: -lse2[128], -D[128]
 constexpr int kKvOffBar = kKvOffVec + kKvQStages * 1024;
 static_assert(sizeof(KvBars) <= 1024, "dK/dV control block");
 constexpr int kKvSmem = kKvOffBar + 1024 + 1024;
@@ -684,8 +692,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = lane + 32 * i;
-          vec[row] = row < valid ? p.lse2t[at + row] : INFINITY;
-          vec[128 + row] = row < valid ? p.dt[at + row] : 0.f;
+          vec[row] = row < valid ? -p.lse2t[at + row] : -INFINITY;  // -l2, -D
+          vec[128 + row] = row < valid ? -p.dt[at + row] : 0.f;
         }
         __syncwarp();
         mbar_arrive_expect_tx_elect(&bars->qd_full[st], 2 * kTileBytes);
@@ -831,6 +839,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (p.causal) c_lo = min(max(jk - qb, 0), kHalf);
         if (p.window > 0) c_hi = min(c_hi, max(jk - qb + p.window, 0));
         const int len = r < t.krows ? max(c_hi - c_lo, 0) : 0;
+        const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
         const float *vec = reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024) + u * kHalf;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -838,7 +847,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_ld32f(t_st + 32 * c, sv);
           tmem_ld32f(t_dpt + 32 * c, dp);
           tmem_wait_ld();
-          mask32(sv, 32 * c, c_lo, len);
+          if (masked) mask32(sv, 32 * c, c_lo, len);
           uint32_t p16[16], ds16[16];
           p_ds_col(sv, dp, p.scale_log2, vec + 32 * c, vec + 128 + 32 * c, p16, ds16);
           tmem_st16(t_pt + 16 * c, p16);
