@@ -186,15 +186,16 @@ __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], 
 // 4w..4w+3, one query row per thread) takes the sub-steps of parity w, in its
 // own TMEM buffer, so the tensor core computes the scores of one half while
 // the other warpgroup turns the previous half into P and dS. Warp 8: TMA
-// (Q and dO double-buffered per item, K/V in a 3-stage ring); warp 9: MMA
-// issue and TMEM owner.
+// (Q and dO double-buffered per item, K/V in a 3-stage ring); warp 9: issues
+// S and dP and owns TMEM; warp 10: issues dQ and Y.
 //
 // TMEM columns: S_w [64w, 64w+64), dP_w [128+64w, ...), dS_w fp16
 // [256+32w, ...), P_w fp16 [320+32w, ...), dQ [384,448), Y [448,512). S_w and
 // dP_w of a sub-step are written only after the softmax warps finished the
-// sub-step two back (the MMA warp waits for them before issuing dQ there),
-// and dS_w / P_w only after the commit that follows those dQ / Y MMAs; dQ and
-// Y of an item start only after the previous item's epilogue has read them.
+// sub-step two back (warp 9 waits for them), and dS_w / P_w only after the
+// dQ / Y MMAs of that sub-step have completed (the softmax waits for their
+// commit); dQ and Y of an item start only after the previous item's epilogue
+// has read them.
 //
 // D from the bf16 forward output (D_a) carries the output's rounding, and
 // dP - D cancels when one key dominates a row. This kernel therefore also
@@ -205,7 +206,7 @@ __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], 
 // sink gradient, which run after this one.
 constexpr int kHalf = 64;                           // keys per sub-step
 constexpr uint32_t kIdescSS64 = idesc_f32acc(128, kHalf, /*bf16=*/false, false, false);
-constexpr int kDqThreads = 320;
+constexpr int kDqThreads = 352;
 constexpr int kDqStages = 3;
 
 struct DqTile {
@@ -217,7 +218,8 @@ struct DqBars {
   uint64_t qd_full[2], qd_empty[2];
   uint64_t kv_full[kDqStages], kv_empty[kDqStages];
   uint64_t s_full[2], ds_full[2];
-  uint64_t dq_done, dq_free, drain;
+  uint64_t pds_free[2];  // dQ / Y of the sub-step in dS_b / P_b have completed
+  uint64_t dq_done, dq_free, drain[2];
   uint64_t dsum_full[2];  // both warpgroups' partial sums of an item are in dsum
   uint32_t tmem_base;
   int abort;
@@ -268,21 +270,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->tile_full[i], 1);
-      mbar_init(&bars->tile_empty[i], 256 + 1);
+      mbar_init(&bars->tile_empty[i], 256 + 2);
       mbar_init(&bars->qd_full[i], 1);
       mbar_init(&bars->qd_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->ds_full[i], 128);
+      mbar_init(&bars->pds_free[i], 1);
+      mbar_init(&bars->drain[i], 1);
     }
     for (int s = 0; s < kDqStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);  // both MMA warps
     }
     mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->dq_free, 256);
     mbar_init(&bars->dsum_full[0], 256);
     mbar_init(&bars->dsum_full[1], 256);
-    mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -347,30 +350,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int i = max(0, J - kDqStages); i < J; ++i)
         mbar_wait_warp(&bars->kv_full[i % kDqStages], (i / kDqStages) & 1, abort, err, true);
     }
-  } else if (warp == 9) {
+  } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------------ MMA
-    const uint64_t qdesc0 = sdesc_sw128(sbase + kDqOffQ);
+    // Two issuing warps, so that neither kind of product waits behind the
+    // other in one instruction stream: warp 9 issues S = Q K^T and
+    // dP = dO V^T of each sub-step as soon as the softmax warps are done
+    // with that TMEM buffer; warp 10 issues dQ += dS K and Y += P K once the
+    // softmax has written dS and P.
     const uint64_t kdesc0 = sdesc_sw128(sbase + kDqOffK);
-    const uint64_t vdesc0 = sdesc_sw128(sbase + kDqOffV);
     constexpr uint64_t kHalfDesc = (kHalf * 128) >> 4;  // 64 rows of 128 B
-    const uint32_t t_dq = tmem + 384, t_y = tmem + 448;
     int J = 0, nq = 0, G = 0;  // K/V tiles, items with keys, global sub-steps
     int dq_items = 0;          // items whose dQ/Y the epilogue has to release
     bool ok = true;
-    // S_b, dP_b of global sub-step g (item-local ss) from Q/dO buffer qb
-    auto issue_s = [&](int g, int ss, int qb, int j0) {
-      const int b = g & 1, u = ss & 1, st = (j0 + (ss >> 1)) % kDqStages;
-      const uint64_t qd = qdesc0 + qb * 2 * kTileDesc, dod = qd + kTileDesc;
-      const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
-      const uint64_t vd = vdesc0 + st * kTileDesc + u * kHalfDesc;
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(tmem + 64 * b, qd + 2 * ks, kd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(tmem + 128 + 64 * b, dod + 2 * ks, vd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
-      umma_commit_elect(&bars->s_full[b]);
-    };
+    const bool is_s = warp == 9;
+    const uint64_t qdesc0 = sdesc_sw128(sbase + kDqOffQ);
+    const uint64_t vdesc0 = sdesc_sw128(sbase + kDqOffV);
+    const uint32_t t_dq = tmem + 384, t_y = tmem + 448;
     for (int nt = 0; ok; ++nt) {
       const int slot = nt & 1;
       if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
@@ -378,57 +373,69 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (!t.valid) break;
       if (t.n > 0) {
         const int qb = nq & 1, steps = 2 * t.n;
-        ok = mbar_wait_warp(&bars->qd_full[qb], (nq >> 1) & 1, abort, err);
-        // first two sub-steps: K/V tile J, both halves
-        if (ok) ok = mbar_wait_warp(&bars->kv_full[J % kDqStages], (J / kDqStages) & 1, abort, err);
-        if (ok) {
-          tc_fence_after();
-          issue_s(G, 0, qb, J);
-          issue_s(G + 1, 1, qb, J);
-        }
-        // dQ/Y of the previous item must have been read by its epilogue
-        if (ok && dq_items > 0)
-          ok = mbar_wait_warp(&bars->dq_free, (dq_items - 1) & 1, abort, err);
-        for (int ss = 0; ok && ss < steps; ++ss) {
-          const int g = G + ss, b = g & 1, j = ss >> 1, u = ss & 1;
-          const int st = (J + j) % kDqStages;
-          if (!mbar_wait_warp(&bars->ds_full[b], (g >> 1) & 1, abort, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
-#pragma unroll
-          for (int kk = 0; kk < kHalf / 16; ++kk)
-            umma_ts_elect(t_dq, tmem + 256 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
-                          (ss > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < kHalf / 16; ++kk)
-            umma_ts_elect(t_y, tmem + 320 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
-                          (ss > 0 || kk > 0) ? 1u : 0u);
-          if (u == 1) umma_commit_elect(&bars->kv_empty[st]);  // both halves done with K/V
-          if (ss + 2 < steps) {
-            if (u == 0 && !mbar_wait_warp(&bars->kv_full[(J + j + 1) % kDqStages],
-                                          ((J + j + 1) / kDqStages) & 1, abort, err)) {
+        if (is_s) {
+          ok = mbar_wait_warp(&bars->qd_full[qb], (nq >> 1) & 1, abort, err);
+          for (int ss = 0; ok && ss < steps; ++ss) {
+            const int g = G + ss, b = g & 1, j = ss >> 1, u = ss & 1;
+            const int st = (J + j) % kDqStages;
+            // the softmax warps are done with S_b / dP_b of sub-step g - 2
+            if ((u == 0 && !mbar_wait_warp(&bars->kv_full[st], ((J + j) / kDqStages) & 1, abort,
+                                           err)) ||
+                (g >= 2 && !mbar_wait_warp(&bars->ds_full[b], ((g - 2) >> 1) & 1, abort, err))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_s(g + 2, ss + 2, qb, J);
+            const uint64_t qd = qdesc0 + qb * 2 * kTileDesc, dod = qd + kTileDesc;
+            const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
+            const uint64_t vd = vdesc0 + st * kTileDesc + u * kHalfDesc;
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+              umma_ss_elect(tmem + 64 * b, qd + 2 * ks, kd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+              umma_ss_elect(tmem + 128 + 64 * b, dod + 2 * ks, vd + 2 * ks, kIdescSS64,
+                            ks > 0 ? 1u : 0u);
+            umma_commit_elect(&bars->s_full[b]);
+            if (u == 1) umma_commit_elect(&bars->kv_empty[st]);  // this warp is done with K/V
           }
+          if (ok) umma_commit_elect(&bars->qd_empty[qb]);
+        } else {
+          // dQ/Y of the previous item must have been read by its epilogue
+          if (dq_items > 0) ok = mbar_wait_warp(&bars->dq_free, (dq_items - 1) & 1, abort, err);
+          for (int ss = 0; ok && ss < steps; ++ss) {
+            const int g = G + ss, b = g & 1, j = ss >> 1, u = ss & 1;
+            const int st = (J + j) % kDqStages;
+            if (!mbar_wait_warp(&bars->ds_full[b], (g >> 1) & 1, abort, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
+#pragma unroll
+            for (int kk = 0; kk < kHalf / 16; ++kk)
+              umma_ts_elect(t_dq, tmem + 256 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                            (ss > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < kHalf / 16; ++kk)
+              umma_ts_elect(t_y, tmem + 320 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                            (ss > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elect(&bars->pds_free[b]);  // dS_b / P_b may be overwritten
+            if (u == 1) umma_commit_elect(&bars->kv_empty[st]);
+          }
+          if (ok) umma_commit_elect(&bars->dq_done);
+          ++dq_items;
         }
         if (!ok) break;
-        umma_commit_elect(&bars->qd_empty[qb]);
-        umma_commit_elect(&bars->dq_done);
-        ++dq_items;
         ++nq;
         J += t.n;
         G += steps;
       }
       if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
     }
-    umma_commit_elect(&bars->drain);
-    mbar_wait_warp(&bars->drain, 0, abort, err, true);
+    // every MMA issued by this warp has finished before TMEM is released
+    umma_commit_elect(&bars->drain[warp - 9]);
+    mbar_wait_warp(&bars->drain[warp - 9], 0, abort, err, true);
   } else {
     // ---------------------------------------- P, dS (one query row / thread)
     const int wg = warp >> 2;             // warpgroup: sub-steps of this parity
@@ -487,9 +494,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (masked) mask32(sv, 32 * c, c_lo, len);
           uint32_t p16[16], ds16[16];
           p_ds_row(sv, dp, p.scale_log2, l2, d, p16, ds16, dsum);
+          // dQ / Y of sub-step g - 2 have finished reading dS / P of this buffer
+          if (c == 0 && g >= 2) {
+            if (!mbar_wait_warp(&bars->pds_free[wg], ((g - 2) >> 1) & 1, abort, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           tmem_st16(t_ds + 16 * c, ds16);
           tmem_st16(t_p + 16 * c, p16);
         }
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->ds_full[wg]);
