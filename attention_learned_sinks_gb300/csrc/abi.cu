@@ -75,7 +75,8 @@ sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (!prefill_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return SINKATTN_OK;
-  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out)
+    return SINKATTN_ERR_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (sinks && !aligned(sinks, 4)) ||
       (lse && !aligned(lse, 4)))
@@ -352,13 +353,14 @@ sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_ls
   if (num_splits < 0 || rows < 0 || hq <= 0) return SINKATTN_ERR_INVALID_ARGUMENT;
   if (!prefill_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   if (rows == 0) return SINKATTN_OK;
-  if (!out || (num_splits > 0 && (!partial_o || !partial_lse))) return SINKATTN_ERR_INVALID_ARGUMENT;
+  if (!out || (num_splits > 0 && (!partial_o || !partial_lse)))
+    return SINKATTN_ERR_INVALID_ARGUMENT;
   if ((partial_o && !aligned(partial_o, 16)) || (partial_lse && !aligned(partial_lse, 4)) ||
       !aligned(out, 16) || (sinks && !aligned(sinks, 4)) || (lse && !aligned(lse, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if ((rows * hq + 7) / 8 > INT32_MAX) return SINKATTN_ERR_UNSUPPORTED;
-  return from_cuda(launch_merge(partial_o, partial_lse, num_splits, rows, hq, head_dim, sinks, out, lse,
-                                static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_merge(partial_o, partial_lse, num_splits, rows, hq, head_dim, sinks, out,
+                                lse, static_cast<cudaStream_t>(stream)));
 }
 
 size_t sinkattn_prefill_backward_workspace_size(int batch, int64_t total_q, int64_t total_k,

@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kv_kernel(const uint4 *__restric
 __global__ void __launch_bounds__(256) bwd_dsink_kernel(const float *__restrict__ sinks,
                                                         const float *__restrict__ lse2t,
                                                         const float *__restrict__ dt,
-                                                        int64_t total_q, float *__restrict__ dsinks) {
+                                                        int64_t total_q,
+                                                        float *__restrict__ dsinks) {
   __shared__ double part[256];
   const int h = blockIdx.x;
   const float c2 = sinks[h] * kLog2e;
@@ -257,9 +258,10 @@ __device__ __forceinline__ void dq_decode(const BwdParams &p, int w, DqTile &t) 
 }
 
 __global__ void __launch_bounds__(kDqThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const BwdParams p) {
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -340,8 +342,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         const int row = t.k0 + (t.kt_lo + j) * kBN;
         mbar_arrive_expect_tx_elect(&bars->kv_full[st], 2 * kTileBytes);
-        tma_load_3d_elect(sbase + kDqOffK + st * kTileBytes, &tm_k, &bars->kv_full[st], 0, t.g, row);
-        tma_load_3d_elect(sbase + kDqOffV + st * kTileBytes, &tm_v, &bars->kv_full[st], 0, t.g, row);
+        tma_load_3d_elect(sbase + kDqOffK + st * kTileBytes, &tm_k, &bars->kv_full[st], 0, t.g,
+                          row);
+        tma_load_3d_elect(sbase + kDqOffV + st * kTileBytes, &tm_v, &bars->kv_full[st], 0, t.g,
+                          row);
       }
     }
     if (*abort) {  // copies already issued still land here: wait for them (bounded)
@@ -457,7 +461,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (t.n == 0) {  // no row of this tile sees a key: dq = 0, D = 0
         if (r < t.rows) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dq_row)[i] = make_uint4(0u, 0u, 0u, 0u);
+          for (int i = 0; i < 4; ++i)
+            reinterpret_cast<uint4 *>(dq_row)[i] = make_uint4(0u, 0u, 0u, 0u);
           if (wg == 0) p.dt[lidx] = 0.f;
         }
         mbar_arrive(&bars->tile_empty[slot]);
@@ -715,8 +720,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         mbar_arrive_expect_tx_elect(&bars->qd_full[st], 2 * kTileBytes);
         tma_load_3d_elect(sbase + kKvOffQ + st * 2 * kTileBytes, &tm_q, &bars->qd_full[st], 0, h,
                           t.q0 + qt * kBM);
-        tma_load_3d_elect(sbase + kKvOffQ + (st * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[st], 0,
-                          h, t.q0 + qt * kBM);
+        tma_load_3d_elect(sbase + kKvOffQ + (st * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[st],
+                          0, h, t.q0 + qt * kBM);
       }
     }
     if (*abort) {
@@ -856,7 +861,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (p.window > 0) c_hi = min(c_hi, max(jk - qb + p.window, 0));
         const int len = r < t.krows ? max(c_hi - c_lo, 0) : 0;
         const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
-        const float *vec = reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024) + u * kHalf;
+        const float *vec =
+            reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024) + u * kHalf;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float sv[32], dp[32];

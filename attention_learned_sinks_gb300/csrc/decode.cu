@@ -604,7 +604,8 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   p.counters = reinterpret_cast<unsigned int *>(ws + w.off_counters);
 
   if (a.plan.max_splits > 1) {
-    cudaError_t e = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(a.batch) * a.hkv * 4, stream);
+    cudaError_t e =
+        cudaMemsetAsync(p.counters, 0, static_cast<size_t>(a.batch) * a.hkv * 4, stream);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(a.plan.max_splits, a.hkv, a.batch);
@@ -675,7 +676,9 @@ cudaError_t noalloc_scratch(int device, void **ptr) {
   return cudaSuccess;
 }
 
-bool is_aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool is_aligned(const void *p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
 
 }  // namespace
 }  // namespace sinkattn

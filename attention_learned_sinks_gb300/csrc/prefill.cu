@@ -53,7 +53,7 @@ namespace {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per KV tile
 constexpr int kMaxStages = 3;                    // K/V ring depth at head_dim 64 (2 at 128)
-constexpr int kBlockBytes = kBM * 64 * 2;        // 16 KB: 128 rows x 64 elements (one swizzle block)
+constexpr int kBlockBytes = kBM * 64 * 2;        // 16 KB: 128 rows x 64 elements, one swizzle block
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;                        // S buffers shared round-robin by the tiles
 constexpr uint32_t kTmemO = kSBufs * 128;        // O_t at 384 + D t
@@ -72,9 +72,6 @@ struct Cfg {
   // NT = 2: three full warpgroups, so setmaxnreg can move registers from the
   // producer/MMA warpgroup to the two softmax warpgroups.
   static constexpr int kThreads = NT * 128 + (NT == 2 ? 128 : 96);
-  static constexpr int kLaunchRegs = NT == 2 ? 168 : 224;  // ptxas limit for kThreads
-  static constexpr int kRegsOther = 104;    // producer / MMA warpgroup after setmaxnreg
-  static constexpr int kRegsSoftmax = 200;  // each softmax warpgroup after setmaxnreg
   static constexpr int kProducerWarp = NT * 4;
   static constexpr int kMmaWarp = NT * 4 + 1;    // P V issuer, TMEM owner
   static constexpr int kQkWarp = NT * 4 + 2;     // Q K^T issuer
@@ -89,8 +86,13 @@ struct Cfg {
   static constexpr int kSmemBytes = kOffPendVs + NT * 128 * 4 + 1024;  // + alignment slack
 };
 
-static_assert(Cfg<2, 64>::kRegsOther * 128 + Cfg<2, 64>::kRegsSoftmax * 256 <=
-                  Cfg<2, 64>::kLaunchRegs * Cfg<2, 64>::kThreads,
+// Register split of the NT = 2 kernel (setmaxnreg): 168 registers a thread at
+// launch (the ptxas limit for 384 threads), then 104 for the producer / MMA
+// warpgroup and 200 for each softmax warpgroup.
+constexpr int kLaunchRegs2 = 168;
+constexpr int kRegsOther2 = 104;
+constexpr int kRegsSoftmax2 = 200;
+static_assert(kRegsOther2 * 128 + kRegsSoftmax2 * 256 <= kLaunchRegs2 * Cfg<2, 64>::kThreads,
               "register split must fit the registers the block is launched with");
 
 constexpr uint32_t kIdescQK = idesc_f32acc(kBM, kBN, /*bf16=*/true, false, false);
@@ -318,7 +320,8 @@ __global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_
 // the current tile's softmax and epilogue.
 template <int NT, int D>
 __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<NT, D>;
   constexpr int kStages = C::kStages;
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= C::kProducerWarp) {
-    if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<2, 64>::kRegsOther));
+    if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther2));
     if (warp == C::kProducerWarp) {
       // ---------------------------------------------------------- producer
       // Fetches tiles, publishes them in the 2-slot ring, and streams each
@@ -542,7 +545,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       mbar_wait_warp(&bars->drain[role], 0, abort, &g_prefill_error, true);
     }
   } else {
-    if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<2, 64>::kRegsSoftmax));
+    if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax2));
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;          // which query tile (head h0 + t)
     const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
@@ -1035,7 +1038,7 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
       if (e != cudaSuccess) return e;
       launch_regs = attr.numRegs;
     }
-    if (launch_regs * C2::kThreads < C2::kRegsOther * 128 + C2::kRegsSoftmax * 256)
+    if (launch_regs * C2::kThreads < kRegsOther2 * 128 + kRegsSoftmax2 * 256)
       return cudaErrorNotSupported;
     prefill_kernel<2, 64><<<grid, C2::kThreads, C2::kSmemBytes, stream>>>(tq, tk, tv, p);
   } else if (d == 64) {
