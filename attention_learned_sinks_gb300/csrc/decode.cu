@@ -535,14 +535,14 @@ DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num
   if (num_splits > 0) {
     chunk = (span + num_splits - 1) / num_splits;
   } else {
-    // About three blocks per (sequence, KV head) for contexts spread up to
+    // About two blocks per (sequence, KV head) for contexts spread up to
     // `span` (mean taken as span / 2), and at least ~4 waves of two blocks per
-    // SM on a 152-SM GB300 for small batches. Measured on GB300: larger blocks
-    // cut the per-block prologue and merge traffic, and three per pair keep
-    // the waves balanced.
+    // SM on a 152-SM GB300 for small batches. Measured on GB300 (bf16 and
+    // fp8, contiguous and paged): larger blocks cut the per-block prologue and
+    // merge traffic; two per pair beat three by 1.5-3%.
     const long pairs = static_cast<long>(batch > 0 ? batch : 1) * (hkv > 0 ? hkv : 1);
     const long est = span / 2 > 0 ? span / 2 : 1;
-    long blocks = 3 * pairs;
+    long blocks = 2 * pairs;
     if (blocks < 4 * 2 * 152) blocks = 4 * 2 * 152;
     chunk = (pairs * est + blocks - 1) / blocks;
     const long cap = (span + 63) / 64;  // at most 64 splits

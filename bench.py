@@ -400,7 +400,7 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "kv_bytes_per_step": nbytes,
                    "l2": "inputs larger than L2 (%.2f GB of KV per step, no flush)" % (nbytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "split_plan": "auto (about 3 blocks per sequence and KV head)"},
+                   "split_plan": "auto (about 2 blocks per sequence and KV head)"},
         "roofline": {"kernel": "decode_kernel<contiguous> (+2 KB counter memset per call)",
                      "bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s",
                      "frac": achieved / peak_hbm, "peak_kind": pk_kind + " hbm_gbs",
