@@ -134,6 +134,17 @@ __device__ __forceinline__ int swz8(int row, int chunk) {
   return row * DCfg<D>::kRowBytes8 + ((chunk ^ x) << 4);
 }
 
+// Zeroes the split-merge counters of one decode call. It allows the decode
+// grid that follows to launch immediately (griddepcontrol.launch_dependents);
+// the decode waits for this grid (griddepcontrol.wait) before its first
+// counter access.
+__global__ void __launch_bounds__(256) zero_counters_kernel(unsigned int *c, int64_t n) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    c[i] = 0u;
+}
+
 template <int D, bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Params p) {
   using C = DCfg<D>;
@@ -488,6 +499,9 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Pa
   __syncthreads();
   __shared__ int s_last;
   if (tid == 0) {
+    // the counters were zeroed by the kernel launched just before this one,
+    // which lets this grid start early: wait for it here, the first use
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const unsigned prev = atomicAdd(p.counters + b * p.hkv + g, 1u);
     s_last = prev == static_cast<unsigned>(nsplit - 1);
   }
@@ -603,15 +617,31 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   p.part_lse = reinterpret_cast<float *>(ws + w.off_lse);
   p.counters = reinterpret_cast<unsigned int *>(ws + w.off_counters);
 
-  if (a.plan.max_splits > 1) {
-    cudaError_t e =
-        cudaMemsetAsync(p.counters, 0, static_cast<size_t>(a.batch) * a.hkv * 4, stream);
+  // With splits, the merge counters are zeroed by a small kernel that lets
+  // the decode grid launch at once (programmatic dependent launch); the decode
+  // waits for it only where it first touches a counter, after its K/V pass.
+  const bool split = a.plan.max_splits > 1;
+  if (split) {
+    const int64_t n = static_cast<int64_t>(a.batch) * a.hkv;
+    const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    zero_counters_kernel<<<blocks, 256, 0, stream>>>(p.counters, n);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   dim3 grid(a.plan.max_splits, a.hkv, a.batch);
   auto go = [&](auto kernel, int smem) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    kernel<<<grid, kThreads, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = split ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, kernel, p);
   };
   const bool paged = a.block_table != nullptr;
   auto pick = [&](auto dim) {
