@@ -182,21 +182,21 @@ __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], 
 
 // ---------------------------------------------------------------- dQ -------
 // Persistent: one CTA per SM takes (query tile, head) items from the query
-// tile list (longest first) through a global counter. Each 128-key tile is
-// handled as two 64-key halves ("sub-steps"); softmax-side warpgroup w (warps
-// 4w..4w+3, one query row per thread) takes the sub-steps of parity w, in its
-// own TMEM buffer, so the tensor core computes the scores of one half while
-// the other warpgroup turns the previous half into P and dS. Warp 8: TMA
-// (Q and dO double-buffered per item, K/V in a 3-stage ring); warp 9: issues
-// S and dP and owns TMEM; warp 10: issues dQ and Y.
+// tile list (longest first) through a global counter. Per 128-key tile,
+// S = Q K^T and dP = dO V^T are single N = 128 products; softmax-side
+// warpgroup w (warps 4w..4w+3, one query row per thread) turns keys
+// 64w..64w+63 into P and dS. The warpgroups release S / dP as soon as they
+// have loaded them, so the next tile's S and dP are computed while they
+// work, and dQ / Y of a tile run while the next one is being softmaxed.
+// Warp 8: TMA (Q and dO double-buffered per item, K/V in a 3-stage ring);
+// warp 9: issues S and dP and owns TMEM; warp 10: issues dQ and Y.
 //
-// TMEM columns: S_w [64w, 64w+64), dP_w [128+64w, ...), dS_w fp16
-// [256+32w, ...), P_w fp16 [320+32w, ...), dQ [384,448), Y [448,512). S_w and
-// dP_w of a sub-step are written only after the softmax warps finished the
-// sub-step two back (warp 9 waits for them), and dS_w / P_w only after the
-// dQ / Y MMAs of that sub-step have completed (the softmax waits for their
-// commit); dQ and Y of an item start only after the previous item's epilogue
-// has read them.
+// TMEM columns: S [0, 128), dP [128, 256), dS fp16 [256, 320), P fp16
+// [320, 384) (warpgroup w's keys in the half at 32w), dQ [384, 448),
+// Y [448, 512). S / dP of tile g are written only after both warpgroups have
+// loaded those of tile g - 1, and dS / P of tile g only after the dQ / Y
+// MMAs of tile g - 1 have completed; dQ and Y of an item start only after the
+// previous item's epilogue has read them.
 //
 // D from the bf16 forward output (D_a) carries the output's rounding, and
 // dP - D cancels when one key dominates a row. This kernel therefore also
@@ -205,8 +205,9 @@ __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], 
 // - (D_e - D_a) Y). The correction is small, so its own fp16 rounding does
 // not matter. D_e replaces D_a in the workspace for the dK/dV kernel and the
 // sink gradient, which run after this one.
-constexpr int kHalf = 64;                           // keys per sub-step
+constexpr int kHalf = 64;                           // keys (dK/dV: queries) per sub-step
 constexpr uint32_t kIdescSS64 = idesc_f32acc(128, kHalf, /*bf16=*/false, false, false);
+constexpr uint32_t kIdescSS128 = idesc_f32acc(128, kBN, /*bf16=*/false, false, false);
 constexpr int kDqThreads = 352;
 constexpr int kDqStages = 3;
 
@@ -218,8 +219,10 @@ struct DqBars {
   uint64_t tile_full[2], tile_empty[2];
   uint64_t qd_full[2], qd_empty[2];
   uint64_t kv_full[kDqStages], kv_empty[kDqStages];
-  uint64_t s_full[2], ds_full[2];
-  uint64_t pds_free[2];  // dQ / Y of the sub-step in dS_b / P_b have completed
+  uint64_t s_full;    // S, dP of the current key tile are in TMEM
+  uint64_t s_read;    // both warpgroups have loaded them (the buffers may be rewritten)
+  uint64_t ds_full;   // both warpgroups have written dS, P of the tile
+  uint64_t pds_free;  // dQ / Y of the tile have read dS, P
   uint64_t dq_done, dq_free, drain[2];
   uint64_t dsum_full[2];  // both warpgroups' partial sums of an item are in dsum
   uint32_t tmem_base;
@@ -275,11 +278,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&bars->tile_empty[i], 256 + 2);
       mbar_init(&bars->qd_full[i], 1);
       mbar_init(&bars->qd_empty[i], 1);
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->ds_full[i], 128);
-      mbar_init(&bars->pds_free[i], 1);
       mbar_init(&bars->drain[i], 1);
     }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_read, 256);
+    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->pds_free, 1);
     for (int s = 0; s < kDqStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);  // both MMA warps
@@ -358,13 +362,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // ------------------------------------------------------------------ MMA
     // Two issuing warps, so that neither kind of product waits behind the
     // other in one instruction stream: warp 9 issues S = Q K^T and
-    // dP = dO V^T of each sub-step as soon as the softmax warps are done
-    // with that TMEM buffer; warp 10 issues dQ += dS K and Y += P K once the
-    // softmax has written dS and P.
+    // dP = dO V^T of a key tile (N = 128) as soon as both softmax warpgroups
+    // have loaded the previous tile's; warp 10 issues dQ += dS K and
+    // Y += P K once they have written dS and P.
     const uint64_t kdesc0 = sdesc_sw128(sbase + kDqOffK);
-    constexpr uint64_t kHalfDesc = (kHalf * 128) >> 4;  // 64 rows of 128 B
-    int J = 0, nq = 0, G = 0;  // K/V tiles, items with keys, global sub-steps
-    int dq_items = 0;          // items whose dQ/Y the epilogue has to release
+    int J = 0, nq = 0;  // K/V tiles (= global tile index), items with keys
+    int dq_items = 0;   // items whose dQ/Y the epilogue has to release
     bool ok = true;
     const bool is_s = warp == 9;
     const uint64_t qdesc0 = sdesc_sw128(sbase + kDqOffQ);
@@ -376,56 +379,54 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const DqTile t = bars->tiles[slot];
       if (!t.valid) break;
       if (t.n > 0) {
-        const int qb = nq & 1, steps = 2 * t.n;
+        const int qb = nq & 1;
         if (is_s) {
           ok = mbar_wait_warp(&bars->qd_full[qb], (nq >> 1) & 1, abort, err);
-          for (int ss = 0; ok && ss < steps; ++ss) {
-            const int g = G + ss, b = g & 1, j = ss >> 1, u = ss & 1;
-            const int st = (J + j) % kDqStages;
-            // the softmax warps are done with S_b / dP_b of sub-step g - 2
-            if ((u == 0 && !mbar_wait_warp(&bars->kv_full[st], ((J + j) / kDqStages) & 1, abort,
-                                           err)) ||
-                (g >= 2 && !mbar_wait_warp(&bars->ds_full[b], ((g - 2) >> 1) & 1, abort, err))) {
+          for (int j = 0; ok && j < t.n; ++j) {
+            const int g = J + j, st = g % kDqStages;
+            // the softmax warps have loaded S / dP of tile g - 1
+            if (!mbar_wait_warp(&bars->kv_full[st], (g / kDqStages) & 1, abort, err) ||
+                (g >= 1 && !mbar_wait_warp(&bars->s_read, (g - 1) & 1, abort, err))) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint64_t qd = qdesc0 + qb * 2 * kTileDesc, dod = qd + kTileDesc;
-            const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
-            const uint64_t vd = vdesc0 + st * kTileDesc + u * kHalfDesc;
+            const uint64_t kd = kdesc0 + st * kTileDesc;
+            const uint64_t vd = vdesc0 + st * kTileDesc;
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              umma_ss_elect(tmem + 64 * b, qd + 2 * ks, kd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
+              umma_ss_elect(tmem, qd + 2 * ks, kd + 2 * ks, kIdescSS128, ks > 0 ? 1u : 0u);
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              umma_ss_elect(tmem + 128 + 64 * b, dod + 2 * ks, vd + 2 * ks, kIdescSS64,
+              umma_ss_elect(tmem + 128, dod + 2 * ks, vd + 2 * ks, kIdescSS128,
                             ks > 0 ? 1u : 0u);
-            umma_commit_elect(&bars->s_full[b]);
-            if (u == 1) umma_commit_elect(&bars->kv_empty[st]);  // this warp is done with K/V
+            umma_commit_elect(&bars->s_full);
+            umma_commit_elect(&bars->kv_empty[st]);  // this warp is done with K/V
           }
           if (ok) umma_commit_elect(&bars->qd_empty[qb]);
         } else {
           // dQ/Y of the previous item must have been read by its epilogue
           if (dq_items > 0) ok = mbar_wait_warp(&bars->dq_free, (dq_items - 1) & 1, abort, err);
-          for (int ss = 0; ok && ss < steps; ++ss) {
-            const int g = G + ss, b = g & 1, j = ss >> 1, u = ss & 1;
-            const int st = (J + j) % kDqStages;
-            if (!mbar_wait_warp(&bars->ds_full[b], (g >> 1) & 1, abort, err)) {
+          for (int j = 0; ok && j < t.n; ++j) {
+            const int g = J + j, st = g % kDqStages;
+            if (!mbar_wait_warp(&bars->ds_full, g & 1, abort, err)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t kd = kdesc0 + st * kTileDesc + u * kHalfDesc;
+            const uint64_t kd = kdesc0 + st * kTileDesc;
+            // dS / P of keys 0..127 are 64 consecutive fp16-pair columns
 #pragma unroll
-            for (int kk = 0; kk < kHalf / 16; ++kk)
-              umma_ts_elect(t_dq, tmem + 256 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
-                            (ss > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_ts_elect(t_dq, tmem + 256 + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                            (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < kHalf / 16; ++kk)
-              umma_ts_elect(t_y, tmem + 320 + 32 * b + kk * 8, kd + kk * kRows16Desc, kIdescTS,
-                            (ss > 0 || kk > 0) ? 1u : 0u);
-            umma_commit_elect(&bars->pds_free[b]);  // dS_b / P_b may be overwritten
-            if (u == 1) umma_commit_elect(&bars->kv_empty[st]);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_ts_elect(t_y, tmem + 320 + kk * 8, kd + kk * kRows16Desc, kIdescTS,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elect(&bars->pds_free);  // dS / P may be overwritten
+            umma_commit_elect(&bars->kv_empty[st]);
           }
           if (ok) umma_commit_elect(&bars->dq_done);
           ++dq_items;
@@ -433,7 +434,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (!ok) break;
         ++nq;
         J += t.n;
-        G += steps;
       }
       if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
     }
@@ -476,47 +476,56 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (p.window > 0) lo = max(lo, pos - p.window + 1);
       if (r >= t.rows) hi = lo = 0;
       float2 dsum = make_float2(0.f, 0.f);
-      const int steps = 2 * t.n;
-      // this warpgroup's sub-steps: global index G + ss with ss = wg, wg + 2, ...
-      for (int ss = wg; ss < steps; ss += 2) {
-        const int g = G + ss;
-        if (!mbar_wait_warp(&bars->s_full[wg], (g >> 1) & 1, abort, err)) {
+      // per key tile: this warpgroup's 64 keys (64 wg .. 64 wg + 63) in two
+      // 32-column chunks; S / dP are released once both chunks are loaded
+      for (int j = 0; j < t.n; ++j) {
+        const int g = G + j;
+        if (!mbar_wait_warp(&bars->s_full, g & 1, abort, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int key0 = (t.kt_lo + (ss >> 1)) * kBN + (ss & 1) * kHalf;
+        const int key0 = (t.kt_lo + j) * kBN + wg * kHalf;
         const int c_lo = min(max(lo - key0, 0), kHalf);
         const int len = max(min(hi - key0, kHalf) - c_lo, 0);
         // boundary halves only (warp-uniform, so the loads stay collective)
         const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        uint32_t p16a[16], ds16a[16];
+        {
           float sv[32], dp[32];
-          tmem_ld32f(t_s + 32 * c, sv);
-          tmem_ld32f(t_dp + 32 * c, dp);
+          tmem_ld32f(t_s, sv);
+          tmem_ld32f(t_dp, dp);
           tmem_wait_ld();
-          if (masked) mask32(sv, 32 * c, c_lo, len);
-          uint32_t p16[16], ds16[16];
-          p_ds_row(sv, dp, p.scale_log2, l2, d, p16, ds16, dsum);
-          // dQ / Y of sub-step g - 2 have finished reading dS / P of this buffer
-          if (c == 0 && g >= 2) {
-            if (!mbar_wait_warp(&bars->pds_free[wg], ((g - 2) >> 1) & 1, abort, err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          tmem_st16(t_ds + 16 * c, ds16);
-          tmem_st16(t_p + 16 * c, p16);
+          if (masked) mask32(sv, 0, c_lo, len);
+          p_ds_row(sv, dp, p.scale_log2, l2, d, p16a, ds16a, dsum);
         }
-        if (!ok) break;
+        float sv[32], dp[32];
+        tmem_ld32f(t_s + 32, sv);
+        tmem_ld32f(t_dp + 32, dp);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_read);  // S / dP of the next tile may be computed
+        if (masked) mask32(sv, 32, c_lo, len);
+        uint32_t p16b[16], ds16b[16];
+        p_ds_row(sv, dp, p.scale_log2, l2, d, p16b, ds16b, dsum);
+        // dQ / Y of tile g - 1 have finished reading dS / P
+        if (g >= 1) {
+          if (!mbar_wait_warp(&bars->pds_free, (g - 1) & 1, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st16(t_ds, ds16a);
+        tmem_st16(t_p, p16a);
+        tmem_st16(t_ds + 16, ds16b);
+        tmem_st16(t_p + 16, p16b);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->ds_full[wg]);
+        mbar_arrive(&bars->ds_full);
       }
       if (!ok) break;
-      G += steps;
+      G += t.n;
       // exact D = both warpgroups' partial sums of P dP (exchanged through
       // shared memory; a bounded mbarrier wait, so an aborting CTA cannot
       // leave the other warpgroup waiting)
