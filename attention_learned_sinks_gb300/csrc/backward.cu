@@ -205,8 +205,8 @@ __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], 
 // - (D_e - D_a) Y). The correction is small, so its own fp16 rounding does
 // not matter. D_e replaces D_a in the workspace for the dK/dV kernel and the
 // sink gradient, which run after this one.
-constexpr int kHalf = 64;                           // keys (dK/dV: queries) per sub-step
-constexpr uint32_t kIdescSS64 = idesc_f32acc(128, kHalf, /*bf16=*/false, false, false);
+constexpr int kHalf = 64;  // keys (dK/dV: queries) of a tile per softmax warpgroup
+// ss: both operands K-major in shared memory, 128 x 128 scores (S = Q K^T, ...)
 constexpr uint32_t kIdescSS128 = idesc_f32acc(128, kBN, /*bf16=*/false, false, false);
 constexpr int kDqThreads = 352;
 constexpr int kDqStages = 3;
@@ -572,17 +572,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // Persistent: one CTA per SM takes (key tile, KV head) items from the key
 // tile list (walked backwards: under a causal mask the low key tiles are seen
 // by the most queries, so this is longest first within each KV head). An
-// item's steps run over
-// (query head of the group, query tile that sees the key tile); each step's
-// 128 queries are two 64-query halves, taken by softmax-side warpgroup w
-// (one key per thread) for halves of parity w, in its own TMEM buffers, so
-// the tensor core computes one half's S^T / dP^T while the other warpgroup
-// forms P^T and dS^T. Warp 8: TMA (K/V double-buffered per item; Q, dO and
-// the step's lse / D vectors in a 3-stage ring); warp 9: MMA issue, TMEM.
+// item's steps run over (query head of the group, query tile that sees the
+// key tile). Per step, S^T = K Q^T and dP^T = V dO^T are single N = 128
+// products; softmax-side warpgroup w (one key per thread) turns queries
+// 64w..64w+63 into P^T and dS^T and releases S^T / dP^T once it has loaded
+// them, so the next step's products are computed while it works. Warp 8: TMA
+// (K/V double-buffered per item; Q, dO and the step's lse / D vectors in a
+// 3-stage ring); warp 9: issues S^T and dP^T and owns TMEM; warp 10: issues
+// dV and dK.
 //
-// TMEM columns: S^T_w [64w, ...), dP^T_w [128+64w, ...), P^T_w fp16
-// [256+32w, ...), dS^T_w fp16 [320+32w, ...), dV [384,448), dK [448,512).
-constexpr int kKvThreads = 320;
+// TMEM columns: S^T [0, 128), dP^T [128, 256), P^T fp16 [256, 320), dS^T
+// fp16 [320, 384) (warpgroup w's queries in the half at 32w), dV [384, 448),
+// dK [448, 512).
+constexpr int kKvThreads = 352;
 constexpr int kKvQStages = 3;
 
 struct KvTile {
@@ -593,8 +595,11 @@ struct KvBars {
   uint64_t tile_full[2], tile_empty[2];
   uint64_t kv_full[2], kv_empty[2];
   uint64_t qd_full[kKvQStages], qd_empty[kKvQStages];
-  uint64_t st_full[2], ew_done[2];
-  uint64_t dkv_done, dkv_free, drain;
+  uint64_t st_full;   // S^T, dP^T of the current step are in TMEM
+  uint64_t s_read;    // both warpgroups have loaded them
+  uint64_t ew_done;   // both warpgroups have written P^T, dS^T of the step
+  uint64_t pds_free;  // dV / dK of the step have read P^T, dS^T
+  uint64_t dkv_done, dkv_free, drain[2];
   uint32_t tmem_base;
   int abort;
   KvTile tiles[2];
@@ -648,19 +653,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->tile_full[i], 1);
-      mbar_init(&bars->tile_empty[i], 256 + 1);
+      mbar_init(&bars->tile_empty[i], 256 + 2);
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
-      mbar_init(&bars->st_full[i], 1);
-      mbar_init(&bars->ew_done[i], 128);
+      mbar_init(&bars->drain[i], 1);
     }
     for (int s = 0; s < kKvQStages; ++s) {
       mbar_init(&bars->qd_full[s], 1);
-      mbar_init(&bars->qd_empty[s], 1);
+      mbar_init(&bars->qd_empty[s], 2);  // both MMA warps
     }
+    mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->s_read, 256);
+    mbar_init(&bars->ew_done, 256);
+    mbar_init(&bars->pds_free, 1);
     mbar_init(&bars->dkv_done, 1);
     mbar_init(&bars->dkv_free, 256);
-    mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -739,88 +746,83 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       for (int i = max(0, S - kKvQStages); i < S; ++i)
         mbar_wait_warp(&bars->qd_full[i % kKvQStages], (i / kKvQStages) & 1, abort, err, true);
     }
-  } else if (warp == 9) {
+  } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------------ MMA
+    // warp 9: S^T, dP^T of each step once both warpgroups have loaded the
+    // previous step's; warp 10: dV += P^T dO and dK += dS^T Q once they have
+    // written P^T and dS^T.
     const uint64_t kvdesc0 = sdesc_sw128(sbase + kKvOffK);
     const uint64_t qdesc0 = sdesc_sw128(sbase + kKvOffQ);
-    constexpr uint64_t kHalfDesc = (kHalf * 128) >> 4;  // 64 rows of 128 B
     const uint32_t t_dv = tmem + 384, t_dk = tmem + 448;
-    int ni = 0, S = 0, G = 0, done_items = 0;
+    const bool is_s = warp == 9;
+    int ni = 0, S = 0, done_items = 0;
     bool ok = true;
-    // S^T_b, dP^T_b of global sub-step g (item-local ss; step stage st)
-    auto issue_s = [&](int g, int ss, int st, int kb) {
-      const int b = g & 1, u = ss & 1;
-      const uint64_t kd = kvdesc0 + kb * 2 * kTileDesc, vd = kd + kTileDesc;
-      const uint64_t qd = qdesc0 + st * 2 * kTileDesc + u * kHalfDesc;
-      const uint64_t dod = qdesc0 + (st * 2 + 1) * kTileDesc + u * kHalfDesc;
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(tmem + 64 * b, kd + 2 * ks, qd + 2 * ks, kIdescSS64, ks > 0 ? 1u : 0u);
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        umma_ss_elect(tmem + 128 + 64 * b, vd + 2 * ks, dod + 2 * ks, kIdescSS64,
-                      ks > 0 ? 1u : 0u);
-      umma_commit_elect(&bars->st_full[b]);
-    };
     for (int nt = 0; ok; ++nt) {
       const int slot = nt & 1;
       if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
       const KvTile t = bars->tiles[slot];
       if (!t.valid) break;
       if (t.steps > 0) {
-        const int kb = ni & 1, subs = 2 * t.steps;
-        ok = mbar_wait_warp(&bars->kv_full[kb], (ni >> 1) & 1, abort, err) &&
-             mbar_wait_warp(&bars->qd_full[S % kKvQStages], (S / kKvQStages) & 1, abort, err);
-        if (ok) {
-          tc_fence_after();
-          issue_s(G, 0, S % kKvQStages, kb);
-          issue_s(G + 1, 1, S % kKvQStages, kb);
-        }
-        // dV/dK of the previous item must have been read by its epilogue
-        if (ok && done_items > 0)
-          ok = mbar_wait_warp(&bars->dkv_free, (done_items - 1) & 1, abort, err);
-        for (int ss = 0; ok && ss < subs; ++ss) {
-          const int g = G + ss, b = g & 1, s = ss >> 1, u = ss & 1;
-          const int st = (S + s) % kKvQStages;
-          if (!mbar_wait_warp(&bars->ew_done[b], (g >> 1) & 1, abort, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t qd = qdesc0 + st * 2 * kTileDesc + u * kHalfDesc;
-          const uint64_t dod = qdesc0 + (st * 2 + 1) * kTileDesc + u * kHalfDesc;
-#pragma unroll
-          for (int kk = 0; kk < kHalf / 16; ++kk)
-            umma_ts_elect(t_dv, tmem + 256 + 32 * b + kk * 8, dod + kk * kRows16Desc, kIdescTS,
-                          (ss > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < kHalf / 16; ++kk)
-            umma_ts_elect(t_dk, tmem + 320 + 32 * b + kk * 8, qd + kk * kRows16Desc, kIdescTS,
-                          (ss > 0 || kk > 0) ? 1u : 0u);
-          if (u == 1) umma_commit_elect(&bars->qd_empty[st]);  // both halves done with the step
-          if (ss + 2 < subs) {
-            const int st2 = (S + s + 1) % kKvQStages;
-            if (u == 0 && !mbar_wait_warp(&bars->qd_full[st2], ((S + s + 1) / kKvQStages) & 1,
-                                          abort, err)) {
+        const int kb = ni & 1;
+        if (is_s) {
+          ok = mbar_wait_warp(&bars->kv_full[kb], (ni >> 1) & 1, abort, err);
+          const uint64_t kd = kvdesc0 + kb * 2 * kTileDesc, vd = kd + kTileDesc;
+          for (int s = 0; ok && s < t.steps; ++s) {
+            const int g = S + s, st = g % kKvQStages;
+            if (!mbar_wait_warp(&bars->qd_full[st], (g / kKvQStages) & 1, abort, err) ||
+                (g >= 1 && !mbar_wait_warp(&bars->s_read, (g - 1) & 1, abort, err))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_s(g + 2, ss + 2, st2, kb);
+            const uint64_t qd = qdesc0 + st * 2 * kTileDesc, dod = qd + kTileDesc;
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+              umma_ss_elect(tmem, kd + 2 * ks, qd + 2 * ks, kIdescSS128, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+              umma_ss_elect(tmem + 128, vd + 2 * ks, dod + 2 * ks, kIdescSS128,
+                            ks > 0 ? 1u : 0u);
+            umma_commit_elect(&bars->st_full);
+            umma_commit_elect(&bars->qd_empty[st]);  // this warp is done with Q / dO
           }
+          if (ok) umma_commit_elect(&bars->kv_empty[kb]);
+        } else {
+          // dV/dK of the previous item must have been read by its epilogue
+          if (done_items > 0)
+            ok = mbar_wait_warp(&bars->dkv_free, (done_items - 1) & 1, abort, err);
+          for (int s = 0; ok && s < t.steps; ++s) {
+            const int g = S + s, st = g % kKvQStages;
+            if (!mbar_wait_warp(&bars->ew_done, g & 1, abort, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t qd = qdesc0 + st * 2 * kTileDesc, dod = qd + kTileDesc;
+            // P^T / dS^T of queries 0..127 are 64 consecutive fp16-pair columns
+#pragma unroll
+            for (int kk = 0; kk < kBM / 16; ++kk)
+              umma_ts_elect(t_dv, tmem + 256 + kk * 8, dod + kk * kRows16Desc, kIdescTS,
+                            (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < kBM / 16; ++kk)
+              umma_ts_elect(t_dk, tmem + 320 + kk * 8, qd + kk * kRows16Desc, kIdescTS,
+                            (s > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elect(&bars->pds_free);      // P^T / dS^T may be overwritten
+            umma_commit_elect(&bars->qd_empty[st]);  // and the stage (its lse / D too)
+          }
+          if (ok) umma_commit_elect(&bars->dkv_done);
+          ++done_items;
         }
         if (!ok) break;
-        umma_commit_elect(&bars->kv_empty[kb]);
-        umma_commit_elect(&bars->dkv_done);
-        ++done_items;
         ++ni;
         S += t.steps;
-        G += subs;
       }
       if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
     }
-    umma_commit_elect(&bars->drain);
-    mbar_wait_warp(&bars->drain, 0, abort, err, true);
+    // every MMA issued by this warp has finished before TMEM is released
+    umma_commit_elect(&bars->drain[warp - 9]);
+    mbar_wait_warp(&bars->drain[warp - 9], 0, abort, err, true);
   } else {
     // ---------------------------------------- P^T, dS^T (one key / thread)
     const int wg = warp >> 2;
@@ -829,7 +831,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const uint32_t t_st = tmem + lane_off + 64 * wg, t_dpt = t_st + 128;
     const uint32_t t_pt = tmem + lane_off + 256 + 32 * wg, t_dst = t_pt + 64;
     const uint32_t t_dv = tmem + lane_off + 384 + 32 * wg, t_dk = t_dv + 64;
-    int S = 0, G = 0, done_items = 0;
+    int S = 0, done_items = 0;
     bool ok = true;
     for (int nt = 0; ok; ++nt) {
       const int slot = nt & 1;
@@ -850,47 +852,62 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         continue;
       }
       const int jk = t.kt * kBN + r;  // this thread's key
-      const int subs = 2 * t.steps;
-      for (int ss = wg; ss < subs; ss += 2) {
-        const int g = G + ss, s = ss >> 1, u = ss & 1;
-        const int st = (S + s) % kKvQStages;
+      for (int s = 0; s < t.steps; ++s) {
+        const int g = S + s, st = g % kKvQStages;
         // the lse / D vectors are plain shared-memory stores: wait on their
         // barrier directly, then on the MMAs
-        if (!mbar_wait_warp(&bars->qd_full[st], ((S + s) / kKvQStages) & 1, abort, err) ||
-            !mbar_wait_warp(&bars->st_full[wg], (g >> 1) & 1, abort, err)) {
+        if (!mbar_wait_warp(&bars->qd_full[st], (g / kKvQStages) & 1, abort, err) ||
+            !mbar_wait_warp(&bars->st_full, g & 1, abort, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int qt = t.qt_lo + s % t.nqt;
-        // visible query columns of this key in the half: [c_lo, c_hi)
-        const int qb = t.lk - t.lq + qt * kBM + u * kHalf;  // position of the half's query 0
-        int c_lo = 0, c_hi = min(kHalf, t.lq - qt * kBM - u * kHalf);
+        // visible query columns of this key among the warpgroup's 64: [c_lo, c_hi)
+        const int qb = t.lk - t.lq + qt * kBM + wg * kHalf;  // position of its query 0
+        int c_lo = 0, c_hi = min(kHalf, t.lq - qt * kBM - wg * kHalf);
         if (p.causal) c_lo = min(max(jk - qb, 0), kHalf);
         if (p.window > 0) c_hi = min(c_hi, max(jk - qb + p.window, 0));
         const int len = r < t.krows ? max(c_hi - c_lo, 0) : 0;
         const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
         const float *vec =
-            reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024) + u * kHalf;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
+            reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024) + wg * kHalf;
+        uint32_t p16a[16], ds16a[16];
+        {
           float sv[32], dp[32];
-          tmem_ld32f(t_st + 32 * c, sv);
-          tmem_ld32f(t_dpt + 32 * c, dp);
+          tmem_ld32f(t_st, sv);
+          tmem_ld32f(t_dpt, dp);
           tmem_wait_ld();
-          if (masked) mask32(sv, 32 * c, c_lo, len);
-          uint32_t p16[16], ds16[16];
-          p_ds_col(sv, dp, p.scale_log2, vec + 32 * c, vec + 128 + 32 * c, p16, ds16);
-          tmem_st16(t_pt + 16 * c, p16);
-          tmem_st16(t_dst + 16 * c, ds16);
+          if (masked) mask32(sv, 0, c_lo, len);
+          p_ds_col(sv, dp, p.scale_log2, vec, vec + 128, p16a, ds16a);
         }
+        float sv[32], dp[32];
+        tmem_ld32f(t_st + 32, sv);
+        tmem_ld32f(t_dpt + 32, dp);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_read);  // S^T / dP^T of the next step may be computed
+        if (masked) mask32(sv, 32, c_lo, len);
+        uint32_t p16b[16], ds16b[16];
+        p_ds_col(sv, dp, p.scale_log2, vec + 32, vec + 128 + 32, p16b, ds16b);
+        // dV / dK of step g - 1 have finished reading P^T / dS^T
+        if (g >= 1) {
+          if (!mbar_wait_warp(&bars->pds_free, (g - 1) & 1, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st16(t_pt, p16a);
+        tmem_st16(t_dst, ds16a);
+        tmem_st16(t_pt + 16, p16b);
+        tmem_st16(t_dst + 16, ds16b);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->ew_done[wg]);
+        mbar_arrive(&bars->ew_done);
       }
       if (!ok) break;
       S += t.steps;
-      G += subs;
       if (!mbar_wait_warp(&bars->dkv_done, done_items & 1, abort, err)) break;
       ++done_items;
       tc_fence_after();
