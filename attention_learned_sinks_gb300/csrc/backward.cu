@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_wait_warp(&bars->drain[warp - 9], 0, abort, err, true);
   } else {
     // ---------------------------------------- P, dS (one query row / thread)
-    const int wg = warp >> 2;             // warpgroup: sub-steps of this parity
+    const int wg = warp >> 2;             // warpgroup: keys 64 wg .. 64 wg + 63 of each tile
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_off + 64 * wg, t_dp = t_s + 128;
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int key0 = (t.kt_lo + j) * kBN + wg * kHalf;
         const int c_lo = min(max(lo - key0, 0), kHalf);
         const int len = max(min(hi - key0, kHalf) - c_lo, 0);
-        // boundary halves only (warp-uniform, so the loads stay collective)
+        // boundary tiles only (warp-uniform, so the loads stay collective)
         const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
         uint32_t p16a[16], ds16a[16];
         {
