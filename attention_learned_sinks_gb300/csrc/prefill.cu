@@ -20,18 +20,22 @@
 // when the group size is even, else 1); every K/V tile is shared by the NT
 // tiles. Warps (NT = 2):
 //   warps 0-3, 4-7  softmax warpgroup t: thread r owns row r of tile t (TMEM lane r)
-//   warp 8          TMA producer: both Q tiles once, then K_j / V_j into a 3-stage ring
+//   warp 8          TMA producer: tiles, both Q tiles once, then K_j into a 3-stage ring
 //   warp 9          P V issuer and TMEM owner
 //   warp 10         Q K^T issuer
-//   warp 11         idle; it completes the third warpgroup so that setmaxnreg
-//                   can hand its registers to the softmax warpgroups (200 each)
-// TMEM (512 columns): three 128-column S buffers shared round-robin by the
-// work items k = NT j + t (KV tile j, query tile t) and O_t at [384 + 64 t, ...).
-// P_k (fp16 pairs) overwrites the first 64 columns of its S buffer once S_k
-// has been read, and feeds P V straight from TMEM. With three buffers the MMA
-// warp computes S for up to two items ahead of the softmax, so a softmax
-// warpgroup rarely waits for its next scores, and the two warpgroups' softmax
-// phases overlap the tensor core's P V and Q K^T work.
+//   warp 11         TMA producer of V_j (its own 3-stage ring)
+// (NT = 1: one softmax warpgroup, warps 4-7 in the same roles.) A K stage is
+// released once the tile's Q K^T has read it and a V stage once its P V has,
+// so K loads never wait for P V. setmaxnreg moves registers from warps 8-11
+// (104 each) to the two softmax warpgroups (200 each).
+// TMEM (512 columns): O_t at [384 + D t, ...) and score buffers in
+// [0, 384). NT = 2: three 128-column S buffers shared round-robin by the work
+// items k = NT j + t (KV tile j, query tile t); P_k (fp16 pairs) overwrites
+// the first 64 columns of its S buffer once S_k has been read, and feeds P V
+// straight from TMEM; Q K^T runs up to two items ahead of the softmax.
+// NT = 1: two S buffers and two separate 64-column P buffers at 256; an S
+// buffer is released as soon as the softmax has loaded it, so the next
+// scores are computed while the softmax works on the current ones.
 // Softmax: one read of the 128 scores of a row from TMEM, a range mask on
 // boundary tiles only, tree reductions (3-input max), packed f32x2 arithmetic
 // and hardware ex2. The running maximum is only
@@ -55,8 +59,7 @@ constexpr int kBN = 128;  // keys per KV tile
 constexpr int kMaxStages = 3;                    // K/V ring depth at head_dim 64 (2 at 128)
 constexpr int kBlockBytes = kBM * 64 * 2;        // 16 KB: 128 rows x 64 elements, one swizzle block
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 3;                        // S buffers shared round-robin by the tiles
-constexpr uint32_t kTmemO = kSBufs * 128;        // O_t at 384 + D t
+constexpr uint32_t kTmemO = 384;                 // O_t at 384 + D t
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -64,17 +67,24 @@ constexpr float kLn2 = 0.6931471805599453f;
 // NT query heads per item (2 when the group size is even), head dimension D:
 // 64 (NT 1 or 2) or 128 (NT 1). A 128-row tile of one head is D / 64
 // blocks of 128 rows x 128 bytes, each loaded by one TMA box with 128-byte
-// swizzle; at D = 128 the K/V ring has two stages so that two Q buffers and
-// the ring fit in shared memory, and O (128 columns) fills TMEM beside the
-// three S buffers.
+// swizzle; at D = 128 the K and V rings have two stages so that two Q
+// buffers and the rings fit in shared memory, and O (128 columns) fills TMEM
+// beside the score buffers.
 template <int NT, int D>
 struct Cfg {
   // NT = 2: three full warpgroups, so setmaxnreg can move registers from the
   // producer/MMA warpgroup to the two softmax warpgroups.
-  static constexpr int kThreads = NT * 128 + (NT == 2 ? 128 : 96);
-  static constexpr int kProducerWarp = NT * 4;
+  static constexpr int kThreads = NT * 128 + 128;
+  static constexpr int kProducerWarp = NT * 4;   // tiles, Q and K loads
   static constexpr int kMmaWarp = NT * 4 + 1;    // P V issuer, TMEM owner
   static constexpr int kQkWarp = NT * 4 + 2;     // Q K^T issuer
+  static constexpr int kVWarp = NT * 4 + 3;      // V loads
+  // Score buffers in TMEM columns [0, 384). Two heads per item: three 128-
+  // column S buffers used round-robin by the items, P written over its S.
+  // One head per item: two S buffers and two separate 64-column P buffers
+  // (at 256), so an S buffer is free as soon as the softmax has loaded it.
+  static constexpr bool kSplitP = NT == 1;
+  static constexpr int kSBufs = kSplitP ? 2 : 3;
   static constexpr int kTile = kBM * D * 2;                        // one 128-row tile of one head
   static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kOffQ = 0;                                  // 2 buffers x NT tiles
@@ -131,12 +141,12 @@ struct Tile {
 
 struct Barriers {
   uint64_t q_full[2], q_empty[2];       // double-buffered Q tiles
-  uint64_t k_full[kMaxStages];
-  uint64_t v_full[kMaxStages];
-  uint64_t kv_empty[kMaxStages];
-  uint64_t s_full[kSBufs];
-  uint64_t p_full[kSBufs];
-  uint64_t pv_done[kSBufs];             // P V of the item in this S buffer has completed
+  uint64_t k_full[kMaxStages], k_empty[kMaxStages];  // K ring: freed once Q K^T has read it
+  uint64_t v_full[kMaxStages], v_empty[kMaxStages];  // V ring: freed once P V has read it
+  uint64_t s_full[3];                   // S of item k in buffer k % kSBufs
+  uint64_t s_read[2];                   // separate P: the softmax has loaded S (buffer free)
+  uint64_t p_full[3];                   // P of item k written (buffer k % kSBufs)
+  uint64_t pv_done[3];                  // P V of that item has completed
   uint64_t o_done[2];                   // one phase per P V into O_t
   uint64_t o_free[2];                   // one phase per tile with keys: epilogue has read O_t
   uint64_t tile_full[2], tile_empty[2]; // tile descriptor ring
@@ -341,18 +351,22 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       mbar_init(&bars->o_done[i], 1);
       mbar_init(&bars->o_free[i], kBM);
       mbar_init(&bars->tile_full[i], 1);
-      mbar_init(&bars->tile_empty[i], NT * kBM + 2);
+      mbar_init(&bars->tile_empty[i], NT * kBM + 3);
       mbar_init(&bars->drain[i], 1);
     }
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
-    for (int i = 0; i < kSBufs; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], kBM);
       mbar_init(&bars->pv_done[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_read[i], kBM);
     }
     bars->abort = 0;
     fence_mbar_init();
@@ -371,12 +385,12 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     if (warp == C::kProducerWarp) {
       // ---------------------------------------------------------- producer
       // Fetches tiles, publishes them in the 2-slot ring, and streams each
-      // tile's Q (double-buffered) and K/V tiles (3-stage ring). The whole warp
-      // runs the loop; lane 0 fetches and publishes, one elected lane issues
-      // each copy.
+      // tile's Q (double-buffered) and K tiles (3-stage ring; V has its own
+      // ring and warp, so a K load never waits for P V to free a V stage).
+      // The whole warp runs the loop; lane 0 fetches and publishes, one
+      // elected lane issues each copy.
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       // one tile = D / 64 boxes of 64 elements, into consecutive 16 KB blocks
       auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint64_t *bar, int head, int row) {
 #pragma unroll
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         bool ok = true;
         for (int j = 0; j < t.n; ++j, ++J) {
           const int st = J % kStages;
-          if (J >= kStages && !mbar_wait_warp(&bars->kv_empty[st], ((J / kStages) - 1) & 1, abort,
+          if (J >= kStages && !mbar_wait_warp(&bars->k_empty[st], ((J / kStages) - 1) & 1, abort,
                                               &g_prefill_error)) {
             ok = false;
             break;
@@ -423,8 +437,6 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           const int row = t.k0 + (t.kt_lo + j) * kBN;
           mbar_arrive_expect_tx_elect(&bars->k_full[st], kTileBytes);
           load_tile(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->k_full[st], t.kvh, row);
-          mbar_arrive_expect_tx_elect(&bars->v_full[st], kTileBytes);
-          load_tile(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->v_full[st], t.kvh, row);
         }
         if (!ok) break;
       }
@@ -433,21 +445,55 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         // for the last ones of each ring (bounded) before the CTA may exit.
         for (int i = max(0, q_loads - 2); i < q_loads; ++i)
           mbar_wait_warp(&bars->q_full[i & 1], (i >> 1) & 1, abort, &g_prefill_error, true);
-        for (int i = max(0, J - kStages); i < J; ++i) {
+        for (int i = max(0, J - kStages); i < J; ++i)
           mbar_wait_warp(&bars->k_full[i % kStages], (i / kStages) & 1, abort, &g_prefill_error,
                          true);
+      }
+    } else if (warp == C::kVWarp) {
+      // --------------------------------------------------------- V producer
+      // Follows the published tiles and streams their V tiles into the V ring.
+      tma_prefetch_desc(&tm_v);
+      int J = 0;
+      for (int nt = 0;; ++nt) {
+        const int slot = nt & 1;
+        if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, &g_prefill_error))
+          break;
+        const Tile t = bars->tiles[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tile_empty[slot]);
+        if (!t.valid) break;
+        bool ok = true;
+        for (int j = 0; j < t.n; ++j, ++J) {
+          const int st = J % kStages;
+          if (J >= kStages && !mbar_wait_warp(&bars->v_empty[st], ((J / kStages) - 1) & 1, abort,
+                                              &g_prefill_error)) {
+            ok = false;
+            break;
+          }
+          const int row = t.k0 + (t.kt_lo + j) * kBN;
+          mbar_arrive_expect_tx_elect(&bars->v_full[st], kTileBytes);
+#pragma unroll
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_3d_elect(sbase + C::kOffV + st * kTileBytes + blk * kBlockBytes, &tm_v,
+                              &bars->v_full[st], blk * 64, t.kvh, row);
+        }
+        if (!ok) break;
+      }
+      if (*abort) {
+        for (int i = max(0, J - kStages); i < J; ++i)
           mbar_wait_warp(&bars->v_full[i % kStages], (i / kStages) & 1, abort, &g_prefill_error,
                          true);
-        }
       }
     } else if (warp == C::kMmaWarp || warp == C::kQkWarp) {
       // ------------------------------------------------------- MMA issuers
       // Work items k = NT j + t of a tile (KV tile j, query tile t), counted
-      // globally across tiles (K). Item K's scores go to S buffer K % 3. The
-      // Q K^T warp issues QK(K) once PV(K - 3) (which read P from that buffer)
-      // has completed; the P V warp issues PV(K) once the softmax has written
-      // P. With three buffers Q K^T runs up to two items ahead of the softmax,
-      // also across tile boundaries. Each warp runs its loop whole (uniform
+      // globally across tiles (K); item K uses score buffer K % kSBufs. With
+      // P written over S (two heads), the Q K^T warp issues QK(K) once PV(K -
+      // 3) has completed, so Q K^T runs up to two items ahead of the softmax;
+      // with separate P buffers (one head), once the softmax has loaded the
+      // scores of item K - 2, so the next scores are computed while the
+      // softmax works on the current ones. The P V warp issues PV(K) once the
+      // softmax has written P. Each warp runs its loop whole (uniform
       // operands); one elected lane issues each MMA and commit.
       constexpr uint64_t kTileDesc = kTileBytes >> 4;   // one tile, in descriptor address units
       constexpr uint64_t kBlockDesc = kBlockBytes >> 4;  // one 64-element block of a tile
@@ -470,9 +516,14 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           const int qb = nt & 1;
           ok = mbar_wait_warp(&bars->q_full[qb], (nt >> 1) & 1, abort, &g_prefill_error);
           for (int k = 0; ok && k < items; ++k) {
-            const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % kSBufs;
-            if (KK >= kSBufs && !mbar_wait_warp(&bars->pv_done[b], ((KK - kSBufs) / kSBufs) & 1,
-                                                abort, &g_prefill_error)) {
+            const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % C::kSBufs;
+            const bool free_ok =
+                C::kSplitP
+                    ? (KK < 2 || mbar_wait_warp(&bars->s_read[b], ((KK - 2) >> 1) & 1, abort,
+                                                &g_prefill_error))
+                    : (KK < 3 || mbar_wait_warp(&bars->pv_done[b], ((KK - 3) / 3) & 1, abort,
+                                                &g_prefill_error));
+            if (!free_ok) {
               ok = false;
               break;
             }
@@ -492,11 +543,13 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
               umma_ss_elect(sbuf, qd + off, kd + off, kIdescQK, ks > 0 ? 1u : 0u);
             }
             umma_commit_elect(&bars->s_full[b]);
+            // the K stage is free once the tile's last Q K^T has read it
+            if (tt == NT - 1) umma_commit_elect(&bars->k_empty[Jc % kStages]);
           }
           if (ok) umma_commit_elect(&bars->q_empty[qb]);  // Q buffer free once these QK finish
         } else {
           for (int k = 0; ok && k < items; ++k) {
-            const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % kSBufs, Jc = J + jj;
+            const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % C::kSBufs, Jc = J + jj;
             // the first P V of a tile into O_t waits until the epilogue of the
             // last tile that used O_t (same softmax warpgroup) has read it; only
             // tiles with keys use O_t and signal o_free, so the phases pair up
@@ -511,13 +564,13 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
               ok = false;
               break;
             }
-            if (!mbar_wait_warp(&bars->p_full[b], (KK / kSBufs) & 1, abort, &g_prefill_error)) {
+            if (!mbar_wait_warp(&bars->p_full[b], (KK / C::kSBufs) & 1, abort, &g_prefill_error)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint64_t vd = vdesc0 + (Jc % kStages) * kTileDesc;
-            const uint32_t pbuf = tmem + b * kBN;
+            const uint32_t pbuf = tmem + (C::kSplitP ? 256 + b * 64 : b * kBN);
             const uint32_t obuf = tmem + kTmemO + tt * D;
 #pragma unroll
             for (int hb = 0; hb < D / 64; ++hb)  // O columns of dims 64 hb.. from V block hb
@@ -528,10 +581,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                               (jj > 0 || kk > 0) ? 1u : 0u);
             umma_commit_elect(&bars->o_done[tt]);
             umma_commit_elect(&bars->pv_done[b]);
-            // PV(K) completing implies QK of every item of this KV tile
-            // completed (it preceded P), so the K/V stage is free after the
-            // tile's last item.
-            if (tt == NT - 1) umma_commit_elect(&bars->kv_empty[Jc % kStages]);
+            // the V stage is free after the tile's last P V
+            if (tt == NT - 1) umma_commit_elect(&bars->v_empty[Jc % kStages]);
           }
         }
         if (!ok) break;
@@ -648,10 +699,12 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const int pos = ti.p_min + r;
       const int n = ti.n;
       for (int j = 0; j < n; ++j) {
-        const int k = K + j * NT + t;  // work item: S buffer k % 3, its (k / 3)-th use
-        const uint32_t s_addr = lane_addr + (k % kSBufs) * kBN;
+        const int k = K + j * NT + t;  // work item: buffer k % kSBufs, its (k / kSBufs)-th use
+        const int kb = k % C::kSBufs;
+        const uint32_t s_addr = lane_addr + kb * kBN;
+        const uint32_t p_addr = C::kSplitP ? lane_addr + 256 + kb * 64 : s_addr;
         // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[k % kSBufs], (k / kSBufs) & 1,
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[kb], (k / C::kSBufs) & 1,
                                                abort, &g_prefill_error))) {
           ok = false;
           break;
@@ -666,6 +719,10 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         tmem_ld32f(s_addr + 64, s2);
         tmem_ld32f(s_addr + 96, s3);
         tmem_wait_ld();
+        if (C::kSplitP) {  // the scores are in registers: the S buffer may take item k + 2's
+          tc_fence_before();
+          mbar_arrive(&bars->s_read[kb]);
+        }
         if (need_mask) {
           // this row's visible keys form one range [lo, hi): sequence end, causal
           // bound and window; as tile columns [c_lo, c_lo + len)
@@ -698,10 +755,19 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           uint32_t pk[32];
           exp32(s0, c2, nb2, acc, pk, 0);
           exp32(s1, c2, nb2, acc, pk, 16);
-          tmem_st32(s_addr, pk);
+          // separate P: P V of item k - 2 has finished reading this P buffer
+          if (C::kSplitP && k >= 2) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[kb], ((k - 2) >> 1) & 1,
+                                                   abort, &g_prefill_error))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st32(p_addr, pk);
           exp32(s2, c2, nb2, acc, pk, 0);
           exp32(s3, c2, nb2, acc, pk, 16);
-          tmem_st32(s_addr + 32, pk);
+          tmem_st32(p_addr + 32, pk);
         }
         const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
         const float2 a03 = __fadd2_rn(a01, a23);
@@ -733,7 +799,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&bars->p_full[k % kSBufs]);
+        mbar_arrive(&bars->p_full[kb]);
         if (j == 0 && pend_on) {  // the previous tile's epilogue, behind this P
           finish();
           if (!ok) break;
