@@ -58,8 +58,6 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per KV tile
 constexpr int kMaxStages = 3;                    // K/V ring depth at head_dim 64 (2 at 128)
 constexpr int kBlockBytes = kBM * 64 * 2;        // 16 KB: 128 rows x 64 elements, one swizzle block
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 384;                 // O_t at 384 + D t
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -79,14 +77,22 @@ struct Cfg {
   static constexpr int kMmaWarp = NT * 4 + 1;    // P V issuer, TMEM owner
   static constexpr int kQkWarp = NT * 4 + 2;     // Q K^T issuer
   static constexpr int kVWarp = NT * 4 + 3;      // V loads
-  // Score buffers in TMEM columns [0, 384). Two heads per item: three 128-
-  // column S buffers used round-robin by the items, P written over its S.
-  // One head per item: two S buffers and two separate 64-column P buffers
-  // (at 256), so an S buffer is free as soon as the softmax has loaded it.
+  // One head per item at head_dim 64: two CTAs per SM, each with half the
+  // TMEM (256 columns) and half the registers.
+  static constexpr bool kDual = NT == 1 && D == 64;
+  static constexpr int kMinBlocks = kDual ? 2 : 1;
+  // Score buffers. Two heads per item: three 128-column S buffers used
+  // round-robin by the items, P written over its S, O_t at 384 + 64 t. One
+  // head per item: kSBufs S buffers and as many separate 64-column P buffers,
+  // so an S buffer is free as soon as the softmax has loaded it (two of each
+  // at head_dim 128, one of each in a dual CTA), then O.
   static constexpr bool kSplitP = NT == 1;
-  static constexpr int kSBufs = kSplitP ? 2 : 3;
+  static constexpr int kSBufs = kSplitP ? (kDual ? 1 : 2) : 3;
+  static constexpr uint32_t kTmemP = kSplitP ? kSBufs * 128 : 0;
+  static constexpr uint32_t kTmemO = kSplitP ? kTmemP + kSBufs * 64 : 384;
+  static constexpr uint32_t kTmemCols = kDual ? 256 : 512;
   static constexpr int kTile = kBM * D * 2;                        // one 128-row tile of one head
-  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kStages = D == 64 && !kDual ? 3 : 2;
   static constexpr int kOffQ = 0;                                  // 2 buffers x NT tiles
   static constexpr int kOffK = kOffQ + 2 * NT * kTile;
   static constexpr int kOffV = kOffK + kStages * kTile;
@@ -103,6 +109,14 @@ constexpr int kLaunchRegs2 = 168;
 constexpr int kRegsOther2 = 104;
 constexpr int kRegsSoftmax2 = 200;
 static_assert(kRegsOther2 * 128 + kRegsSoftmax2 * 256 <= kLaunchRegs2 * Cfg<2, 64>::kThreads,
+              "register split must fit the registers the block is launched with");
+// Dual CTAs (one head per item, head_dim 64, two CTAs per SM): 128 registers
+// a thread at launch, then 64 for the producer / MMA warps and 192 for the
+// softmax warpgroup.
+constexpr int kLaunchRegsD = 128;
+constexpr int kRegsOtherD = 64;
+constexpr int kRegsSoftmaxD = 192;
+static_assert(kRegsOtherD * 128 + kRegsSoftmaxD * 128 <= kLaunchRegsD * Cfg<1, 64>::kThreads,
               "register split must fit the registers the block is launched with");
 
 constexpr uint32_t kIdescQK = idesc_f32acc(kBM, kBN, /*bf16=*/true, false, false);
@@ -329,7 +343,7 @@ __global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_
 // Q buffers, tiles) across tiles, so the next tile's loads and Q K^T overlap
 // the current tile's softmax and epilogue.
 template <int NT, int D>
-__global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -372,7 +386,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == C::kMmaWarp) {
-    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -381,7 +395,10 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= C::kProducerWarp) {
-    if (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther2));
+    if constexpr (NT == 2)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther2));
+    else if constexpr (C::kDual)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOtherD));
     if (warp == C::kProducerWarp) {
       // ---------------------------------------------------------- producer
       // Fetches tiles, publishes them in the 2-slot ring, and streams each
@@ -519,8 +536,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             const int tt = k % NT, jj = k / NT, KK = K + k, b = KK % C::kSBufs;
             const bool free_ok =
                 C::kSplitP
-                    ? (KK < 2 || mbar_wait_warp(&bars->s_read[b], ((KK - 2) >> 1) & 1, abort,
-                                                &g_prefill_error))
+                    ? (KK < C::kSBufs ||
+                       mbar_wait_warp(&bars->s_read[b], ((KK - C::kSBufs) / C::kSBufs) & 1,
+                                      abort, &g_prefill_error))
                     : (KK < 3 || mbar_wait_warp(&bars->pv_done[b], ((KK - 3) / 3) & 1, abort,
                                                 &g_prefill_error));
             if (!free_ok) {
@@ -570,8 +588,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             }
             tc_fence_after();
             const uint64_t vd = vdesc0 + (Jc % kStages) * kTileDesc;
-            const uint32_t pbuf = tmem + (C::kSplitP ? 256 + b * 64 : b * kBN);
-            const uint32_t obuf = tmem + kTmemO + tt * D;
+            const uint32_t pbuf = tmem + (C::kSplitP ? C::kTmemP + b * 64 : b * kBN);
+            const uint32_t obuf = tmem + C::kTmemO + tt * D;
 #pragma unroll
             for (int hb = 0; hb < D / 64; ++hb)  // O columns of dims 64 hb.. from V block hb
 #pragma unroll
@@ -596,12 +614,15 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       mbar_wait_warp(&bars->drain[role], 0, abort, &g_prefill_error, true);
     }
   } else {
-    if (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax2));
+    if constexpr (NT == 2)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax2));
+    else if constexpr (C::kDual)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxD));
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;          // which query tile (head h0 + t)
     const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t o_addr = lane_addr + kTmemO + t * D;
+    const uint32_t o_addr = lane_addr + C::kTmemO + t * D;
     int K = 0;        // items of earlier tiles
     int o_waits = 0;  // o_done[t] phases consumed
     // The epilogue of a tile runs after the first P of the next tile has been
@@ -702,7 +723,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         const int k = K + j * NT + t;  // work item: buffer k % kSBufs, its (k / kSBufs)-th use
         const int kb = k % C::kSBufs;
         const uint32_t s_addr = lane_addr + kb * kBN;
-        const uint32_t p_addr = C::kSplitP ? lane_addr + 256 + kb * 64 : s_addr;
+        const uint32_t p_addr = C::kSplitP ? lane_addr + C::kTmemP + kb * 64 : s_addr;
         // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[kb], (k / C::kSBufs) & 1,
                                                abort, &g_prefill_error))) {
@@ -755,10 +776,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           uint32_t pk[32];
           exp32(s0, c2, nb2, acc, pk, 0);
           exp32(s1, c2, nb2, acc, pk, 16);
-          // separate P: P V of item k - 2 has finished reading this P buffer
-          if (C::kSplitP && k >= 2) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[kb], ((k - 2) >> 1) & 1,
-                                                   abort, &g_prefill_error))) {
+          // separate P: P V of item k - kSBufs has finished reading this P buffer
+          if (C::kSplitP && k >= C::kSBufs) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&bars->pv_done[kb], ((k - C::kSBufs) / C::kSBufs) & 1,
+                                      abort, &g_prefill_error))) {
               ok = false;
               break;
             }
@@ -826,7 +848,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   __syncthreads();
   if (warp == C::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -1088,8 +1110,9 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   // upper bound on the number of work items, for the grid size
   const int64_t max_pairs = a.total_q / kBM + a.batch;
   const int64_t max_work = max_pairs * (a.hq / nt) * splits;
-  const int num_sms = sm_count();
-  const unsigned grid = static_cast<unsigned>(max_work < num_sms ? max_work : num_sms);
+  // one resident CTA per SM, two for the dual (one head, head_dim 64) kernel
+  const int num_ctas = sm_count() * (nt == 1 && d == 64 ? 2 : 1);
+  const unsigned grid = static_cast<unsigned>(max_work < num_ctas ? max_work : num_ctas);
   if (nt == 2) {
     using C2 = Cfg<2, 64>;
     e = cudaFuncSetAttribute(prefill_kernel<2, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1112,6 +1135,15 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
     e = cudaFuncSetAttribute(prefill_kernel<1, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C1::kSmemBytes);
     if (e != cudaSuccess) return e;
+    static int launch_regs = -1;  // as above, for the dual CTAs' split
+    if (launch_regs < 0) {
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, prefill_kernel<1, 64>);
+      if (e != cudaSuccess) return e;
+      launch_regs = attr.numRegs;
+    }
+    if (launch_regs * C1::kThreads < kRegsOtherD * 128 + kRegsSoftmaxD * 128)
+      return cudaErrorNotSupported;
     prefill_kernel<1, 64><<<grid, C1::kThreads, C1::kSmemBytes, stream>>>(tq, tk, tv, p);
   } else {
     using C1 = Cfg<1, 128>;

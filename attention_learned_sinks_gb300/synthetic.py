@@ -20,6 +20,8 @@ are not available here, so seeded normal values stand in for them):
                    causal context (few query tiles: the split-KV case)
   decode_contig_d128 decode_contig's lengths and heads with head_dim 128
   varlen_prefill_d128  varlen_prefill's lengths and heads with head_dim 128
+  varlen_prefill_g3    varlen_prefill's lengths with 24 q / 8 kv heads (groups
+                   of 3: one head per work item)
   decode_contig_fp8  decode_contig's lengths and geometry over an fp8 e4m3 KV
                    cache with per-KV-head scales 2^-4 * U(0.5, 2)
   paged_chunked_prefill  the same as chunked_prefill, with K/V in 16-token pages and a randomly
@@ -330,6 +332,12 @@ def varlen_prefill_d128(device="cpu", nseq=16) -> PrefillCase:
                         device=device, head_dim=128)
 
 
+def varlen_prefill_g3(device="cpu", nseq=16) -> PrefillCase:
+    lens = uniform_lengths(nseq, 512, 4096, seed=3000)
+    return make_prefill("varlen_prefill_g3", lens, lens, 24, 8, seed=13, causal=True,
+                        device=device)
+
+
 def decode_contig_fp8(device="cpu", batch=64) -> DecodeCase:
     lens = uniform_lengths(batch, 1024, 8192, seed=2000)
     return make_decode("decode_contig_fp8", lens, 64, 8, seed=9, device=device, kv_dtype="fp8")
@@ -378,6 +386,7 @@ WORKLOADS = {
     "decode_contig_fp8": decode_contig_fp8,
     "decode_contig_d128": decode_contig_d128,
     "varlen_prefill_d128": varlen_prefill_d128,
+    "varlen_prefill_g3": varlen_prefill_g3,
     "chunked_prefill": chunked_prefill,
     "long_context_prefill": long_context_prefill,
     "paged_chunked_prefill": paged_chunked_prefill,

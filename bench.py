@@ -456,6 +456,7 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
             ("varlen_prefill", lambda: S.varlen_prefill(device="cuda"), 0),
             ("varlen_prefill_w128", lambda: S.varlen_prefill(window=128, device="cuda"), 0),
             ("varlen_prefill_d128", lambda: S.varlen_prefill_d128(device="cuda"), 0),
+            ("varlen_prefill_g3", lambda: S.varlen_prefill_g3(device="cuda"), 0),
             ("chunked_prefill", lambda: S.chunked_prefill(device="cuda"), 0),
             ("long_context_prefill", lambda: S.long_context_prefill(device="cuda"), 0),
             ("long_context_prefill_unsplit", lambda: S.long_context_prefill(device="cuda"), 1)):

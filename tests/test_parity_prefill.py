@@ -251,3 +251,13 @@ def test_prefill_head_dim_128_varlen_full_config(oracle_lib):
     torch.cuda.synchronize()
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 16, 139), "varlen_prefill_d128")
     assert sa.sinkattn_get_device_error() == 0
+
+
+def test_prefill_groups_of_three_full_config(oracle_lib):
+    """varlen_prefill's lengths with 24 q / 8 kv heads: one head per work
+    item, two CTAs per SM. Sampled rows against the oracle."""
+    c = S.varlen_prefill_g3()
+    out, lse = run_prefill(c)
+    torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 16, 177), "varlen_prefill_g3")
+    assert sa.sinkattn_get_device_error() == 0
