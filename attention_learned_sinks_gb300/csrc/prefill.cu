@@ -469,6 +469,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
     } else if (warp == C::kVWarp) {
       // --------------------------------------------------------- V producer
       // Follows the published tiles and streams their V tiles into the V ring.
+      // V may still be being converted to fp16 by the grid launched before
+      // this one: wait for it here, the kernel's only use of V.
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       tma_prefetch_desc(&tm_v);
       int J = 0;
       for (int nt = 0;; ++nt) {
@@ -853,8 +856,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
 }
 
 // bf16 V -> fp16 copy for the P V product (8 elements per thread per step).
+// The prefill kernel launched after it may start at once (programmatic
+// dependent launch): only its V producer waits for this grid.
 __global__ void __launch_bounds__(256) convert_v_kernel(const uint4 *__restrict__ src,
                                                         uint4 *__restrict__ dst, int64_t n8) {
+  asm volatile("griddepcontrol.launch_dependents;");
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     dst[i] = bf16x8_to_f16x8(src[i]);
@@ -1056,9 +1062,12 @@ __global__ void __launch_bounds__(256) gather_paged_kernel(
 // and, with splits, the merge. k (bf16) and v16 (fp16) are [k_rows, hkv, 64];
 // cu_k may live on the device only; sched is the schedule area (tile counter +
 // work list), followed by the split partials.
+// v_src / n8: bf16 V to convert into v16 (n8 16-byte chunks) after the work
+// list is built, overlapped with the start of the prefill kernel; n8 = 0:
+// v16 is ready.
 cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, int64_t k_rows,
                         const int32_t *cu_k, uint8_t *sched, cudaStream_t stream,
-                        bool *encode_failed) {
+                        bool *encode_failed, const void *v_src = nullptr, int64_t n8 = 0) {
   const int max_qtiles = (a.max_seqlen_q + kBM - 1) / kBM;
   EncodeTiledFn fn = get_encode_fn();
   CUtensorMap tq, tk, tv;
@@ -1107,12 +1116,34 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
                                                 p.work_counter);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const bool pdl = n8 > 0;
+  if (pdl) {
+    const int64_t blocks = (n8 + 255) / 256;
+    convert_v_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+        static_cast<const uint4 *>(v_src), static_cast<uint4 *>(const_cast<void *>(v16)), n8);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   // upper bound on the number of work items, for the grid size
   const int64_t max_pairs = a.total_q / kBM + a.batch;
   const int64_t max_work = max_pairs * (a.hq / nt) * splits;
   // one resident CTA per SM, two for the dual (one head, head_dim 64) kernel
   const int num_ctas = sm_count() * (nt == 1 && d == 64 ? 2 : 1);
   const unsigned grid = static_cast<unsigned>(max_work < num_ctas ? max_work : num_ctas);
+  // launch one of the kernels, overlapping the V conversion when there is one
+  auto go = [&](auto kernel, int threads, int smem_bytes) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+  };
   if (nt == 2) {
     using C2 = Cfg<2, 64>;
     e = cudaFuncSetAttribute(prefill_kernel<2, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1129,7 +1160,7 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
     }
     if (launch_regs * C2::kThreads < kRegsOther2 * 128 + kRegsSoftmax2 * 256)
       return cudaErrorNotSupported;
-    prefill_kernel<2, 64><<<grid, C2::kThreads, C2::kSmemBytes, stream>>>(tq, tk, tv, p);
+    e = go(prefill_kernel<2, 64>, C2::kThreads, C2::kSmemBytes);
   } else if (d == 64) {
     using C1 = Cfg<1, 64>;
     e = cudaFuncSetAttribute(prefill_kernel<1, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1144,15 +1175,15 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
     }
     if (launch_regs * C1::kThreads < kRegsOtherD * 128 + kRegsSoftmaxD * 128)
       return cudaErrorNotSupported;
-    prefill_kernel<1, 64><<<grid, C1::kThreads, C1::kSmemBytes, stream>>>(tq, tk, tv, p);
+    e = go(prefill_kernel<1, 64>, C1::kThreads, C1::kSmemBytes);
   } else {
     using C1 = Cfg<1, 128>;
     e = cudaFuncSetAttribute(prefill_kernel<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C1::kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_kernel<1, 128><<<grid, C1::kThreads, C1::kSmemBytes, stream>>>(tq, tk, tv, p);
+    e = go(prefill_kernel<1, 128>, C1::kThreads, C1::kSmemBytes);
   }
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
   // split 0 carried the sink: the merge adds no sink of its own
   return launch_merge(p.part_o, p.part_lse, splits, a.total_q, a.hq, d, nullptr, a.out, a.lse,
@@ -1165,15 +1196,13 @@ cudaError_t launch_prefill(const PrefillLaunch &a, cudaStream_t stream, bool *en
   *encode_failed = false;
   const int max_qtiles = (a.max_seqlen_q + kBM - 1) / kBM;
   if (a.batch == 0 || a.total_q == 0 || max_qtiles == 0) return cudaSuccess;
+  // the bf16 -> fp16 copy of V runs after the work list, overlapped with the
+  // prefill kernel's start
   const int64_t n8 = a.total_k * a.hkv * a.head_dim / 8;
-  if (n8 > 0) {
-    const int64_t blocks = (n8 + 255) / 256;
-    convert_v_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
-        static_cast<const uint4 *>(a.v), static_cast<uint4 *>(a.v_f16), n8);
-  }
   uint8_t *ws = static_cast<uint8_t *>(a.v_f16);
   return launch_core(a, a.k, a.v_f16, a.total_k, a.cu_k,
-                     ws + vcopy_bytes(a.total_k, a.hkv, a.head_dim), stream, encode_failed);
+                     ws + vcopy_bytes(a.total_k, a.hkv, a.head_dim), stream, encode_failed, a.v,
+                     n8);
 }
 
 cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t stream,
