@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(256) bwd_dsink_kernel(const float *__restrict_
                                                         const float *__restrict__ dt,
                                                         int64_t total_q,
                                                         float *__restrict__ dsinks) {
+  // the dK/dV kernel does not read dsinks: it may start at once
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ double part[256];
   const int h = blockIdx.x;
   const float c2 = sinks[h] * kLog2e;
@@ -1048,15 +1050,28 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
     bwd_dq_kernel<<<static_cast<unsigned>(grid), kDqThreads, kDqSmem, stream>>>(tq, tdo, tk, tv, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (a.sinks != nullptr && a.dsinks != nullptr) {  // after dQ: D is exact by now
+  const bool dsink = a.sinks != nullptr && a.dsinks != nullptr;
+  if (dsink) {  // after dQ: D is exact by now
     bwd_dsink_kernel<<<a.hq, 256, 0, stream>>>(a.sinks, lse2t, dt, a.total_q, a.dsinks);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.total_k > 0) {
     const int64_t items = (a.total_k / kBN + a.batch) * a.hkv;
     const int64_t grid = items < sm_count() ? items : sm_count();
-    bwd_dkdv_kernel<<<static_cast<unsigned>(grid), kKvThreads, kKvSmem, stream>>>(tq, tdo, tk, tv,
-                                                                                 p);
+    // overlaps the sink gradient (programmatic dependent launch); everything
+    // it reads was written before that kernel started
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kKvThreads);
+    cfg.dynamicSmemBytes = kKvSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dsink ? 1 : 0;
+    if ((e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel, tq, tdo, tk, tv, p)) != cudaSuccess)
+      return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
