@@ -51,15 +51,14 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;  // per-warp pipeline depth (both caches)
 constexpr int kMaxGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Shapes for head dimension D (64 or 128). A warp step covers kSlab tokens:
 // 32 at D = 64, 16 at D = 128, so that a slab of K and V is the same number
-// of bytes for both and the shared memory per block stays at 96 KB (bf16,
-// two blocks per SM) or 48 KB (fp8, four per SM).
+// of bytes for both: 8 KB per stage for bf16, 4 KB for fp8 (ring depths
+// and blocks per SM in Ring below).
 template <int D>
 struct DCfg {
   static constexpr int kSlab = D == 64 ? 32 : 16;
@@ -68,12 +67,30 @@ struct DCfg {
   static constexpr int kRowBytes = D * 2;        // bf16 row
   static constexpr int kSlabBytes = kSlab * kRowBytes;
   static constexpr int kStageBytes = 2 * kSlabBytes;
-  static constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
   static constexpr int kRowBytes8 = D;           // fp8 row
   static constexpr int kSlabBytes8 = kSlab * kRowBytes8;
   static constexpr int kStageBytes8 = 2 * kSlabBytes8;
-  static constexpr int kSmemBytes8 = kWarps * kStages * kStageBytes8;
   static constexpr int kOutPer = D / 16;         // output dims per thread in the epilogue
+};
+
+// Per-warp ring depth and resident blocks per SM for each cache form,
+// measured on GB300 (same results bitwise, only the schedule differs):
+// - contiguous bf16: three stages at two blocks per SM (101.4 us on the
+//   contiguous decode workload; 104.9 us with two stages at three blocks);
+// - paged bf16 (2 KB pieces per 16-token page): two stages at three blocks
+//   (1218 us vs 1280 us on the paged decode workload, 2% at head_dim 128);
+// - contiguous fp8 at head_dim 64: two stages at five blocks (64 us vs
+//   65 us); paged fp8 keeps three stages at four blocks (639 us vs 651 us
+//   with five), as does head_dim 128 over fp8.
+template <int D, bool kPaged, bool kFp8>
+struct Ring {
+  static constexpr bool kFp8Wide = kFp8 && !kPaged && D == 64;
+  static constexpr int kStages = kFp8 ? (kFp8Wide ? 2 : 3) : (kPaged ? 2 : 3);
+  static constexpr int kBlocks = kFp8 ? (kFp8Wide ? 5 : 4) : (kPaged ? 3 : 2);
+  static constexpr int kSmemBytes =
+      kWarps * kStages * (kFp8 ? DCfg<D>::kStageBytes8 : DCfg<D>::kStageBytes);
+  // the warps' states are combined in the ring's memory after the loop
+  static_assert(kSmemBytes >= (2 + D) * kWarps * kMaxGroup * 4, "combine area");
 };
 
 struct Params {
@@ -146,8 +163,10 @@ __global__ void __launch_bounds__(256) zero_counters_kernel(unsigned int *c, int
 }
 
 template <int D, bool kPaged, bool kFp8>
-__global__ void __launch_bounds__(kThreads, kFp8 ? 4 : 2) decode_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8>::kBlocks))
+    decode_kernel(const Params p) {
   using C = DCfg<D>;
+  constexpr int kStages = Ring<D, kPaged, kFp8>::kStages;
   constexpr int kSlab = C::kSlab, kMT = C::kMT, kKS = C::kKS;
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -646,17 +665,16 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   const bool paged = a.block_table != nullptr;
   auto pick = [&](auto dim) {
     constexpr int D = decltype(dim)::value;
-    using C = DCfg<D>;
     if (a.fp8) {
       if (paged)
-        go(decode_kernel<D, true, true>, C::kSmemBytes8);
+        go(decode_kernel<D, true, true>, Ring<D, true, true>::kSmemBytes);
       else
-        go(decode_kernel<D, false, true>, C::kSmemBytes8);
+        go(decode_kernel<D, false, true>, Ring<D, false, true>::kSmemBytes);
     } else {
       if (paged)
-        go(decode_kernel<D, true, false>, C::kSmemBytes);
+        go(decode_kernel<D, true, false>, Ring<D, true, false>::kSmemBytes);
       else
-        go(decode_kernel<D, false, false>, C::kSmemBytes);
+        go(decode_kernel<D, false, false>, Ring<D, false, false>::kSmemBytes);
     }
   };
   if (a.head_dim == 128)

@@ -91,6 +91,15 @@ def prefill_pairs(case):
     return tot
 
 
+def prefill_io_bytes(case, kv_bytes):
+    """The prefill's other roofline (HBM): Q and the visible K/V read once,
+    out and lse written once, the sinks read. A short window makes the call
+    HBM- or latency-bound rather than tensor-bound, so both are reported."""
+    rows = sum(case.seqlens_q)
+    return (rows * case.hq * case.head_dim * 2 * 2 + kv_bytes + rows * case.hq * 4
+            + case.hq * 4)
+
+
 def prefill_flops(case):
     return 4 * case.head_dim * prefill_pairs(case) * case.hq
 
@@ -444,6 +453,7 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
     import torch
     res = {}
     burst = float(pk["bf16_tflops"])
+    hbm = float(pk["hbm_gbs"])
     # L2 flush between timed calls by READING 256 MB (twice the L2): a written
     # flush buffer would leave dirty lines whose write-back then lands inside
     # the next timed call (measured: +10 us on a 100 us decode)
@@ -482,10 +492,12 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         t = time_calls(call, 10, stream, flush)
         fl = prefill_flops(c)
         tokens = sum(c.seqlens_q)
+        io = prefill_io_bytes(c, c.k.numel() * 2 + c.v.numel() * 2)
         res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3, "tokens_per_s": tokens / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,
                      "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)",
-                     "flops": fl, "num_splits": "auto" if ns == 0 else ns}
+                     "flops": fl, "num_splits": "auto" if ns == 0 else ns,
+                     "io_bytes": io, "frac_of_hbm_peak": io / t / 1e9 / hbm}
         del c, out, lse, ws
         torch.cuda.empty_cache()
 
@@ -522,11 +534,13 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         t = time_calls(call, 10, stream, flush)
         fl = prefill_flops(c)
         kv = sum(c.seqlens_k) * c.hkv * c.head_dim * 2 * (1 if fp8 else 2)
+        io = prefill_io_bytes(c, kv)
         res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3,
                      "tokens_per_s": sum(c.seqlens_q) / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,
                      "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)",
-                     "flops": fl, "kv_bytes": kv}
+                     "flops": fl, "kv_bytes": kv,
+                     "io_bytes": io, "frac_of_hbm_peak": io / t / 1e9 / hbm}
         del c, out, lse, ws
         torch.cuda.empty_cache()
 
