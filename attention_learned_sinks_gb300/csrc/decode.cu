@@ -12,8 +12,9 @@
 //
 // Block = (split s, KV head g, sequence b), 4 warps. The block owns a chunk of
 // the visible keys; each warp streams 32-token slabs of K and V (slabs w,
-// w+4, ...) into its own 3-stage shared-memory ring with 16-byte cp.async
-// copies, so no block-wide barrier sits in the loop. All group query heads of
+// w+4, ...) into its own shared-memory ring (two or three stages, per cache
+// form) with 16-byte cp.async copies, so no block-wide barrier sits in the
+// loop. All group query heads of
 // KV head g (up to 8) are served from one read of each K/V byte:
 //
 //   S^T[16 tokens x 8 heads] = K[16 x 64] . Q^T   (mma.sync m16n8k16, N = heads)
