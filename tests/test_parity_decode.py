@@ -77,6 +77,27 @@ def test_decode_large_sink_and_empty(oracle_lib):
     assert torch.all(out[0] == 0) and torch.allclose(lse[0].cpu(), torch.full((8,), 60.0))
 
 
+# Unsplit calls with a visible span of at most 128 tokens run one warp per
+# (sequence, KV head); num_splits = 2 forces the four-warp blocks on the same
+# inputs. 7 sequences x 3 KV heads = 21 pairs leave three warps of the last
+# block without work.
+SHORT = [0, 1, 31, 100, 128, 33, 127]
+
+
+@pytest.mark.parametrize("paged,page_size", [(False, 16), (True, 16), (True, 7)])
+@pytest.mark.parametrize("window,d", [(0, 64), (77, 64), (0, 128), (64, 128)])
+def test_decode_one_warp_per_pair(oracle_lib, paged, page_size, window, d):
+    c = S.make_decode("pair", SHORT, 6, 3, seed=49 + window + d + page_size, window=window,
+                      sink_std=1.5, paged=paged, page_size=page_size, head_dim=d)
+    ro, rl = oracle_decode(oracle_lib, c)
+    for num_splits in (0, 2):
+        out, lse = run_decode(c, num_splits=num_splits)
+        check_close(out, lse, ro, rl, "pair paged=%s w=%d d=%d splits=%d"
+                    % (paged, window, d, num_splits))
+    e = SHORT.index(0)
+    assert torch.all(out[e] == 0)
+
+
 @pytest.mark.parametrize("window", [0, 16, 200])
 @pytest.mark.parametrize("page_size", [16, 32, 24])
 def test_decode_paged_small(oracle_lib, window, page_size):
