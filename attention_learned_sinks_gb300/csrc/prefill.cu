@@ -189,9 +189,11 @@ __device__ __forceinline__ float row_max32(const float (&sv)[32]) {
 }
 
 // 32 scores -> 2^(x c - m) as 16 fp16 pairs into pk[off..off+16); row sums into acc.
-// Exponentials on the special-function unit (ex2(-inf) = 0 for masked keys).
-// Measured on GB300: moving a share of them to an FMA-pipe polynomial made
-// this kernel slower (the softmax is bound by ALU/FMA issue, not by ex2).
+// Exponentials on the special-function unit (ex2(-inf) = 0 for masked keys),
+// which retires about 30 results per clock per SM on GB300. Moving a share of
+// them to an FMA-pipe polynomial made this kernel slower: the extra
+// instructions lengthen the softmax, which sits on each tile's dependency
+// chain (Q K^T -> softmax -> P V -> the next Q K^T into the same buffer).
 __device__ __forceinline__ void exp32(const float (&sv)[32], float2 c2, float2 nb2,
                                       float2 (&acc)[4], uint32_t (&pk)[32], int off) {
 #pragma unroll
