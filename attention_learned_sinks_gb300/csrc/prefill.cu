@@ -285,8 +285,9 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *total) {
 // One block: the list of non-empty (sequence b, query tile qt) pairs, ordered
 // by qt descending (the tiles with the most keys first under a causal mask),
 // and the zeroed work counter. Levels (one per qt) are counted, offset by a
-// block scan, then filled. Sequences longer than max_qtiles tiles are cut to
-// that bound (the host passes an upper bound on every length).
+// block scan, then filled. The host passes an upper bound on every length: a
+// sequence longer than max_qtiles tiles is cut to that bound and recorded in
+// the device error word (code 3).
 __global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_q, int batch,
                                                                int max_qtiles, unsigned *pairs,
                                                                int *num_pairs,
@@ -303,7 +304,9 @@ __global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_
     }
     __syncthreads();
     for (int b = tid; b < batch; b += blockDim.x) {
-      const int nq = min((cu_q[b + 1] - cu_q[b] + kBM - 1) / kBM, max_qtiles);
+      const int full = (cu_q[b + 1] - cu_q[b] + kBM - 1) / kBM;
+      if (full > max_qtiles) atomicExch(&g_prefill_error, kErrBadLength);
+      const int nq = min(full, max_qtiles);
       for (int qt = 0; qt < nq; ++qt) atomicAdd(&level_start[max_qtiles - 1 - qt], 1);
     }
     __syncthreads();
@@ -332,7 +335,9 @@ __global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_
   } else if (tid == 0) {
     int run = 0;
     for (int b = 0; b < batch; ++b) {
-      const int nq = min((cu_q[b + 1] - cu_q[b] + kBM - 1) / kBM, max_qtiles);
+      const int full = (cu_q[b + 1] - cu_q[b] + kBM - 1) / kBM;
+      if (full > max_qtiles) atomicExch(&g_prefill_error, kErrBadLength);
+      const int nq = min(full, max_qtiles);
       for (int qt = nq - 1; qt >= 0; --qt)
         pairs[run++] = (static_cast<unsigned>(b) << 16) | static_cast<unsigned>(qt);
     }

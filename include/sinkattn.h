@@ -88,7 +88,9 @@ const char *sinkattn_last_cuda_error(void);
  *   total_q, total_k            host copies of those last entries (bounds for
  *            the tensor maps that stage Q/K/V tiles).
  *   max_seqlen_q, max_seqlen_k  host upper bounds on any sequence's length
- *            (grid sizing only; a smaller bound silently drops rows).
+ *            (grid sizing). A query length above max_seqlen_q is cut to the
+ *            bound (the rows past it are not written) and recorded as code 3
+ *            in the device error word.
  *   sinks    float32 [hq] or NULL.
  *   num_splits     key-range splits (section "Kernels for GPT-OSS / Sink
  *            Attention": the KV sequence split into blocks, the sink in one
@@ -357,8 +359,10 @@ sinkattn_status_t sinkattn_prefill_backward(
  * runs out records a nonzero code here and the kernel returns early instead of
  * hanging. This call synchronises `stream`, copies the word to *code and
  * resets it to 0. Codes: 0 none; 1 a pipeline barrier wait timed out;
- * 2 a paged-prefill block-table entry was outside [0, num_pages); 3 a
- * paged-prefill key length was outside [0, max_seqlen_k].
+ * 2 a paged-prefill block-table entry was outside [0, num_pages); 3 a length
+ * above its host bound (a query length past max_seqlen_q in a prefill or
+ * backward call, a key length past max_seqlen_k in a backward call, a
+ * paged-prefill key length outside [0, max_seqlen_k]).
  */
 sinkattn_status_t sinkattn_get_device_error(void *stream, int *code);
 

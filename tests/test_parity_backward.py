@@ -120,3 +120,22 @@ def test_backward_varlen_full_config(window):
 
 def test_no_device_error_after_backward():
     assert sa.sinkattn_get_device_error() == 0
+
+
+def test_backward_key_length_above_bound_is_reported():
+    """A key length above the host's max_seqlen_k: the key-tile list is cut to
+    the bound and the device error word records code 3; dq, whose kernel walks
+    every key of its sequence, still matches the oracle."""
+    c = S.make_prefill("bbound", [300, 64], [300, 64], 8, 2, seed=95)
+    dout = S.bf16_normal(tuple(c.q.shape), 96)
+    args = (c.q.cuda(), c.k.cuda(), c.v.cuda())
+    cq, ck = c.cu_seqlens_q.cuda(), c.cu_seqlens_k.cuda()
+    out, lse = sa.sinkattn_prefill(*args, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
+                                   sinks=cuda(c.sinks), scale=c.scale)
+    assert sa.sinkattn_get_device_error() == 0
+    dq, dk, dv, ds = sa.sinkattn_prefill_backward(*args, out, lse, dout.cuda(), cq, ck,
+                                                  c.max_seqlen_q, 200, sinks=cuda(c.sinks),
+                                                  scale=c.scale)
+    assert sa.sinkattn_get_device_error() == 3
+    rq = reference(c, dout)[0]
+    check_grad(dq, rq, "dq with a short key bound")

@@ -261,3 +261,20 @@ def test_prefill_groups_of_three_full_config(oracle_lib):
     torch.cuda.synchronize()
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 16, 177), "varlen_prefill_g3")
     assert sa.sinkattn_get_device_error() == 0
+
+
+def test_prefill_length_above_bound_is_reported(oracle_lib):
+    """A query length above the host's max_seqlen_q: that sequence's tiles past
+    the bound are dropped and the device error word records code 3; the other
+    sequences are unaffected."""
+    c = S.make_prefill("bound", [300, 100], [300, 100], 8, 2, seed=93)
+    assert sa.sinkattn_get_device_error() == 0
+    out, lse = sa.sinkattn_prefill(c.q.cuda(), c.k.cuda(), c.v.cuda(), c.cu_seqlens_q.cuda(),
+                                   c.cu_seqlens_k.cuda(), 200, c.max_seqlen_k,
+                                   sinks=cuda(c.sinks))
+    assert sa.sinkattn_get_device_error() == 3
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out[:256], lse[:256], ro[:256], rl[:256], "rows within the bound")
+    check_close(out[300:], lse[300:], ro[300:], rl[300:], "the other sequence")
+    out, lse = run_prefill(c)
+    assert sa.sinkattn_get_device_error() == 0
