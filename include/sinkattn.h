@@ -201,25 +201,28 @@ sinkattn_status_t sinkattn_prefill_paged_fp8(
  * only). Block partials are merged by log-sum-exp inside the same launch: the
  * last block of each (sequence, KV head) to finish merges them.
  *
- *   q        bf16 [batch, hq, 64]. The query sits at position Lk_b - 1.
+ *   q        bf16 [batch, hq, D]. The query sits at position Lk_b - 1.
  * Contiguous cache (block_table == NULL):
- *   k_cache, v_cache  bf16 [kv_rows, hkv, 64]; sequence b owns rows
+ *   k_cache, v_cache  bf16 [kv_rows, hkv, D]; sequence b owns rows
  *            kv_indptr[b]..kv_indptr[b+1]; kv_indptr int32 [batch+1], device,
  *            starting at 0; kv_rows = kv_indptr[batch] (host copy).
  *            seqlens_k must be NULL.
  * Paged cache (page "Fast embeddings on GPUs", section "ROSE": paged decode):
- *   k_cache, v_cache  bf16 [kv_rows, hkv, page_size, 64]; kv_rows = number of
+ *   k_cache, v_cache  bf16 [kv_rows, hkv, page_size, D]; kv_rows = number of
  *            pages. block_table int32 [batch, max_pages_per_seq], device:
  *            key j of sequence b is slot j % page_size of page
  *            block_table[b][j / page_size]. seqlens_k int32 [batch], device.
  *            kv_indptr must be NULL. Any page_size >= 1 works; 16 is the
- *            tested serving layout.
+ *            tested serving layout. The caller guarantees every entry the
+ *            lengths reach is in [0, kv_rows) and seqlens_k[b] <=
+ *            max_pages_per_seq * page_size: the decode kernel does not check
+ *            them (checks measured 3-13% slower on the paged workloads).
  *   max_seqlen_k   host upper bound on Lk_b (sizes the split grid).
  *   num_splits     0 = automatic; n > 0 = split the longest sequence into
  *            about n blocks (shorter ones get proportionally fewer).
  *   hq / hkv must be at most 8 (one KV head and all its query heads per block).
  *   head_dim 64 or 128. q, out and every K/V row have head_dim elements.
- *   out      bf16 [batch, hq, 64];  lse float32 [batch, hq] or NULL.
+ *   out      bf16 [batch, hq, D];  lse float32 [batch, hq] or NULL.
  *   workspace      device scratch of at least sinkattn_decode_workspace_size()
  *            bytes for the same (batch, max_seqlen_k, hq, hkv, head_dim,
  *            window, num_splits), 256-byte aligned; its contents need not be
