@@ -29,6 +29,10 @@ sinkattn_status_t from_cuda(cudaError_t e) {
 
 }  // namespace
 
+namespace sinkattn {
+int cuda_status(cudaError_t e) { return from_cuda(e); }
+}  // namespace sinkattn
+
 extern "C" {
 
 const char *sinkattn_last_cuda_error(void) {

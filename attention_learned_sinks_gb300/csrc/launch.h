@@ -9,6 +9,10 @@ namespace sinkattn {
 
 constexpr int kHeadDim = 64;
 
+// Status code of the C ABI for a CUDA result (0 = ok); a failure is recorded
+// as the calling thread's last CUDA error (sinkattn_last_cuda_error).
+int cuda_status(cudaError_t e);
+
 // ---- decode ----------------------------------------------------------------
 // Split plan: the visible KV range of every (sequence, KV head) is cut into
 // blocks of `chunk` tokens; max_splits bounds the block count of any sequence.

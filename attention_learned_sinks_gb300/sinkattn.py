@@ -19,6 +19,8 @@ SINKATTN_ERR_INVALID_ARGUMENT = 1
 SINKATTN_ERR_UNSUPPORTED = 2
 SINKATTN_ERR_WORKSPACE_TOO_SMALL = 3
 SINKATTN_ERR_CUDA = 4
+# size of the fixed scratch array behind sinkattn_decode_noalloc (as in the header)
+SINKATTN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTED = (
     "sinkattn_status_string",

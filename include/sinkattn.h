@@ -282,8 +282,12 @@ sinkattn_status_t sinkattn_decode_fp8(const void *q, const void *k_cache, const 
  *    arguments) exceeds SINKATTN_NOALLOC_SCRATCH_BYTES is rejected with
  *    SINKATTN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (an
  *    explicit, smaller num_splits shrinks the scratch a batch needs).
- *  - The first call on each device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *  - The first call in each CUDA context (normally each device's primary
+ *    context) looks up the array's device address with that context current;
+ *    make that first call before any stream capture. A context created
+ *    later (e.g. after cudaDeviceReset) gets its own lookup on its first call.
+ *  - Failures of that lookup or of the launch return SINKATTN_ERR_CUDA and
+ *    are reported by sinkattn_last_cuda_error, as for the other calls.
  *  - All calls on a device share the array and it keeps the last call's
  *    contents (counters are cleared on the stream by each call). Calls whose
  *    work can overlap on the GPU, e.g. on unordered streams, race on it.

@@ -14,7 +14,7 @@ import torch
 
 import attention_learned_sinks_gb300 as sa
 from attention_learned_sinks_gb300 import synthetic as S
-from helpers import check_close, to_np
+from helpers import check_pair
 
 pytestmark = pytest.mark.gpu
 
@@ -89,8 +89,8 @@ def test_decode_equals_last_prefill_row(window):
     out_d, lse_d = sa.sinkattn_decode(q_last.cuda(), p.k.cuda(), p.v.cuda(),
                                       kv_indptr=p.cu_seqlens_k.cuda(), max_seqlen_k=max(lens),
                                       sinks=p.sinks.cuda(), window=window)
-    check_close(out_d, lse_d, to_np(out_p[last.cuda()]), to_np(lse_p[last.cuda()]),
-                "decode vs last prefill row w=%d" % window)
+    check_pair(out_d, lse_d, out_p[last.cuda()], lse_p[last.cuda()],
+               "decode vs last prefill row w=%d" % window)
 
 
 def test_decode_independent_of_split_count():
@@ -98,7 +98,7 @@ def test_decode_independent_of_split_count():
     ref_o, ref_l = _decode_contig(c, 1)
     for ns in (2, 5, 17, 64):
         o, l = _decode_contig(c, ns)
-        check_close(o, l, to_np(ref_o), to_np(ref_l), "splits %d vs 1" % ns)
+        check_pair(o, l, ref_o, ref_l, "splits %d vs 1" % ns)
 
 
 def test_repeated_calls_are_bitwise_identical():

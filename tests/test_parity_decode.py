@@ -145,14 +145,15 @@ def test_decode_contig_full_config(oracle_lib):
 @pytest.mark.parametrize("window", [0, 128])
 def test_decode_paged_full_config(oracle_lib, window):
     """256 sequences, contexts uniform in [1024, 32768], 16-token pages with a
-    permuted block table: the whole batch on the GPU, sampled sequences
-    (all heads) against the oracle."""
+    permuted block table: the whole batch on the GPU; against the oracle, every
+    sequence (all heads) with the 128-token window and 64 sampled sequences
+    (all heads) without it."""
     c = S.paged_decode(window=window, device="cuda")
     out, lse = sa.sinkattn_decode(c.q, c.k_cache, c.v_cache, block_table=c.block_table.cuda(),
                                   seqlens_k=c.seqlens_k_t.cuda(), max_seqlen_k=c.max_seqlen_k,
                                   sinks=c.sinks.cuda(), window=window, scale=c.scale)
     torch.cuda.synchronize()
-    seqs = _sample_seqs(c.batch, 6, 51)
+    seqs = _sample_seqs(c.batch, 62, 51) if window == 0 else list(range(c.batch))
     # compact copy of the sampled sequences' pages for the oracle
     tabs, lens, pages = [], [], []
     at = 0

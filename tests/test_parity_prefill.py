@@ -146,6 +146,23 @@ def _sample_rows(c, per_seq, seed):
     return np.array(rows, dtype=np.int32)
 
 
+def _every_item_rows(c, seed):
+    """One random row of every (sequence, 128-row query tile, query head) in
+    the call, plus every head of each sequence's first and last row: every
+    work item the kernel schedules (a tile and its heads) is checked, ragged
+    last tiles included."""
+    g = torch.Generator().manual_seed(seed)
+    rows = []
+    for b, lq in enumerate(c.seqlens_q):
+        for qt in range((lq + 127) // 128):
+            n = min(128, lq - qt * 128)
+            pick = torch.randint(0, n, (c.hq,), generator=g).tolist()
+            rows += [(b, h, qt * 128 + i) for h, i in enumerate(pick)]
+        if lq > 0:
+            rows += [(b, h, i) for i in sorted({0, lq - 1}) for h in range(c.hq)]
+    return np.array(sorted(set(rows)), dtype=np.int32)
+
+
 def _check_rows(oracle, c, out, lse, rows, what):
     ro, rl = oracle.attention_rows(rows, c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k, hq=c.hq,
                                    hkv=c.hkv, head_dim=c.head_dim, sinks=c.sinks, causal=c.causal,
@@ -159,11 +176,14 @@ def _check_rows(oracle, c, out, lse, rows, what):
 @pytest.mark.parametrize("window", [0, 128])
 def test_prefill_varlen_full_config(oracle_lib, window):
     """16 sequences, lengths uniform in [512, 4096], 64 q / 8 kv heads, causal;
-    full and sliding window 128. Sampled rows against the oracle."""
+    full and sliding window 128. Every output row and head against the
+    oracle."""
     c = S.varlen_prefill(window=window)
     out, lse = run_prefill(c)
     torch.cuda.synchronize()
-    _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 24, 71), "varlen_prefill w=%d" % window)
+    ro, rl = oracle_prefill(oracle_lib, c)
+    check_close(out, lse, ro, rl, "varlen_prefill w=%d (every row)" % window)
+    assert sa.sinkattn_get_device_error() == 0
 
 
 def test_prefill_long_context_auto_splits(oracle_lib):
@@ -190,10 +210,12 @@ def test_prefill_long_context_auto_splits(oracle_lib):
 
 def test_prefill_chunked_full_config(oracle_lib):
     """4096 query tokens at positions 126976..131071 of a 131072-token causal
-    context. Sampled rows against the oracle."""
+    context. One row of every (query tile, head) item, and sampled rows,
+    against the oracle."""
     c = S.chunked_prefill()
     out, lse = run_prefill(c)
     torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _every_item_rows(c, 72), "chunked_prefill items")
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 40, 73), "chunked_prefill")
 
 
@@ -244,21 +266,24 @@ def test_prefill_head_dim_128_splits(oracle_lib, shape, num_splits):
 
 
 def test_prefill_head_dim_128_varlen_full_config(oracle_lib):
-    """varlen_prefill's lengths and heads at head_dim 128. Sampled rows against
-    the oracle."""
+    """varlen_prefill's lengths and heads at head_dim 128. One row of every
+    (query tile, head) item, and sampled rows, against the oracle."""
     c = S.varlen_prefill_d128()
     out, lse = run_prefill(c)
     torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _every_item_rows(c, 138), "varlen_prefill_d128 items")
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 16, 139), "varlen_prefill_d128")
     assert sa.sinkattn_get_device_error() == 0
 
 
 def test_prefill_groups_of_three_full_config(oracle_lib):
     """varlen_prefill's lengths with 24 q / 8 kv heads: one head per work
-    item, two CTAs per SM. Sampled rows against the oracle."""
+    item, two CTAs per SM. One row of every (query tile, head) item, and
+    sampled rows, against the oracle."""
     c = S.varlen_prefill_g3()
     out, lse = run_prefill(c)
     torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _every_item_rows(c, 176), "varlen_prefill_g3 items")
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 16, 177), "varlen_prefill_g3")
     assert sa.sinkattn_get_device_error() == 0
 

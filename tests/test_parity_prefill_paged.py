@@ -151,6 +151,19 @@ def _sample_rows(c, per_seq, seed):
     return np.array(rows, dtype=np.int32)
 
 
+def _every_item_rows(c, seed):
+    """One random row of every (sequence, 128-row query tile, query head): every
+    work item of the call, ragged last tiles included."""
+    g = torch.Generator().manual_seed(seed)
+    rows = []
+    for b, lq in enumerate(c.seqlens_q):
+        for qt in range((lq + 127) // 128):
+            n = min(128, lq - qt * 128)
+            pick = torch.randint(0, n, (c.hq,), generator=g).tolist()
+            rows += [(b, h, qt * 128 + i) for h, i in enumerate(pick)]
+    return np.array(rows, dtype=np.int32)
+
+
 def _check_rows(oracle, c, out, lse, rows, what):
     ro, rl = oracle.attention_rows(rows, c.q, c.k_cache, c.v_cache, c.cu_seqlens_q,
                                    block_table=c.block_table, seqlens_k=c.seqlens_k_t, hq=c.hq,
@@ -164,18 +177,23 @@ def _check_rows(oracle, c, out, lse, rows, what):
 
 def test_paged_chunked_prefill_full_config(oracle_lib):
     """4096 queries at the end of a 131072-token context held in 16-token pages
-    under a permuted block table. Sampled rows against the oracle."""
+    under a permuted block table. One row of every (query tile, head) item,
+    and sampled rows, against the oracle."""
     c = S.paged_chunked_prefill()
     out, lse = run_paged(c)
     torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _every_item_rows(c, 92), "paged_chunked_prefill items")
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 40, 93), "paged_chunked_prefill")
 
 
 def test_paged_prefill_batch_full_config(oracle_lib):
-    """16 sequences, new chunks of 256..2048 tokens after 1k..32k cached tokens."""
+    """16 sequences, new chunks of 256..2048 tokens after 1k..32k cached tokens.
+    One row of every (query tile, head) item, and sampled rows, against the
+    oracle."""
     c = S.paged_prefill_batch()
     out, lse = run_paged(c)
     torch.cuda.synchronize()
+    _check_rows(oracle_lib, c, out, lse, _every_item_rows(c, 94), "paged_prefill_batch items")
     _check_rows(oracle_lib, c, out, lse, _sample_rows(c, 12, 95), "paged_prefill_batch")
     assert sa.sinkattn_get_device_error() == 0
 
