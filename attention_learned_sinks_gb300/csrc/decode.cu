@@ -64,10 +64,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Shapes for head dimension D (64 or 128). A warp step covers kSlab tokens:
 // 32 at D = 64, 16 at D = 128, so that a slab of K and V is the same number
 // of bytes for both: 8 KB per stage for bf16, 4 KB for fp8 (ring depths
-// and blocks per SM in Ring below).
-template <int D>
+// and blocks per SM in Ring below). kHalfSlab: 16-token steps at D = 64 too
+// (the one-warp-per-pair bf16 form, whose rings must be small).
+template <int D, bool kHalfSlab = false>
 struct DCfg {
-  static constexpr int kSlab = D == 64 ? 32 : 16;
+  static constexpr int kSlab = D == 64 && !kHalfSlab ? 32 : 16;
   static constexpr int kMT = kSlab / 16;         // 16-token m-tiles per slab
   static constexpr int kKS = D / 16;             // k-steps of Q K^T, dim tiles of P V
   static constexpr int kRowBytes = D * 2;        // bf16 row
@@ -87,14 +88,21 @@ struct DCfg {
 //   (1218 us vs 1280 us on the paged decode workload, 2% at head_dim 128);
 // - contiguous fp8 at head_dim 64: two stages at five blocks (64 us vs
 //   65 us); paged fp8 keeps three stages at four blocks (639 us vs 651 us
-//   with five), as does head_dim 128 over fp8.
-template <int D, bool kPaged, bool kFp8>
+//   with five), as does head_dim 128 over fp8;
+// - one warp per pair, bf16 at head_dim 64: three stages of 16 tokens (4 KB)
+//   at four blocks per SM. The paged window-128 workload (2048 pairs, 512
+//   blocks) then runs in one wave of 608 block slots instead of two of 456
+//   with 32-token slabs at three blocks.
+template <int D, bool kPaged, bool kFp8, bool kPair = false>
 struct Ring {
+  static constexpr bool kHalfSlab = kPair && !kFp8 && D == 64;
+  using C = DCfg<D, kHalfSlab>;
   static constexpr bool kFp8Wide = kFp8 && !kPaged && D == 64;
-  static constexpr int kStages = kFp8 ? (kFp8Wide ? 2 : 3) : (kPaged ? 2 : 3);
-  static constexpr int kBlocks = kFp8 ? (kFp8Wide ? 5 : 4) : (kPaged ? 3 : 2);
-  static constexpr int kSmemBytes =
-      kWarps * kStages * (kFp8 ? DCfg<D>::kStageBytes8 : DCfg<D>::kStageBytes);
+  static constexpr int kStages =
+      kHalfSlab ? 3 : kFp8 ? (kFp8Wide ? 2 : 3) : (kPaged ? 2 : 3);
+  static constexpr int kBlocks =
+      kHalfSlab ? 4 : kFp8 ? (kFp8Wide ? 5 : 4) : (kPaged ? 3 : 2);
+  static constexpr int kSmemBytes = kWarps * kStages * (kFp8 ? C::kStageBytes8 : C::kStageBytes);
   // the warps' states are combined in the ring's memory after the loop (in
   // the one-warp-per-pair form each warp uses its own quarter)
   static_assert(kSmemBytes >= (2 + D) * kWarps * kMaxGroup * 4, "combine area");
@@ -175,10 +183,11 @@ __global__ void __launch_bounds__(256) zero_counters_kernel(unsigned int *c, int
 // four warps per pair a 128-token window gives each warp a single slab, and
 // the many short blocks run in latency-bound waves.
 template <int D, bool kPaged, bool kFp8, bool kPair>
-__global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8>::kBlocks))
+__global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBlocks))
     decode_kernel(const Params p) {
-  using C = DCfg<D>;
-  constexpr int kStages = Ring<D, kPaged, kFp8>::kStages;
+  using R = Ring<D, kPaged, kFp8, kPair>;
+  using C = typename R::C;
+  constexpr int kStages = R::kStages;
   constexpr int kSlab = C::kSlab, kMT = C::kMT, kKS = C::kKS;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -217,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8>::kBlocks))
   const int t1 = min(L, t0 + chunk);
   const int nslab = (max(0, t1 - t0) + kSlab - 1) / kSlab;
 
-  __shared__ int s_pages[kPaged ? kMaxBlockPages : 1];
+  __shared__ int s_pages[kPaged && !kPair ? kMaxBlockPages : 1];
   int pg0 = 0;
   bool staged = false;
   if (kPaged && !kPair) {
@@ -301,12 +310,13 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8>::kBlocks))
       }
       return;
     }
-    // kSlab rows of D/8 chunks: 256 chunks, eight per lane
+    // kSlab rows of D/8 chunks: 256 chunks, eight per lane (128, four per
+    // lane, in 16-token slabs at D = 64)
     constexpr int kCols = D / 8;
     const uint32_t kdst = wbase + (i % kStages) * C::kStageBytes;
     const uint32_t vdst = kdst + C::kSlabBytes;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < kSlab * kCols / 32; ++r) {
       const int idx = r * 32 + lane;
       const int row = idx / kCols, col = idx % kCols;
       const int j = slab0 + row;
@@ -748,14 +758,14 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
     constexpr bool P = decltype(one_pair)::value;
     if (a.fp8) {
       if (paged)
-        go(decode_kernel<D, true, true, P>, Ring<D, true, true>::kSmemBytes);
+        go(decode_kernel<D, true, true, P>, Ring<D, true, true, P>::kSmemBytes);
       else
-        go(decode_kernel<D, false, true, P>, Ring<D, false, true>::kSmemBytes);
+        go(decode_kernel<D, false, true, P>, Ring<D, false, true, P>::kSmemBytes);
     } else {
       if (paged)
-        go(decode_kernel<D, true, false, P>, Ring<D, true, false>::kSmemBytes);
+        go(decode_kernel<D, true, false, P>, Ring<D, true, false, P>::kSmemBytes);
       else
-        go(decode_kernel<D, false, false, P>, Ring<D, false, false>::kSmemBytes);
+        go(decode_kernel<D, false, false, P>, Ring<D, false, false, P>::kSmemBytes);
     }
   };
   auto pick = [&](auto dim) {
@@ -794,20 +804,65 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SINKATTN_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch for one device, looked up once while
-// that device is current (the host-side symbol is not a device address).
-cudaError_t noalloc_scratch(int device, void **ptr) {
+// Device address of g_noalloc_scratch in the calling thread's current
+// context, looked up once per context with that context's device current (the
+// host-side symbol is not a device address). The cache is keyed by the
+// driver's context id, which is never reused within a process, so a context
+// created after cudaDeviceReset (where the module, and so the array, may sit
+// at another address) gets a fresh lookup.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// *id = the current context's id, or 0 when no context is current yet.
+cudaError_t current_context_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  *id = 0;
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+cudaError_t noalloc_scratch(void **ptr) {
   static std::mutex mu;
-  static void *addr[256] = {};
-  if (device < 0 || device >= 256) return cudaErrorInvalidDevice;
+  static unsigned long long ids[64] = {};
+  static void *addr[64] = {};
+  static int used = 0, next = 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[device] == nullptr) {
-    void *p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    addr[device] = p;
-  }
-  *ptr = addr[device];
+  unsigned long long id = 0;
+  cudaError_t e = current_context_id(&id);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; id != 0 && i < used; ++i)
+    if (ids[i] == id) {
+      *ptr = addr[i];
+      return cudaSuccess;
+    }
+  // The lookup makes the current device's primary context current if no
+  // context was, so the id is read again after it.
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e == cudaSuccess) e = current_context_id(&id);
+  if (e != cudaSuccess) return e;
+  if (id == 0) return cudaErrorDeviceUninitialized;
+  const int slot = used < 64 ? used++ : (next++ & 63);  // past 64 contexts, recycle entries
+  ids[slot] = id;
+  addr[slot] = p;
+  *ptr = p;
   return cudaSuccess;
 }
 
@@ -847,10 +902,9 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
       decode_workspace_layout(batch, hq, hkv, plan, head_dim).bytes >
           SINKATTN_NOALLOC_SCRATCH_BYTES)
     return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) return SINKATTN_ERR_CUDA;
   void *scratch = nullptr;
-  if (noalloc_scratch(device, &scratch) != cudaSuccess) return SINKATTN_ERR_CUDA;
+  const cudaError_t se = noalloc_scratch(&scratch);
+  if (se != cudaSuccess) return static_cast<sinkattn_status_t>(cuda_status(se));
   DecodeLaunch a;
   a.q = q;
   a.k = k_cache;
@@ -872,6 +926,5 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
   a.workspace = scratch;
   a.plan = plan;
   a.head_dim = head_dim;
-  return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
-                                                                             : SINKATTN_ERR_CUDA;
+  return static_cast<sinkattn_status_t>(cuda_status(launch_decode(a, static_cast<cudaStream_t>(stream))));
 }
