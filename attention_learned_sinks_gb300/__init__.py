@@ -10,6 +10,7 @@ from .sinkattn import (  # noqa: F401
     load,
     sinkattn_decode,
     sinkattn_decode_fp8,
+    sinkattn_debug_stall_waits,
     sinkattn_decode_workspace_size,
     sinkattn_get_device_error,
     sinkattn_merge,

@@ -432,6 +432,12 @@ sinkattn_status_t sinkattn_prefill_backward(
   return from_cuda(e);
 }
 
+sinkattn_status_t sinkattn_debug_stall_waits(uint64_t limit_ns) {
+  cudaError_t e = prefill_set_stall(limit_ns);
+  if (e == cudaSuccess) e = backward_set_stall(limit_ns);
+  return from_cuda(e);
+}
+
 sinkattn_status_t sinkattn_get_device_error(void *stream, int *code) {
   if (code == nullptr) return SINKATTN_ERR_INVALID_ARGUMENT;
   *code = 0;

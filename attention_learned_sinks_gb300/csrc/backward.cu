@@ -32,6 +32,8 @@
 // accumulation is fp32. Every mbarrier wait is bounded.
 #include <math.h>
 
+#include <atomic>
+
 #include "launch.h"
 #include "ptx.cuh"
 #include "tma_host.h"
@@ -51,6 +53,8 @@ constexpr uint64_t kTileDesc = kTileBytes >> 4;        // one tile in descriptor
 constexpr uint64_t kRows16Desc = (16 * 128) >> 4;      // 16 rows of 128 B
 
 __device__ int g_backward_error;
+// testing hook (sinkattn_debug_stall_waits): stall_ns of later launches
+std::atomic<uint64_t> g_bwd_stall_ns{0};
 
 struct BwdParams {
   const int32_t *cu_q, *cu_k;
@@ -63,6 +67,10 @@ struct BwdParams {
   const int *num_q_pairs, *num_k_pairs;
   unsigned *q_counter, *k_counter;  // work counters of the persistent kernels (zeroed by the lists)
   __nv_bfloat16 *dq, *dk, *dv;
+  // Testing hook (0: off): the dQ kernel's softmax-side warps wait at most
+  // stall_ns on a barrier that nothing completes before their first scores,
+  // so that every CTA of that kernel takes its timeout path.
+  uint64_t stall_ns;
 };
 
 // ----------------------------------------------------------------- prep ---
@@ -227,6 +235,7 @@ struct DqBars {
   uint64_t pds_free;  // dQ / Y of the tile have read dS, P
   uint64_t dq_done, dq_free, drain[2];
   uint64_t dsum_full[2];  // both warpgroups' partial sums of an item are in dsum
+  uint64_t never;         // testing hook: a barrier nothing completes
   uint32_t tmem_base;
   int abort;
   DqTile tiles[2];
@@ -294,6 +303,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bars->dq_free, 256);
     mbar_init(&bars->dsum_full[0], 256);
     mbar_init(&bars->dsum_full[1], 256);
+    mbar_init(&bars->never, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -451,7 +461,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t t_ds = tmem + lane_off + 256 + 32 * wg, t_p = t_ds + 64;
     const uint32_t t_dq = tmem + lane_off + 384 + 32 * wg, t_y = t_dq + 64;
     int G = 0, dq_items = 0;
-    bool ok = true;
+    // testing hook: a wait that runs out while the first copies and products
+    // are in flight
+    bool ok = p.stall_ns == 0 || mbar_wait_warp(&bars->never, 0, abort, err, false, p.stall_ns);
     for (int nt = 0; ok; ++nt) {
       const int slot = nt & 1;
       if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
@@ -1016,6 +1028,7 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
   p.num_k_pairs = reinterpret_cast<const int *>(klist + 4);
   p.dq = static_cast<__nv_bfloat16 *>(a.dq);
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
+  p.stall_ns = g_bwd_stall_ns.load();
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
   if ((e = launch_tile_list(a.cu_q, a.batch, max_qtiles, reinterpret_cast<unsigned *>(qlist + 256),
                             reinterpret_cast<int *>(qlist + 4), reinterpret_cast<unsigned *>(qlist),
@@ -1074,6 +1087,11 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
       return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+cudaError_t backward_set_stall(uint64_t ns) {
+  g_bwd_stall_ns.store(ns);
   return cudaSuccess;
 }
 

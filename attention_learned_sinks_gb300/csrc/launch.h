@@ -129,5 +129,9 @@ cudaError_t backward_read_error(cudaStream_t stream, int *code);
 
 // Reads and clears the prefill kernel's device error word (synchronises stream).
 cudaError_t prefill_read_error(cudaStream_t stream, int *code);
+// Testing hook: prefill / backward kernels launched from now on make one wait
+// of at most ns nanoseconds on a barrier that nothing completes (0: off).
+cudaError_t prefill_set_stall(uint64_t ns);
+cudaError_t backward_set_stall(uint64_t ns);
 
 }  // namespace sinkattn

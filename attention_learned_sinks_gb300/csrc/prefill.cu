@@ -45,6 +45,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "launch.h"
@@ -144,6 +145,10 @@ struct Params {
   // stands for k_scale[g] * K_j: k_scale multiplies the softmax scale, and
   // v_scale the normalised output (it is linear in V).
   const float *k_scale, *v_scale;
+  // Testing hook (0: off): the softmax warps' first score wait of each CTA is
+  // preceded by a wait of at most stall_ns on a barrier that nothing
+  // completes, so that every CTA takes its timeout path.
+  uint64_t stall_ns;
 };
 
 // One unit of work: 128 query rows of sequence b for the NT heads h0...
@@ -165,6 +170,7 @@ struct Barriers {
   uint64_t o_free[2];                   // one phase per tile with keys: epilogue has read O_t
   uint64_t tile_full[2], tile_empty[2]; // tile descriptor ring
   uint64_t drain[2];
+  uint64_t never;                       // testing hook: a barrier nothing completes
   uint32_t tmem_base;
   int abort;
   Tile tiles[2];
@@ -389,6 +395,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_read[i], kBM);
     }
+    mbar_init(&bars->never, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -645,7 +652,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
     float4 *pend_slot = reinterpret_cast<float4 *>(smem + C::kOffPend) + threadIdx.x;
     float *pend_vs = reinterpret_cast<float *>(smem + C::kOffPendVs) + threadIdx.x;
     bool pend_on = false;
-    bool ok = true;
+    // testing hook: a wait that runs out while the first copies and products
+    // are in flight
+    bool ok = p.stall_ns == 0 ||
+              __all_sync(0xffffffffu, mbar_wait(&bars->never, 0, abort, &g_prefill_error, false,
+                                                p.stall_ns));
     auto finish = [&]() {  // epilogue of the pending tile
       const float4 st = *pend_slot;
       const float pm = st.x, pd = st.y;
@@ -885,6 +896,9 @@ cudaError_t launch_tile_list(const int32_t *cu, int batch, int max_tiles, unsign
 
 namespace {
 
+// testing hook (sinkattn_debug_stall_waits): stall_ns of later launches
+std::atomic<uint64_t> g_stall_ns{0};
+
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace pieces (head dimension d). Every piece starts on a 256-byte boundary.
@@ -1112,6 +1126,7 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   p.total_q = static_cast<int>(a.total_q);
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
+  p.stall_ns = g_stall_ns.load();
   uint8_t *part = sched + schedule_bytes(a.batch, a.total_q);
   p.part_o = splits > 1 ? reinterpret_cast<float *>(part) : nullptr;
   p.part_lse = splits > 1 ? reinterpret_cast<float *>(
@@ -1239,6 +1254,11 @@ cudaError_t launch_prefill_paged(const PrefillPagedLaunch &a, cudaStream_t strea
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_core(c, k_st, v_st, cap, cu_k, sched, stream, encode_failed);
+}
+
+cudaError_t prefill_set_stall(uint64_t ns) {
+  g_stall_ns.store(ns);
+  return cudaSuccess;
 }
 
 cudaError_t prefill_read_error(cudaStream_t stream, int *code) {

@@ -66,17 +66,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete. Bounded: returns false
 // (after storing kErrWaitTimeout into *err and raising *abort) if the phase
-// does not complete within kWaitLimitNs, or as soon as *abort is raised by
-// another thread of the CTA (unless `ignore_abort`, used to drain copies that
-// are already in flight before the CTA exits).
+// does not complete within limit_ns (default kWaitLimitNs), or as soon as
+// *abort is raised by another thread of the CTA (unless `ignore_abort`, used
+// to drain copies that are already in flight before the CTA exits).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          int *err, bool ignore_abort = false) {
+                                          int *err, bool ignore_abort = false,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (!ignore_abort && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicExch(err, kErrWaitTimeout);
       *abort = 1;
       return false;
@@ -304,8 +305,9 @@ __device__ __forceinline__ void tma_load_3d_elect(uint32_t dst, const CUtensorMa
 }
 // Warp-collective bounded wait: every lane waits, the result is the same in all lanes.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                               int *err, bool ignore_abort = false) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, ignore_abort));
+                                               int *err, bool ignore_abort = false,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, ignore_abort, limit_ns));
 }
 
 #define SINKATTN_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \

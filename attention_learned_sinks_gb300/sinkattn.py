@@ -38,6 +38,7 @@ EXPORTED = (
     "sinkattn_prefill_paged_fp8",
     "sinkattn_merge",
     "sinkattn_get_device_error",
+    "sinkattn_debug_stall_waits",
 )
 
 
@@ -107,6 +108,8 @@ def load(path: str = LIB_PATH):
     lib.sinkattn_merge.restype = I
     lib.sinkattn_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
     lib.sinkattn_get_device_error.restype = I
+    lib.sinkattn_debug_stall_waits.argtypes = [ctypes.c_uint64]
+    lib.sinkattn_debug_stall_waits.restype = I
     _LIB = lib
     return lib
 
@@ -444,3 +447,10 @@ def sinkattn_get_device_error(stream=None) -> int:
     _check(load().sinkattn_get_device_error(_stream(stream), ctypes.byref(code)),
            "sinkattn_get_device_error")
     return code.value
+
+
+def sinkattn_debug_stall_waits(limit_ns: int) -> None:
+    """Testing hook: later prefill / backward calls make one wait of at most
+    limit_ns on a barrier nothing completes, so every CTA takes its timeout
+    path (0 turns it off)."""
+    _check(load().sinkattn_debug_stall_waits(int(limit_ns)), "sinkattn_debug_stall_waits")

@@ -373,6 +373,21 @@ sinkattn_status_t sinkattn_prefill_backward(
  */
 sinkattn_status_t sinkattn_get_device_error(void *stream, int *code);
 
+/*
+ * Testing hook, not part of the computation: exercises the timeout path of
+ * the bounded waits. With limit_ns > 0, every prefill, paged prefill and
+ * backward call launched afterwards (in this process) makes one extra wait,
+ * before the first scores of each CTA (the backward: of its dQ kernel), on a
+ * barrier that nothing completes, bounded by limit_ns nanoseconds. Each CTA
+ * then does what any timed-out wait makes it do: records code 1 in the
+ * device error word, stops issuing work, waits (with the normal one-second
+ * bound) for the copies and tensor-core products it already issued,
+ * releases its tensor memory and exits. The outputs of such calls are
+ * unspecified. limit_ns = 0 turns the hook off. The setting is read at
+ * launch time (host side), so it is safe to change between launches.
+ */
+sinkattn_status_t sinkattn_debug_stall_waits(uint64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif
