@@ -370,9 +370,9 @@ sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_ls
 size_t sinkattn_prefill_backward_workspace_size(int batch, int64_t total_q, int64_t total_k,
                                                 int hq, int hkv, int head_dim) {
   if (batch < 0 || total_q < 0 || total_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 ||
-      head_dim != kHeadDim)
+      !backward_head_dim_ok(head_dim))
     return 0;
-  return backward_workspace_bytes(batch, total_q, total_k, hq, hkv);
+  return backward_workspace_bytes(batch, total_q, total_k, hq, hkv, head_dim);
 }
 
 sinkattn_status_t sinkattn_prefill_backward(
@@ -384,7 +384,7 @@ sinkattn_status_t sinkattn_prefill_backward(
   if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || hq <= 0 ||
       hkv <= 0 || hq % hkv != 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+  if (!backward_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   if (batch == 0 || (total_q == 0 && total_k == 0)) return SINKATTN_OK;
   if (!q || !k || !v || !out || !dout || !lse || !cu_seqlens_q || !cu_seqlens_k || !dq || !dk ||
       !dv)
@@ -396,9 +396,10 @@ sinkattn_status_t sinkattn_prefill_backward(
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (batch > 65535 || total_q > INT32_MAX || total_k > INT32_MAX ||
       (max_seqlen_q + 127) / 128 > 65535 || (max_seqlen_k + 127) / 128 > 65535 ||
-      (total_q / 128 + batch) * hq > INT32_MAX || (total_k / 128 + batch) * hkv > INT32_MAX)
+      (total_q / 128 + batch) * hq * (head_dim / 64) > INT32_MAX ||
+      (total_k / 128 + batch) * hkv * (head_dim / 64) > INT32_MAX)
     return SINKATTN_ERR_UNSUPPORTED;
-  const size_t need = backward_workspace_bytes(batch, total_q, total_k, hq, hkv);
+  const size_t need = backward_workspace_bytes(batch, total_q, total_k, hq, hkv, head_dim);
   if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 256)) return SINKATTN_ERR_INVALID_ARGUMENT;
   BackwardLaunch a;
@@ -426,6 +427,7 @@ sinkattn_status_t sinkattn_prefill_backward(
   a.dv = dv;
   a.dsinks = dsinks;
   a.workspace = workspace;
+  a.head_dim = head_dim;
   bool encode_failed = false;
   cudaError_t e = launch_backward(a, static_cast<cudaStream_t>(stream), &encode_failed);
   if (encode_failed) return SINKATTN_ERR_CUDA;

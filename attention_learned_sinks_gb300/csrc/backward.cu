@@ -26,6 +26,15 @@
 //     head, query tile) step, S^T = K Q^T and dP^T = V dO^T, P^T and dS^T in
 //     registers, dV += P^T dO and dK += dS^T Q with P^T / dS^T as TMEM A
 //     operands.
+// head_dim 128 (D = 128): the same kernels with items that also carry a
+// 64-dimension half h of the output gradient: S and dP run over all 128
+// dimensions (eight k-steps over two 64-column swizzle blocks), dQ, Y, dK and
+// dV accumulate dimensions 64h..64h+63 (the K, Q and dO tiles' block h as the
+// B operand), so the TMEM plan of D = 64 is kept; the two halves of one tile
+// recompute S and dP. The exact D of a row is then written to its own array
+// (both halves read the forward's D first). Shared memory: one Q/dO buffer
+// and a two-stage K/V ring (dQ), one K/V buffer and a two-stage Q/dO ring
+// (dK/dV).
 // Every gradient element is written by exactly one CTA (no atomics), so the
 // results are deterministic. All MMA operands are fp16 (bf16 inputs convert
 // exactly except below 2^-14, and P, dS in fp16 keep 11 significant bits);
@@ -43,14 +52,27 @@ namespace {
 
 constexpr int kBM = 128;                        // query rows per tile
 constexpr int kBN = 128;                        // keys per tile
-constexpr int kTileBytes = 128 * kHeadDim * 2;  // 16 KB
+constexpr int kBlockBytes = 128 * 64 * 2;       // 16 KB: 128 rows x 64 dims, one swizzle block
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// ts: A from TMEM, B MN-major in shared memory (dQ += dS K, ...). fp16 inputs.
-constexpr uint32_t kIdescTS = idesc_f32acc(128, kHeadDim, /*bf16=*/false, false, true);
-constexpr uint64_t kTileDesc = kTileBytes >> 4;        // one tile in descriptor units
+// ts: A from TMEM, B MN-major in shared memory (dQ += dS K, ...), 64 output
+// dimensions per product. fp16 inputs.
+constexpr uint32_t kIdescTS = idesc_f32acc(128, 64, /*bf16=*/false, false, true);
+constexpr uint64_t kBlockDesc = kBlockBytes >> 4;      // one 64-dim block in descriptor units
 constexpr uint64_t kRows16Desc = (16 * 128) >> 4;      // 16 rows of 128 B
+
+// one 128-row tile of one head at head dimension D (D / 64 swizzle blocks)
+template <int D>
+struct TileShape {
+  static constexpr int kHalves = D / 64;  // 64-dim halves of an output gradient
+  static constexpr int kBytes = 128 * D * 2;
+  static constexpr uint64_t kDesc = kBytes >> 4;
+};
+// k-step ks of a D-dim K-major product: swizzle block ks / 4, 32-byte step ks % 4
+__device__ __forceinline__ uint64_t kstep_off(int ks) {
+  return (ks >> 2) * kBlockDesc + 2 * (ks & 3);
+}
 
 __device__ int g_backward_error;
 // testing hook (sinkattn_debug_stall_waits): stall_ns of later launches
@@ -62,7 +84,8 @@ struct BwdParams {
   int total_q;
   float scale, scale_log2;
   const float *lse2t;  // [hq][total_q]: lse * log2(e) (+inf: row with no key and no sink)
-  float *dt;           // [hq][total_q]: D, from the forward output, then exact (dQ kernel)
+  float *dt;           // [hq][total_q]: D from the forward output
+  float *de;           // [hq][total_q]: exact D (dQ kernel; the same array as dt at D = 64)
   const unsigned *q_pairs, *k_pairs;
   const int *num_q_pairs, *num_k_pairs;
   unsigned *q_counter, *k_counter;  // work counters of the persistent kernels (zeroed by the lists)
@@ -74,14 +97,16 @@ struct BwdParams {
 };
 
 // ----------------------------------------------------------------- prep ---
-// Thread = 8 consecutive elements of one (row, head). Every iteration of the
-// block loop is uniform across the block, so the 8-lane shuffles always see
-// full warps.
+// Thread = 8 consecutive elements of one (row, head), D / 8 threads a row.
+// Every iteration of the block loop is uniform across the block, so the
+// D / 8-lane shuffles always see full warps.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_q_kernel(
     const uint4 *__restrict__ q, const uint4 *__restrict__ dout, const uint4 *__restrict__ out,
     const float *__restrict__ lse, int64_t total_q, int hq, uint4 *__restrict__ q16,
     uint4 *__restrict__ do16, float *__restrict__ lse2t, float *__restrict__ dt) {
-  const int64_t n = total_q * hq * 8;
+  constexpr int kPer = D / 8;  // threads per (row, head)
+  const int64_t n = total_q * hq * kPer;
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < n;
        base += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = base + threadIdx.x;
@@ -95,11 +120,10 @@ __global__ void __launch_bounds__(256) bwd_prep_q_kernel(
              bf16_lo(g.z) * bf16_lo(o.z) + bf16_hi(g.z) * bf16_hi(o.z) +
              bf16_lo(g.w) * bf16_lo(o.w) + bf16_hi(g.w) * bf16_hi(o.w);
     }
-    part += __shfl_xor_sync(0xffffffffu, part, 4);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    if (i < n && (i & 7) == 0) {
-      const int64_t rh = i >> 3;
+#pragma unroll
+    for (int o = kPer / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (i < n && (i % kPer) == 0) {
+      const int64_t rh = i / kPer;
       const int64_t row = rh / hq;
       const int h = static_cast<int>(rh % hq);
       const float l = lse[rh];
@@ -219,10 +243,24 @@ constexpr int kHalf = 64;  // keys (dK/dV: queries) of a tile per softmax warpgr
 // ss: both operands K-major in shared memory, 128 x 128 scores (S = Q K^T, ...)
 constexpr uint32_t kIdescSS128 = idesc_f32acc(128, kBN, /*bf16=*/false, false, false);
 constexpr int kDqThreads = 352;
-constexpr int kDqStages = 3;
+constexpr int kDqStages = 3;  // K/V ring at D = 64 (the array size of the barriers)
+
+// Shared memory of the dQ kernel: Q/dO buffers (two at D = 64, one at 128),
+// the K/V ring (three stages at 64, two at 128), then the control block.
+template <int D>
+struct DqCfg {
+  static constexpr int kTile = TileShape<D>::kBytes;
+  static constexpr int kQdBufs = D == 64 ? 2 : 1;
+  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kQdBufs * 2 * kTile;
+  static constexpr int kOffV = kOffK + kStages * kTile;
+  static constexpr int kOffBar = kOffV + kStages * kTile;
+  static constexpr int kSmem = kOffBar + 4096 + 1024;
+};
 
 struct DqTile {
-  int valid, b, qt, h, g, q0, lq, k0, lk, rows, p_min, kt_lo, n;
+  int valid, b, qt, h, g, q0, lq, k0, lk, rows, p_min, kt_lo, n, half;
 };
 
 struct DqBars {
@@ -242,15 +280,14 @@ struct DqBars {
   float dsum[2][2][128];  // [item parity][warpgroup][row]: partial exact D
 };
 
-constexpr int kDqOffQ = 0;                                // 2 buffers of Q and dO
-constexpr int kDqOffK = 4 * kTileBytes;
-constexpr int kDqOffV = kDqOffK + kDqStages * kTileBytes;
-constexpr int kDqOffBar = kDqOffV + kDqStages * kTileBytes;
 static_assert(sizeof(DqBars) <= 4096, "dQ control block");
-constexpr int kDqSmem = kDqOffBar + 4096 + 1024;
+static_assert(DqCfg<128>::kSmem <= 227 * 1024, "dQ shared memory at head_dim 128");
 
-// (sequence, query tile) list entry w / hq, head w % hq -> item
-__device__ __forceinline__ void dq_decode(const BwdParams &p, int w, DqTile &t) {
+// work index w -> item: 64-dim half w % halves of the output, then
+// (sequence, query tile) list entry (w / halves) / hq and head (w / halves) % hq
+__device__ __forceinline__ void dq_decode(const BwdParams &p, int halves, int w, DqTile &t) {
+  t.half = w % halves;
+  w /= halves;
   const unsigned e = p.q_pairs[w / p.hq];
   t.valid = 1;
   t.h = w % p.hq;
@@ -271,15 +308,21 @@ __device__ __forceinline__ void dq_decode(const BwdParams &p, int w, DqTile &t) 
   t.n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - t.kt_lo : 0;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
+  using C = DqCfg<D>;
+  constexpr int kTileBytes = C::kTile;
+  constexpr uint64_t kTileDesc = TileShape<D>::kDesc;
+  constexpr int kHalves = TileShape<D>::kHalves;
+  constexpr int kQdBufs = C::kQdBufs, kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
-  DqBars *bars = reinterpret_cast<DqBars *>(smem_raw + (sbase - raw) + kDqOffBar);
+  DqBars *bars = reinterpret_cast<DqBars *>(smem_raw + (sbase - raw) + C::kOffBar);
   volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int *err = &g_backward_error;
@@ -295,7 +338,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bars->s_read, 256);
     mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->pds_free, 1);
-    for (int s = 0; s < kDqStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);  // both MMA warps
     }
@@ -322,7 +365,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    const int num_work = *p.num_q_pairs * p.hq;
+    const int num_work = *p.num_q_pairs * p.hq * kHalves;
+    // one tile = D / 64 boxes of 64 dims into consecutive swizzle blocks
+    auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint64_t *bar, int head, int row) {
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d_elect(dst + blk * kBlockBytes, map, bar, blk * 64, head, row);
+    };
     int J = 0, nq = 0;
     bool ok = true;
     for (int nt = 0; ok; ++nt) {
@@ -333,7 +382,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         DqTile t;
         t.valid = 0;
         const int w = static_cast<int>(atomicAdd(p.q_counter, 1u));
-        if (w < num_work) dq_decode(p, w, t);
+        if (w < num_work) dq_decode(p, kHalves, w, t);
         bars->tiles[slot] = t;
         mbar_arrive(&bars->tile_full[slot]);
       }
@@ -341,34 +390,34 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const DqTile t = bars->tiles[slot];
       if (!t.valid) break;
       if (t.n == 0) continue;  // nothing to load (and no MMAs) for this item
-      const int qb = nq & 1;
-      if (nq >= 2 && !mbar_wait_warp(&bars->qd_empty[qb], ((nq >> 1) - 1) & 1, abort, err)) break;
+      const int qb = nq % kQdBufs;
+      if (nq >= kQdBufs &&
+          !mbar_wait_warp(&bars->qd_empty[qb], ((nq / kQdBufs) - 1) & 1, abort, err))
+        break;
       mbar_arrive_expect_tx_elect(&bars->qd_full[qb], 2 * kTileBytes);
-      tma_load_3d_elect(sbase + kDqOffQ + qb * 2 * kTileBytes, &tm_q, &bars->qd_full[qb], 0, t.h,
-                        t.q0 + t.qt * kBM);
-      tma_load_3d_elect(sbase + kDqOffQ + (qb * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[qb], 0,
-                        t.h, t.q0 + t.qt * kBM);
+      load_tile(sbase + C::kOffQ + qb * 2 * kTileBytes, &tm_q, &bars->qd_full[qb], t.h,
+                t.q0 + t.qt * kBM);
+      load_tile(sbase + C::kOffQ + (qb * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[qb], t.h,
+                t.q0 + t.qt * kBM);
       ++nq;
       for (int j = 0; j < t.n; ++j, ++J) {
-        const int st = J % kDqStages;
-        if (J >= kDqStages &&
-            !mbar_wait_warp(&bars->kv_empty[st], ((J / kDqStages) - 1) & 1, abort, err)) {
+        const int st = J % kStages;
+        if (J >= kStages &&
+            !mbar_wait_warp(&bars->kv_empty[st], ((J / kStages) - 1) & 1, abort, err)) {
           ok = false;
           break;
         }
         const int row = t.k0 + (t.kt_lo + j) * kBN;
         mbar_arrive_expect_tx_elect(&bars->kv_full[st], 2 * kTileBytes);
-        tma_load_3d_elect(sbase + kDqOffK + st * kTileBytes, &tm_k, &bars->kv_full[st], 0, t.g,
-                          row);
-        tma_load_3d_elect(sbase + kDqOffV + st * kTileBytes, &tm_v, &bars->kv_full[st], 0, t.g,
-                          row);
+        load_tile(sbase + C::kOffK + st * kTileBytes, &tm_k, &bars->kv_full[st], t.g, row);
+        load_tile(sbase + C::kOffV + st * kTileBytes, &tm_v, &bars->kv_full[st], t.g, row);
       }
     }
     if (*abort) {  // copies already issued still land here: wait for them (bounded)
-      for (int i = max(0, nq - 2); i < nq; ++i)
-        mbar_wait_warp(&bars->qd_full[i & 1], (i >> 1) & 1, abort, err, true);
-      for (int i = max(0, J - kDqStages); i < J; ++i)
-        mbar_wait_warp(&bars->kv_full[i % kDqStages], (i / kDqStages) & 1, abort, err, true);
+      for (int i = max(0, nq - kQdBufs); i < nq; ++i)
+        mbar_wait_warp(&bars->qd_full[i % kQdBufs], (i / kQdBufs) & 1, abort, err, true);
+      for (int i = max(0, J - kStages); i < J; ++i)
+        mbar_wait_warp(&bars->kv_full[i % kStages], (i / kStages) & 1, abort, err, true);
     }
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------------ MMA
@@ -377,13 +426,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // dP = dO V^T of a key tile (N = 128) as soon as both softmax warpgroups
     // have loaded the previous tile's; warp 10 issues dQ += dS K and
     // Y += P K once they have written dS and P.
-    const uint64_t kdesc0 = sdesc_sw128(sbase + kDqOffK);
+    const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK);
     int J = 0, nq = 0;  // K/V tiles (= global tile index), items with keys
     int dq_items = 0;   // items whose dQ/Y the epilogue has to release
     bool ok = true;
     const bool is_s = warp == 9;
-    const uint64_t qdesc0 = sdesc_sw128(sbase + kDqOffQ);
-    const uint64_t vdesc0 = sdesc_sw128(sbase + kDqOffV);
+    const uint64_t qdesc0 = sdesc_sw128(sbase + C::kOffQ);
+    const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV);
     const uint32_t t_dq = tmem + 384, t_y = tmem + 448;
     for (int nt = 0; ok; ++nt) {
       const int slot = nt & 1;
@@ -391,13 +440,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const DqTile t = bars->tiles[slot];
       if (!t.valid) break;
       if (t.n > 0) {
-        const int qb = nq & 1;
+        const int qb = nq % kQdBufs;
         if (is_s) {
-          ok = mbar_wait_warp(&bars->qd_full[qb], (nq >> 1) & 1, abort, err);
+          ok = mbar_wait_warp(&bars->qd_full[qb], (nq / kQdBufs) & 1, abort, err);
           for (int j = 0; ok && j < t.n; ++j) {
-            const int g = J + j, st = g % kDqStages;
+            const int g = J + j, st = g % kStages;
             // the softmax warps have loaded S / dP of tile g - 1
-            if (!mbar_wait_warp(&bars->kv_full[st], (g / kDqStages) & 1, abort, err) ||
+            if (!mbar_wait_warp(&bars->kv_full[st], (g / kStages) & 1, abort, err) ||
                 (g >= 1 && !mbar_wait_warp(&bars->s_read, (g - 1) & 1, abort, err))) {
               ok = false;
               break;
@@ -407,11 +456,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const uint64_t kd = kdesc0 + st * kTileDesc;
             const uint64_t vd = vdesc0 + st * kTileDesc;
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              umma_ss_elect(tmem, qd + 2 * ks, kd + 2 * ks, kIdescSS128, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_ss_elect(tmem, qd + kstep_off(ks), kd + kstep_off(ks), kIdescSS128,
+                            ks > 0 ? 1u : 0u);
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              umma_ss_elect(tmem + 128, dod + 2 * ks, vd + 2 * ks, kIdescSS128,
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_ss_elect(tmem + 128, dod + kstep_off(ks), vd + kstep_off(ks), kIdescSS128,
                             ks > 0 ? 1u : 0u);
             umma_commit_elect(&bars->s_full);
             umma_commit_elect(&bars->kv_empty[st]);  // this warp is done with K/V
@@ -421,13 +471,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           // dQ/Y of the previous item must have been read by its epilogue
           if (dq_items > 0) ok = mbar_wait_warp(&bars->dq_free, (dq_items - 1) & 1, abort, err);
           for (int j = 0; ok && j < t.n; ++j) {
-            const int g = J + j, st = g % kDqStages;
+            const int g = J + j, st = g % kStages;
             if (!mbar_wait_warp(&bars->ds_full, g & 1, abort, err)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t kd = kdesc0 + st * kTileDesc;
+            // dims 64 half .. of K: the tile's swizzle block `half`
+            const uint64_t kd = kdesc0 + st * kTileDesc + t.half * kBlockDesc;
             // dS / P of keys 0..127 are 64 consecutive fp16-pair columns
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
@@ -471,13 +522,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (!t.valid) break;
       const size_t qrow = static_cast<size_t>(t.q0 + t.qt * kBM + r);
       const size_t lidx = static_cast<size_t>(t.h) * p.total_q + qrow;
-      __nv_bfloat16 *dq_row = p.dq + (qrow * p.hq + t.h) * kHeadDim + 32 * wg;
+      __nv_bfloat16 *dq_row = p.dq + (qrow * p.hq + t.h) * D + 64 * t.half + 32 * wg;
       if (t.n == 0) {  // no row of this tile sees a key: dq = 0, D = 0
         if (r < t.rows) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             reinterpret_cast<uint4 *>(dq_row)[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (wg == 0) p.dt[lidx] = 0.f;
+          if (wg == 0 && t.half == 0) p.de[lidx] = 0.f;
         }
         mbar_arrive(&bars->tile_empty[slot]);
         continue;
@@ -568,7 +619,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
                              pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
         }
-        if (wg == 0) p.dt[lidx] = d_e;
+        if (wg == 0 && t.half == 0) p.de[lidx] = d_e;
       }
       mbar_arrive(&bars->tile_empty[slot]);
     }
@@ -599,10 +650,26 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // fp16 [320, 384) (warpgroup w's queries in the half at 32w), dV [384, 448),
 // dK [448, 512).
 constexpr int kKvThreads = 352;
-constexpr int kKvQStages = 3;
+constexpr int kKvQStages = 3;  // Q/dO ring at D = 64 (the array size of the barriers)
+
+// Shared memory of the dK/dV kernel: K/V item buffers (two at D = 64, one at
+// 128), the Q/dO ring (three stages at 64, two at 128) with each stage's
+// -lse / -D vectors, then the control block.
+template <int D>
+struct KvCfg {
+  static constexpr int kTile = TileShape<D>::kBytes;
+  static constexpr int kKvBufs = D == 64 ? 2 : 1;
+  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffQ = kKvBufs * 2 * kTile;
+  static constexpr int kOffVec = kOffQ + kStages * 2 * kTile;
+  static constexpr int kOffBar = kOffVec + kStages * 1024;
+  static constexpr int kSmem = kOffBar + 1024 + 1024;
+};
+static_assert(KvCfg<128>::kSmem <= 227 * 1024, "dK/dV shared memory at head_dim 128");
 
 struct KvTile {
-  int valid, b, kt, g, q0, lq, k0, lk, krows, qt_lo, nqt, steps;
+  int valid, b, kt, g, q0, lq, k0, lk, krows, qt_lo, nqt, steps, half;
 };
 
 struct KvBars {
@@ -619,18 +686,18 @@ struct KvBars {
   KvTile tiles[2];
 };
 
-constexpr int kKvOffK = 0;                                   // 2 item buffers of K and V
-constexpr int kKvOffQ = 4 * kTileBytes;                      // per stage: Q, dO
-constexpr int kKvOffVec = kKvOffQ + kKvQStages * 2 * kTileBytes;  // per stage: -lse2[128], -D[128]
-constexpr int kKvOffBar = kKvOffVec + kKvQStages * 1024;
 static_assert(sizeof(KvBars) <= 1024, "dK/dV control block");
-constexpr int kKvSmem = kKvOffBar + 1024 + 1024;
 
 // Items are KV-head major: the CTAs in flight at one time work on key tiles
 // of one KV head, so the Q / dO tiles of that head's query heads that they
 // all stream stay in L2 between them (KV-head minor, every concurrent CTA
 // streamed a different head: 10 GB from DRAM per call instead of 0.8 GB).
-__device__ __forceinline__ void kv_decode(const BwdParams &p, int npairs, int w, KvTile &t) {
+// With 64-dim halves, work index w -> half w % halves, then (w / halves) as
+// above.
+__device__ __forceinline__ void kv_decode(const BwdParams &p, int npairs, int halves, int w,
+                                          KvTile &t) {
+  t.half = w % halves;
+  w /= halves;
   const unsigned e = p.k_pairs[npairs - 1 - w % npairs];
   t.valid = 1;
   t.g = w / npairs;
@@ -651,16 +718,23 @@ __device__ __forceinline__ void kv_decode(const BwdParams &p, int npairs, int w,
   t.steps = t.nqt * p.group;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
+  using C = KvCfg<D>;
+  constexpr int kTileBytes = C::kTile;
+  constexpr uint64_t kTileDesc = TileShape<D>::kDesc;
+  constexpr int kHalves = TileShape<D>::kHalves;
+  constexpr int kKvBufs = C::kKvBufs, kQStages = C::kStages;
+  constexpr int kKvOffK = C::kOffK, kKvOffQ = C::kOffQ, kKvOffVec = C::kOffVec;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (sbase - raw);
-  KvBars *bars = reinterpret_cast<KvBars *>(smem + kKvOffBar);
+  KvBars *bars = reinterpret_cast<KvBars *>(smem + C::kOffBar);
   volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int *err = &g_backward_error;
@@ -672,7 +746,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       mbar_init(&bars->kv_empty[i], 1);
       mbar_init(&bars->drain[i], 1);
     }
-    for (int s = 0; s < kKvQStages; ++s) {
+    for (int s = 0; s < kQStages; ++s) {
       mbar_init(&bars->qd_full[s], 1);
       mbar_init(&bars->qd_empty[s], 2);  // both MMA warps
     }
@@ -701,7 +775,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     const int npairs = *p.num_k_pairs;
-    const int num_work = npairs * p.hkv;
+    const int num_work = npairs * p.hkv * kHalves;
+    auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint64_t *bar, int head, int row) {
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d_elect(dst + blk * kBlockBytes, map, bar, blk * 64, head, row);
+    };
     int ni = 0, S = 0;  // items with work, steps so far
     bool ok = true;
     for (int nt = 0; ok; ++nt) {
@@ -712,7 +791,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         KvTile t;
         t.valid = 0;
         const int w = static_cast<int>(atomicAdd(p.k_counter, 1u));
-        if (w < num_work) kv_decode(p, npairs, w, t);
+        if (w < num_work) kv_decode(p, npairs, kHalves, w, t);
         bars->tiles[slot] = t;
         mbar_arrive(&bars->tile_full[slot]);
       }
@@ -720,19 +799,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const KvTile t = bars->tiles[slot];
       if (!t.valid) break;
       if (t.steps == 0) continue;
-      const int kb = ni & 1;
-      if (ni >= 2 && !mbar_wait_warp(&bars->kv_empty[kb], ((ni >> 1) - 1) & 1, abort, err)) break;
+      const int kb = ni % kKvBufs;
+      if (ni >= kKvBufs &&
+          !mbar_wait_warp(&bars->kv_empty[kb], ((ni / kKvBufs) - 1) & 1, abort, err))
+        break;
       mbar_arrive_expect_tx_elect(&bars->kv_full[kb], 2 * kTileBytes);
-      tma_load_3d_elect(sbase + kKvOffK + kb * 2 * kTileBytes, &tm_k, &bars->kv_full[kb], 0, t.g,
-                        t.k0 + t.kt * kBN);
-      tma_load_3d_elect(sbase + kKvOffK + (kb * 2 + 1) * kTileBytes, &tm_v, &bars->kv_full[kb], 0,
-                        t.g, t.k0 + t.kt * kBN);
+      load_tile(sbase + kKvOffK + kb * 2 * kTileBytes, &tm_k, &bars->kv_full[kb], t.g,
+                t.k0 + t.kt * kBN);
+      load_tile(sbase + kKvOffK + (kb * 2 + 1) * kTileBytes, &tm_v, &bars->kv_full[kb], t.g,
+                t.k0 + t.kt * kBN);
       ++ni;
       for (int s = 0; s < t.steps; ++s, ++S) {
-        const int st = S % kKvQStages;
+        const int st = S % kQStages;
         const int h = t.g * p.group + s / t.nqt, qt = t.qt_lo + s % t.nqt;
-        if (S >= kKvQStages &&
-            !mbar_wait_warp(&bars->qd_empty[st], ((S / kKvQStages) - 1) & 1, abort, err)) {
+        if (S >= kQStages &&
+            !mbar_wait_warp(&bars->qd_empty[st], ((S / kQStages) - 1) & 1, abort, err)) {
           ok = false;
           break;
         }
@@ -744,21 +825,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int i = 0; i < 4; ++i) {
           const int row = lane + 32 * i;
           vec[row] = row < valid ? -p.lse2t[at + row] : -INFINITY;  // -l2, -D
-          vec[128 + row] = row < valid ? -p.dt[at + row] : 0.f;
+          vec[128 + row] = row < valid ? -p.de[at + row] : 0.f;
         }
         __syncwarp();
         mbar_arrive_expect_tx_elect(&bars->qd_full[st], 2 * kTileBytes);
-        tma_load_3d_elect(sbase + kKvOffQ + st * 2 * kTileBytes, &tm_q, &bars->qd_full[st], 0, h,
-                          t.q0 + qt * kBM);
-        tma_load_3d_elect(sbase + kKvOffQ + (st * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[st],
-                          0, h, t.q0 + qt * kBM);
+        load_tile(sbase + kKvOffQ + st * 2 * kTileBytes, &tm_q, &bars->qd_full[st], h,
+                  t.q0 + qt * kBM);
+        load_tile(sbase + kKvOffQ + (st * 2 + 1) * kTileBytes, &tm_do, &bars->qd_full[st], h,
+                  t.q0 + qt * kBM);
       }
     }
     if (*abort) {
-      for (int i = max(0, ni - 2); i < ni; ++i)
-        mbar_wait_warp(&bars->kv_full[i & 1], (i >> 1) & 1, abort, err, true);
-      for (int i = max(0, S - kKvQStages); i < S; ++i)
-        mbar_wait_warp(&bars->qd_full[i % kKvQStages], (i / kKvQStages) & 1, abort, err, true);
+      for (int i = max(0, ni - kKvBufs); i < ni; ++i)
+        mbar_wait_warp(&bars->kv_full[i % kKvBufs], (i / kKvBufs) & 1, abort, err, true);
+      for (int i = max(0, S - kQStages); i < S; ++i)
+        mbar_wait_warp(&bars->qd_full[i % kQStages], (i / kQStages) & 1, abort, err, true);
     }
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------------ MMA
@@ -777,13 +858,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const KvTile t = bars->tiles[slot];
       if (!t.valid) break;
       if (t.steps > 0) {
-        const int kb = ni & 1;
+        const int kb = ni % kKvBufs;
         if (is_s) {
-          ok = mbar_wait_warp(&bars->kv_full[kb], (ni >> 1) & 1, abort, err);
+          ok = mbar_wait_warp(&bars->kv_full[kb], (ni / kKvBufs) & 1, abort, err);
           const uint64_t kd = kvdesc0 + kb * 2 * kTileDesc, vd = kd + kTileDesc;
           for (int s = 0; ok && s < t.steps; ++s) {
-            const int g = S + s, st = g % kKvQStages;
-            if (!mbar_wait_warp(&bars->qd_full[st], (g / kKvQStages) & 1, abort, err) ||
+            const int g = S + s, st = g % kQStages;
+            if (!mbar_wait_warp(&bars->qd_full[st], (g / kQStages) & 1, abort, err) ||
                 (g >= 1 && !mbar_wait_warp(&bars->s_read, (g - 1) & 1, abort, err))) {
               ok = false;
               break;
@@ -791,11 +872,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tc_fence_after();
             const uint64_t qd = qdesc0 + st * 2 * kTileDesc, dod = qd + kTileDesc;
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              umma_ss_elect(tmem, kd + 2 * ks, qd + 2 * ks, kIdescSS128, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_ss_elect(tmem, kd + kstep_off(ks), qd + kstep_off(ks), kIdescSS128,
+                            ks > 0 ? 1u : 0u);
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)
-              umma_ss_elect(tmem + 128, vd + 2 * ks, dod + 2 * ks, kIdescSS128,
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_ss_elect(tmem + 128, vd + kstep_off(ks), dod + kstep_off(ks), kIdescSS128,
                             ks > 0 ? 1u : 0u);
             umma_commit_elect(&bars->st_full);
             umma_commit_elect(&bars->qd_empty[st]);  // this warp is done with Q / dO
@@ -806,13 +888,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (done_items > 0)
             ok = mbar_wait_warp(&bars->dkv_free, (done_items - 1) & 1, abort, err);
           for (int s = 0; ok && s < t.steps; ++s) {
-            const int g = S + s, st = g % kKvQStages;
+            const int g = S + s, st = g % kQStages;
             if (!mbar_wait_warp(&bars->ew_done, g & 1, abort, err)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t qd = qdesc0 + st * 2 * kTileDesc, dod = qd + kTileDesc;
+            // dims 64 half .. of Q and dO: the tiles' swizzle block `half`
+            const uint64_t qd = qdesc0 + st * 2 * kTileDesc + t.half * kBlockDesc,
+                           dod = qd + kTileDesc;
             // P^T / dS^T of queries 0..127 are 64 consecutive fp16-pair columns
 #pragma unroll
             for (int kk = 0; kk < kBM / 16; ++kk)
@@ -852,8 +936,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
       const KvTile t = bars->tiles[slot];
       if (!t.valid) break;
-      const size_t krow = (static_cast<size_t>(t.k0 + t.kt * kBN + r) * p.hkv + t.g) * kHeadDim +
-                          32 * wg;
+      const size_t krow = (static_cast<size_t>(t.k0 + t.kt * kBN + r) * p.hkv + t.g) * D +
+                          64 * t.half + 32 * wg;
       if (t.steps == 0) {  // no query sees this key tile
         if (r < t.krows) {
 #pragma unroll
@@ -867,10 +951,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       }
       const int jk = t.kt * kBN + r;  // this thread's key
       for (int s = 0; s < t.steps; ++s) {
-        const int g = S + s, st = g % kKvQStages;
+        const int g = S + s, st = g % kQStages;
         // the lse / D vectors are plain shared-memory stores: wait on their
         // barrier directly, then on the MMAs
-        if (!mbar_wait_warp(&bars->qd_full[st], (g / kKvQStages) & 1, abort, err) ||
+        if (!mbar_wait_warp(&bars->qd_full[st], (g / kQStages) & 1, abort, err) ||
             !mbar_wait_warp(&bars->st_full, g & 1, abort, err)) {
           ok = false;
           break;
@@ -964,40 +1048,49 @@ size_t list_bytes(int batch, int64_t total) {  // counter + pairs of one tile li
 
 }  // namespace
 
-// Workspace: q16, do16 [total_q, hq, 64] fp16; k16, v16 [total_k, hkv, 64]
-// fp16; lse2t, dt [hq, total_q] fp32; the query-tile and key-tile lists.
-size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv) {
-  const size_t qb = round256(static_cast<size_t>(total_q) * hq * kHeadDim * 2);
-  const size_t kb = round256(static_cast<size_t>(total_k) * hkv * kHeadDim * 2);
+// Workspace: q16, do16 [total_q, hq, D] fp16; k16, v16 [total_k, hkv, D]
+// fp16; lse2t, dt [hq, total_q] fp32 (+ the exact D de at D = 128); the
+// query-tile and key-tile lists.
+size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv,
+                                int head_dim) {
+  const size_t qb = round256(static_cast<size_t>(total_q) * hq * head_dim * 2);
+  const size_t kb = round256(static_cast<size_t>(total_k) * hkv * head_dim * 2);
   const size_t vb = round256(static_cast<size_t>(total_q) * hq * 4);
-  return 2 * qb + 2 * kb + 2 * vb + list_bytes(batch, total_q) + list_bytes(batch, total_k);
+  return 2 * qb + 2 * kb + (head_dim == 64 ? 2 : 3) * vb + list_bytes(batch, total_q) +
+         list_bytes(batch, total_k);
 }
 
-cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed) {
-  *encode_failed = false;
-  if (a.batch == 0) return cudaSuccess;
+namespace {
+
+template <int D>
+cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed) {
+  constexpr int kHalves = TileShape<D>::kHalves;
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-  const size_t qb = round256(static_cast<size_t>(a.total_q) * a.hq * kHeadDim * 2);
-  const size_t kb = round256(static_cast<size_t>(a.total_k) * a.hkv * kHeadDim * 2);
+  const size_t qb = round256(static_cast<size_t>(a.total_q) * a.hq * D * 2);
+  const size_t kb = round256(static_cast<size_t>(a.total_k) * a.hkv * D * 2);
   const size_t vb = round256(static_cast<size_t>(a.total_q) * a.hq * 4);
   uint8_t *q16 = ws, *do16 = ws + qb, *k16 = ws + 2 * qb, *v16 = ws + 2 * qb + kb;
   float *lse2t = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb);
   float *dt = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb + vb);
-  uint8_t *qlist = ws + 2 * qb + 2 * kb + 2 * vb;
+  // exact D: in place of the forward's at D = 64 (one item per row and head);
+  // its own array at D = 128, where both halves of a row read the forward's
+  float *de = D == 64 ? dt : reinterpret_cast<float *>(ws + 2 * qb + 2 * kb + 2 * vb);
+  uint8_t *qlist = ws + 2 * qb + 2 * kb + (D == 64 ? 2 : 3) * vb;
   uint8_t *klist = qlist + list_bytes(a.batch, a.total_q);
 
   cudaError_t e;
   if (a.total_q > 0) {
-    const int64_t n = a.total_q * a.hq * 8;
+    const int64_t n = a.total_q * a.hq * (D / 8);
     const int64_t blocks = (n + 255) / 256;
-    bwd_prep_q_kernel<<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
+    bwd_prep_q_kernel<D><<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0,
+                           stream>>>(
         static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.dout),
         static_cast<const uint4 *>(a.out), a.lse, a.total_q, a.hq, reinterpret_cast<uint4 *>(q16),
         reinterpret_cast<uint4 *>(do16), lse2t, dt);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.total_k > 0) {
-    const int64_t n8 = a.total_k * a.hkv * 8;
+    const int64_t n8 = a.total_k * a.hkv * (D / 8);
     const int64_t blocks = (n8 + 255) / 256;
     bwd_prep_kv_kernel<<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(
         static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
@@ -1020,6 +1113,7 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
   p.scale_log2 = a.scale * kLog2e;
   p.lse2t = lse2t;
   p.dt = dt;
+  p.de = de;
   p.q_pairs = reinterpret_cast<const unsigned *>(qlist + 256);
   p.num_q_pairs = reinterpret_cast<const int *>(qlist + 4);
   p.q_counter = reinterpret_cast<unsigned *>(qlist);
@@ -1028,8 +1122,8 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
   p.num_k_pairs = reinterpret_cast<const int *>(klist + 4);
   p.dq = static_cast<__nv_bfloat16 *>(a.dq);
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
-  p.stall_ns = g_bwd_stall_ns.load();
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+  p.stall_ns = g_bwd_stall_ns.load();
   if ((e = launch_tile_list(a.cu_q, a.batch, max_qtiles, reinterpret_cast<unsigned *>(qlist + 256),
                             reinterpret_cast<int *>(qlist + 4), reinterpret_cast<unsigned *>(qlist),
                             stream)) != cudaSuccess)
@@ -1045,31 +1139,33 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
   // with no keys (or queries) nothing reads those maps; they then point at q16
   const void *kbase = a.total_k > 0 ? static_cast<const void *>(k16) : q16;
   const void *vbase = a.total_k > 0 ? static_cast<const void *>(v16) : q16;
-  if (fn == nullptr || !encode_rows_heads(fn, &tq, q16, a.total_q, a.hq, f16) ||
-      !encode_rows_heads(fn, &tdo, do16, a.total_q, a.hq, f16) ||
-      !encode_rows_heads(fn, &tk, kbase, a.total_k, a.hkv, f16) ||
-      !encode_rows_heads(fn, &tv, vbase, a.total_k, a.hkv, f16)) {
+  if (fn == nullptr || !encode_rows_heads(fn, &tq, q16, a.total_q, a.hq, f16, D) ||
+      !encode_rows_heads(fn, &tdo, do16, a.total_q, a.hq, f16, D) ||
+      !encode_rows_heads(fn, &tk, kbase, a.total_k, a.hkv, f16, D) ||
+      !encode_rows_heads(fn, &tv, vbase, a.total_k, a.hkv, f16, D)) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
-  if ((e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr int kDqSmem = DqCfg<D>::kSmem, kKvSmem = KvCfg<D>::kSmem;
+  if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kDqSmem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kKvSmem)) != cudaSuccess)
     return e;
   if (a.total_q > 0) {
-    const int64_t items = (a.total_q / kBM + a.batch) * a.hq;
+    const int64_t items = (a.total_q / kBM + a.batch) * a.hq * kHalves;
     const int64_t grid = items < sm_count() ? items : sm_count();
-    bwd_dq_kernel<<<static_cast<unsigned>(grid), kDqThreads, kDqSmem, stream>>>(tq, tdo, tk, tv, p);
+    bwd_dq_kernel<D><<<static_cast<unsigned>(grid), kDqThreads, kDqSmem, stream>>>(tq, tdo, tk,
+                                                                                   tv, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const bool dsink = a.sinks != nullptr && a.dsinks != nullptr;
   if (dsink) {  // after dQ: D is exact by now
-    bwd_dsink_kernel<<<a.hq, 256, 0, stream>>>(a.sinks, lse2t, dt, a.total_q, a.dsinks);
+    bwd_dsink_kernel<<<a.hq, 256, 0, stream>>>(a.sinks, lse2t, de, a.total_q, a.dsinks);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.total_k > 0) {
-    const int64_t items = (a.total_k / kBN + a.batch) * a.hkv;
+    const int64_t items = (a.total_k / kBN + a.batch) * a.hkv * kHalves;
     const int64_t grid = items < sm_count() ? items : sm_count();
     // overlaps the sink gradient (programmatic dependent launch); everything
     // it reads was written before that kernel started
@@ -1083,11 +1179,20 @@ cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dsink ? 1 : 0;
-    if ((e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel, tq, tdo, tk, tv, p)) != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D>, tq, tdo, tk, tv, p)) != cudaSuccess)
       return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed) {
+  *encode_failed = false;
+  if (a.batch == 0) return cudaSuccess;
+  return a.head_dim == 128 ? launch_backward_d<128>(a, stream, encode_failed)
+                           : launch_backward_d<64>(a, stream, encode_failed);
 }
 
 cudaError_t backward_set_stall(uint64_t ns) {

@@ -119,11 +119,15 @@ struct BackwardLaunch {
   const float *sinks;
   int causal, window;
   float scale;
-  void *dq, *dk, *dv;  // bf16
+  void *dq, *dk, *dv;  // bf16 [.., D]
   float *dsinks;       // [hq] or null
   void *workspace;     // backward_workspace_bytes
+  int head_dim = kHeadDim;  // 64 or 128
 };
-size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv);
+size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv,
+                                int head_dim);
+// head dims the backward kernels are built for
+inline bool backward_head_dim_ok(int d) { return d == 64 || d == 128; }
 cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed);
 cudaError_t backward_read_error(cudaStream_t stream, int *code);
 

@@ -550,11 +550,13 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         torch.cuda.empty_cache()
 
     # backward of the varlen prefill (dq, dk, dv, dsinks), forward outputs
-    # precomputed; algorithmic flops: 5 products of 2 * 64 per visible pair
-    for name, w in (("varlen_backward", 0), ("varlen_backward_w128", 128)):
+    # precomputed; algorithmic flops: 5 products of 2 * D per visible pair
+    for name, w, d in (("varlen_backward", 0, 64), ("varlen_backward_w128", 128, 64),
+                       ("varlen_backward_d128", 0, 128)):
         if only is not None and name != only:
             continue
-        c = S.varlen_prefill(window=w, device="cuda")
+        c = (S.varlen_prefill(window=w, device="cuda") if d == 64
+             else S.varlen_prefill_d128(device="cuda"))
         cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
         sk = c.sinks.to(dev)
         out, lse = sa.sinkattn_prefill(c.q, c.k, c.v, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
@@ -563,7 +565,8 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         dq, dk, dv = torch.empty_like(c.q), torch.empty_like(c.k), torch.empty_like(c.v)
         dsk = torch.empty_like(sk)
         ws = torch.empty(sa.sinkattn_prefill_backward_workspace_size(c.batch, c.q.shape[0],
-                                                                     c.k.shape[0], c.hq, c.hkv),
+                                                                     c.k.shape[0], c.hq, c.hkv,
+                                                                     c.head_dim),
                          dtype=torch.uint8, device=dev)
 
         def call():
@@ -573,7 +576,7 @@ def extras(sa, S, dev, stream, pk, pk_kind, only=None):
         for _ in range(3):
             call()
         t = time_calls(call, 10, stream, flush)
-        fl = 10 * 64 * prefill_pairs(c) * c.hq
+        fl = 10 * c.head_dim * prefill_pairs(c) * c.hq
         res[name] = {"tflops": fl / t / 1e12, "ms": t * 1e3, "tokens_per_s": sum(c.seqlens_q) / t,
                      "frac_of_bf16_peak": fl / t / 1e12 / burst,
                      "peak": burst, "peak_kind": pk_kind + " bf16_tflops (burst)", "flops": fl}

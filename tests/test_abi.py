@@ -165,7 +165,12 @@ def backward(lib, **kw):
 
 
 def test_backward_rejects_bad_arguments(lib):
-    assert backward(lib, d=128) == B.SINKATTN_ERR_UNSUPPORTED
+    assert backward(lib, d=96) == B.SINKATTN_ERR_UNSUPPORTED
+    # head_dim 128 is accepted; its workspace holds twice the fp16 copies
+    need64 = lib.sinkattn_prefill_backward_workspace_size(2, 10, 10, 8, 2, 64)
+    need128 = lib.sinkattn_prefill_backward_workspace_size(2, 10, 10, 8, 2, 128)
+    assert need128 > need64 and lib.sinkattn_prefill_backward_workspace_size(2, 10, 10, 8, 2, 96) == 0
+    assert backward(lib, d=128, batch=0) == B.SINKATTN_OK
     assert backward(lib, hq=6, hkv=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert backward(lib, lse=None) == B.SINKATTN_ERR_INVALID_ARGUMENT   # lse is required
     assert backward(lib, out=None) == B.SINKATTN_ERR_INVALID_ARGUMENT

@@ -118,6 +118,56 @@ def test_backward_varlen_full_config(window):
     compare(c, got, ref, "bwd varlen w=%d" % window, rows_q=rq, rows_k=rk)
 
 
+# head_dim 128: items carry a 64-dim half of the output gradient; S and dP
+# run over both 64-dim swizzle blocks
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
+@pytest.mark.parametrize("causal,window", [(True, 0), (False, 0), (True, 1), (True, 128)])
+def test_backward_head_dim_128_shapes(shape, causal, window):
+    lq, lk = shape
+    c = S.make_prefill("bwd128", lq, lk, 8, 2, seed=151 + sum(lk), causal=causal, window=window,
+                       sink_std=1.5, head_dim=128)
+    dout = dout_for(c, 29 + sum(lq))
+    compare(c, run(c, dout), reference(c, dout),
+            "bwd d128 %s causal=%s w=%d" % (shape, causal, window))
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (12, 3), (16, 2)])
+def test_backward_head_dim_128_groups_and_no_sink(hq, hkv):
+    for with_sinks in (True, False):
+        c = S.make_prefill("bgrp128", [190, 260], [390, 260], hq, hkv, seed=153 + hq,
+                           with_sinks=with_sinks, head_dim=128)
+        dout = dout_for(c, 31 + hq)
+        compare(c, run(c, dout), reference(c, dout), "bwd d128 hq=%d hkv=%d sinks=%s"
+                % (hq, hkv, with_sinks))
+
+
+def test_backward_head_dim_128_large_sinks_and_repeat():
+    c = S.make_prefill("bsink128", [300, 700], [300, 900], 4, 1, seed=155, head_dim=128)
+    c.sinks = torch.tensor([9.0, -30.0, 0.0, 4.0])
+    dout = dout_for(c, 33)
+    a = run(c, dout)
+    compare(c, a, reference(c, dout), "bwd d128 large sinks")
+    b = run(c, dout)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_backward_head_dim_128_varlen_full_config():
+    """varlen_prefill's lengths and heads at head_dim 128: the whole batch on
+    the GPU; the first and the last sequence (every head, every row) against
+    the oracle."""
+    c = S.varlen_prefill_d128()
+    dout = dout_for(c, 35)
+    got = run(c, dout)
+    torch.cuda.synchronize()
+    seqs = [0, c.batch - 1]
+    ref = reference(c, dout, seqs=seqs)
+    cq, ck = c.cu_seqlens_q.tolist(), c.cu_seqlens_k.tolist()
+    rq = np.concatenate([np.arange(cq[b], cq[b + 1]) for b in seqs])
+    rk = np.concatenate([np.arange(ck[b], ck[b + 1]) for b in seqs])
+    compare(c, got[:3] + (None,), ref[:3] + (None,), "bwd varlen d128", rows_q=rq, rows_k=rk)
+
+
 def test_no_device_error_after_backward():
     assert sa.sinkattn_get_device_error() == 0
 
