@@ -251,7 +251,7 @@ size_t sinkattn_decode_workspace_size(int batch, int max_seqlen_k, int hq, int h
   if (batch <= 0 || hq <= 0 || hkv <= 0 || !decode_head_dim_ok(head_dim) || max_seqlen_k < 0 ||
       window < 0 || num_splits < 0)
     return 0;
-  const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, window, num_splits);
+  const DecodePlan plan = plan_decode(batch, hq, hkv, max_seqlen_k, window, num_splits);
   return decode_workspace_layout(batch, hq, hkv, plan, head_dim).bytes;
 }
 
@@ -271,7 +271,6 @@ sinkattn_status_t decode_impl(const void *q, const void *k_cache, const void *v_
       kv_rows < 0 || !mask_ok(mask))
     return SINKATTN_ERR_INVALID_ARGUMENT;
   if (!decode_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
-  if (hq / hkv > 8) return SINKATTN_ERR_UNSUPPORTED;
   const bool paged = block_table != nullptr;
   if (paged == (kv_indptr != nullptr)) return SINKATTN_ERR_INVALID_ARGUMENT;
   if (paged && (seqlens_k == nullptr || page_size <= 0 || max_pages_per_seq <= 0))
@@ -285,8 +284,9 @@ sinkattn_status_t decode_impl(const void *q, const void *k_cache, const void *v_
       (lse && !aligned(lse, 4)) || (k_scale && !aligned(k_scale, 4)) ||
       (v_scale && !aligned(v_scale, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
-  const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
+  if (batch > 65535 || static_cast<int64_t>(hkv) * decode_head_tiles(hq, hkv) > 65535)
+    return SINKATTN_ERR_UNSUPPORTED;
+  const DecodePlan plan = plan_decode(batch, hq, hkv, max_seqlen_k, mask.window, num_splits);
   if (plan.max_splits > 1) {
     const size_t need = decode_workspace_layout(batch, hq, hkv, plan, head_dim).bytes;
     if (workspace == nullptr || workspace_bytes < need) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;

@@ -116,6 +116,7 @@ struct Params {
   int max_pages, page_size;
   int page_shift;  // log2(page_size) when it is a power of two, else -1
   int batch, hq, hkv, group, window, chunk;
+  int nht;  // tiles of up to 8 query heads per KV head
   const float *sinks;
   float scale_log2;
   __nv_bfloat16 *out;
@@ -192,17 +193,25 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lr = lane >> 2, lc = lane & 3;  // mma fragment row / column group
-  int split = 0, g, b;
+  int split = 0, g, b, ht;
   if (kPair) {
     const int pair = static_cast<int>(blockIdx.x) * kWarps + warp;
-    if (pair >= p.batch * p.hkv) return;  // the warp has no pair (no block barrier follows)
-    b = pair / p.hkv;
-    g = pair - b * p.hkv;
+    if (pair >= p.batch * p.hkv * p.nht) return;  // no pair for this warp (no block barrier follows)
+    b = pair / (p.hkv * p.nht);
+    const int gh = pair - b * p.hkv * p.nht;
+    g = gh / p.nht;
+    ht = gh - g * p.nht;
   } else {
     split = blockIdx.x;
-    g = blockIdx.y;
+    g = static_cast<int>(blockIdx.y) / p.nht;
+    ht = static_cast<int>(blockIdx.y) - g * p.nht;
     b = blockIdx.z;
   }
+  // this block's query heads: gt (at most 8) heads from hbase, tile ht of
+  // KV head g's group
+  const int hbase = g * p.group + ht * kMaxGroup;
+  const int gt = min(kMaxGroup, p.group - ht * kMaxGroup);
+  const int cidx = (b * p.hkv + g) * p.nht + ht;  // split-merge counter
 
   int kv_base = 0, L;
   if (kPaged) {
@@ -248,9 +257,8 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
   // dims ks*16 + 2lc + {0,1} and + 8 (fp8 cache: as fp16, clamped to its range).
   uint32_t qf[kKS][2];
   {
-    const bool valid = lr < p.group;
-    const __nv_bfloat16 *qrow =
-        p.q + (static_cast<size_t>(b) * p.hq + g * p.group + (valid ? lr : 0)) * D;
+    const bool valid = lr < gt;
+    const __nv_bfloat16 *qrow = p.q + (static_cast<size_t>(b) * p.hq + hbase + (valid ? lr : 0)) * D;
     auto frag = [&](int at) -> uint32_t {
       if (!valid) return 0u;
       const uint32_t x = *reinterpret_cast<const uint32_t *>(qrow + at);
@@ -276,9 +284,9 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
   // since d is summed over the 8 lane rows at the end).
   float m0 = -INFINITY, m1 = -INFINITY, d0 = 0.f, d1 = 0.f;
   if (p.sinks != nullptr && split == 0 && (kPair || warp == 0)) {
-    const int h0 = min(2 * lc, p.group - 1), h1 = min(2 * lc + 1, p.group - 1);
-    m0 = p.sinks[g * p.group + h0] * kLog2e;
-    m1 = p.sinks[g * p.group + h1] * kLog2e;
+    const int h0 = min(2 * lc, gt - 1), h1 = min(2 * lc + 1, gt - 1);
+    m0 = p.sinks[hbase + h0] * kLog2e;
+    m1 = p.sinks[hbase + h1] * kLog2e;
     if (lr == 0) d0 = d1 = 1.f;
   }
   float o[kKS][4];
@@ -496,10 +504,10 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
     const int hh = lane >> 2;
     constexpr int kPer = D / 4;
     const int c0 = (lane & 3) * kPer;
-    if (hh < p.group) {
+    if (hh < gt) {
       const float dn = pd[hh];
       const float inv = dn > 0.f ? out_scale / dn : 0.f;
-      const size_t row_h = static_cast<size_t>(b) * p.hq + g * p.group + hh;
+      const size_t row_h = static_cast<size_t>(b) * p.hq + hbase + hh;
 #pragma unroll
       for (int q8 = 0; q8 < kPer / 8; ++q8) {
         const float4 x = *reinterpret_cast<const float4 *>(po + hh * D + c0 + 8 * q8);
@@ -566,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
   const float inv = Dn > 0.f ? out_scale / Dn : 0.f;
   // block lse in natural log (-inf when nothing is visible and no sink)
   const float blse = Dn > 0.f ? (M + fast_log2(Dn)) * kLn2 : -INFINITY;
-  const bool head_ok = hh < p.group;
-  const int qh = g * p.group + hh;
+  const bool head_ok = hh < gt;
+  const int qh = hbase + hh;
   const size_t row_h = static_cast<size_t>(b) * p.hq + qh;
   // kOut values times `mul` -> bf16 at out[row_h][c0...]
   auto store_out = [&](const float *x, float mul) {
@@ -604,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
     // the counters were zeroed by the kernel launched just before this one,
     // which lets this grid start early: wait for it here, the first use
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const unsigned prev = atomicAdd(p.counters + b * p.hkv + g, 1u);
+    const unsigned prev = atomicAdd(p.counters + cidx, 1u);
     s_last = prev == static_cast<unsigned>(nsplit - 1);
   }
   __syncthreads();
@@ -639,12 +647,13 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
     if (p.lse != nullptr && (tid & 15) == 0)
       p.lse[row_h] = W > 0.f ? Mx + fast_log2(W) * kLn2 : -INFINITY;
   }
-  if (tid == 0) p.counters[b * p.hkv + g] = 0u;  // ready for the next call / graph replay
+  if (tid == 0) p.counters[cidx] = 0u;  // ready for the next call / graph replay
 }
 
 }  // namespace
 
-DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num_splits) {
+DecodePlan plan_decode(int batch, int hq, int hkv, int max_seqlen_k, int window, int num_splits) {
+  hkv = hkv * decode_head_tiles(hq, hkv);  // blocks per sequence and split
   int span = window > 0 ? (window < max_seqlen_k ? window : max_seqlen_k) : max_seqlen_k;
   if (span < 1) span = 1;
   long chunk;
@@ -680,7 +689,8 @@ DecodeWorkspace decode_workspace_layout(int batch, int hq, int hkv, const Decode
   const size_t rows = static_cast<size_t>(plan.max_splits) * batch * hq;
   w.off_lse = up(rows * head_dim * sizeof(float));
   w.off_counters = w.off_lse + up(rows * sizeof(float));
-  w.bytes = w.off_counters + up(static_cast<size_t>(batch) * hkv * sizeof(unsigned));
+  w.bytes = w.off_counters + up(static_cast<size_t>(batch) * hkv * decode_head_tiles(hq, hkv) *
+                                sizeof(unsigned));
   return w;
 }
 
@@ -707,6 +717,7 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   p.hq = a.hq;
   p.hkv = a.hkv;
   p.group = a.hq / a.hkv;
+  p.nht = decode_head_tiles(a.hq, a.hkv);
   p.window = a.window;
   p.chunk = a.plan.chunk;
   p.sinks = a.sinks;
@@ -724,7 +735,7 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   // waits for it only where it first touches a counter, after its K/V pass.
   const bool split = a.plan.max_splits > 1;
   if (split) {
-    const int64_t n = static_cast<int64_t>(a.batch) * a.hkv;
+    const int64_t n = static_cast<int64_t>(a.batch) * a.hkv * p.nht;
     const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
     zero_counters_kernel<<<blocks, 256, 0, stream>>>(p.counters, n);
     const cudaError_t e = cudaGetLastError();
@@ -736,8 +747,9 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
   const int span = a.window > 0 && a.window < a.max_seqlen_k ? a.window : a.max_seqlen_k;
   const bool pair = !split && span <= kPairMaxSpan;
   const dim3 grid = pair ? dim3(static_cast<unsigned>(
-                               (static_cast<int64_t>(a.batch) * a.hkv + kWarps - 1) / kWarps))
-                         : dim3(a.plan.max_splits, a.hkv, a.batch);
+                               (static_cast<int64_t>(a.batch) * a.hkv * p.nht + kWarps - 1) /
+                               kWarps))
+                         : dim3(a.plan.max_splits, a.hkv * p.nht, a.batch);
   auto go = [&](auto kernel, int smem) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaLaunchConfig_t cfg = {};
@@ -882,7 +894,7 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
   if (batch < 0 || max_seqlen_k < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || num_splits < 0 ||
       kv_rows < 0 || mask.window < 0 || !isfinite(mask.scale) || !(mask.scale > 0.f))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (!decode_head_dim_ok(head_dim) || hq / hkv > 8) return SINKATTN_ERR_UNSUPPORTED;
+  if (!decode_head_dim_ok(head_dim)) return SINKATTN_ERR_UNSUPPORTED;
   const bool paged = block_table != nullptr;
   if (paged == (kv_indptr != nullptr)) return SINKATTN_ERR_INVALID_ARGUMENT;
   if (paged && (seqlens_k == nullptr || page_size <= 0 || max_pages_per_seq <= 0))
@@ -895,8 +907,9 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(
       (block_table && !is_aligned(block_table, 4)) || (seqlens_k && !is_aligned(seqlens_k, 4)) ||
       (sinks && !is_aligned(sinks, 4)) || (lse && !is_aligned(lse, 4)))
     return SINKATTN_ERR_INVALID_ARGUMENT;
-  if (batch > 65535 || hkv > 65535) return SINKATTN_ERR_UNSUPPORTED;
-  const DecodePlan plan = plan_decode(batch, hkv, max_seqlen_k, mask.window, num_splits);
+  if (batch > 65535 || static_cast<int64_t>(hkv) * decode_head_tiles(hq, hkv) > 65535)
+    return SINKATTN_ERR_UNSUPPORTED;
+  const DecodePlan plan = plan_decode(batch, hq, hkv, max_seqlen_k, mask.window, num_splits);
   // the plan's scratch must fit the fixed array
   if (plan.max_splits > 1 &&
       decode_workspace_layout(batch, hq, hkv, plan, head_dim).bytes >

@@ -20,7 +20,10 @@ struct DecodePlan {
   int chunk;
   int max_splits;
 };
-DecodePlan plan_decode(int batch, int hkv, int max_seqlen_k, int window, int num_splits);
+// Query heads of a KV head are served in tiles of up to 8 (the MMA's N);
+// groups above 8 take several tiles, each its own block (or warp).
+inline int decode_head_tiles(int hq, int hkv) { return (hq / hkv + 7) / 8; }
+DecodePlan plan_decode(int batch, int hq, int hkv, int max_seqlen_k, int window, int num_splits);
 // Workspace layout for a plan: [partial_o | partial_lse | counters].
 struct DecodeWorkspace {
   size_t off_lse, off_counters, bytes;

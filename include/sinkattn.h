@@ -220,7 +220,11 @@ sinkattn_status_t sinkattn_prefill_paged_fp8(
  *   max_seqlen_k   host upper bound on Lk_b (sizes the split grid).
  *   num_splits     0 = automatic; n > 0 = split the longest sequence into
  *            about n blocks (shorter ones get proportionally fewer).
- *   hq / hkv must be at most 8 (one KV head and all its query heads per block).
+ *   hq / hkv: any group size. Up to 8 query heads share one read of each
+ *            K/V row inside a block; larger groups are served in tiles of 8
+ *            query heads, one block (or warp) per tile, whose reads of the same
+ *            K/V rows are issued close together so that the repeats are
+ *            served from L2.
  *   head_dim 64 or 128. q, out and every K/V row have head_dim elements.
  *   out      bf16 [batch, hq, D];  lse float32 [batch, hq] or NULL.
  *   workspace      device scratch of at least sinkattn_decode_workspace_size()

@@ -190,7 +190,11 @@ def test_backward_rejects_bad_arguments(lib):
 
 def test_decode_rejects_bad_arguments(lib):
     assert decode(lib, d=80) == B.SINKATTN_ERR_UNSUPPORTED
-    assert decode(lib, hq=32, hkv=2) == B.SINKATTN_ERR_UNSUPPORTED   # group of 16
+    # groups above 8 run in tiles of 8 query heads, each with its own counter
+    n16 = lib.sinkattn_decode_workspace_size(2, 5000, 32, 2, 64, 0, 0)
+    n8 = lib.sinkattn_decode_workspace_size(2, 5000, 16, 2, 64, 0, 0)
+    assert n16 > n8 > 0
+    assert decode(lib, hq=32, hkv=2, batch=0) == B.SINKATTN_OK
     assert decode(lib, hq=9, hkv=2) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert decode(lib, table=FAKE, seqlens=FAKE, page=16, maxp=4) == B.SINKATTN_ERR_INVALID_ARGUMENT
     assert decode(lib, indptr=None) == B.SINKATTN_ERR_INVALID_ARGUMENT

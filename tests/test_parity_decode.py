@@ -177,3 +177,30 @@ def test_decode_paged_full_config(oracle_lib, window):
                                   head_dim=64, sinks=c.sinks, causal=True, window=window,
                                   scale=c.scale)
     check_close(out[seqs], lse[seqs], ro, rl, "paged_decode w=%d" % window)
+
+
+# Groups above 8 query heads per KV head: tiles of 8 heads (the last one
+# partial for 12 and 24), one block or warp per tile, over contiguous and
+# paged caches, automatic and explicit split plans, the one-warp-per-pair
+# form (window 100) and head_dim 128.
+@pytest.mark.parametrize("hq,hkv", [(16, 1), (64, 4), (12, 1), (24, 1), (64, 1)])
+@pytest.mark.parametrize("paged,window", [(False, 0), (True, 0), (False, 100), (True, 100)])
+def test_decode_groups_above_eight(oracle_lib, hq, hkv, paged, window):
+    c = S.make_decode("bigroup", LENS, hq, hkv, seed=171 + hq + hkv + window, window=window,
+                      paged=paged, page_size=16, sink_std=1.5)
+    ro, rl = oracle_decode(oracle_lib, c)
+    for num_splits in (0, 3):
+        out, lse = run_decode(c, num_splits=num_splits)
+        check_close(out, lse, ro, rl, "group %d paged=%s w=%d splits=%d"
+                    % (hq // hkv, paged, window, num_splits))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_group_sixteen_long_contexts(oracle_lib, d):
+    """64 q / 4 kv heads (groups of 16) over long contexts: split plans with
+    the last-block merge per (sequence, KV head, head tile)."""
+    c = S.make_decode("g16long", [5000, 4097, 1, 300, 6144, 0, 12000], 64, 4, seed=181 + d,
+                      head_dim=d)
+    out, lse = run_decode(c)
+    ro, rl = oracle_decode(oracle_lib, c)
+    check_close(out, lse, ro, rl, "group 16 long d=%d" % d)

@@ -58,7 +58,7 @@ def reference(c, seqs=None, scales=True):
 LENS = [1, 31, 32, 33, 127, 128, 129, 511, 512, 513, 1000, 1537, 2048, 3001, 0, 77]
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (64, 8), (24, 3)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (64, 8), (24, 3), (32, 2)])
 @pytest.mark.parametrize("window", [0, 1, 100])
 def test_decode_fp8_contiguous(hq, hkv, window):
     c = S.make_decode("fp8", LENS, hq, hkv, seed=141 + hq + window, window=window,
