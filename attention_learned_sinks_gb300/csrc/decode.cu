@@ -268,10 +268,14 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
     };
 #pragma unroll
     for (int ks = 0; ks < kKS; ++ks) {
-      // fp8: k positions 2lc, 2lc+1 / 2lc+8, 2lc+9 of the k-step stand for
-      // dims 4lc, 4lc+1 / 4lc+2, 4lc+3 (the K fragments use the same order)
-      qf[ks][0] = frag(ks * 16 + (kFp8 ? 4 * lc : 2 * lc));
-      qf[ks][1] = frag(ks * 16 + (kFp8 ? 4 * lc + 2 : 2 * lc + 8));
+      // fp8: k positions 2lc, 2lc+1 / 2lc+8, 2lc+9 of k-step ks stand for
+      // dims f, f+1 / f+2, f+3 with f = 16 (lc + 4 (ks / 4)) + 4 (ks % 4), so
+      // that one 16-byte load of K row r at chunk lc + 4 (ks / 4) holds the
+      // row's A-fragment bytes of four k-steps (the K fragments use the same
+      // order; a dot product does not depend on it)
+      const int f = kFp8 ? 16 * (lc + 4 * (ks >> 2)) + 4 * (ks & 3) : ks * 16 + 2 * lc;
+      qf[ks][0] = frag(f);
+      qf[ks][1] = frag(kFp8 ? f + 2 : f + 8);
     }
   }
   // fp8: the K scale multiplies every score, the V scale every output
@@ -362,14 +366,19 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
     for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[mt][e] = 0.f;
+      uint4 kx0, kx1;  // fp8: rows lr / lr + 8, 16 bytes = four k-steps' words
 #pragma unroll
       for (int ks = 0; ks < kKS; ++ks) {
         uint32_t a[4];
         if (kFp8) {
-          // rows lr and lr + 8: dims 4lc..4lc+3 of the k-step, one word each
-          const int r0 = mt * 16 + lr, r1 = r0 + 8;
-          const uint32_t x0 = *reinterpret_cast<const uint32_t *>(k8 + swz8<D>(r0, ks) + 4 * lc);
-          const uint32_t x1 = *reinterpret_cast<const uint32_t *>(k8 + swz8<D>(r1, ks) + 4 * lc);
+          if ((ks & 3) == 0) {
+            const int r0 = mt * 16 + lr, r1 = r0 + 8;
+            kx0 = *reinterpret_cast<const uint4 *>(k8 + swz8<D>(r0, lc + 4 * (ks >> 2)));
+            kx1 = *reinterpret_cast<const uint4 *>(k8 + swz8<D>(r1, lc + 4 * (ks >> 2)));
+          }
+          const int q = ks & 3;
+          const uint32_t x0 = q == 0 ? kx0.x : q == 1 ? kx0.y : q == 2 ? kx0.z : kx0.w;
+          const uint32_t x1 = q == 0 ? kx1.x : q == 1 ? kx1.y : q == 2 ? kx1.z : kx1.w;
           e4m3x4_to_f16x4(x0, a[0], a[2]);
           e4m3x4_to_f16x4(x1, a[1], a[3]);
           mma_f16_16816(s[mt], a, qf[ks][0], qf[ks][1]);
@@ -441,25 +450,50 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
       o[dt][3] *= al1;
     }
     // O^T += V^T P^T
+    if constexpr (kFp8) {
+      // MMA rows lr / lr + 8 of dim tile dt stand for dims (D / 8) lr + 2 dt
+      // and + 1: one (D / 8)-byte load per token (tokens t, t+1, t+8, t+9)
+      // holds the lane's bytes of every dim tile, paired across tokens with a
+      // byte permute (undone when O is stored)
+      constexpr int kW = D / 32;  // 32-bit words per token load
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int t = mt * 16 + 2 * lc;
+        const int byte0 = (D / 8) * lr;
+        const int chunk = byte0 >> 4, within = byte0 & 15;
+        uint32_t w[4][kW];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = t + (i & 1) + 8 * (i >> 1);
+          const uint8_t *src = v8 + swz8<D>(tok, chunk) + within;
+          if constexpr (kW == 2) {
+            const uint2 x = *reinterpret_cast<const uint2 *>(src);
+            w[i][0] = x.x;
+            w[i][1] = x.y;
+          } else {
+            const uint4 x = *reinterpret_cast<const uint4 *>(src);
+            w[i][0] = x.x;
+            w[i][1] = x.y;
+            w[i][2] = x.z;
+            w[i][3] = x.w;
+          }
+        }
+#pragma unroll
+        for (int dt = 0; dt < kKS; ++dt) {
+          uint32_t a[4];
+          const unsigned sel = (dt & 1) ? 0x7362u : 0x5140u;
+          e4m3x4_to_f16x4(__byte_perm(w[0][dt >> 1], w[1][dt >> 1], sel), a[0], a[1]);
+          e4m3x4_to_f16x4(__byte_perm(w[2][dt >> 1], w[3][dt >> 1], sel), a[2], a[3]);
+          mma_f16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
+        }
+      }
+    } else
 #pragma unroll
     for (int dt = 0; dt < kKS; ++dt)
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         uint32_t a[4];
-        if (kFp8) {
-          // MMA rows lr / lr + 8 are dims 2lr / 2lr + 1 of the 16-dim tile:
-          // one 16-bit load per token (tokens t, t+1, t+8, t+9), bytes paired
-          // across tokens with a byte permute
-          const int t = mt * 16 + 2 * lc;
-          const int off = 2 * lr;
-          const uint32_t w0 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t, dt) + off);
-          const uint32_t w1 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t + 1, dt) + off);
-          const uint32_t w2 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t + 8, dt) + off);
-          const uint32_t w3 = *reinterpret_cast<const uint16_t *>(v8 + swz8<D>(t + 9, dt) + off);
-          e4m3x4_to_f16x4(__byte_perm(w0, w1, 0x5140), a[0], a[1]);
-          e4m3x4_to_f16x4(__byte_perm(w2, w3, 0x5140), a[2], a[3]);
-          mma_f16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
-        } else {
+        {
           const int row = mt * 16 + (mi >> 1) * 8 + mr;
           ldmatrix_x4_trans(vb + swz<D>(row, dt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
           mma_bf16_16816(o[dt], a, pb[mt][0], pb[mt][1]);
@@ -476,8 +510,9 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
   }
 
   // O^T rows lr / lr + 8 of dim tile dt are dims dt*16 + lr / + 8 (bf16),
-  // dt*16 + 2lr / + 1 (fp8)
-  const int dr0 = kFp8 ? 2 * lr : lr, dr1 = kFp8 ? 2 * lr + 1 : lr + 8;
+  // (D / 8) lr + 2 dt / + 1 (fp8)
+  auto odim0 = [&](int dt) { return kFp8 ? (D / 8) * lr + 2 * dt : dt * 16 + lr; };
+  auto odim1 = [&](int dt) { return kFp8 ? (D / 8) * lr + 2 * dt + 1 : dt * 16 + lr + 8; };
 
   if constexpr (kPair) {
     // ---- one pair per warp: the state is final; stage it in this warp's
@@ -495,10 +530,10 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
     }
 #pragma unroll
     for (int dt = 0; dt < kKS; ++dt) {
-      po[(2 * lc) * D + dt * 16 + dr0] = o[dt][0];
-      po[(2 * lc + 1) * D + dt * 16 + dr0] = o[dt][1];
-      po[(2 * lc) * D + dt * 16 + dr1] = o[dt][2];
-      po[(2 * lc + 1) * D + dt * 16 + dr1] = o[dt][3];
+      po[(2 * lc) * D + odim0(dt)] = o[dt][0];
+      po[(2 * lc + 1) * D + odim0(dt)] = o[dt][1];
+      po[(2 * lc) * D + odim1(dt)] = o[dt][2];
+      po[(2 * lc + 1) * D + odim1(dt)] = o[dt][3];
     }
     __syncwarp();
     const int hh = lane >> 2;
@@ -539,10 +574,10 @@ __global__ void __launch_bounds__(kThreads, (Ring<D, kPaged, kFp8, kPair>::kBloc
 #pragma unroll
   for (int dt = 0; dt < kKS; ++dt) {
     float *ow = sm_o + warp * kMaxGroup * D;
-    ow[(2 * lc) * D + dt * 16 + dr0] = o[dt][0];
-    ow[(2 * lc + 1) * D + dt * 16 + dr0] = o[dt][1];
-    ow[(2 * lc) * D + dt * 16 + dr1] = o[dt][2];
-    ow[(2 * lc + 1) * D + dt * 16 + dr1] = o[dt][3];
+    ow[(2 * lc) * D + odim0(dt)] = o[dt][0];
+    ow[(2 * lc + 1) * D + odim0(dt)] = o[dt][1];
+    ow[(2 * lc) * D + odim1(dt)] = o[dt][2];
+    ow[(2 * lc + 1) * D + odim1(dt)] = o[dt][3];
   }
   __syncthreads();
 
