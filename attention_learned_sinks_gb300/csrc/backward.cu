@@ -83,9 +83,11 @@ struct BwdParams {
   int batch, hq, hkv, group, causal, window;
   int total_q;
   float scale, scale_log2;
-  const float *lse2t;  // [hq][total_q]: lse * log2(e) (+inf: row with no key and no sink)
-  float *dt;           // [hq][total_q]: D from the forward output
-  float *de;           // [hq][total_q]: exact D (dQ kernel; the same array as dt at D = 64)
+  // Per (head, row) vectors, stored negated so that the dK/dV kernel's copies
+  // of a tile's 128 entries are the softmax-side operands as they stand:
+  const float *nl2t;  // [hq][total_q]: -lse * log2(e) (-inf: row with no key and no sink)
+  float *ndt;         // [hq][total_q]: -D from the forward output
+  float *nde;         // [hq][total_q]: -(exact D) (dQ kernel; the same array as ndt at D = 64)
   const unsigned *q_pairs, *k_pairs;
   const int *num_q_pairs, *num_k_pairs;
   unsigned *q_counter, *k_counter;  // work counters of the persistent kernels (zeroed by the lists)
@@ -104,7 +106,7 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_q_kernel(
     const uint4 *__restrict__ q, const uint4 *__restrict__ dout, const uint4 *__restrict__ out,
     const float *__restrict__ lse, int64_t total_q, int hq, uint4 *__restrict__ q16,
-    uint4 *__restrict__ do16, float *__restrict__ lse2t, float *__restrict__ dt) {
+    uint4 *__restrict__ do16, float *__restrict__ nl2t, float *__restrict__ ndt) {
   constexpr int kPer = D / 8;  // threads per (row, head)
   const int64_t n = total_q * hq * kPer;
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < n;
@@ -127,8 +129,8 @@ __global__ void __launch_bounds__(256) bwd_prep_q_kernel(
       const int64_t row = rh / hq;
       const int h = static_cast<int>(rh % hq);
       const float l = lse[rh];
-      lse2t[h * total_q + row] = l == -INFINITY ? INFINITY : l * kLog2e;
-      dt[h * total_q + row] = part;
+      nl2t[h * total_q + row] = l == -INFINITY ? -INFINITY : -(l * kLog2e);
+      ndt[h * total_q + row] = -part;
     }
   }
 }
@@ -147,8 +149,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kv_kernel(const uint4 *__restric
 // dc_h = -sum_i e^{c_h - lse_i} D_i over every row of head h; double
 // accumulation in a fixed order (per-thread strides, then a fixed tree).
 __global__ void __launch_bounds__(256) bwd_dsink_kernel(const float *__restrict__ sinks,
-                                                        const float *__restrict__ lse2t,
-                                                        const float *__restrict__ dt,
+                                                        const float *__restrict__ nl2t,
+                                                        const float *__restrict__ ndt,
                                                         int64_t total_q,
                                                         float *__restrict__ dsinks) {
   // the dK/dV kernel does not read dsinks: it may start at once
@@ -158,8 +160,8 @@ __global__ void __launch_bounds__(256) bwd_dsink_kernel(const float *__restrict_
   const float c2 = sinks[h] * kLog2e;
   double acc = 0.0;
   for (int64_t r = threadIdx.x; r < total_q; r += blockDim.x) {
-    const float l2 = lse2t[h * total_q + r];
-    if (l2 != INFINITY) acc -= static_cast<double>(exp2f(c2 - l2)) * dt[h * total_q + r];
+    const float nl2 = nl2t[h * total_q + r];  // -lse log2(e); the second factor is -D
+    if (nl2 != -INFINITY) acc += static_cast<double>(exp2f(c2 + nl2)) * ndt[h * total_q + r];
   }
   part[threadIdx.x] = acc;
   __syncthreads();
@@ -222,7 +224,8 @@ __device__ __forceinline__ void p_ds_col(float (&s)[32], const float (&dp)[32], 
 // 64w..64w+63 into P and dS. The warpgroups release S / dP as soon as they
 // have loaded them, so the next tile's S and dP are computed while they
 // work, and dQ / Y of a tile run while the next one is being softmaxed.
-// Warp 8: TMA (Q and dO double-buffered per item, K/V in a 3-stage ring);
+// Warp 8: TMA (Q and dO double-buffered per item, K/V in a 4-stage ring at
+// head_dim 64, 2 stages at 128);
 // warp 9: issues S and dP and owns TMEM; warp 10: issues dQ and Y.
 //
 // TMEM columns: S [0, 128), dP [128, 256), dS fp16 [256, 320), P fp16
@@ -243,15 +246,15 @@ constexpr int kHalf = 64;  // keys (dK/dV: queries) of a tile per softmax warpgr
 // ss: both operands K-major in shared memory, 128 x 128 scores (S = Q K^T, ...)
 constexpr uint32_t kIdescSS128 = idesc_f32acc(128, kBN, /*bf16=*/false, false, false);
 constexpr int kDqThreads = 352;
-constexpr int kDqStages = 3;  // K/V ring at D = 64 (the array size of the barriers)
+constexpr int kDqStages = 4;  // K/V ring at D = 64 (the array size of the barriers)
 
 // Shared memory of the dQ kernel: Q/dO buffers (two at D = 64, one at 128),
-// the K/V ring (three stages at 64, two at 128), then the control block.
+// the K/V ring (four stages at 64, two at 128), then the control block.
 template <int D>
 struct DqCfg {
   static constexpr int kTile = TileShape<D>::kBytes;
   static constexpr int kQdBufs = D == 64 ? 2 : 1;
-  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kQdBufs * 2 * kTile;
   static constexpr int kOffV = kOffK + kStages * kTile;
@@ -281,6 +284,7 @@ struct DqBars {
 };
 
 static_assert(sizeof(DqBars) <= 4096, "dQ control block");
+static_assert(DqCfg<64>::kSmem <= 227 * 1024, "dQ shared memory at head_dim 64");
 static_assert(DqCfg<128>::kSmem <= 227 * 1024, "dQ shared memory at head_dim 128");
 
 // work index w -> item: 64-dim half w % halves of the output, then
@@ -528,13 +532,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             reinterpret_cast<uint4 *>(dq_row)[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (wg == 0 && t.half == 0) p.de[lidx] = 0.f;
+          if (wg == 0 && t.half == 0) p.nde[lidx] = 0.f;
         }
         mbar_arrive(&bars->tile_empty[slot]);
         continue;
       }
-      const float l2 = r < t.rows ? p.lse2t[lidx] : INFINITY;
-      const float d = r < t.rows ? p.dt[lidx] : 0.f;
+      const float l2 = r < t.rows ? -p.nl2t[lidx] : INFINITY;
+      const float d = r < t.rows ? -p.ndt[lidx] : 0.f;
       const int pos = t.p_min + r;
       int hi = t.lk, lo = 0;
       if (p.causal) hi = min(hi, pos + 1);
@@ -619,7 +623,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
                              pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
         }
-        if (wg == 0 && t.half == 0) p.de[lidx] = d_e;
+        if (wg == 0 && t.half == 0) p.nde[lidx] = -d_e;
       }
       mbar_arrive(&bars->tile_empty[slot]);
     }
@@ -642,30 +646,31 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // products; softmax-side warpgroup w (one key per thread) turns queries
 // 64w..64w+63 into P^T and dS^T and releases S^T / dP^T once it has loaded
 // them, so the next step's products are computed while it works. Warp 8: TMA
-// (K/V double-buffered per item; Q, dO and the step's lse / D vectors in a
-// 3-stage ring); warp 9: issues S^T and dP^T and owns TMEM; warp 10: issues
+// (K/V double-buffered per item; Q, dO and the step's -lse / -D vectors in a
+// 4-stage ring at head_dim 64, 2 stages at 128); warp 9: issues S^T and dP^T and owns TMEM; warp 10: issues
 // dV and dK.
 //
 // TMEM columns: S^T [0, 128), dP^T [128, 256), P^T fp16 [256, 320), dS^T
 // fp16 [320, 384) (warpgroup w's queries in the half at 32w), dV [384, 448),
 // dK [448, 512).
 constexpr int kKvThreads = 352;
-constexpr int kKvQStages = 3;  // Q/dO ring at D = 64 (the array size of the barriers)
+constexpr int kKvQStages = 4;  // Q/dO ring at D = 64 (the array size of the barriers)
 
 // Shared memory of the dK/dV kernel: K/V item buffers (two at D = 64, one at
-// 128), the Q/dO ring (three stages at 64, two at 128) with each stage's
+// 128), the Q/dO ring (four stages at 64, two at 128) with each stage's
 // -lse / -D vectors, then the control block.
 template <int D>
 struct KvCfg {
   static constexpr int kTile = TileShape<D>::kBytes;
   static constexpr int kKvBufs = D == 64 ? 2 : 1;
-  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffQ = kKvBufs * 2 * kTile;
   static constexpr int kOffVec = kOffQ + kStages * 2 * kTile;
   static constexpr int kOffBar = kOffVec + kStages * 1024;
   static constexpr int kSmem = kOffBar + 1024 + 1024;
 };
+static_assert(KvCfg<64>::kSmem <= 227 * 1024, "dK/dV shared memory at head_dim 64");
 static_assert(KvCfg<128>::kSmem <= 227 * 1024, "dK/dV shared memory at head_dim 128");
 
 struct KvTile {
@@ -817,16 +822,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           ok = false;
           break;
         }
-        // lse2 / D of the tile's 128 query rows (rows past the sequence: empty)
-        float *vec = reinterpret_cast<float *>(smem + kKvOffVec + st * 1024);
+        // -l2 / -D of the tile's 128 query rows, copied asynchronously and
+        // tracked by the stage's barrier (the pending count each lane adds is
+        // released when its copies land). Rows past the sequence read as 0:
+        // their columns are masked, so P and dS are 0 there whatever the value.
+        const uint32_t vec = sbase + kKvOffVec + st * 1024;
         const int valid = t.lq - qt * kBM;
         const size_t at = static_cast<size_t>(h) * p.total_q + t.q0 + qt * kBM;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = lane + 32 * i;
-          vec[row] = row < valid ? -p.lse2t[at + row] : -INFINITY;  // -l2, -D
-          vec[128 + row] = row < valid ? -p.de[at + row] : 0.f;
+          const bool in = row < valid;
+          cp_async_4(vec + 4 * row, p.nl2t + at + (in ? row : 0), in ? 4u : 0u);
+          cp_async_4(vec + 512 + 4 * row, p.nde + at + (in ? row : 0), in ? 4u : 0u);
         }
+        cp_async_mbar_arrive(&bars->qd_full[st]);
         __syncwarp();
         mbar_arrive_expect_tx_elect(&bars->qd_full[st], 2 * kTileBytes);
         load_tile(sbase + kKvOffQ + st * 2 * kTileBytes, &tm_q, &bars->qd_full[st], h,
@@ -1049,7 +1059,7 @@ size_t list_bytes(int batch, int64_t total) {  // counter + pairs of one tile li
 }  // namespace
 
 // Workspace: q16, do16 [total_q, hq, D] fp16; k16, v16 [total_k, hkv, D]
-// fp16; lse2t, dt [hq, total_q] fp32 (+ the exact D de at D = 128); the
+// fp16; nl2t, ndt [hq, total_q] fp32 (+ the exact D nde at D = 128); the
 // query-tile and key-tile lists.
 size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int hq, int hkv,
                                 int head_dim) {
@@ -1070,11 +1080,11 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
   const size_t kb = round256(static_cast<size_t>(a.total_k) * a.hkv * D * 2);
   const size_t vb = round256(static_cast<size_t>(a.total_q) * a.hq * 4);
   uint8_t *q16 = ws, *do16 = ws + qb, *k16 = ws + 2 * qb, *v16 = ws + 2 * qb + kb;
-  float *lse2t = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb);
-  float *dt = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb + vb);
+  float *nl2t = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb);
+  float *ndt = reinterpret_cast<float *>(ws + 2 * qb + 2 * kb + vb);
   // exact D: in place of the forward's at D = 64 (one item per row and head);
   // its own array at D = 128, where both halves of a row read the forward's
-  float *de = D == 64 ? dt : reinterpret_cast<float *>(ws + 2 * qb + 2 * kb + 2 * vb);
+  float *nde = D == 64 ? ndt : reinterpret_cast<float *>(ws + 2 * qb + 2 * kb + 2 * vb);
   uint8_t *qlist = ws + 2 * qb + 2 * kb + (D == 64 ? 2 : 3) * vb;
   uint8_t *klist = qlist + list_bytes(a.batch, a.total_q);
 
@@ -1086,7 +1096,7 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
                            stream>>>(
         static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.dout),
         static_cast<const uint4 *>(a.out), a.lse, a.total_q, a.hq, reinterpret_cast<uint4 *>(q16),
-        reinterpret_cast<uint4 *>(do16), lse2t, dt);
+        reinterpret_cast<uint4 *>(do16), nl2t, ndt);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.total_k > 0) {
@@ -1111,9 +1121,9 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
   p.total_q = static_cast<int>(a.total_q);
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
-  p.lse2t = lse2t;
-  p.dt = dt;
-  p.de = de;
+  p.nl2t = nl2t;
+  p.ndt = ndt;
+  p.nde = nde;
   p.q_pairs = reinterpret_cast<const unsigned *>(qlist + 256);
   p.num_q_pairs = reinterpret_cast<const int *>(qlist + 4);
   p.q_counter = reinterpret_cast<unsigned *>(qlist);
@@ -1161,7 +1171,7 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
   }
   const bool dsink = a.sinks != nullptr && a.dsinks != nullptr;
   if (dsink) {  // after dQ: D is exact by now
-    bwd_dsink_kernel<<<a.hq, 256, 0, stream>>>(a.sinks, lse2t, de, a.total_q, a.dsinks);
+    bwd_dsink_kernel<<<a.hq, 256, 0, stream>>>(a.sinks, nl2t, nde, a.total_q, a.dsinks);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.total_k > 0) {

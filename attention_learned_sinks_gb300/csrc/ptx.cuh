@@ -92,6 +92,17 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
                "r"(src_bytes)
                : "memory");
 }
+// 4-byte copy (zero-filled past src_bytes, which is 0 or 4).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// The barrier's current phase also waits for this thread's earlier cp.async
+// copies: the pending count is raised by one now and lowered when they land.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
