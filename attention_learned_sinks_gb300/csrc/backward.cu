@@ -557,15 +557,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int key0 = (t.kt_lo + j) * kBN + wg * kHalf;
         const int c_lo = min(max(lo - key0, 0), kHalf);
         const int len = max(min(hi - key0, kHalf) - c_lo, 0);
-        // boundary tiles only (warp-uniform, so the loads stay collective)
-        const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
+        // 32-column chunks that some row of the warp does not see whole only
+        // (warp-uniform, so the loads stay collective)
+        const int end = c_lo + len;
+        const bool mask_a = !__all_sync(0xffffffffu, c_lo <= 0 && end >= 32);
+        const bool mask_b = !__all_sync(0xffffffffu, c_lo <= 32 && end >= 64);
         uint32_t p16a[16], ds16a[16];
         {
           float sv[32], dp[32];
           tmem_ld32f(t_s, sv);
           tmem_ld32f(t_dp, dp);
           tmem_wait_ld();
-          if (masked) mask32(sv, 0, c_lo, len);
+          if (mask_a) mask32(sv, 0, c_lo, len);
           p_ds_row(sv, dp, p.scale_log2, l2, d, p16a, ds16a, dsum);
         }
         float sv[32], dp[32];
@@ -574,7 +577,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars->s_read);  // S / dP of the next tile may be computed
-        if (masked) mask32(sv, 32, c_lo, len);
+        if (mask_b) mask32(sv, 32, c_lo, len);
         uint32_t p16b[16], ds16b[16];
         p_ds_row(sv, dp, p.scale_log2, l2, d, p16b, ds16b, dsum);
         // dQ / Y of tile g - 1 have finished reading dS / P
@@ -977,7 +980,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (p.causal) c_lo = min(max(jk - qb, 0), kHalf);
         if (p.window > 0) c_hi = min(c_hi, max(jk - qb + p.window, 0));
         const int len = r < t.krows ? max(c_hi - c_lo, 0) : 0;
-        const bool masked = __any_sync(0xffffffffu, c_lo != 0 || len != kHalf);
+        // 32-column chunks that some key of the warp does not see whole only
+        const int end = c_lo + len;
+        const bool mask_a = !__all_sync(0xffffffffu, c_lo <= 0 && end >= 32);
+        const bool mask_b = !__all_sync(0xffffffffu, c_lo <= 32 && end >= 64);
         const float *vec =
             reinterpret_cast<const float *>(smem + kKvOffVec + st * 1024) + wg * kHalf;
         uint32_t p16a[16], ds16a[16];
@@ -986,7 +992,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_ld32f(t_st, sv);
           tmem_ld32f(t_dpt, dp);
           tmem_wait_ld();
-          if (masked) mask32(sv, 0, c_lo, len);
+          if (mask_a) mask32(sv, 0, c_lo, len);
           p_ds_col(sv, dp, p.scale_log2, vec, vec + 128, p16a, ds16a);
         }
         float sv[32], dp[32];
@@ -995,7 +1001,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars->s_read);  // S^T / dP^T of the next step may be computed
-        if (masked) mask32(sv, 32, c_lo, len);
+        if (mask_b) mask32(sv, 32, c_lo, len);
         uint32_t p16b[16], ds16b[16];
         p_ds_col(sv, dp, p.scale_log2, vec + 32, vec + 128 + 32, p16b, ds16b);
         // dV / dK of step g - 1 have finished reading P^T / dS^T

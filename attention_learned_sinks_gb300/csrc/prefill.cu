@@ -773,10 +773,14 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
           if (p.window > 0) lo = max(lo, pos - p.window + 1);
           const int c_lo = min(max(lo - key0, 0), kBN);
           const int len = max(min(hi - key0, kBN) - c_lo, 0);
-          mask32(s0, 0, c_lo, len);
-          mask32(s1, 32, c_lo, len);
-          mask32(s2, 64, c_lo, len);
-          mask32(s3, 96, c_lo, len);
+          // a 32-column chunk that every row of the warp sees whole needs no
+          // test (under a causal or window bound, only the chunks that the
+          // warp's rows' bounds fall in do)
+          const int c_hi = c_lo + len;
+          if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 32)) mask32(s0, 0, c_lo, len);
+          if (!__all_sync(0xffffffffu, c_lo <= 32 && c_hi >= 64)) mask32(s1, 32, c_lo, len);
+          if (!__all_sync(0xffffffffu, c_lo <= 64 && c_hi >= 96)) mask32(s2, 64, c_lo, len);
+          if (!__all_sync(0xffffffffu, c_lo <= 96 && c_hi >= 128)) mask32(s3, 96, c_lo, len);
         }
         const float mx = max3(fmaxf(row_max32(s0), row_max32(s1)), row_max32(s2), row_max32(s3));
         const float m_tile = mx * c;

@@ -360,10 +360,16 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
 
 // Columns outside this row's visible range [c_lo, c_lo + len) of the tile -> -inf.
 // col0 is the first tile column held in sv.
+// The range is first turned into a 32-bit visibility mask of the held columns,
+// so each column costs one bit test and one select.
 __device__ __forceinline__ void mask32(float (&sv)[32], int col0, int c_lo, int len) {
+  const int a = min(max(c_lo - col0, 0), 32), b = min(max(c_lo + len - col0, 0), 32);
+  const unsigned below_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
+  const unsigned below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
+  const unsigned vis = below_b & ~below_a;
 #pragma unroll
   for (int i = 0; i < 32; ++i)
-    if (static_cast<unsigned>(col0 + i - c_lo) >= static_cast<unsigned>(len)) sv[i] = -INFINITY;
+    if (!(vis & (1u << i))) sv[i] = -INFINITY;
 }
 
 // registers -> 16 consecutive 32-bit TMEM columns of this thread's lane.
