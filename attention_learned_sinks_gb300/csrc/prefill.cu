@@ -27,7 +27,7 @@
 // (NT = 1: one softmax warpgroup, warps 4-7 in the same roles.) A K stage is
 // released once the tile's Q K^T has read it and a V stage once its P V has,
 // so K loads never wait for P V. setmaxnreg moves registers from warps 8-11
-// (104 each) to the two softmax warpgroups (200 each).
+// (88 each) to the two softmax warpgroups (208 each).
 // TMEM (512 columns): O_t at [384 + D t, ...) and score buffers in
 // [0, 384). NT = 2: three 128-column S buffers shared round-robin by the work
 // items k = NT j + t (KV tile j, query tile t); P_k (fp16 pairs) overwrites
@@ -104,11 +104,12 @@ struct Cfg {
 };
 
 // Register split of the NT = 2 kernel (setmaxnreg): 168 registers a thread at
-// launch (the ptxas limit for 384 threads), then 104 for the producer / MMA
-// warpgroup and 200 for each softmax warpgroup.
+// launch (the ptxas limit for 384 threads), then 88 for the producer / MMA
+// warpgroup and 208 for each softmax warpgroup (72 / 216 made the producer
+// path spill: window-128 prefill 6% slower).
 constexpr int kLaunchRegs2 = 168;
-constexpr int kRegsOther2 = 104;
-constexpr int kRegsSoftmax2 = 200;
+constexpr int kRegsOther2 = 88;
+constexpr int kRegsSoftmax2 = 208;
 static_assert(kRegsOther2 * 128 + kRegsSoftmax2 * 256 <= kLaunchRegs2 * Cfg<2, 64>::kThreads,
               "register split must fit the registers the block is launched with");
 // Dual CTAs (one head per item, head_dim 64, two CTAs per SM): 128 registers
