@@ -519,6 +519,51 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // testing hook: a wait that runs out while the first copies and products
     // are in flight
     bool ok = p.stall_ns == 0 || mbar_wait_warp(&bars->never, 0, abort, err, false, p.stall_ns);
+    // An item's epilogue (exact D, dQ from TMEM, store) runs after the next
+    // item's first dS / P have been handed to the tensor core: the item's last
+    // dQ / Y products then complete while this warpgroup already computes, and
+    // the next item's scores are not held up behind the stores. The pending
+    // item's row, D and flags are kept here; its partial exact-D sums wait in
+    // the dsum buffer of its parity.
+    bool pend_on = false, pend_row = false, pend_de = false;
+    __nv_bfloat16 *pend_dq = nullptr;
+    size_t pend_lidx = 0;
+    float pend_d = 0.f;
+    auto finish = [&]() {
+      const int par = dq_items & 1;
+      if (!mbar_wait_warp(&bars->dsum_full[par], (dq_items >> 1) & 1, abort, err)) {
+        ok = false;
+        return;
+      }
+      const float *xs = bars->dsum[par][0];
+      const float d_e = xs[r] + xs[128 + r];
+      const float corr = d_e - pend_d;
+      if (!mbar_wait_warp(&bars->dq_done, par, abort, err)) {
+        ok = false;
+        return;
+      }
+      ++dq_items;
+      tc_fence_after();
+      float a[32], y[32];
+      tmem_ld32f(t_dq, a);
+      tmem_ld32f(t_y, y);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);  // the next item's dQ / Y may start
+      if (pend_row) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(pend_dq);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = p.scale * fmaf(-corr, y[8 * i + e], a[8 * i + e]);
+          d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                             pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+        }
+        if (pend_de) p.nde[pend_lidx] = -d_e;
+      }
+      pend_on = false;
+    };
     for (int nt = 0; ok; ++nt) {
       const int slot = nt & 1;
       if (!mbar_wait_warp(&bars->tile_full[slot], (nt >> 1) & 1, abort, err)) break;
@@ -595,41 +640,27 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->ds_full);
+        if (j == 0 && pend_on) {
+          finish();
+          if (!ok) break;
+        }
       }
       if (!ok) break;
       G += t.n;
       // exact D = both warpgroups' partial sums of P dP (exchanged through
       // shared memory; a bounded mbarrier wait, so an aborting CTA cannot
       // leave the other warpgroup waiting)
-      float *xs = bars->dsum[dq_items & 1][0];
-      xs[wg * 128 + r] = dsum.x + dsum.y;
+      (&bars->dsum[dq_items & 1][0][0])[wg * 128 + r] = dsum.x + dsum.y;
       mbar_arrive(&bars->dsum_full[dq_items & 1]);
-      if (!mbar_wait_warp(&bars->dsum_full[dq_items & 1], (dq_items >> 1) & 1, abort, err)) break;
-      const float d_e = xs[r] + xs[128 + r];
-      const float corr = d_e - d;
-      if (!mbar_wait_warp(&bars->dq_done, dq_items & 1, abort, err)) break;
-      ++dq_items;
-      tc_fence_after();
-      float a[32], y[32];
-      tmem_ld32f(t_dq, a);
-      tmem_ld32f(t_y, y);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);  // the next item's dQ / Y may start
-      if (r < t.rows) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(dq_row);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float o[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = p.scale * fmaf(-corr, y[8 * i + e], a[8 * i + e]);
-          d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                             pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-        }
-        if (wg == 0 && t.half == 0) p.nde[lidx] = -d_e;
-      }
+      pend_on = true;
+      pend_row = r < t.rows;
+      pend_de = wg == 0 && t.half == 0;
+      pend_dq = dq_row;
+      pend_lidx = lidx;
+      pend_d = d;
       mbar_arrive(&bars->tile_empty[slot]);
     }
+    if (ok && pend_on) finish();
   }
 
   tc_fence_before();
