@@ -96,6 +96,9 @@ struct BwdParams {
   // stall_ns on a barrier that nothing completes before their first scores,
   // so that every CTA of that kernel takes its timeout path.
   uint64_t stall_ns;
+  // dq, dk and dv start on 32-byte boundaries: rows are stored with 32-byte
+  // stores (whole sectors, half the store instructions)
+  int grad_v8;
 };
 
 // ----------------------------------------------------------------- prep ---
@@ -551,14 +554,26 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->dq_free);  // the next item's dQ / Y may start
       if (pend_row) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(pend_dq);
+        if (p.grad_v8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float o[8];
+          for (int i = 0; i < 2; ++i) {
+            uint32_t w[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = p.scale * fmaf(-corr, y[8 * i + e], a[8 * i + e]);
-          d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                             pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack_bf16x2(p.scale * fmaf(-corr, y[16 * i + 2 * e], a[16 * i + 2 * e]),
+                                 p.scale * fmaf(-corr, y[16 * i + 2 * e + 1], a[16 * i + 2 * e + 1]));
+            st_global_v8(pend_dq + 16 * i, w);
+          }
+        } else {
+          uint4 *d4 = reinterpret_cast<uint4 *>(pend_dq);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = p.scale * fmaf(-corr, y[8 * i + e], a[8 * i + e]);
+            d4[i] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                               pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+          }
         }
         if (pend_de) p.nde[pend_lidx] = -d_e;
       }
@@ -1063,17 +1078,33 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->dkv_free);
       if (r < t.krows) {
-        uint4 *v4 = reinterpret_cast<uint4 *>(p.dv + krow);
-        uint4 *k4 = reinterpret_cast<uint4 *>(p.dk + krow);
+        const float sc = p.scale;
+        if (p.grad_v8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float *x = reinterpret_cast<const float *>(&dvv[8 * i]);
-          const float *y = reinterpret_cast<const float *>(&dkv[8 * i]);
-          v4[i] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                             pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-          const float sc = p.scale;
-          k4[i] = make_uint4(pack_bf16x2(y[0] * sc, y[1] * sc), pack_bf16x2(y[2] * sc, y[3] * sc),
-                             pack_bf16x2(y[4] * sc, y[5] * sc), pack_bf16x2(y[6] * sc, y[7] * sc));
+          for (int i = 0; i < 2; ++i) {
+            const float *x = reinterpret_cast<const float *>(&dvv[16 * i]);
+            const float *y = reinterpret_cast<const float *>(&dkv[16 * i]);
+            uint32_t wv[8], wk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              wv[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+              wk[e] = pack_bf16x2(y[2 * e] * sc, y[2 * e + 1] * sc);
+            }
+            st_global_v8(p.dv + krow + 16 * i, wv);
+            st_global_v8(p.dk + krow + 16 * i, wk);
+          }
+        } else {
+          uint4 *v4 = reinterpret_cast<uint4 *>(p.dv + krow);
+          uint4 *k4 = reinterpret_cast<uint4 *>(p.dk + krow);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float *x = reinterpret_cast<const float *>(&dvv[8 * i]);
+            const float *y = reinterpret_cast<const float *>(&dkv[8 * i]);
+            v4[i] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                               pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+            k4[i] = make_uint4(pack_bf16x2(y[0] * sc, y[1] * sc), pack_bf16x2(y[2] * sc, y[3] * sc),
+                               pack_bf16x2(y[4] * sc, y[5] * sc), pack_bf16x2(y[6] * sc, y[7] * sc));
+          }
         }
       }
       mbar_arrive(&bars->tile_empty[slot]);
@@ -1170,6 +1201,8 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
   p.dq = static_cast<__nv_bfloat16 *>(a.dq);
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+  p.grad_v8 = ((reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |
+                reinterpret_cast<uintptr_t>(a.dv)) & 31u) == 0;
   p.stall_ns = g_bwd_stall_ns.load();
   if ((e = launch_tile_list(a.cu_q, a.batch, max_qtiles, reinterpret_cast<unsigned *>(qlist + 256),
                             reinterpret_cast<int *>(qlist + 4), reinterpret_cast<unsigned *>(qlist),

@@ -46,6 +46,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <mutex>
 
 #include "launch.h"
@@ -356,7 +357,10 @@ __global__ void __launch_bounds__(1024) build_worklist_kernel(const int32_t *cu_
 // is exhausted. Every role keeps running counters (S buffer items, K/V stages,
 // Q buffers, tiles) across tiles, so the next tile's loads and Q K^T overlap
 // the current tile's softmax and epilogue.
-template <int NT, int D>
+// kV8: out (and part_o) start on 32-byte boundaries, and each output row is
+// stored with 32-byte stores (whole sectors, half the store instructions);
+// otherwise with 16-byte ones.
+template <int NT, int D, bool kV8>
 __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -699,29 +703,56 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
       const float lse = pd > 0.f ? (pm + fast_log2(pd)) * kLn2 : -INFINITY;
       if (r < prows && p.num_splits > 1) {
         const size_t at = static_cast<size_t>(psplit) * p.total_q * p.hq + prow_h;
-        float4 *dst = reinterpret_cast<float4 *>(p.part_o + at * D);
+        if constexpr (kV8) {
+          float *dst = p.part_o + at * D;
 #pragma unroll
-        for (int q = 0; q < kQ; ++q)
+          for (int q = 0; q < kQ; ++q)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float *o = reinterpret_cast<const float *>(&ov[q][4 * i]);
-            dst[q * 8 + i] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-          }
+            for (int i = 0; i < 4; ++i) {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(ov[q][8 * i + e]) * inv);
+              st_global_v8(dst + q * 32 + 8 * i, w);
+            }
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(p.part_o + at * D);
+#pragma unroll
+          for (int q = 0; q < kQ; ++q)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float *o = reinterpret_cast<const float *>(&ov[q][4 * i]);
+              dst[q * 8 + i] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+            }
+        }
         p.part_lse[at] = lse;
       } else if (r < prows) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + prow_h * D);
+        if constexpr (kV8) {
+          __nv_bfloat16 *dst = p.out + prow_h * D;
 #pragma unroll
-        for (int q = 0; q < kQ; ++q)
+          for (int q = 0; q < kQ; ++q)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float *o = reinterpret_cast<const float *>(&ov[q][8 * i]);
-            uint4 v;
-            v.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-            v.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-            v.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-            v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-            dst[q * 4 + i] = v;
-          }
+            for (int i = 0; i < 2; ++i) {
+              const float *o = reinterpret_cast<const float *>(&ov[q][16 * i]);
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
+              st_global_v8(dst + q * 32 + 16 * i, w);
+            }
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.out + prow_h * D);
+#pragma unroll
+          for (int q = 0; q < kQ; ++q)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float *o = reinterpret_cast<const float *>(&ov[q][8 * i]);
+              uint4 v;
+              v.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+              v.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+              v.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+              v.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+              dst[q * 4 + i] = v;
+            }
+        }
         if (p.lse != nullptr) p.lse[prow_h] = lse;
       }
       pend_on = false;
@@ -1137,6 +1168,8 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
   p.part_lse = splits > 1 ? reinterpret_cast<float *>(
                                 part + partial_o_bytes(a.total_q, a.hq, splits, d))
                           : nullptr;
+  const bool v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0 &&
+                  (reinterpret_cast<uintptr_t>(p.part_o) & 31u) == 0;
   // head_dim 64: two heads per item when the group size is even; 128: one
   const int nt = d == 64 && p.group % 2 == 0 ? 2 : 1;
   build_worklist_kernel<<<1, 1024, 0, stream>>>(a.cu_q, a.batch, max_qtiles, pairs, num_pairs,
@@ -1171,45 +1204,41 @@ cudaError_t launch_core(const PrefillLaunch &a, const void *k, const void *v16, 
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
   };
-  if (nt == 2) {
-    using C2 = Cfg<2, 64>;
-    e = cudaFuncSetAttribute(prefill_kernel<2, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C2::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // setmaxnreg.inc waits until the registers exist: the block must be launched
-    // with at least the split's total, or the softmax warps would never start.
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
-      cudaFuncAttributes attr;
-      e = cudaFuncGetAttributes(&attr, prefill_kernel<2, 64>);
-      if (e != cudaSuccess) return e;
-      launch_regs = attr.numRegs;
+  // setmaxnreg.inc waits until the registers exist: a kernel with a register
+  // split must be launched with at least the split's total, or its softmax
+  // warps would never start.
+  auto launch = [&](auto ntc, auto dc, auto v8c) -> cudaError_t {
+    constexpr int NT = decltype(ntc)::value, D = decltype(dc)::value;
+    constexpr bool V8 = decltype(v8c)::value;
+    using CC = Cfg<NT, D>;
+    auto kernel = prefill_kernel<NT, D, V8>;
+    cudaError_t e2 =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CC::kSmemBytes);
+    if (e2 != cudaSuccess) return e2;
+    constexpr int need = NT == 2 ? kRegsOther2 * 128 + kRegsSoftmax2 * 256
+                         : D == 64 ? kRegsOtherD * 128 + kRegsSoftmaxD * 128
+                                   : 0;
+    if (need > 0) {
+      static int launch_regs = -1;  // one per instantiation
+      if (launch_regs < 0) {
+        cudaFuncAttributes attr;
+        e2 = cudaFuncGetAttributes(&attr, kernel);
+        if (e2 != cudaSuccess) return e2;
+        launch_regs = attr.numRegs;
+      }
+      if (launch_regs * CC::kThreads < need) return cudaErrorNotSupported;
     }
-    if (launch_regs * C2::kThreads < kRegsOther2 * 128 + kRegsSoftmax2 * 256)
-      return cudaErrorNotSupported;
-    e = go(prefill_kernel<2, 64>, C2::kThreads, C2::kSmemBytes);
-  } else if (d == 64) {
-    using C1 = Cfg<1, 64>;
-    e = cudaFuncSetAttribute(prefill_kernel<1, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C1::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    static int launch_regs = -1;  // as above, for the dual CTAs' split
-    if (launch_regs < 0) {
-      cudaFuncAttributes attr;
-      e = cudaFuncGetAttributes(&attr, prefill_kernel<1, 64>);
-      if (e != cudaSuccess) return e;
-      launch_regs = attr.numRegs;
-    }
-    if (launch_regs * C1::kThreads < kRegsOtherD * 128 + kRegsSoftmaxD * 128)
-      return cudaErrorNotSupported;
-    e = go(prefill_kernel<1, 64>, C1::kThreads, C1::kSmemBytes);
-  } else {
-    using C1 = Cfg<1, 128>;
-    e = cudaFuncSetAttribute(prefill_kernel<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C1::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = go(prefill_kernel<1, 128>, C1::kThreads, C1::kSmemBytes);
-  }
+    return go(kernel, CC::kThreads, CC::kSmemBytes);
+  };
+  auto launch_v8 = [&](auto ntc, auto dc) {
+    return v8 ? launch(ntc, dc, std::true_type()) : launch(ntc, dc, std::false_type());
+  };
+  if (nt == 2)
+    e = launch_v8(std::integral_constant<int, 2>(), std::integral_constant<int, 64>());
+  else if (d == 64)
+    e = launch_v8(std::integral_constant<int, 1>(), std::integral_constant<int, 64>());
+  else
+    e = launch_v8(std::integral_constant<int, 1>(), std::integral_constant<int, 128>());
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
   // split 0 carried the sink: the merge adds no sink of its own

@@ -92,6 +92,13 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
                "r"(src_bytes)
                : "memory");
 }
+// 32-byte global store (one full sector per lane); the address must be
+// 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 // 4-byte copy (zero-filled past src_bytes, which is 0 or 4).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),

@@ -116,3 +116,43 @@ def test_repeated_calls_are_bitwise_identical():
 
 def test_no_device_error_after_the_suite():
     assert sa.sinkattn_get_device_error() == 0
+
+
+def _off16(like):
+    """A tensor shaped like `like` whose data starts 16 bytes past a 32-byte
+    boundary (the ABI asks for 16-byte alignment only)."""
+    n = like.numel()
+    buf = torch.empty(n + 64, dtype=like.dtype, device=like.device)
+    base = buf.data_ptr()
+    start = ((32 - base % 32) % 32 + 16) // like.element_size()
+    t = buf[start:start + n].view(like.shape)
+    assert t.data_ptr() % 32 == 16
+    return t
+
+
+def test_outputs_aligned_to_16_bytes_only_match():
+    """Outputs on a 16-byte (not 32-byte) boundary take the 16-byte store path
+    and give bitwise the same results as 32-byte aligned ones."""
+    c = S.make_prefill("al", [1, 300, 129, 513], [1, 500, 129, 1000], 8, 2, seed=41,
+                       device="cuda")
+    cq, ck, sk = c.cu_seqlens_q.cuda(), c.cu_seqlens_k.cuda(), c.sinks.cuda()
+    for w in (0, 100):
+        out, lse = sa.sinkattn_prefill(c.q, c.k, c.v, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
+                                       sinks=sk, window=w)
+        o16 = _off16(out)
+        sa.sinkattn_prefill(c.q, c.k, c.v, cq, ck, c.max_seqlen_q, c.max_seqlen_k, sinks=sk,
+                            window=w, out=o16)
+        torch.cuda.synchronize()
+        assert torch.equal(out, o16)
+        dout = S.bf16_normal(tuple(c.q.shape), 43, device="cuda")
+        g = sa.sinkattn_prefill_backward(c.q, c.k, c.v, out, lse, dout, cq, ck, c.max_seqlen_q,
+                                         c.max_seqlen_k, sinks=sk, window=w)
+        dq16, dk16, dv16 = _off16(g[0]), _off16(g[1]), _off16(g[2])
+        g16 = sa.sinkattn_prefill_backward(c.q, c.k, c.v, out, lse, dout, cq, ck,
+                                           c.max_seqlen_q, c.max_seqlen_k, sinks=sk, window=w,
+                                           dq=dq16, dk=dk16, dv=dv16)
+        torch.cuda.synchronize()
+        for a, b in zip(g[:3], g16[:3]):
+            assert torch.equal(a, b)
+        assert torch.equal(g[3], g16[3])
+    assert sa.sinkattn_get_device_error() == 0
