@@ -96,9 +96,6 @@ struct BwdParams {
   // stall_ns on a barrier that nothing completes before their first scores,
   // so that every CTA of that kernel takes its timeout path.
   uint64_t stall_ns;
-  // dq, dk and dv start on 32-byte boundaries: rows are stored with 32-byte
-  // stores (whole sectors, half the store instructions)
-  int grad_v8;
 };
 
 // ----------------------------------------------------------------- prep ---
@@ -315,7 +312,10 @@ __device__ __forceinline__ void dq_decode(const BwdParams &p, int halves, int w,
   t.n = key_hi > key_lo ? (key_hi + kBN - 1) / kBN - t.kt_lo : 0;
 }
 
-template <int D>
+// kV8 (both gradient kernels): dq, dk and dv start on 32-byte boundaries, and
+// each thread's row segment is stored with 32-byte stores (whole sectors, half
+// the store instructions); otherwise with 16-byte ones.
+template <int D, bool kV8>
 __global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_do,
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->dq_free);  // the next item's dQ / Y may start
       if (pend_row) {
-        if (p.grad_v8) {
+        if constexpr (kV8) {
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             uint32_t w[8];
@@ -772,7 +772,7 @@ __device__ __forceinline__ void kv_decode(const BwdParams &p, int npairs, int ha
   t.steps = t.nqt * p.group;
 }
 
-template <int D>
+template <int D, bool kV8>
 __global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
@@ -1079,7 +1079,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       mbar_arrive(&bars->dkv_free);
       if (r < t.krows) {
         const float sc = p.scale;
-        if (p.grad_v8) {
+        if constexpr (kV8) {
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const float *x = reinterpret_cast<const float *>(&dvv[16 * i]);
@@ -1140,7 +1140,7 @@ size_t backward_workspace_bytes(int batch, int64_t total_q, int64_t total_k, int
 
 namespace {
 
-template <int D>
+template <int D, bool kV8>
 cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed) {
   constexpr int kHalves = TileShape<D>::kHalves;
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
@@ -1201,8 +1201,6 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
   p.dq = static_cast<__nv_bfloat16 *>(a.dq);
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
-  p.grad_v8 = ((reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |
-                reinterpret_cast<uintptr_t>(a.dv)) & 31u) == 0;
   p.stall_ns = g_bwd_stall_ns.load();
   if ((e = launch_tile_list(a.cu_q, a.batch, max_qtiles, reinterpret_cast<unsigned *>(qlist + 256),
                             reinterpret_cast<int *>(qlist + 4), reinterpret_cast<unsigned *>(qlist),
@@ -1227,16 +1225,16 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
     return cudaErrorInvalidValue;
   }
   constexpr int kDqSmem = DqCfg<D>::kSmem, kKvSmem = KvCfg<D>::kSmem;
-  if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, kV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kDqSmem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kKvSmem)) != cudaSuccess)
     return e;
   if (a.total_q > 0) {
     const int64_t items = (a.total_q / kBM + a.batch) * a.hq * kHalves;
     const int64_t grid = items < sm_count() ? items : sm_count();
-    bwd_dq_kernel<D><<<static_cast<unsigned>(grid), kDqThreads, kDqSmem, stream>>>(tq, tdo, tk,
-                                                                                   tv, p);
+    bwd_dq_kernel<D, kV8><<<static_cast<unsigned>(grid), kDqThreads, kDqSmem, stream>>>(
+        tq, tdo, tk, tv, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const bool dsink = a.sinks != nullptr && a.dsinks != nullptr;
@@ -1259,7 +1257,7 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dsink ? 1 : 0;
-    if ((e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D>, tq, tdo, tk, tv, p)) != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D, kV8>, tq, tdo, tk, tv, p)) != cudaSuccess)
       return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -1271,8 +1269,13 @@ cudaError_t launch_backward_d(const BackwardLaunch &a, cudaStream_t stream, bool
 cudaError_t launch_backward(const BackwardLaunch &a, cudaStream_t stream, bool *encode_failed) {
   *encode_failed = false;
   if (a.batch == 0) return cudaSuccess;
-  return a.head_dim == 128 ? launch_backward_d<128>(a, stream, encode_failed)
-                           : launch_backward_d<64>(a, stream, encode_failed);
+  const bool v8 = ((reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |
+                   reinterpret_cast<uintptr_t>(a.dv)) & 31u) == 0;
+  if (a.head_dim == 128)
+    return v8 ? launch_backward_d<128, true>(a, stream, encode_failed)
+              : launch_backward_d<128, false>(a, stream, encode_failed);
+  return v8 ? launch_backward_d<64, true>(a, stream, encode_failed)
+            : launch_backward_d<64, false>(a, stream, encode_failed);
 }
 
 cudaError_t backward_set_stall(uint64_t ns) {
