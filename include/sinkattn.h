@@ -28,6 +28,9 @@
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers owned by the caller, row-major,
  *    contiguous, 16-byte aligned. bf16 data is passed as `const void*`.
+ *    Prefill outputs (out) and backward gradients (dq, dk, dv) that start on
+ *    a 32-byte boundary are written with 32-byte stores, a faster path with
+ *    bitwise the same results.
  *  - The library allocates no device memory and never synchronises: every
  *    call only enqueues work on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and returns. Device-side metadata (sequence offsets,
