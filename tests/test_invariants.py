@@ -114,6 +114,27 @@ def test_repeated_calls_are_bitwise_identical():
     assert torch.equal(x[0], y[0]) and torch.equal(x[1], y[1])
 
 
+@pytest.mark.parametrize("causal,window", [(False, 0), (False, 100), (True, 0), (True, 50)])
+def test_split_prefill_repeats_bitwise(causal, window):
+    """Split-KV prefill repeated 12 times gives bitwise the same output each
+    time (a race between the softmax's O rescaling or epilogue and the P V
+    products would show up here as run-to-run differences)."""
+    p = S.make_prefill("dets", [1, 77, 300, 129, 0, 513, 1000],
+                       [1, 200, 300, 129, 5, 1000, 1000], 8, 2, seed=3, causal=causal,
+                       window=window)
+    args = (p.q.cuda(), p.k.cuda(), p.v.cuda(), p.cu_seqlens_q.cuda(), p.cu_seqlens_k.cuda(),
+            p.max_seqlen_q, p.max_seqlen_k)
+    ref = None
+    for _ in range(12):
+        o, l = sa.sinkattn_prefill(*args, sinks=p.sinks.cuda(), causal=causal, window=window,
+                                   num_splits=3)
+        torch.cuda.synchronize()
+        if ref is None:
+            ref = (o.clone(), l.clone())
+        else:
+            assert torch.equal(o, ref[0]) and torch.equal(l, ref[1])
+
+
 def test_no_device_error_after_the_suite():
     assert sa.sinkattn_get_device_error() == 0
 
