@@ -646,7 +646,22 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t o_addr = lane_addr + C::kTmemO + t * D;
     int K = 0;        // items of earlier tiles
-    int o_waits = 0;  // o_done[t] phases consumed
+    int o_waits = 0;  // o_done[t] phases consumed (one head per item: every phase, in order)
+    // Two heads per item: within an item the softmax waits for the previous
+    // P V into O_t only where it must rescale O_t, and on the item's last
+    // tile; the epilogue waits for the item's last P V. The waits name the
+    // phase by index: o_base = P V products into O_t before this item, o_pend
+    // = index of the pending item's last one. A parity wait is unambiguous
+    // when the barrier is at most one phase from the one waited for:
+    // - at tile j, S of item k is in only after P V(k - 3) has completed, and
+    //   a commit completes only after every earlier product of its issuing
+    //   thread, so P V(t, j - 2) is complete; P V(t, j) is not yet issued;
+    // - the epilogue can run without a later score wait in between (after an
+    //   item without keys, or at the end), so the wait on the item's last
+    //   tile (for P V(t, n - 2)) is what bounds it from below; the next P V
+    //   into O_t waits for o_free. Without that last-tile wait, split-KV
+    //   prefill gave run-to-run different results.
+    int o_base = 0, o_pend = 0;
     // The epilogue of a tile runs after the first P of the next tile has been
     // handed to the tensor core: the last P V of the tile then completes while
     // this warpgroup already works on the next tile (it only needs O once
@@ -674,8 +689,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
       const size_t prow_h = static_cast<size_t>(qrow) * p.hq + ph;
       bool have_o = false;
       if (pkeys) {
-        have_o = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], o_waits & 1, abort,
-                                                   &g_prefill_error));
+        have_o = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->o_done[t], (C::kSplitP ? o_waits : o_pend) & 1, abort,
+                                      &g_prefill_error));
         ++o_waits;
         if (!have_o) {
           ok = false;
@@ -852,10 +868,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
         const float2 a03 = __fadd2_rn(a01, a23);
         d_run += a03.x + a03.y;
         tmem_wait_st();
-        if (j > 0) {
-          // O_t holds P_0..P_{j-1} V; it must be complete before it is rescaled,
-          // and waiting for every phase in order keeps the parity unambiguous.
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], o_waits & 1, abort,
+        // O_t holds P_0..P_{j-1} V; it must be complete before it is rescaled
+        // (one head per item: waited for on every tile, every phase in order)
+        if (j > 0 && (C::kSplitP || j == n - 1 || __any_sync(0xffffffffu, rescale))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t],
+                                                 (C::kSplitP ? o_waits : o_base + j - 1) & 1, abort,
                                                  &g_prefill_error))) {
             ok = false;
             break;
@@ -896,6 +913,10 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
                           (n > 0 ? 1u << 15 : 0u) | (static_cast<unsigned>(h) << 16)));
       *pend_vs = p.v_scale != nullptr ? __ldg(p.v_scale + ti.kvh) : 1.f;
       mbar_arrive(&bars->tile_empty[slot]);
+      if (n > 0) {
+        o_pend = o_base + n - 1;
+        o_base += n;
+      }
       K += NT * n;
     }
     if (ok && pend_on) finish();
