@@ -646,16 +646,17 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t o_addr = lane_addr + C::kTmemO + t * D;
     int K = 0;        // items of earlier tiles
-    int o_waits = 0;  // o_done[t] phases consumed (one head per item: every phase, in order)
-    // Two heads per item: within an item the softmax waits for the previous
-    // P V into O_t only where it must rescale O_t, and on the item's last
-    // tile; the epilogue waits for the item's last P V. The waits name the
-    // phase by index: o_base = P V products into O_t before this item, o_pend
-    // = index of the pending item's last one. A parity wait is unambiguous
-    // when the barrier is at most one phase from the one waited for:
-    // - at tile j, S of item k is in only after P V(k - 3) has completed, and
-    //   a commit completes only after every earlier product of its issuing
-    //   thread, so P V(t, j - 2) is complete; P V(t, j) is not yet issued;
+    // Within an item the softmax waits for the previous P V into O_t only
+    // where it must rescale O_t, and on the item's last tile; the epilogue
+    // waits for the item's last P V. The waits name the phase by index:
+    // o_base = P V products into O_t before this item, o_pend = index of the
+    // pending item's last one. A parity wait is unambiguous when the barrier
+    // is at most one phase from the one waited for:
+    // - at tile j, P V(t, j - 2) is complete: with P over S (two heads), S of
+    //   item k is in only after P V(k - 3) has completed; with separate P
+    //   buffers (one head), P of item k is written only after P V(k - kSBufs)
+    //   has completed, kSBufs <= 2; and a commit completes only after every
+    //   earlier product of its issuing thread. P V(t, j) is not yet issued;
     // - the epilogue can run without a later score wait in between (after an
     //   item without keys, or at the end), so the wait on the item's last
     //   tile (for P V(t, n - 2)) is what bounds it from below; the next P V
@@ -690,9 +691,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
       bool have_o = false;
       if (pkeys) {
         have_o = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->o_done[t], (C::kSplitP ? o_waits : o_pend) & 1, abort,
+                            mbar_wait(&bars->o_done[t], o_pend & 1, abort,
                                       &g_prefill_error));
-        ++o_waits;
         if (!have_o) {
           ok = false;
           return;
@@ -869,15 +869,12 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, Cfg<NT, D>::kMinBlocks)
         d_run += a03.x + a03.y;
         tmem_wait_st();
         // O_t holds P_0..P_{j-1} V; it must be complete before it is rescaled
-        // (one head per item: waited for on every tile, every phase in order)
-        if (j > 0 && (C::kSplitP || j == n - 1 || __any_sync(0xffffffffu, rescale))) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t],
-                                                 (C::kSplitP ? o_waits : o_base + j - 1) & 1, abort,
+        if (j > 0 && (j == n - 1 || __any_sync(0xffffffffu, rescale))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (o_base + j - 1) & 1, abort,
                                                  &g_prefill_error))) {
             ok = false;
             break;
           }
-          ++o_waits;
           // one lane's rescale makes the whole warp run the (collective) O round
           // trip; lanes that did not move their maximum multiply by alpha = 1
           if (__any_sync(0xffffffffu, rescale)) {

@@ -114,14 +114,17 @@ def test_repeated_calls_are_bitwise_identical():
     assert torch.equal(x[0], y[0]) and torch.equal(x[1], y[1])
 
 
+@pytest.mark.parametrize("hq,d", [(8, 64), (6, 64), (4, 128)])
 @pytest.mark.parametrize("causal,window", [(False, 0), (False, 100), (True, 0), (True, 50)])
-def test_split_prefill_repeats_bitwise(causal, window):
+def test_split_prefill_repeats_bitwise(causal, window, hq, d):
     """Split-KV prefill repeated 12 times gives bitwise the same output each
     time (a race between the softmax's O rescaling or epilogue and the P V
-    products would show up here as run-to-run differences)."""
+    products would show up here as run-to-run differences): two heads per
+    item (groups of 4), one head per item in two CTAs per SM (groups of 3)
+    and head_dim 128."""
     p = S.make_prefill("dets", [1, 77, 300, 129, 0, 513, 1000],
-                       [1, 200, 300, 129, 5, 1000, 1000], 8, 2, seed=3, causal=causal,
-                       window=window)
+                       [1, 200, 300, 129, 5, 1000, 1000], hq, 2, seed=3, causal=causal,
+                       window=window, head_dim=d)
     args = (p.q.cuda(), p.k.cuda(), p.v.cuda(), p.cu_seqlens_q.cuda(), p.cu_seqlens_k.cuda(),
             p.max_seqlen_q, p.max_seqlen_k)
     ref = None
