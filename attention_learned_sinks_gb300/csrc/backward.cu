@@ -259,7 +259,8 @@ struct DqCfg {
   static constexpr int kOffK = kQdBufs * 2 * kTile;
   static constexpr int kOffV = kOffK + kStages * kTile;
   static constexpr int kOffBar = kOffV + kStages * kTile;
-  static constexpr int kSmem = kOffBar + 4096 + 1024;
+  static constexpr int kOffVec = kOffBar + 4096;  // per tile slot: -l2, -D of its 128 rows
+  static constexpr int kSmem = kOffVec + 2048 + 1024;
 };
 
 struct DqTile {
@@ -391,10 +392,28 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int w = static_cast<int>(atomicAdd(p.q_counter, 1u));
         if (w < num_work) dq_decode(p, kHalves, w, t);
         bars->tiles[slot] = t;
-        mbar_arrive(&bars->tile_full[slot]);
       }
       __syncwarp();
       const DqTile t = bars->tiles[slot];
+      // head_dim 64: the item's rows' -l2 / -D for the softmax warps, copied
+      // ahead and tracked by the descriptor's barrier (rows past the tile read
+      // as 0), so that an item's first step does not wait for two global
+      // loads (3.45 -> 3.39 ms on the varlen backward; at head_dim 128 the
+      // softmax warps load them themselves, 10.64 vs 10.70 ms)
+      if (D == 64 && t.valid && t.n > 0) {
+        const uint32_t vs = sbase + C::kOffVec + slot * 1024;
+        const size_t at = static_cast<size_t>(t.h) * p.total_q + t.q0 + t.qt * kBM;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = lane + 32 * i;
+          const bool in = row < t.rows;
+          cp_async_4(vs + 4 * row, p.nl2t + at + (in ? row : 0), in ? 4u : 0u);
+          cp_async_4(vs + 512 + 4 * row, p.ndt + at + (in ? row : 0), in ? 4u : 0u);
+        }
+        cp_async_mbar_arrive(&bars->tile_full[slot]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tile_full[slot]);
       if (!t.valid) break;
       if (t.n == 0) continue;  // nothing to load (and no MMAs) for this item
       const int qb = nq % kQdBufs;
@@ -426,6 +445,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int i = max(0, J - kStages); i < J; ++i)
         mbar_wait_warp(&bars->kv_full[i % kStages], (i / kStages) & 1, abort, err, true);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // the vector copies have landed
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------------ MMA
     // Two issuing warps, so that neither kind of product waits behind the
@@ -597,8 +617,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mbar_arrive(&bars->tile_empty[slot]);
         continue;
       }
-      const float l2 = r < t.rows ? -p.nl2t[lidx] : INFINITY;
-      const float d = r < t.rows ? -p.ndt[lidx] : 0.f;
+      const float *vec =
+          reinterpret_cast<const float *>(smem_raw + (sbase - raw) + C::kOffVec + slot * 1024);
+      const float l2 = r >= t.rows ? INFINITY : D == 64 ? -vec[r] : -p.nl2t[lidx];
+      const float d = r >= t.rows ? 0.f : D == 64 ? -vec[128 + r] : -p.ndt[lidx];
       const int pos = t.p_min + r;
       int hi = t.lk, lo = 0;
       if (p.causal) hi = min(hi, pos + 1);
