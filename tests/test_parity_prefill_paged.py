@@ -54,7 +54,8 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
-@pytest.mark.parametrize("page_size", [16, 1, 7, 128])
+# page sizes below, at and above the 8-row swizzle atom and the 128-key tile
+@pytest.mark.parametrize("page_size", [16, 1, 7, 128, 8, 64, 256])
 def test_prefill_paged_shapes(oracle_lib, shape, page_size):
     lq, lk = shape
     c = S.make_prefill_paged("pshape", lq, lk, 8, 2, seed=81 + sum(lk) + page_size,
